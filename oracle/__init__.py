@@ -1,0 +1,301 @@
+"""Python face of the reference oracle (``k3moe_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the bench's CPU
+baseline may import this; the library never does. It computes one Stable-LatentMoE
+routed-expert layer with MXFP4 experts in plain scalar C with double accumulation.
+
+Every function takes and returns numpy arrays; bf16 values travel as uint16 bit patterns.
+Parity status: every step is pinned by the ``-m "not gpu"`` tests except the SiTU-GLU
+activation, which the pages name without a formula (parity unpinned; the oracle refuses
+act != 0).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "k3moe_oracle.c")
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "libk3moe_oracle.so")
+
+
+def build(force: bool = False) -> str:
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+                               "-o", _LIB, _SRC, "-lm"])
+    return _LIB
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("hidden", "latent", "inter", "n_experts", "top_k", "act", "actq")]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [("w_router", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("w_in", ctypes.c_void_p), ("w_out", ctypes.c_void_p),
+                ("gate_q", ctypes.c_void_p), ("gate_s", ctypes.c_void_p),
+                ("up_q", ctypes.c_void_p), ("up_s", ctypes.c_void_p),
+                ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        p, i, d = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
+        L.k3o_bf16_to_double.argtypes = [ctypes.c_uint16]
+        L.k3o_bf16_to_double.restype = d
+        L.k3o_bf16_from_double.argtypes = [d]
+        L.k3o_bf16_from_double.restype = ctypes.c_uint16
+        for f in ("k3o_e2m1", "k3o_e8m0", "k3o_e4m3"):
+            getattr(L, f).argtypes = [i]
+            getattr(L, f).restype = d
+        L.k3o_e4m3_encode.argtypes = [d]
+        L.k3o_e4m3_encode.restype = i
+        L.k3o_mxfp8_block.argtypes = [p, p, p]
+        L.k3o_mxfp8_roundtrip.argtypes = [p, i]
+        L.k3o_mx_weight.argtypes = [p, p, i]
+        L.k3o_mx_weight.restype = d
+        L.k3o_dequant.argtypes = [p, p, i, i, p]
+        L.k3o_expert_params.argtypes = [p]
+        L.k3o_expert_params.restype = ctypes.c_int64
+        L.k3o_expert_bytes.argtypes = [p]
+        L.k3o_expert_bytes.restype = ctypes.c_int64
+        L.k3o_router_logits.argtypes = [p, p, i, p, p, p]
+        L.k3o_select_topk.argtypes = [p, i, i, i, p]
+        L.k3o_route_weights.argtypes = [p, p, i, i, i, p]
+        L.k3o_permute.argtypes = [p, i, i, i, p, p, p, p]
+        L.k3o_dense_proj.argtypes = [p, p, i, i, i, p, p]
+        L.k3o_expert_row.argtypes = [p, p, i, p, p, p]
+        L.k3o_expert_row.restype = i
+        L.k3o_combine_token.argtypes = [i, i, p, p, p, p]
+        L.k3o_layer_forward.argtypes = [p, p, p, i, p, p, p, p, p, p, i]
+        L.k3o_layer_forward.restype = i
+        L.k3o_max_threads.restype = i
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ------------------------------------------------------------------ formats
+def bf16_to_f64(b) -> np.ndarray:
+    b = np.asarray(b, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_from_f64(x) -> np.ndarray:
+    x = np.asarray(x, np.float64)
+    f = lib().k3o_bf16_from_double
+    return np.array([f(float(v)) for v in x.ravel()], np.uint16).reshape(x.shape)
+
+
+def e2m1(code: int) -> float:
+    return lib().k3o_e2m1(code)
+
+
+def e8m0(e: int) -> float:
+    return lib().k3o_e8m0(e)
+
+
+def e4m3(code: int) -> float:
+    return lib().k3o_e4m3(code)
+
+
+def e4m3_encode(v: float) -> int:
+    return lib().k3o_e4m3_encode(v)
+
+
+def mxfp8_block(v):
+    v = _c(v, np.float64)
+    assert v.shape == (32,)
+    codes = np.empty(32, np.uint8)
+    sc = np.empty(1, np.uint8)
+    lib().k3o_mxfp8_block(v.ctypes.data, codes.ctypes.data, sc.ctypes.data)
+    return codes, int(sc[0])
+
+
+def mxfp8_roundtrip(v):
+    v = _c(v, np.float64).copy()
+    lib().k3o_mxfp8_roundtrip(v.ctypes.data, v.size)
+    return v
+
+
+def dequant(q, s, N, K) -> np.ndarray:
+    q, s = _c(q, np.uint8), _c(s, np.uint8)
+    out = np.empty((N, K), np.float64)
+    lib().k3o_dequant(q.ctypes.data, s.ctypes.data, N, K, out.ctypes.data)
+    return out
+
+
+def mx_weight(q_row, s_row, j) -> float:
+    q_row, s_row = _c(q_row, np.uint8), _c(s_row, np.uint8)
+    return lib().k3o_mx_weight(q_row.ctypes.data, s_row.ctypes.data, j)
+
+
+def make_dims(d, act=0, actq=0) -> Dims:
+    return Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, act, actq)
+
+
+def expert_params(d) -> int:
+    return lib().k3o_expert_params(ctypes.byref(make_dims(d)))
+
+
+def expert_bytes(d) -> int:
+    return lib().k3o_expert_bytes(ctypes.byref(make_dims(d)))
+
+
+# ------------------------------------------------------------------ steps
+def router_logits(d, x, w_router, bias=None) -> np.ndarray:
+    x, wr = _c(x, np.uint16), _c(w_router, np.uint16)
+    T = x.shape[0]
+    b = None if bias is None else _c(bias, np.float32)
+    out = np.empty((T, d.n_experts), np.float64)
+    lib().k3o_router_logits(ctypes.byref(make_dims(d)), x.ctypes.data, T, wr.ctypes.data,
+                            _ptr(b), out.ctypes.data)
+    return out
+
+
+def select_topk(logits, k) -> np.ndarray:
+    lg = _c(logits, np.float64)
+    T, E = lg.shape
+    idx = np.empty((T, k), np.int32)
+    lib().k3o_select_topk(lg.ctypes.data, T, E, k, idx.ctypes.data)
+    return idx
+
+
+def route_weights(logits, idx) -> np.ndarray:
+    lg, idx = _c(logits, np.float64), _c(idx, np.int32)
+    T, E = lg.shape
+    k = idx.shape[1]
+    w = np.empty((T, k), np.float64)
+    lib().k3o_route_weights(lg.ctypes.data, idx.ctypes.data, T, E, k, w.ctypes.data)
+    return w
+
+
+def permute(idx, E):
+    idx = _c(idx, np.int32)
+    T, k = idx.shape
+    off = np.empty(E + 1, np.int32)
+    rt = np.empty(T * k, np.int32)
+    rs = np.empty(T * k, np.int32)
+    sr = np.empty(T * k, np.int32)
+    lib().k3o_permute(idx.ctypes.data, T, E, k, off.ctypes.data, rt.ctypes.data, rs.ctypes.data,
+                      sr.ctypes.data)
+    return off, rt, rs, sr
+
+
+def dense_proj(W, x):
+    """out = W x for every token row; returns (double [T][N], bf16 bits [T][N])."""
+    W, x = _c(W, np.uint16), _c(x, np.uint16)
+    N, K = W.shape
+    T = x.shape[0]
+    out = np.empty((T, N), np.float64)
+    ob = np.empty((T, N), np.uint16)
+    lib().k3o_dense_proj(W.ctypes.data, x.ctypes.data, T, N, K, out.ctypes.data, ob.ctypes.data)
+    return out, ob
+
+
+class ExpertTables:
+    """Keeps per-expert pointer tables (and the arrays behind them) alive."""
+
+    NAMES = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
+
+    def __init__(self, n_experts: int, experts: dict):
+        self.keep = []
+        self.tables = {}
+        for name in self.NAMES:
+            tab = (ctypes.c_void_p * n_experts)()
+            for e, t in experts.items():
+                a = _c(t[name], np.uint8)
+                self.keep.append(a)
+                tab[e] = a.ctypes.data
+            self.tables[name] = tab
+
+    def fill(self, w: Weights):
+        for name in self.NAMES:
+            setattr(w, name, ctypes.cast(self.tables[name], ctypes.c_void_p))
+
+
+class Layer:
+    """A layer for the oracle: dense weights (bf16 bits) plus the experts that may be
+    selected ({e: {gate_q, gate_s, up_q, up_s, down_q, down_s}})."""
+
+    def __init__(self, d, w_router, w_in, w_out, experts: dict, bias=None, act=0, actq=0):
+        self.d = d
+        self.dims = make_dims(d, act, actq)
+        self.wr = _c(w_router, np.uint16)
+        self.wi = _c(w_in, np.uint16)
+        self.wo = _c(w_out, np.uint16)
+        self.bias = None if bias is None else _c(bias, np.float32)
+        self.experts = experts
+        self.et = ExpertTables(d.n_experts, experts)
+        self.w = Weights()
+        self.w.w_router = self.wr.ctypes.data
+        self.w.router_bias = _ptr(self.bias)
+        self.w.w_in = self.wi.ctypes.data
+        self.w.w_out = self.wo.ctypes.data
+        self.et.fill(self.w)
+
+    def expert_row(self, e, z_row):
+        z = _c(z_row, np.uint16)
+        o = np.empty(self.d.latent, np.float64)
+        a = np.empty(self.d.inter, np.uint16)
+        rc = lib().k3o_expert_row(ctypes.byref(self.dims), ctypes.byref(self.w), e, z.ctypes.data,
+                                  o.ctypes.data, a.ctypes.data)
+        if rc != 0:
+            raise ValueError("oracle: unsupported activation")
+        return o, a
+
+    def forward(self, x, nthreads=1):
+        x = _c(x, np.uint16)
+        T = x.shape[0]
+        d = self.d
+        y = np.empty((T, d.hidden), np.uint16)
+        idx = np.empty((T, d.top_k), np.int32)
+        wt = np.empty((T, d.top_k), np.float64)
+        lg = np.empty((T, d.n_experts), np.float64)
+        z = np.empty((T, d.latent), np.uint16)
+        c = np.empty((T, d.latent), np.uint16)
+        rc = lib().k3o_layer_forward(ctypes.byref(self.dims), ctypes.byref(self.w), x.ctypes.data,
+                                     T, y.ctypes.data, idx.ctypes.data, wt.ctypes.data,
+                                     lg.ctypes.data, z.ctypes.data, c.ctypes.data, nthreads)
+        if rc != 0:
+            raise ValueError("oracle: unsupported mode or missing expert tensors")
+        return {"y": y, "idx": idx, "w": wt, "logits": lg, "z": z, "c": c}
+
+
+def combine(o_rows, slot_row, w, T, k):
+    """c[t] = bf16(sum_j w[t][j] * o_rows[slot_row[t*k+j]]), j ascending."""
+    o_rows = _c(o_rows, np.float64)
+    w = _c(w, np.float64)
+    L = o_rows.shape[1]
+    c = np.empty((T, L), np.uint16)
+    for t in range(T):
+        rows = [o_rows[slot_row[t * k + j]] for j in range(k)]
+        tab = (ctypes.c_void_p * k)(*[r.ctypes.data for r in rows])
+        wt = _c(w[t], np.float64)
+        ct = np.empty(L, np.uint16)
+        lib().k3o_combine_token(L, k, ctypes.cast(tab, ctypes.c_void_p), wt.ctypes.data,
+                                ct.ctypes.data, None)
+        c[t] = ct
+    return c
+
+
+def max_threads() -> int:
+    return lib().k3o_max_threads()

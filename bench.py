@@ -1,0 +1,427 @@
+"""Benchmark of the routed-expert layer (one Stable-LatentMoE layer with MXFP4 experts).
+
+  python bench.py [--workload decode_b1|decode_b64|prefill_4k|prefill_32k] [--steps K]
+                  [--warmup W] [--gpus N] [--impl ours|reference]
+
+A step is one k3moe_layer_forward over one batch of synthetic tokens (seeded generator, K3
+shapes: hidden 7168, latent 3584, 896 experts of 17,547,264 bytes, top-16). Prints one JSON
+line. ``value`` is device-timed throughput (CUDA events around exactly K steps, inputs
+resident in HBM); ``e2e`` is the same through the C ABI with the step's tokens copied from
+pinned host memory and its output copied back inside the timed region. Caches: the expert
+store (15.7 GB) is far larger than L2, tokens are fresh every step, and the dense weights
+rotate over 4 copies (462 MB) so no step finds them in L2.
+
+--impl reference times the CPU oracle (plain C, double accumulation) on the host cores on a
+bounded sample of the same workload; see cpu_sample().
+
+Multi-GPU: the layer does not shard across GPUs in this build (replicas only): under torchrun
+every rank runs its own replica on its own GPU and rank 0 reports the sum of tokens/s over
+the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (decode b1/b64, prefill 4K/32K) + % of HBM / FP4 roofline"
+DENSE_COPIES = 4
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"], "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm, mx, reasons = [], None, set()
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except ValueError:
+                continue
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        loaded = [s for s in sm if mx and s > 0.5 * mx] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- algorithmic work
+def algorithmic(d, T, distinct_experts):
+    """Bytes and flops one layer step must move / compute (dense weights once, each selected
+    expert's bytes once, activations of the step)."""
+    dense_w = 2 * (d.n_experts * d.hidden + 2 * d.latent * d.hidden)
+    act = 2 * T * d.hidden * 2 + T * d.n_experts * 4
+    expert = distinct_experts * d.expert_bytes
+    flops = 2 * T * (d.n_experts * d.hidden + 2 * d.latent * d.hidden) + \
+        2 * T * d.top_k * 3 * d.latent * d.inter
+    return dense_w + expert + act, flops
+
+
+def kernel_bytes(name, d, T, distinct, rows):
+    """Algorithmic bytes of one launch of a profiled kernel."""
+    L, I, H, E = d.latent, d.inter, d.hidden, d.n_experts
+    glu_w = 2 * (d.gate_q_bytes + d.gate_s_bytes)
+    down_w = d.down_q_bytes + d.down_s_bytes
+    return {
+        "router_latent_in_gemv": 2 * (E + L) * H + 2 * T * H + 4 * T * E + 2 * T * L * 2,
+        "latent_out_gemv": 2 * H * L + 2 * T * L + 2 * T * H,
+        "expert_glu_gemv": distinct * glu_w + rows * (2 * L + 4 * I),
+        "expert_down_gemv": distinct * down_w + rows * (2 * I + 4 * L),
+        "combine": rows * 4 * L + 2 * T * L,
+    }.get(name)
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads):
+    """Times the oracle on (token, slot) units: each unit is one routed expert row through the
+    oracle (gate/up, GLU, down; ~33M MACs) plus 1/k of that token's dense work (router, latent
+    in and latent out rows), i.e. 1/k of a token. Units run on `nthreads` host threads.
+    Returns (tokens/s, units timed, seconds)."""
+    import oracle
+    import synth
+
+    d = w.dims
+    k = d.top_k
+    wr, wi, wo = synth.host_dense(d, layer_seed)
+    experts = {}
+    units = []
+    for t in range(idx_sample.shape[0]):
+        for j in range(k):
+            e = int(idx_sample[t, j])
+            units.append((t, j, e))
+    need = {e for (_, _, e) in units[: units_per_step * steps]}
+    for e in need:
+        experts[e] = synth.host_expert(d, layer_seed, e)
+    lay = oracle.Layer(d, wr, wi, wo, experts)
+    _, z_all = oracle.dense_proj(wi, x_np[: idx_sample.shape[0]])
+    E_sl, L_sl, H_sl = d.n_experts // k, d.latent // k, d.hidden // k
+
+    def run_unit(u):
+        t, j, e = u
+        xt = x_np[t:t + 1]
+        oracle.dense_proj(wr[j * E_sl:(j + 1) * E_sl], xt)
+        oracle.dense_proj(wi[j * L_sl:(j + 1) * L_sl], xt)
+        lay.expert_row(e, z_all[t])
+        oracle.dense_proj(wo[j * H_sl:(j + 1) * H_sl], z_all[t:t + 1])
+
+    def run_step(s):
+        us = units[(s * units_per_step) % len(units):][:units_per_step]
+        if len(us) < units_per_step:
+            us = us + units[: units_per_step - len(us)]
+        ths = [threading.Thread(target=lambda grp=us[i::nthreads]: [run_unit(u) for u in grp])
+               for i in range(min(nthreads, len(us)))]
+        for th in ths:
+            th.start()
+        for th in ths:
+            th.join()
+
+    return lay, run_step
+
+
+def run_reference(args, w):
+    """Reference arm: the CPU oracle on the host cores (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import synth
+    nth = os.cpu_count() or 1
+    d = w.dims
+    T = min(w.tokens, 64)
+    x = synth.host_x(w, 0, T)
+    import oracle
+    wr, _, _ = synth.host_dense(d, 0)
+    idx = oracle.select_topk(oracle.router_logits_np(x, wr, synth.router_bias(w)), d.top_k)
+    # per-step sample sized so warmup + steps stay within ~150 s of wall time, calibrated on
+    # one unit (a step never takes less than one unit's time)
+    _, step1 = cpu_sample(w, 0, x, idx, 1, 1, 1)
+    t0 = time.perf_counter()
+    step1(0)
+    per_unit_s = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    units = max(1, min(nth * 4, int(budget * nth / per_unit_s)))
+    units = max(1, (units // nth) * nth) if units >= nth else units
+    _, step = cpu_sample(w, 0, x, idx, units, args.steps + args.warmup, nth)
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(args.warmup + s)
+    el = time.perf_counter() - t0
+    tokens = args.steps * units / d.top_k
+    val = tokens / el
+    sample = (f"{units} (token, expert-slot) units per step = {units / d.top_k:.3g} tokens of the "
+              f"{w.name} workload (expert row + 1/{d.top_k} of the token's dense rows each)")
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
+           "config": {"workload": w.name, "tokens_per_step": w.tokens},
+           "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": nth, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_ours(args, w):
+    import torch
+    import mxfp4_expert_ffn_top16_gb300 as k3
+    import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    d = w.dims
+    T = w.tokens
+    E = d.n_experts
+
+    # --- layer: one expert store, DENSE_COPIES copies of the dense weights
+    t_setup = time.time()
+    sizes = {"gate_q": E * d.gate_q_bytes, "gate_s": E * d.gate_s_bytes, "up_q": E * d.gate_q_bytes,
+             "up_s": E * d.gate_s_bytes, "down_q": E * d.down_q_bytes, "down_s": E * d.down_s_bytes}
+    ex = {n: torch.empty(b, dtype=torch.uint8, device=dev) for n, b in sizes.items()}
+    dense = []
+    for c in range(DENSE_COPIES):
+        dd = {"w_router": torch.empty(E * d.hidden, dtype=torch.int16, device=dev),
+              "w_in": torch.empty(d.latent * d.hidden, dtype=torch.int16, device=dev),
+              "w_out": torch.empty(d.hidden * d.latent, dtype=torch.int16, device=dev)}
+        dense.append(dd)
+    ptrs = {n: t.data_ptr() for n, t in ex.items()}
+    ptrs.update({n: t.data_ptr() for n, t in dense[0].items()})
+    synth.dev_fill_layer(d, 0, ptrs, sh)
+    for c in range(1, DENSE_COPIES):
+        for n in dense[c]:
+            dense[c][n].copy_(dense[0][n])
+    bias_np = synth.router_bias(w)
+    bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
+    dims = k3.Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, 0, args.actq)
+    wts = [k3.Weights(dd["w_router"].data_ptr(), None if bias is None else bias.data_ptr(),
+                      dd["w_in"].data_ptr(), dd["w_out"].data_ptr(),
+                      *[ex[n].data_ptr() for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q",
+                                                   "down_s")]) for dd in dense]
+    nx = w.x_count
+    x = torch.empty((nx, d.hidden), dtype=torch.int16, device=dev)
+    synth.dev_fill_x(w, x.data_ptr(), cuda_stream=sh)
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device=dev)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=dev)
+    nbytes = k3.k3moe_workspace_size(dims, T)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    setup_s = time.time() - t_setup
+    nsteps_x = max(1, nx // T)
+
+    def step(i, xp=None, yp=None):
+        xi = xp if xp is not None else x[(i % nsteps_x) * T:].data_ptr()
+        k3.k3moe_layer_forward(dims, wts[i % DENSE_COPIES], xi, T, yp or y.data_ptr(),
+                               idx.data_ptr(), None, ws.data_ptr(), nbytes, sh)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+            torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    st = k3.k3moe_check(ws.data_ptr(), sh)
+    if st != 0:
+        raise RuntimeError("warmup: " + k3.status_string(st))
+
+    # --- pass 1: device-timed value
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    ev1.record(stream)
+    barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1))
+    st = k3.k3moe_check(ws.data_ptr(), sh)
+    if st != 0:
+        raise RuntimeError("timed: " + k3.status_string(st))
+    idx_last = idx.cpu().numpy()
+    distinct = int(len(np.unique(idx_last)))
+
+    # --- pass 2: the same steps with per-kernel CUDA events (roofline of the top kernel)
+    barrier()
+    k3.k3moe_profile(1)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    prof = k3.k3moe_profile(0)
+    barrier()
+
+    # --- pass 3: end to end through the C ABI with pinned host buffers
+    xh = torch.empty((nx, d.hidden), dtype=torch.int16, pin_memory=True)
+    xh.copy_(x.cpu())
+    yh = torch.empty((args.steps, T, d.hidden), dtype=torch.int16, pin_memory=True)
+    xs = torch.empty((T, d.hidden), dtype=torch.int16, device=dev)
+    barrier()
+    ev0.record(stream)
+    for i in range(args.steps):
+        j = (args.warmup + i) % nsteps_x
+        xs.copy_(xh[j * T:(j + 1) * T], non_blocking=True)
+        step(args.warmup + i, xp=xs.data_ptr())
+        yh[i].copy_(y, non_blocking=True)
+    ev1.record(stream)
+    barrier()
+    ms_e2e = max_over_ranks(ev0.elapsed_time(ev1))
+    clk = clocks.stop()
+
+    tokens_all = args.steps * T * world
+    value = tokens_all / (ms / 1e3)
+    e2e = tokens_all / (ms_e2e / 1e3)
+    pk = peaks()
+    # dominant kernel by time share
+    top = max(prof.items(), key=lambda kv: kv[1][0])
+    name, (tot_ms, launches) = top
+    per_launch_ms = tot_ms / max(1, launches)
+    kb = kernel_bytes(name, d, T, distinct, T * d.top_k)
+    achieved = kb / (per_launch_ms / 1e3) / 1e9 if kb else None
+    step_bytes, step_flops = algorithmic(d, T, distinct)
+    kernels_per_step = {"permute": 1 if T <= 256 else 3}
+    launches_total = sum(n for _, n in prof.values()) + \
+        (kernels_per_step["permute"] - 1) * prof.get("permute", (0, 0))[1]
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "mxfp4 weights x " + ("mxfp8" if args.actq else "bf16") + " activations, fp32 accumulate",
+        "data": "synthetic (seeded SplitMix64; bf16 ~N(0,1) tokens, ~N(0,0.02) dense, U{0..15} codes, U{120..127} e8m0)",
+        "config": {"workload": w.name, "tokens_per_step": T, "hidden": d.hidden, "latent": d.latent,
+                   "inter": d.inter, "n_experts": d.n_experts, "top_k": d.top_k,
+                   "router_bias": w.bias, "actq": "mxfp8" if args.actq else "bf16",
+                   "l2": "expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 4 copies",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
+                     "traffic": None, "peak_src": pk["src"] + " (burst copy)",
+                     "algorithmic_bytes_per_launch": kb, "avg_launch_ms": per_launch_ms},
+        "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
+                          "achieved_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
+                          "frac_hbm": step_bytes / (ms / args.steps / 1e3) / 1e9 / pk["hbm_gbs"]},
+        "kernels": {n: {"ms_per_launch": (t / c if c else None), "launches": c,
+                        "share": t / sum(v[0] for v in prof.values())} for n, (t, c) in prof.items()},
+        "distinct_experts_last_step": distinct,
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * d.hidden * 2,
+                "d2h_bytes_per_step": T * d.hidden * 2},
+        "gpu_launches": int(launches_total / max(1, 1)),
+        "clocks": clk,
+        "setup_s": setup_s,
+    }
+    out["gpu_launches"] = int(launches_total)
+    if rank == 0 and not args.no_cpu_baseline:
+        nth = os.cpu_count() or 1
+        xs_np = synth.host_x(w, 0, min(T, 8) if T > 1 else 16)
+        import oracle
+        wr, _, _ = synth.host_dense(d, 0)
+        isamp = oracle.select_topk(oracle.router_logits_np(xs_np, wr, bias_np), d.top_k)
+        units = nth * 2
+        steps_cpu = 3
+        _, cstep = cpu_sample(w, 0, xs_np, isamp, units, steps_cpu + 1, nth)
+        cstep(0)
+        t0 = time.perf_counter()
+        for s in range(steps_cpu):
+            cstep(1 + s)
+        el = time.perf_counter() - t0
+        out["cpu_baseline"] = {
+            "value": steps_cpu * units / d.top_k / el, "unit": "tokens/s", "cores": nth,
+            "kind": "oracle",
+            "sample": f"{steps_cpu * units} (token, expert-slot) units = {steps_cpu * units / d.top_k:.2f} "
+                      f"tokens of {w.name}; each unit = one expert row + 1/{d.top_k} of the token's "
+                      f"dense rows, {el:.1f} s on {nth} threads"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_b1")
+    ap.add_argument("--actq", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    import synth
+    w = synth.WORKLOADS[args.workload]
+    default_steps = {"decode_b1": 1000, "decode_b64": 200, "prefill_4k": 20, "prefill_32k": 4}
+    if args.steps is None:
+        args.steps = default_steps.get(w.name, 20)
+    if args.warmup is None:
+        args.warmup = max(3, min(20, args.steps // 10))
+    args.warmup = max(3, args.warmup)
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+/*
+ * libk3moe -- one Stable-LatentMoE routed-expert layer with MXFP4 experts, on one GPU.
+ *
+ * The layer (Kimi K3, as the pages describe it):
+ *   - "kimi-k3-mlx" digest, "Architecture" table: 896 routed experts, top-16 per token;
+ *     the routed experts work in a 3584-wide latent space, not on the 7168-wide residual
+ *     (Stable LatentMoE); the activation is a GLU evaluated in fp32.
+ *   - "kimi-k3-in-c", "MXFP4 experts": expert weights are 4-bit codes indexing a 16-entry
+ *     table, 32 consecutive weights share one 8-bit exponent, 17,547,264 bytes per expert.
+ *   - "Kimi K3 hardware deep dive", quantisation-aware training: MXFP4 weights with MXFP8
+ *     activations.
+ *
+ * Per token t (x_t in R^H, H = hidden):
+ *   l      = W_r x_t + b                       router logits over E experts      (k3moe_route)
+ *   S_t    = the k largest l (ties -> lowest index), reported in ascending index order
+ *   w_j    = softmax(l)_j / sum_{i in S_t} softmax(l)_i, i.e. softmax over the kept logits
+ *   z_t    = bf16(W_in x_t)                    latent in, [L][H]                 (k3moe_project)
+ *   rows   = (token, slot) pairs grouped by expert, token order within an expert (k3moe_permute)
+ *   o_tj   = D_e bf16(silu(G_e z_t) * (U_e z_t))  for e = S_t[j], MXFP4 G,U [I][L], D [L][I]
+ *                                                                             (k3moe_expert_ffn_mxfp4)
+ *   c_t    = bf16(sum_j w_j o_tj)              combine in latent space           (k3moe_combine)
+ *   y_t    = bf16(W_out c_t)                   latent out, [H][L]                (k3moe_project)
+ * k3moe_layer_forward runs all of it. In MXFP8 mode (actq = 1) z and the GLU output go
+ * through an MXFP8 round trip (E4M3 elements, one E8M0 scale per 32, OCP MX v1.0) before
+ * they enter an expert matrix.
+ *
+ * Storage (all row-major, K contiguous; bf16 as uint16_t bit patterns):
+ *   w_router [E][H] bf16, router_bias [E] fp32 (may be NULL), w_in [L][H], w_out [H][L] bf16.
+ *   gate_q, up_q [E][I][L/2] uint8: two e2m1 codes per byte, weight 2j in the low nibble.
+ *   gate_s, up_s [E][I][L/32] uint8: e8m0, value 2^(s-127), one per 32 weights along K.
+ *   down_q [E][L][I/2], down_s [E][L][I/32] likewise.
+ *
+ * Conventions for every call:
+ *   - Pointers are device pointers unless stated; the caller owns all memory. No call
+ *     allocates device memory or synchronises the stream (except k3moe_check).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *   - Work is enqueued asynchronously; a returned K3MOE_OK means the launches were accepted.
+ *   - T = 0 is valid and does nothing.
+ *   - Arguments are checked before anything is launched; a failed check launches nothing.
+ *   - Device pointers must be 16-byte aligned (K3MOE_E_ALIGN otherwise).
+ *   - hidden, latent and inter must be positive multiples of 64; 1 <= top_k <= 32,
+ *     top_k <= n_experts <= 1024.
+ *   - Faults the device detects (a bounded wait that ran out) are recorded in the
+ *     workspace and reported by k3moe_check.
+ *   - No call throws, exits or aborts.
+ * Reported rather than guaranteed: e8m0 = 0 (2^-127) is flushed to zero by the expert
+ * kernels, and e8m0 = 255 (NaN) makes the affected outputs non-finite.
+ */
+#ifndef K3MOE_H
+#define K3MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum k3moe_status {
+  K3MOE_OK = 0,
+  K3MOE_E_NULL = 1,      /* a required pointer is NULL */
+  K3MOE_E_SHAPE = 2,     /* a size is out of range or not a supported multiple */
+  K3MOE_E_ALIGN = 3,     /* a device pointer is not 16-byte aligned */
+  K3MOE_E_WORKSPACE = 4, /* workspace missing or smaller than k3moe_workspace_size() */
+  K3MOE_E_MODE = 5,      /* act / actq not supported (act = 1, SiTU-GLU, has no formula) */
+  K3MOE_E_CUDA = 6,      /* a CUDA runtime call or launch failed */
+  K3MOE_E_TIMEOUT = 7,   /* a device-side bounded wait ran out (see k3moe_check) */
+  K3MOE_E_DEVICE = 8     /* no usable sm_100-family device, or a device-side check failed */
+} k3moe_status;
+
+typedef struct k3moe_dims {
+  int32_t hidden;    /* H, residual width (K3: 7168) */
+  int32_t latent;    /* L, latent width (K3: 3584) */
+  int32_t inter;     /* I, expert intermediate width (K3: 3072) */
+  int32_t n_experts; /* E (K3: 896) */
+  int32_t top_k;     /* k (K3: 16) */
+  int32_t act;       /* 0 = SiLU-GLU silu(gate) * up, fp32; 1 = SiTU-GLU -> K3MOE_E_MODE */
+  int32_t actq;      /* 0 = bf16 activations; 1 = MXFP8 activations (E4M3 + E8M0 per 32) */
+} k3moe_dims;
+
+typedef struct k3moe_weights {
+  const uint16_t* w_router;   /* [E][H] bf16 */
+  const float* router_bias;   /* [E] fp32, added to the logits; may be NULL */
+  const uint16_t* w_in;       /* [L][H] bf16 */
+  const uint16_t* w_out;      /* [H][L] bf16 */
+  const uint8_t* gate_q;      /* [E][I][L/2] */
+  const uint8_t* gate_s;      /* [E][I][L/32] */
+  const uint8_t* up_q;        /* [E][I][L/2] */
+  const uint8_t* up_s;        /* [E][I][L/32] */
+  const uint8_t* down_q;      /* [E][L][I/2] */
+  const uint8_t* down_s;      /* [E][L][I/32] */
+} k3moe_weights;
+
+/* Bytes of device workspace that every call below needs for up to `max_tokens` tokens.
+ * The workspace is caller-owned scratch; its first 256 bytes hold the device error word.
+ * Zero it once after allocation (cudaMemset) so the error word starts clear. */
+k3moe_status k3moe_workspace_size(const k3moe_dims* dims, int32_t max_tokens, size_t* bytes);
+
+/* Router scores and top-k ("kimi-k3-mlx", Architecture table: 896 experts, top-16).
+ *   x [T][H] bf16, w_router [E][H] bf16, bias [E] fp32 or NULL.
+ *   logits [T][E] fp32 out (may be NULL), topk_idx [T][k] int32 out (ascending expert
+ *   index within a token), topk_w [T][k] fp32 out (renormalised softmax weights). */
+k3moe_status k3moe_route(const k3moe_dims* dims, const uint16_t* x, int32_t T,
+                         const uint16_t* w_router, const float* bias, float* logits,
+                         int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Token-by-expert permutation: histogram over experts, exclusive scan, stable scatter.
+ *   topk_idx [T][k] int32 in [0, E): each token's experts, distinct.
+ *   expert_offsets [E+1] out: rows of expert e are [offsets[e], offsets[e+1]).
+ *   row_token, row_slot [T*k] out: the (token, slot) behind sorted row r; rows of one
+ *   expert are in ascending token order. slot_row [T*k] out: sorted row of pair (t, j). */
+k3moe_status k3moe_permute(const k3moe_dims* dims, const int32_t* topk_idx, int32_t T,
+                           int32_t* expert_offsets, int32_t* row_token, int32_t* row_slot,
+                           int32_t* slot_row, void* ws, size_t ws_bytes, void* stream);
+
+/* Dense bf16 projection out = bf16(W x) per token: the latent in (W_in [L][H]) and latent
+ * out (W_out [H][L]) steps of Stable LatentMoE ("kimi-k3-mlx", LatentMoE: routed experts
+ * compress the 7168-wide residual to 3584).
+ *   W [N][K] bf16, x [T][K] bf16, out [T][N] bf16; N, K positive multiples of 64. */
+k3moe_status k3moe_project(const uint16_t* W, const uint16_t* x, int32_t T, int32_t N,
+                           int32_t K, uint16_t* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Routed expert FFN over the permuted rows ("kimi-k3-in-c", MXFP4 experts):
+ *   for each sorted row r of expert e with token t = row_token[r]:
+ *   o_rows[r] = D_e bf16(act(G_e z_t) * (U_e z_t))   (fp32 accumulation, fp32 GLU)
+ *   z [T][L] bf16; expert_offsets [E+1], row_token [T*k] as from k3moe_permute;
+ *   o_rows [T*k][L] fp32 out, in sorted-row order. */
+k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights* weights,
+                                    const uint16_t* z, int32_t T, const int32_t* expert_offsets,
+                                    const int32_t* row_token, float* o_rows, void* ws,
+                                    size_t ws_bytes, void* stream);
+
+/* Routing-weighted combine in latent space: c[t] = bf16(sum_{j<k} w[t][j] o_rows[slot_row[t*k+j]]),
+ * summed in fp32 with j ascending. o_rows [T*k][L] fp32, slot_row [T*k], topk_w [T][k],
+ * c [T][L] bf16 out. */
+k3moe_status k3moe_combine(const k3moe_dims* dims, const float* o_rows, const int32_t* slot_row,
+                           const float* topk_w, int32_t T, uint16_t* c, void* stream);
+
+/* The whole routed-expert layer: x [T][H] bf16 -> y [T][H] bf16. topk_idx_out [T][k] and
+ * topk_w_out [T][k] may be NULL; when given they receive the routing decisions. */
+k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* weights,
+                                 const uint16_t* x, int32_t T, uint16_t* y,
+                                 int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, reads and clears the workspace error word. Returns K3MOE_OK,
+ * K3MOE_E_TIMEOUT (a bounded wait ran out) or K3MOE_E_DEVICE (another device-side check),
+ * or K3MOE_E_CUDA if the stream reported an error. */
+k3moe_status k3moe_check(void* ws, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* k3moe_status_string(k3moe_status status);
+
+/* Diagnostic per-kernel timing of k3moe_layer_forward (not needed for normal use; no
+ * counterpart on the pages). mode = 1 starts recording: every kernel launch of later
+ * layer_forward calls is bracketed by CUDA events on the caller's stream. mode = 0 stops,
+ * synchronises those events and writes, for kernel ids 0 .. n-1, the summed milliseconds
+ * (total_ms[n]) and launch counts (launches[n]); either array may be NULL. Returns
+ * K3MOE_E_CUDA if an event call fails. Kernel names: k3moe_profile_name(id), NULL past the
+ * last id. Not thread-safe; recording holds at most 65,536 launches. */
+k3moe_status k3moe_profile(int32_t mode, int32_t n, float* total_ms, int32_t* launches);
+const char* k3moe_profile_name(int32_t id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* K3MOE_H */

@@ -1,0 +1,394 @@
+// C entry points of libk3moe (declared in include/k3moe.h): argument checks, workspace
+// layout and the launch sequence of each call. Every device step runs in this library's
+// kernels; nothing here computes on the host.
+#include <cstdint>
+#include <cstring>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "k3moe.h"
+#include "k3moe_internal.cuh"
+
+namespace k3moe {
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
+  WsLayout L{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t E = (size_t)d.n_experts, k = (size_t)d.top_k, Lw = (size_t)d.latent,
+               I = (size_t)d.inter, Tt = (size_t)T;
+  const size_t rows = Tt * k;
+  L.err = take(256);
+  L.logits = take(Tt * E * 4);
+  L.idx = take(rows * 4);
+  L.wts = take(rows * 4);
+  L.offsets = take((E + 1) * 4);
+  L.row_token = take(rows * 4);
+  L.row_slot = take(rows * 4);
+  L.slot_row = take(rows * 4);
+  L.plan = take(plan_ints((int)E) * 4);
+  L.z = take(Tt * Lw * 2);
+  L.zh = take(Tt * Lw * 2);
+  L.zs = take(Tt * Lw / 32);
+  L.a = take(rows * I * 2);
+  L.ah = take(rows * I * 2);
+  L.as = take(rows * I / 32);
+  L.o = take(rows * Lw * 4);
+  L.c = take(Tt * Lw * 2);
+  L.perm = take(((Tt + 255) / 256) * E * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace k3moe
+
+using namespace k3moe;
+
+namespace {
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(ws) + off);
+}
+
+bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+k3moe_status check_dims(const k3moe_dims* d) {
+  if (!d) return K3MOE_E_NULL;
+  if (d->hidden <= 0 || d->latent <= 0 || d->inter <= 0) return K3MOE_E_SHAPE;
+  if (d->hidden % 64 || d->latent % 64 || d->inter % 64) return K3MOE_E_SHAPE;
+  if (d->n_experts < 1 || d->n_experts > 1024) return K3MOE_E_SHAPE;
+  if (d->top_k < 1 || d->top_k > 32 || d->top_k > d->n_experts) return K3MOE_E_SHAPE;
+  if (d->act != 0) return K3MOE_E_MODE;
+  if (d->actq != 0 && d->actq != 1) return K3MOE_E_MODE;
+  return K3MOE_OK;
+}
+
+k3moe_status check_ws(const k3moe_dims& d, int32_t T, void* ws, size_t ws_bytes) {
+  if (!ws) return K3MOE_E_WORKSPACE;
+  if (misaligned(ws)) return K3MOE_E_ALIGN;
+  if (ws_layout(d, T).total > ws_bytes) return K3MOE_E_WORKSPACE;
+  return K3MOE_OK;
+}
+
+k3moe_status check_weights(const k3moe_weights* w, bool dense, bool experts) {
+  if (!w) return K3MOE_E_NULL;
+  if (dense) {
+    if (!w->w_router || !w->w_in || !w->w_out) return K3MOE_E_NULL;
+    if (misaligned(w->w_router) || misaligned(w->w_in) || misaligned(w->w_out) ||
+        misaligned(w->router_bias))
+      return K3MOE_E_ALIGN;
+  }
+  if (experts) {
+    const void* p[6] = {w->gate_q, w->gate_s, w->up_q, w->up_s, w->down_q, w->down_s};
+    for (const void* q : p) {
+      if (!q) return K3MOE_E_NULL;
+      if (misaligned(q)) return K3MOE_E_ALIGN;
+    }
+  }
+  return K3MOE_OK;
+}
+
+// ---------------------------------------------------------------- diagnostic profiling
+enum ProfId {
+  P_ROUTER_LATENT = 0, P_TOPK, P_PERMUTE, P_GLU, P_DOWN, P_COMBINE, P_LATENT_OUT, P_COUNT
+};
+const char* const kProfNames[P_COUNT] = {"router_latent_in_gemv", "topk", "permute",
+                                         "expert_glu_gemv", "expert_down_gemv", "combine",
+                                         "latent_out_gemv"};
+struct Profiler {
+  bool on = false;
+  static constexpr int kMax = 65536;
+  cudaEvent_t* ev = nullptr;  // pairs
+  int* id = nullptr;
+  int used = 0;
+};
+Profiler g_prof;
+
+struct ProfScope {
+  int slot = -1;
+  cudaStream_t s;
+  ProfScope(int pid, cudaStream_t st) : s(st) {
+    if (!g_prof.on || g_prof.used >= Profiler::kMax) return;
+    slot = g_prof.used++;
+    g_prof.id[slot] = pid;
+    cudaEventRecord(g_prof.ev[2 * slot], s);
+  }
+  ~ProfScope() {
+    if (slot >= 0) cudaEventRecord(g_prof.ev[2 * slot + 1], s);
+  }
+};
+
+#define K3_TRY(expr)                        \
+  do {                                      \
+    const k3moe_status st_ = (expr);        \
+    if (st_ != K3MOE_OK) return st_;        \
+  } while (0)
+#define K3_CUDA(expr)                                  \
+  do {                                                 \
+    if ((expr) != cudaSuccess) return K3MOE_E_CUDA;    \
+  } while (0)
+
+// Route + permute + experts + combine for T tokens whose logits / z are already in ws.
+k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int32_t T, void* ws,
+                                const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s) {
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  {
+    ProfScope p(P_TOPK, s);
+    K3_CUDA(launch_topk(at<float>(ws, L.logits), T, d.n_experts, d.top_k, idx, wts, s));
+  }
+  {
+    ProfScope p(P_PERMUTE, s);
+    K3_CUDA(launch_permute(idx, T, d.n_experts, d.top_k, at<int32_t>(ws, L.offsets),
+                           at<int32_t>(ws, L.row_token), at<int32_t>(ws, L.row_slot),
+                           at<int32_t>(ws, L.slot_row), at<int32_t>(ws, L.plan),
+                           at<int32_t>(ws, L.perm), err, s));
+  }
+  const int rows = T * d.top_k;
+  {
+    ProfScope p(P_GLU, s);
+    K3_CUDA(launch_expert_glu(d, w, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.offsets),
+                              at<int32_t>(ws, L.row_token), at<__half>(ws, L.zh),
+                              at<int8_t>(ws, L.zs), at<uint16_t>(ws, L.a), at<__half>(ws, L.ah),
+                              at<int8_t>(ws, L.as), rows, err, s));
+  }
+  {
+    ProfScope p(P_DOWN, s);
+    K3_CUDA(launch_expert_down(d, w, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.offsets),
+                               at<__half>(ws, L.ah), at<int8_t>(ws, L.as), at<float>(ws, L.o),
+                               rows, err, s));
+  }
+  {
+    ProfScope p(P_COMBINE, s);
+    K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,
+                           d.latent, at<uint16_t>(ws, L.c), s));
+  }
+  return K3MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* k3moe_status_string(k3moe_status s) {
+  switch (s) {
+    case K3MOE_OK: return "K3MOE_OK";
+    case K3MOE_E_NULL: return "K3MOE_E_NULL: a required pointer is NULL";
+    case K3MOE_E_SHAPE: return "K3MOE_E_SHAPE: unsupported size";
+    case K3MOE_E_ALIGN: return "K3MOE_E_ALIGN: pointer not 16-byte aligned";
+    case K3MOE_E_WORKSPACE: return "K3MOE_E_WORKSPACE: workspace missing or too small";
+    case K3MOE_E_MODE: return "K3MOE_E_MODE: unsupported activation or activation format";
+    case K3MOE_E_CUDA: return "K3MOE_E_CUDA: CUDA call or launch failed";
+    case K3MOE_E_TIMEOUT: return "K3MOE_E_TIMEOUT: a device-side bounded wait ran out";
+    case K3MOE_E_DEVICE: return "K3MOE_E_DEVICE: device-side check failed";
+  }
+  return "K3MOE: unknown status";
+}
+
+k3moe_status k3moe_workspace_size(const k3moe_dims* dims, int32_t max_tokens, size_t* bytes) {
+  K3_TRY(check_dims(dims));
+  if (!bytes) return K3MOE_E_NULL;
+  if (max_tokens < 0) return K3MOE_E_SHAPE;
+  *bytes = ws_layout(*dims, max_tokens).total;
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_route(const k3moe_dims* dims, const uint16_t* x, int32_t T,
+                         const uint16_t* w_router, const float* bias, float* logits,
+                         int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
+                         void* stream) {
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  if (T < 0) return K3MOE_E_SHAPE;
+  if (!x || !w_router || !topk_idx || !topk_w) return K3MOE_E_NULL;
+  if (misaligned(x) || misaligned(w_router) || misaligned(bias) || misaligned(logits) ||
+      misaligned(topk_idx) || misaligned(topk_w))
+    return K3MOE_E_ALIGN;
+  K3_TRY(check_ws(d, T, ws, ws_bytes));
+  if (T == 0) return K3MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(d, T);
+  float* lg = logits ? logits : at<float>(ws, L.logits);
+  K3_CUDA(launch_dense_gemv(w_router, d.n_experts, lg, nullptr, bias, nullptr, 0, nullptr, nullptr,
+                            nullptr, 0, x, T, d.hidden, at<uint32_t>(ws, L.err), s));
+  K3_CUDA(launch_topk(lg, T, d.n_experts, d.top_k, topk_idx, topk_w, s));
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_permute(const k3moe_dims* dims, const int32_t* topk_idx, int32_t T,
+                           int32_t* expert_offsets, int32_t* row_token, int32_t* row_slot,
+                           int32_t* slot_row, void* ws, size_t ws_bytes, void* stream) {
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  if (T < 0) return K3MOE_E_SHAPE;
+  if (!topk_idx || !expert_offsets || !row_token || !row_slot || !slot_row) return K3MOE_E_NULL;
+  if (misaligned(topk_idx) || misaligned(expert_offsets) || misaligned(row_token) ||
+      misaligned(row_slot) || misaligned(slot_row))
+    return K3MOE_E_ALIGN;
+  K3_TRY(check_ws(d, T, ws, ws_bytes));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(d, T);
+  K3_CUDA(launch_permute(topk_idx, T, d.n_experts, d.top_k, expert_offsets, row_token, row_slot,
+                         slot_row, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.perm),
+                         at<uint32_t>(ws, L.err), s));
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_project(const uint16_t* W, const uint16_t* x, int32_t T, int32_t N, int32_t K,
+                           uint16_t* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!W || !x || !out) return K3MOE_E_NULL;
+  if (T < 0 || N <= 0 || K <= 0 || N % 64 || K % 64) return K3MOE_E_SHAPE;
+  if (misaligned(W) || misaligned(x) || misaligned(out)) return K3MOE_E_ALIGN;
+  if (!ws || ws_bytes < 256) return K3MOE_E_WORKSPACE;
+  if (misaligned(ws)) return K3MOE_E_ALIGN;
+  if (T == 0) return K3MOE_OK;
+  K3_CUDA(launch_dense_gemv(W, N, nullptr, out, nullptr, nullptr, 0, nullptr, nullptr, nullptr, 0,
+                            x, T, K, static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)));
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights* weights,
+                                    const uint16_t* z, int32_t T, const int32_t* expert_offsets,
+                                    const int32_t* row_token, float* o_rows, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  K3_TRY(check_weights(weights, false, true));
+  if (T < 0) return K3MOE_E_SHAPE;
+  if (!z || !expert_offsets || !row_token || !o_rows) return K3MOE_E_NULL;
+  if (misaligned(z) || misaligned(expert_offsets) || misaligned(row_token) || misaligned(o_rows))
+    return K3MOE_E_ALIGN;
+  K3_TRY(check_ws(d, T, ws, ws_bytes));
+  if (T == 0) return K3MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(d, T);
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  const int rows = T * d.top_k;
+  K3_CUDA(launch_act_prep(z, T, d.latent, d.actq, at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), s));
+  K3_CUDA(launch_plan(expert_offsets, d.n_experts, at<int32_t>(ws, L.plan), s));
+  K3_CUDA(launch_expert_glu(d, *weights, at<int32_t>(ws, L.plan), expert_offsets, row_token,
+                            at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), at<uint16_t>(ws, L.a),
+                            at<__half>(ws, L.ah), at<int8_t>(ws, L.as), rows, err, s));
+  K3_CUDA(launch_expert_down(d, *weights, at<int32_t>(ws, L.plan), expert_offsets,
+                             at<__half>(ws, L.ah), at<int8_t>(ws, L.as), o_rows, rows, err, s));
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_combine(const k3moe_dims* dims, const float* o_rows, const int32_t* slot_row,
+                           const float* topk_w, int32_t T, uint16_t* c, void* stream) {
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  if (T < 0) return K3MOE_E_SHAPE;
+  if (!o_rows || !slot_row || !topk_w || !c) return K3MOE_E_NULL;
+  if (misaligned(o_rows) || misaligned(slot_row) || misaligned(topk_w) || misaligned(c))
+    return K3MOE_E_ALIGN;
+  if (T == 0) return K3MOE_OK;
+  K3_CUDA(launch_combine(o_rows, slot_row, topk_w, T, d.top_k, d.latent, c,
+                         static_cast<cudaStream_t>(stream)));
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* weights,
+                                 const uint16_t* x, int32_t T, uint16_t* y,
+                                 int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  K3_TRY(check_weights(weights, true, true));
+  if (T < 0) return K3MOE_E_SHAPE;
+  if (!x || !y) return K3MOE_E_NULL;
+  if (misaligned(x) || misaligned(y) || misaligned(topk_idx_out) || misaligned(topk_w_out))
+    return K3MOE_E_ALIGN;
+  K3_TRY(check_ws(d, T, ws, ws_bytes));
+  if (T == 0) return K3MOE_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(d, T);
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.idx);
+  float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.wts);
+  const k3moe_weights& w = *weights;
+  // router logits and z = bf16(W_in x) (+ its f16 block-scaled copy) in one pass over x
+  {
+    ProfScope p(P_ROUTER_LATENT, s);
+    K3_CUDA(launch_dense_gemv(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr,
+                              w.router_bias, w.w_in, d.latent, at<uint16_t>(ws, L.z),
+                              at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), d.actq, x, T, d.hidden,
+                              err, s));
+  }
+  K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s));
+  {
+    ProfScope p(P_LATENT_OUT, s);
+    K3_CUDA(launch_dense_gemv(w.w_out, d.hidden, nullptr, y, nullptr, nullptr, 0, nullptr, nullptr,
+                              nullptr, 0, at<uint16_t>(ws, L.c), T, d.latent, err, s));
+  }
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_profile(int32_t mode, int32_t n, float* total_ms, int32_t* launches) {
+  if (mode == 1) {
+    if (!g_prof.ev) {
+      g_prof.ev = new cudaEvent_t[2 * Profiler::kMax];
+      g_prof.id = new int[Profiler::kMax];
+      for (int i = 0; i < 2 * Profiler::kMax; ++i)
+        if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) return K3MOE_E_CUDA;
+    }
+    g_prof.used = 0;
+    g_prof.on = true;
+    return K3MOE_OK;
+  }
+  g_prof.on = false;
+  for (int i = 0; i < n; ++i) {
+    if (total_ms) total_ms[i] = 0.f;
+    if (launches) launches[i] = 0;
+  }
+  for (int j = 0; j < g_prof.used; ++j) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(g_prof.ev[2 * j + 1]) != cudaSuccess) return K3MOE_E_CUDA;
+    if (cudaEventElapsedTime(&ms, g_prof.ev[2 * j], g_prof.ev[2 * j + 1]) != cudaSuccess)
+      return K3MOE_E_CUDA;
+    const int i = g_prof.id[j];
+    if (i < n) {
+      if (total_ms) total_ms[i] += ms;
+      if (launches) launches[i] += 1;
+    }
+  }
+  g_prof.used = 0;
+  return K3MOE_OK;
+}
+
+const char* k3moe_profile_name(int32_t id) {
+  return (id >= 0 && id < P_COUNT) ? kProfNames[id] : nullptr;
+}
+
+k3moe_status k3moe_check(void* ws, void* stream) {
+  if (!ws) return K3MOE_E_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return K3MOE_E_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return K3MOE_E_CUDA;
+  if (word != 0) {
+    if (cudaMemset(ws, 0, sizeof(word)) != cudaSuccess) return K3MOE_E_CUDA;
+    return (word & kErrTimeout) ? K3MOE_E_TIMEOUT : K3MOE_E_DEVICE;
+  }
+  return K3MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Small elementwise kernels: the routing-weighted combine, and the f16 block-scaled
+// activation copy the expert GEMV reads.
+#include <cuda_fp16.h>
+
+#include "k3moe_device.cuh"
+#include "k3moe_internal.cuh"
+
+namespace k3moe {
+namespace {
+
+// c[t][n] = bf16(sum_{j<k} w[t][j] * o[slot_row[t*k+j]][n]), fp32, j ascending.
+// Routed outputs are combined in latent space before the projection back to the residual
+// ("kimi-k3-mlx", LatentMoE).
+__global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_row,
+                               const float* __restrict__ w, int T, int k, int L, uint16_t* c) {
+  const int t = blockIdx.y;
+  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (t >= T || n >= L) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < k; ++j) {
+    const float wj = w[(size_t)t * k + j];
+    const float4 v = *reinterpret_cast<const float4*>(o + (size_t)slot_row[(size_t)t * k + j] * L + n);
+    acc.x = fmaf(wj, v.x, acc.x);
+    acc.y = fmaf(wj, v.y, acc.y);
+    acc.z = fmaf(wj, v.z, acc.z);
+    acc.w = fmaf(wj, v.w, acc.w);
+  }
+  ushort4 r;
+  r.x = f32_to_bf16(acc.x);
+  r.y = f32_to_bf16(acc.y);
+  r.z = f32_to_bf16(acc.z);
+  r.w = f32_to_bf16(acc.w);
+  *reinterpret_cast<ushort4*>(c + (size_t)t * L + n) = r;
+}
+
+// One warp per (token, block of 32 values): optional MXFP8 round trip, then an f16 copy
+// scaled by 2^-e with e chosen from the block maximum, and the exponent e.
+__global__ void act_prep_kernel(const uint16_t* __restrict__ z, int T, int L, int actq, __half* zh,
+                                int8_t* zs) {
+  const int lane = threadIdx.x & 31;
+  const long long blk = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long nblk = (long long)T * (L / 32);
+  if (blk >= nblk) return;
+  const size_t i = (size_t)blk * 32 + lane;
+  float q = bf16_to_f32(z[i]);
+  if (actq) q = mxfp8_roundtrip(q, mxfp8_block_exp(warp_max(fabsf(q))));
+  const int e = f16_block_exp(warp_max(fabsf(q)));
+  zh[i] = __float2half_rn(ldexpf(q, -e));
+  if (lane == 0) zs[blk] = (int8_t)e;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
+                           int k, int L, uint16_t* c, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  dim3 grid((L / 4 + 127) / 128, T);
+  combine_kernel<<<grid, 128, 0, s>>>(o_rows, slot_row, w, T, k, L, c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,
+                            cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const long long nblk = (long long)T * (L / 32);
+  const int warps = 8;
+  act_prep_kernel<<<(unsigned)((nblk + warps - 1) / warps), 32 * warps, 0, s>>>(z, T, L, actq, zh, zs);
+  return cudaGetLastError();
+}
+
+}  // namespace k3moe

@@ -66,6 +66,7 @@ def lib():
         L.k3o_mx_weight.argtypes = [p, p, i]
         L.k3o_mx_weight.restype = d
         L.k3o_dequant.argtypes = [p, p, i, i, p]
+        L.k3o_dequant_row.argtypes = [p, p, i, p]
         L.k3o_expert_params.argtypes = [p]
         L.k3o_expert_params.restype = ctypes.c_int64
         L.k3o_expert_bytes.argtypes = [p]
@@ -143,6 +144,13 @@ def dequant(q, s, N, K) -> np.ndarray:
     return out
 
 
+def dequant_row(q_row, s_row, K) -> np.ndarray:
+    q_row, s_row = _c(q_row, np.uint8), _c(s_row, np.uint8)
+    out = np.empty(K, np.float64)
+    lib().k3o_dequant_row(q_row.ctypes.data, s_row.ctypes.data, K, out.ctypes.data)
+    return out
+
+
 def mx_weight(q_row, s_row, j) -> float:
     q_row, s_row = _c(q_row, np.uint8), _c(s_row, np.uint8)
     return lib().k3o_mx_weight(q_row.ctypes.data, s_row.ctypes.data, j)
@@ -169,6 +177,15 @@ def router_logits(d, x, w_router, bias=None) -> np.ndarray:
     lib().k3o_router_logits(ctypes.byref(make_dims(d)), x.ctypes.data, T, wr.ctypes.data,
                             _ptr(b), out.ctypes.data)
     return out
+
+
+def router_logits_np(x, w_router, bias=None) -> np.ndarray:
+    """Router logits for many tokens: the same sum as router_logits, taken as one float64
+    matrix product of the bf16 values (a library matmul as the summation step)."""
+    lg = bf16_to_f64(x) @ bf16_to_f64(w_router).T
+    if bias is not None:
+        lg = lg + np.asarray(bias, np.float32).astype(np.float64)
+    return lg
 
 
 def select_topk(logits, k) -> np.ndarray:

@@ -94,7 +94,8 @@ uint16_t k3o_bf16_from_double(double x) {
  * Exponent field 0 is subnormal: value = m * 2^(1-1) * 0.5. */
 double k3o_e2m1(int code) {
   int s = (code >> 3) & 1, ex = (code >> 1) & 3, m = code & 1;
-  double mag = (ex == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, ex - 1);
+  /* 2^(ex-1) for ex in {1, 2, 3} is 1, 2 or 4: an exact small integer */
+  double mag = (ex == 0) ? 0.5 * m : (1.0 + 0.5 * m) * (double)(1 << (ex - 1));
   return s ? -mag : mag;
 }
 
@@ -177,6 +178,22 @@ double k3o_mx_weight(const uint8_t* q_row, const uint8_t* s_row, int j) {
   int byte = q_row[j / 2];
   int code = (j % 2 == 0) ? (byte & 0xF) : ((byte >> 4) & 0xF);
   return k3o_e2m1(code) * k3o_e8m0(s_row[j / 32]);
+}
+
+/* One MXFP4 row of K weights to doubles: block b of 32 consecutive weights shares the scale
+ * s_row[b]; weight j is the nibble j (low nibble first) times that scale. */
+void k3o_dequant_row(const uint8_t* q_row, const uint8_t* s_row, int K, double* out) {
+  double table[16]; /* the 16-entry value table the nibbles index */
+  for (int c = 0; c < 16; ++c) table[c] = k3o_e2m1(c);
+  for (int b = 0; b < K / 32; ++b) {
+    const double scale = k3o_e8m0(s_row[b]);
+    for (int i = 0; i < 32; ++i) {
+      const int j = 32 * b + i;
+      const int byte = q_row[j / 2];
+      const int code = (j % 2 == 0) ? (byte & 0xF) : ((byte >> 4) & 0xF);
+      out[j] = table[code] * scale;
+    }
+  }
 }
 
 /* Whole MXFP4 matrix [N][K] to doubles (row-major). */
@@ -299,18 +316,18 @@ int k3o_expert_row(const k3o_dims* d, const k3o_weights* w, int e, const uint16_
   if (d->act != 0) return -1;
   double* zin = (double*)malloc(sizeof(double) * (size_t)L);
   double* a = (double*)malloc(sizeof(double) * (size_t)I);
+  double* wg = (double*)malloc(sizeof(double) * (size_t)(L > I ? L : I));
+  double* wu = (double*)malloc(sizeof(double) * (size_t)L);
   for (int k = 0; k < L; ++k) zin[k] = k3o_bf16_to_double(z[k]);
   if (d->actq == 1) k3o_mxfp8_roundtrip(zin, L);
   const uint8_t *gq = w->gate_q[e], *gs = w->gate_s[e], *uq = w->up_q[e], *us = w->up_s[e];
   for (int n = 0; n < I; ++n) {
     double g = 0.0, u = 0.0;
-    const uint8_t* gqr = gq + (size_t)n * (L / 2);
-    const uint8_t* gsr = gs + (size_t)n * (L / 32);
-    const uint8_t* uqr = uq + (size_t)n * (L / 2);
-    const uint8_t* usr = us + (size_t)n * (L / 32);
+    k3o_dequant_row(gq + (size_t)n * (L / 2), gs + (size_t)n * (L / 32), L, wg);
+    k3o_dequant_row(uq + (size_t)n * (L / 2), us + (size_t)n * (L / 32), L, wu);
     for (int k = 0; k < L; ++k) {
-      g += k3o_mx_weight(gqr, gsr, k) * zin[k];
-      u += k3o_mx_weight(uqr, usr, k) * zin[k];
+      g += wg[k] * zin[k];
+      u += wu[k] * zin[k];
     }
     uint16_t ab = k3o_bf16_from_double(k3o_silu(g) * u);
     if (a_out) a_out[n] = ab;
@@ -320,13 +337,14 @@ int k3o_expert_row(const k3o_dims* d, const k3o_weights* w, int e, const uint16_
   const uint8_t *dq = w->down_q[e], *ds = w->down_s[e];
   for (int n = 0; n < L; ++n) {
     double acc = 0.0;
-    const uint8_t* dqr = dq + (size_t)n * (I / 2);
-    const uint8_t* dsr = ds + (size_t)n * (I / 32);
-    for (int k = 0; k < I; ++k) acc += k3o_mx_weight(dqr, dsr, k) * a[k];
+    k3o_dequant_row(dq + (size_t)n * (I / 2), ds + (size_t)n * (I / 32), I, wg);
+    for (int k = 0; k < I; ++k) acc += wg[k] * a[k];
     o[n] = acc;
   }
   free(zin);
   free(a);
+  free(wg);
+  free(wu);
   return 0;
 }
 

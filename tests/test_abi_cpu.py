@@ -1,0 +1,85 @@
+"""The C ABI without a GPU: the library builds and loads, exports every function that
+include/k3moe.h declares, and rejects bad arguments on the host before any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mxfp4_expert_ffn_top16_gb300 as k3
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    k3.build()
+    return k3.lib()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "k3moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(k3moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_function(L):
+    declared = header_functions()
+    assert declared, "no declarations parsed"
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(k3.EXPORTS) == declared
+
+
+def test_status_strings(L):
+    for code, name in k3.STATUS.items():
+        assert k3.status_string(code).startswith(name)
+
+
+K3 = dict(hidden=7168, latent=3584, inter=3072, n_experts=896, top_k=16, act=0, actq=0)
+
+
+def dims(**kw):
+    v = dict(K3)
+    v.update(kw)
+    return k3.Dims(**v)
+
+
+def test_workspace_size_monotone(L):
+    a = k3.k3moe_workspace_size(dims(), 1)
+    b = k3.k3moe_workspace_size(dims(), 64)
+    c = k3.k3moe_workspace_size(dims(), 4096)
+    assert 256 < a < b < c
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(hidden=7000), 2), (dict(latent=0), 2), (dict(inter=100), 2), (dict(n_experts=2000), 2),
+    (dict(top_k=0), 2), (dict(top_k=33), 2), (dict(n_experts=8, top_k=9), 2),
+    (dict(act=1), 5), (dict(actq=2), 5)])
+def test_bad_dims_rejected(L, kw, status):
+    out = ctypes.c_size_t(0)
+    assert L.k3moe_workspace_size(ctypes.byref(dims(**kw)), 4, ctypes.byref(out)) == status
+
+
+def test_null_misaligned_and_small_workspace_rejected(L):
+    d = dims()
+    good = 0x10000
+    # null inputs
+    assert k3.k3moe_route(d, None, 4, good, None, None, good, good, good, 1 << 30, check=False) == 1
+    assert L.k3moe_route(None, good, 4, good, None, None, good, good, good, 1 << 30, None) == 1
+    # misaligned
+    assert k3.k3moe_route(d, good + 2, 4, good, None, None, good, good, good, 1 << 30, check=False) == 3
+    # workspace too small / missing
+    assert k3.k3moe_route(d, good, 4, good, None, None, good, good, good, 100, check=False) == 4
+    assert k3.k3moe_route(d, good, 4, good, None, None, good, good, None, 1 << 30, check=False) == 4
+    # negative T
+    assert k3.k3moe_permute(d, good, -1, good, good, good, good, good, 1 << 30, check=False) == 2
+    # projection shape rules
+    assert k3.k3moe_project(good, good, 1, 100, 64, good, good, 256, check=False) == 2
+    w = k3.Weights(good, None, good, good, good, None, good, good, good, good)
+    assert k3.k3moe_expert_ffn_mxfp4(d, w, good, 1, good, good, good, good, 1 << 30, check=False) == 1
+    w.gate_s = good + 8
+    assert k3.k3moe_layer_forward(d, w, good, 1, good, None, None, good, 1 << 30, check=False) == 3
+    # SiTU-GLU has no formula on the pages: refused
+    assert k3.k3moe_layer_forward(dims(act=1), w, good, 1, good, None, None, good, 1 << 30,
+                                  check=False) == 5

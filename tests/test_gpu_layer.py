@@ -1,0 +1,235 @@
+"""GPU parity of the expert half and of the whole layer against the oracle: dense projection
+(k3moe_project), routed expert FFN (k3moe_expert_ffn_mxfp4), combine (k3moe_combine) and
+k3moe_layer_forward, on the tiny layer (every token) and on K3-sized layers (sampled tokens,
+each recomputed independently by the oracle)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import mxfp4_expert_ffn_top16_gb300 as k3
+import oracle
+import synth
+from k3help import (DEV, REL_L2, LOGIT_ATOL, LOGIT_RTOL, DeviceLayer, bf16_np, dims, up, stream,
+                    workspace, check_ok, rel_l2_rows, topk_gap_ambiguous)
+
+pytestmark = pytest.mark.gpu
+NCPU = os.cpu_count() or 4
+
+
+@pytest.fixture(scope="module")
+def k3_layer():
+    lay = DeviceLayer(synth.K3, seed=0)
+    torch.cuda.synchronize()
+    yield lay
+    del lay
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ projection
+@pytest.mark.parametrize("T,N,K", [(1, 3584, 7168), (5, 128, 256), (64, 7168, 3584), (200, 192, 320)])
+def test_project(T, N, K):
+    W = synth.host_bf16_normal(1, 3, 0, N * K, 0.02).reshape(N, K)
+    x = synth.host_bf16_normal(1, 1, 0, T * K, 1.0).reshape(T, K)
+    out = torch.empty((T, N), dtype=torch.int16, device=DEV)
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    k3.k3moe_project(up(W).data_ptr(), up(x).data_ptr(), T, N, K, out.data_ptr(), ws.data_ptr(), 256,
+                     stream())
+    check_ok(ws)
+    got = bf16_np(out)
+    want_exact, want_b = oracle.dense_proj(W, x)
+    want = oracle.bf16_to_f64(want_b)
+    # same bf16 rounding of sums that differ only in fp32 summation order: at most 1 ulp apart
+    ulp = np.abs(want) * 2.0**-7 + 1e-30
+    assert np.all(np.abs(got - want) <= ulp)
+    assert rel_l2_rows(got, want_exact).max() < 4e-3
+    assert (got != want).mean() < 0.02
+
+
+# ------------------------------------------------------------------ expert FFN
+def _expert_ffn(lay, z_np, idx_np, actq=0):
+    d = lay.d
+    dm = dims(d, actq)
+    T = z_np.shape[0]
+    off, rt, rs, sr = oracle.permute(idx_np, d.n_experts)  # permutation from the host side
+    o = torch.empty((T * d.top_k, d.latent), dtype=torch.float32, device=DEV)
+    ws, n = workspace(dm, T)
+    k3.k3moe_expert_ffn_mxfp4(dm, lay.weights, up(z_np).data_ptr(), T, up(off).data_ptr(),
+                              up(rt).data_ptr(), o.data_ptr(), ws.data_ptr(), n, stream())
+    check_ok(ws)
+    return o.cpu().numpy().astype(np.float64), (off, rt, rs, sr)
+
+
+@pytest.mark.parametrize("actq", [0, 1])
+def test_expert_ffn_tiny_all_rows(actq):
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=0, actq=actq)
+    T = 24
+    z = synth.host_bf16_normal(3, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
+    idx = synth.host_topk_sets(4, T, d.n_experts, d.top_k, "zipf")
+    o, (off, rt, rs, sr) = _expert_ffn(lay, z, idx, actq)
+    ol = lay.oracle(actq=actq)
+    want = np.stack([ol.expert_row(int(idx[rt[r], rs[r]]), z[rt[r]])[0] for r in range(T * d.top_k)])
+    err = rel_l2_rows(o, want)
+    assert err.max() <= REL_L2, err.max()
+
+
+def test_expert_ffn_k3_sampled_rows(k3_layer):
+    d = synth.K3
+    T = 40
+    z = synth.host_bf16_normal(7, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
+    idx = synth.host_topk_sets(8, T, d.n_experts, d.top_k, "zipf")  # skewed: multi-chunk experts
+    o, (off, rt, rs, sr) = _expert_ffn(k3_layer, z, idx)
+    rng = np.random.default_rng(0)
+    rows = sorted(set(rng.choice(T * d.top_k, 12, replace=False).tolist()) | {0, T * d.top_k - 1})
+    ol = k3_layer.oracle(experts={int(idx[rt[r], rs[r]]) for r in rows})
+    for r in rows:
+        want = ol.expert_row(int(idx[rt[r], rs[r]]), z[rt[r]])[0]
+        assert rel_l2_rows(o[r], want) <= REL_L2, (r, rel_l2_rows(o[r], want))
+
+
+def test_expert_ffn_invariants_bit_exact():
+    """All-zero codes give exactly 0; +1 on every up exponent doubles every output exactly."""
+    d = synth.TINY
+    T = 8
+    z = synth.host_bf16_normal(2, synth.S_X, 0, T * d.latent, 1.0).reshape(T, d.latent)
+    idx = synth.host_topk_sets(5, T, d.n_experts, d.top_k, "uniform")
+    base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
+    zero = {e: {n: (np.zeros_like(a) if n.endswith("_q") else a) for n, a in t.items()} for e, t in base.items()}
+    dbl = {e: dict(t, up_s=(t["up_s"] + 1).astype(np.uint8)) for e, t in base.items()}
+    o0, _ = _expert_ffn(DeviceLayer(d, experts=zero), z, idx)
+    assert np.all(o0 == 0.0)
+    o1, _ = _expert_ffn(DeviceLayer(d, experts=base), z, idx)
+    o2, _ = _expert_ffn(DeviceLayer(d, experts=dbl), z, idx)
+    np.testing.assert_array_equal(o2, 2 * o1)
+
+
+def test_expert_ffn_nan_scale_gives_nonfinite():
+    d = synth.TINY
+    T = 4
+    base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
+    base[0]["down_s"] = base[0]["down_s"].copy()
+    base[0]["down_s"][:, 0] = 255
+    idx = np.tile(np.arange(d.top_k, dtype=np.int32), (T, 1))
+    z = synth.host_bf16_normal(2, synth.S_X, 0, T * d.latent, 1.0).reshape(T, d.latent)
+    o, (off, rt, rs, sr) = _expert_ffn(DeviceLayer(d, experts=base), z, idx)
+    rows0 = np.arange(off[0], off[1])
+    assert np.all(~np.isfinite(o[rows0]).all(axis=1))
+    assert np.all(np.isfinite(o[off[1]:]))
+
+
+# ------------------------------------------------------------------ combine
+def test_combine():
+    d = synth.K3
+    T = 33
+    rng = np.random.default_rng(1)
+    o = rng.normal(0, 1e5, (T * d.top_k, d.latent)).astype(np.float32)
+    sr = rng.permutation(T * d.top_k).astype(np.int32)
+    w = rng.dirichlet(np.ones(d.top_k), T).astype(np.float32)
+    c = torch.empty((T, d.latent), dtype=torch.int16, device=DEV)
+    k3.k3moe_combine(dims(d), up(o).data_ptr(), up(sr).data_ptr(), up(w).data_ptr(), T, c.data_ptr(),
+                     stream())
+    torch.cuda.synchronize()
+    got = bf16_np(c)
+    want = oracle.bf16_to_f64(oracle.combine(o.astype(np.float64), sr, w.astype(np.float64), T, d.top_k))
+    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0**-7 + 1e-30)
+    assert rel_l2_rows(got, want).max() < 1e-3
+
+
+# ------------------------------------------------------------------ whole layer
+def _forward(lay, x_np, weights=None, dm=None):
+    d = lay.d
+    dm = dm or lay.dims
+    T = x_np.shape[0]
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device=DEV)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, d.top_k), dtype=torch.float32, device=DEV)
+    ws, n = workspace(dm, T)
+    k3.k3moe_layer_forward(dm, weights or lay.weights, up(x_np).data_ptr(), T, y.data_ptr(),
+                           idx.data_ptr(), w.data_ptr(), ws.data_ptr(), n, stream())
+    check_ok(ws)
+    return bf16_np(y), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def _compare_layer(lay, x, y, idx, sample):
+    """Oracle on the sampled tokens; tokens with an fp32-level tie at the top-k boundary are
+    only checked for a valid selection."""
+    d = lay.d
+    wr, _, _ = lay.dense()
+    lg = oracle.router_logits_np(x[sample], wr, lay.bias_host)
+    ref_idx = oracle.select_topk(lg, d.top_k)
+    amb = topk_gap_ambiguous(lg, d.top_k, 2 * (LOGIT_ATOL + LOGIT_RTOL * np.abs(lg).max()))
+    same = np.all(idx[sample] == ref_idx, axis=1)
+    assert np.all(same | amb)
+    ol = lay.oracle(experts=set(ref_idx.ravel().tolist()))
+    ref = ol.forward(x[sample], nthreads=NCPU)
+    np.testing.assert_array_equal(ref["idx"], ref_idx)
+    err = rel_l2_rows(y[sample], oracle.bf16_to_f64(ref["y"]))
+    assert err[same].max() <= REL_L2, err
+    return err, int((~same).sum())
+
+
+@pytest.mark.parametrize("actq", [0, 1])
+def test_layer_tiny_every_token(actq):
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=0, actq=actq)
+    x = synth.host_x(synth.WORKLOADS["tiny"])
+    y, idx, w = _forward(lay, x)
+    err, flips = _compare_layer(lay, x, y, idx, np.arange(x.shape[0]))
+    assert flips == 0
+
+
+def test_layer_tiny_ragged_and_edge_T():
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=1, bias=synth.host_f32_normal(1, synth.S_BIAS, 0, d.n_experts, 1.0))
+    for T in (1, 3, 9, 70):
+        x = synth.host_bf16_normal(T, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+        y, idx, w = _forward(lay, x)
+        _compare_layer(lay, x, y, idx, np.arange(T))
+    # T = 0 is a no-op
+    dm = lay.dims
+    ws, n = workspace(dm, 0)
+    assert k3.k3moe_layer_forward(dm, lay.weights, 0, 0, 0, None, None, ws.data_ptr(), n, stream(),
+                                  check=False) in (k3.K3MOE_OK, 1)
+
+
+def test_layer_k3_decode_b1(k3_layer):
+    w = synth.WORKLOADS["decode_b1"]
+    x = synth.host_x(w, 0, 3)
+    for t in range(3):
+        y, idx, _ = _forward(k3_layer, x[t:t + 1])
+        _compare_layer(k3_layer, x[t:t + 1], y, idx, np.array([0]))
+
+
+def test_layer_k3_decode_b64_biased(k3_layer):
+    w = synth.WORKLOADS["decode_b64"]
+    bias = synth.router_bias(w)
+    b = up(bias)
+    lw = k3.Weights(*[getattr(k3_layer.weights, f) for f, _ in k3.Weights._fields_])
+    lw.router_bias = b.data_ptr()
+    k3_layer.bias_host = bias
+    try:
+        x = synth.host_x(w)
+        y, idx, _ = _forward(k3_layer, x, weights=lw)
+        distinct = len(np.unique(idx))
+        assert distinct < 64 * 16  # reuse across the batch
+        _compare_layer(k3_layer, x, y, idx, np.array([0, 1, 17, 40, 63]))
+    finally:
+        k3_layer.bias_host = None
+
+
+def test_layer_k3_prefill_sampled(k3_layer):
+    w = synth.WORKLOADS["prefill_4k"]
+    T = 1024  # several chunks per expert, skewed routing
+    bias = synth.router_bias(w)
+    b = up(bias)
+    lw = k3.Weights(*[getattr(k3_layer.weights, f) for f, _ in k3.Weights._fields_])
+    lw.router_bias = b.data_ptr()
+    k3_layer.bias_host = bias
+    try:
+        x = synth.host_x(w, 0, T)
+        y, idx, _ = _forward(k3_layer, x, weights=lw)
+        _compare_layer(k3_layer, x, y, idx, np.array([0, 511, T - 1]))
+    finally:
+        k3_layer.bias_host = None

@@ -149,6 +149,8 @@ def test_dequant_vs_numpy_and_scale_axis():
     q = rng.integers(0, 256, (N, K // 2), dtype=np.uint8)
     s = rng.integers(100, 140, (N, K // 32), dtype=np.uint8)
     np.testing.assert_array_equal(oracle.dequant(q, s, N, K), numpy_dequant(q, s))
+    for n in range(N):
+        np.testing.assert_array_equal(oracle.dequant_row(q[n], s[n], K), numpy_dequant(q, s)[n])
     # scale j//32 applies to weights 32j..32j+31 only
     q1 = np.full((1, K // 2), 0x22, np.uint8)  # every weight = 1.0 * scale
     s1 = np.array([[127, 128, 129, 130]], np.uint8)
@@ -215,6 +217,7 @@ def test_router_logits_vs_numpy_with_bias():
     got = oracle.router_logits(d, x, wr, b)
     want = oracle.bf16_to_f64(x) @ oracle.bf16_to_f64(wr).T + b.astype(np.float64)
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(oracle.router_logits_np(x, wr, b), got, rtol=1e-12, atol=1e-12)
 
 
 def test_permute_vs_sorted_brute_force():

@@ -44,13 +44,13 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.row_token = take(rows * 4);
   L.row_slot = take(rows * 4);
   L.slot_row = take(rows * 4);
-  L.plan = take(plan_ints((int)E) * 4);
+  L.plan = take(plan_bytes((int)E, (long long)rows));
   L.z = take(Tt * Lw * 2);
   L.zh = take(Tt * Lw * 2);
-  L.zs = take(Tt * Lw / 32);
+  L.zs = take(Tt * (size_t)exp_pitch(d.latent));
   L.a = take(rows * I * 2);
   L.ah = take(rows * I * 2);
-  L.as = take(rows * I / 32);
+  L.as = take(rows * (size_t)exp_pitch(d.inter));
   L.o = take(rows * Lw * 4);
   L.c = take(Tt * Lw * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
@@ -162,19 +162,18 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
                            at<int32_t>(ws, L.slot_row), at<int32_t>(ws, L.plan),
                            at<int32_t>(ws, L.perm), err, s));
   }
-  const int rows = T * d.top_k;
   {
     ProfScope p(P_GLU, s);
     K3_CUDA(launch_expert_glu(d, w, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.offsets),
                               at<int32_t>(ws, L.row_token), at<__half>(ws, L.zh),
                               at<int8_t>(ws, L.zs), at<uint16_t>(ws, L.a), at<__half>(ws, L.ah),
-                              at<int8_t>(ws, L.as), rows, err, s));
+                              at<int8_t>(ws, L.as), T, err, s));
   }
   {
     ProfScope p(P_DOWN, s);
     K3_CUDA(launch_expert_down(d, w, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.offsets),
                                at<__half>(ws, L.ah), at<int8_t>(ws, L.as), at<float>(ws, L.o),
-                               rows, err, s));
+                               T, err, s));
   }
   {
     ProfScope p(P_COMBINE, s);
@@ -281,14 +280,13 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(d, T);
   uint32_t* err = at<uint32_t>(ws, L.err);
-  const int rows = T * d.top_k;
   K3_CUDA(launch_act_prep(z, T, d.latent, d.actq, at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), s));
-  K3_CUDA(launch_plan(expert_offsets, d.n_experts, at<int32_t>(ws, L.plan), s));
+  K3_CUDA(launch_plan(expert_offsets, d.n_experts, T * d.top_k, at<int32_t>(ws, L.plan), err, s));
   K3_CUDA(launch_expert_glu(d, *weights, at<int32_t>(ws, L.plan), expert_offsets, row_token,
                             at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), at<uint16_t>(ws, L.a),
-                            at<__half>(ws, L.ah), at<int8_t>(ws, L.as), rows, err, s));
+                            at<__half>(ws, L.ah), at<int8_t>(ws, L.as), T, err, s));
   K3_CUDA(launch_expert_down(d, *weights, at<int32_t>(ws, L.plan), expert_offsets,
-                             at<__half>(ws, L.ah), at<int8_t>(ws, L.as), o_rows, rows, err, s));
+                             at<__half>(ws, L.ah), at<int8_t>(ws, L.as), o_rows, T, err, s));
   return K3MOE_OK;
 }
 

@@ -132,6 +132,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 2-D tiled copy global -> shared (TMA): the box at (x, y) of the tensor map lands at dst
+// (1024-byte aligned for the 128-byte swizzle); completion counted on `bar` in bytes (out of
+// range parts of the box are zero-filled and still counted). x * element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte offset of (row r, byte c) inside a box whose rows are 128 bytes and which was written
+// with the 128-byte swizzle: the 16-byte chunk index is XORed with r mod 8.
+__device__ __forceinline__ int swz128(int r, int c) {
+  return r * 128 + ((((c >> 4) ^ r) & 7) << 4) + (c & 15);
+}
+
 // ------------------------------------------------------------------ mma.sync tiles
 // D(16x8 f32) += A(16x16 f16, row) * B(16x8 f16, col)
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -168,12 +187,14 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return r;
 }
 
-// Barrier over a fixed group of threads (the mbarrier's arrival count), with the same
-// bounded wait as the pipeline barriers, so a group member that gave up cannot strand the
-// others. `phase` is the caller's running parity for this barrier.
+// Barrier over a fixed group of warps (the mbarrier's arrival count = number of warps; lane 0
+// of each warp arrives after the warp synchronises), with the same bounded wait as the
+// pipeline barriers, so a group member that gave up cannot strand the others. `phase` is the
+// caller's running parity for this barrier. Call with the whole warp.
 __device__ __forceinline__ bool group_barrier(uint64_t* bar, uint32_t& phase, volatile int* abort,
                                               uint32_t* err) {
-  mbar_arrive(bar);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
   const bool ok = mbar_wait_bounded(bar, phase, abort, err);
   phase ^= 1u;
   return ok;

@@ -5,12 +5,19 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "k3moe.h"
 
 namespace k3moe {
+
+// 2-D tensor map over a row-major array: `inner` elements per row (contiguous), `rows` rows
+// `pitch_bytes` apart, box of box_inner x box_rows elements, optional 128-byte swizzle.
+// Cached by its arguments. Returns false if the driver entry point or the encoding fails.
+bool make_tmap_2d(CUtensorMap* out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
+                  uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
 
 // ------------------------------------------------------------------ error word
 // Bits of the uint32 error word at offset 0 of the workspace.
@@ -35,6 +42,9 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T);
 
 // Tokens per column tile of the expert GEMV (one mma.m16n8 n-tile).
 constexpr int kGemvTokens = 8;
+// Row pitch in bytes of the per-32-block exponent arrays of the f16 activation copies
+// (K/32 bytes rounded up to 16 so rows can be bulk-copied).
+inline __host__ __device__ int exp_pitch(int K) { return ((K / 32) + 15) & ~15; }
 // Features per unit of the expert GEMV and of the dense GEMV.
 constexpr int kUnitRows = 32;
 
@@ -42,7 +52,16 @@ constexpr int kUnitRows = 32;
 //   plan[0] = number of active experts D, plan[1] = total chunks C,
 //   plan[2 .. 2+E)        = active expert ids (first D valid),
 //   plan[2+E .. 2+2E+1)   = chunk prefix over active experts (first D+1 valid).
-inline size_t plan_ints(int E) { return 2 + 2 * (size_t)E + 1; }
+inline __host__ __device__ size_t plan_ints(int E) { return 2 + 2 * (size_t)E + 1; }
+// The chunk table follows the plan ints: int4 {expert, first sorted row, rows, 0} per chunk of
+// up to kGemvTokens rows, for at most rows/kGemvTokens + E chunks.
+inline __host__ __device__ size_t plan_ctab_offset(int E) { return (plan_ints(E) * 4 + 15) & ~(size_t)15; }
+inline __host__ __device__ int4* plan_ctab(int32_t* plan, int E) {
+  return reinterpret_cast<int4*>(reinterpret_cast<char*>(plan) + plan_ctab_offset(E));
+}
+inline __host__ __device__ size_t plan_bytes(int E, long long rows) {
+  return plan_ctab_offset(E) + (size_t)(rows / kGemvTokens + E + 1) * 16;
+}
 
 // ------------------------------------------------------------------ launchers
 // Each returns cudaSuccess or the launch error.
@@ -55,16 +74,17 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, 
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* offsets,
                            int32_t* row_token, int32_t* row_slot, int32_t* slot_row,
                            int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s);
-cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* plan, cudaStream_t s);
+cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,
+                        cudaStream_t s);
 cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,
                             cudaStream_t s);
 cudaError_t launch_expert_glu(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
                               const int32_t* offsets, const int32_t* row_token, const __half* zh,
-                              const int8_t* zs, uint16_t* a, __half* ah, int8_t* as, int rows_max,
+                              const int8_t* zs, uint16_t* a, __half* ah, int8_t* as, int T,
                               uint32_t* err, cudaStream_t s);
 cudaError_t launch_expert_down(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
                                const int32_t* offsets, const __half* ah, const int8_t* as,
-                               float* o_rows, int rows_max, uint32_t* err, cudaStream_t s);
+                               float* o_rows, int T, uint32_t* err, cudaStream_t s);
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s);
 

@@ -6,11 +6,16 @@
 // Stable LatentMoE: the routed experts see the residual projected to 3584 and their combined
 // output is projected back.
 //
-// HBM-bound: every weight byte is read once. A persistent CTA takes units of 32 weight rows;
-// a producer warp streams each unit's rows through a ring of shared-memory stages with
-// per-row bulk copies (TMA engine), eight consumer warps split K and run mma.sync bf16 tiles
-// (weight rows on M, tokens on N), and a shared-memory reduction in fixed warp order keeps the
-// result deterministic. Rows land with a 64-byte pad so the fragment loads are conflict-free.
+// HBM-bound: every weight byte is read once per chunk of up to 64 tokens. A persistent CTA
+// takes units of 32 weight rows; a producer warp streams, per stage, NB tiles of the unit's
+// rows (32 rows x 64 bf16 = 4 KB each) and the matching tiles of the chunk's token rows
+// through the TMA engine (2-D tensor maps, 128-byte swizzle) into a ring of shared-memory
+// stages; eight consumer warps split K and run mma.sync bf16 tiles (weight rows on M, tokens
+// on N). Each 32-wide K block is accumulated in a fresh tile and then added in IEEE fp32, so
+// the result does not inherit the tensor core's internal accumulation over the whole of K.
+// A shared-memory reduction in fixed warp order keeps the result deterministic.
+// Fragment row g of an mma tile reads tile row pi(g) = (g >> 1) | ((g & 1) << 2): with the
+// 128-byte swizzle, the rows read in one shared-memory phase then hit disjoint banks.
 // Epilogues: fp32 + bias (router logits), bf16 (z, y), and for z also the f16 block-scaled
 // copy the expert GEMV reads (one power-of-two exponent per token and 32 features; in MXFP8
 // mode the copy holds the MXFP8 round trip of z).
@@ -24,10 +29,9 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
-constexpr int kStages = 3;
+constexpr int kMaxStages = 4;
 
 struct DenseProblem {
-  const uint16_t* W;
   int N;
   float* out_f32;
   const float* bias;
@@ -38,68 +42,74 @@ struct DenseProblem {
 };
 
 struct DenseArgs {
+  CUtensorMap tw[2];   // W of each problem: {K, N} bf16, box {64, 32}, 128-byte swizzle
+  CUtensorMap tx;      // tokens: {K, T} bf16, box {64, 8*NTT}, 128-byte swizzle
   DenseProblem p[2];
-  int units0, units;  // units of problem 0, total units
-  const uint16_t* x;
-  int T, K, KC;       // tokens, reduction length, K elements per stage
+  int units0, units;   // units of problem 0, total units
+  int T, K, NB, NS;    // tokens, reduction length, tiles per stage along K, stages
   uint32_t* err;
 };
 
+__device__ __forceinline__ int pi8(int g) { return (g >> 1) | ((g & 1) << 2); }
+
 template <int NTT>
 __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_constant__ DenseArgs args) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int K = args.K, KC = args.KC, T = args.T;
-  const int row_stride = KC * 2 + 64;
-  const int stage_bytes = kUnitRows * row_stride;
-  const int ntok = 8 * NTT;
-  uint8_t* stages = smem;
-  float* red = reinterpret_cast<float*>(smem + kStages * stage_bytes);
+  constexpr int ntok = 8 * NTT;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int K = args.K, NB = args.NB, NS = args.NS, T = args.T;
+  const int wbox = kUnitRows * 128, xbox = ntok * 128;
+  const int stage_bytes = NB * (wbox + xbox);
+  uint8_t* stages = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+  float* red = reinterpret_cast<float*>(stages + NS * stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(red + kConsumerWarps * kUnitRows * ntok);
-  uint64_t* empty = full + kStages;
-  uint64_t* cbar = empty + kStages;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* cbar = empty + kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(cbar + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
-    mbar_init(cbar, 32 * kConsumerWarps);
+    mbar_init(cbar, kConsumerWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
+  const int KC = 64 * NB;
   const int nkc = K / KC;
   const int nchunks = (T + ntok - 1) / ntok;
 
   if (warp == 0) {
-    // ---------------- producer
+    // ---------------- producer (lane 0 issues)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < args.units && ok; u += gridDim.x) {
       const int pi = u < args.units0 ? 0 : 1;
-      const DenseProblem& P = args.p[pi];
       const int row0 = (pi == 0 ? u : u - args.units0) * kUnitRows;
-      const int nrows = min(kUnitRows, P.N - row0);
       for (int ch = 0; ch < nchunks && ok; ++ch) {
         for (int kc = 0; kc < nkc; ++kc) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
-          if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(nrows * KC * 2));
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+            uint8_t* dst = stages + s * stage_bytes;
+            for (int b = 0; b < NB; ++b) {
+              const int x = kc * KC + b * 64;
+              tma_load_2d(dst + b * wbox, &args.tw[pi], x, row0, &full[s]);
+              tma_load_2d(dst + NB * wbox + b * xbox, &args.tx, x, ch * ntok, &full[s]);
+            }
+          }
           __syncwarp();
-          if (lane < nrows)
-            bulk_g2s(stages + s * stage_bytes + lane * row_stride,
-                     P.W + (size_t)(row0 + lane) * K + (size_t)kc * KC, KC * 2, &full[s]);
-          if (++s == kStages) { s = 0; ph ^= 1; }
+          if (++s == NS) { s = 0; ph ^= 1; }
         }
       }
     }
     if (!ok) {
-      // drain: wait (bounded) for copies this warp issued into the stages
-      for (int i = 0; i < kStages; ++i) {
-        if (--s < 0) { s = kStages - 1; ph ^= 1; }
+      for (int i = 0; i < NS; ++i) {
+        if (--s < 0) { s = NS - 1; ph ^= 1; }
         volatile int dummy = 0;
         mbar_wait_bounded(&full[s], ph, &dummy, args.err);
       }
@@ -110,7 +120,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
   // ---------------- consumers
   const int cw = warp - 1;
   const int g = lane >> 2, t = lane & 3;
-  const int kb_per_stage = KC / 32;
+  const int pg = pi8(g);
+  const int kb_per_stage = 2 * NB;  // 32-wide K blocks per stage
   const int kb_per_warp = (kb_per_stage + kConsumerWarps - 1) / kConsumerWarps;
   int s = 0;
   uint32_t ph = 0, cph = 0;
@@ -120,13 +131,15 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
     const int row0 = (pi == 0 ? u : u - args.units0) * kUnitRows;
     for (int ch = 0; ch < nchunks; ++ch) {
       const int tok0 = ch * ntok;
-      float acc[2][NTT][4];
+      // Kahan-compensated sums of the per-block tiles: bf16 rounding of the result (z, y)
+      // then depends on the exact sum except within ~1 fp32 ulp of a rounding boundary
+      float acc[2][NTT][4], cmp[2][NTT][4];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int n = 0; n < NTT; ++n)
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[m][n][i] = 0.f;
+          for (int i = 0; i < 4; ++i) acc[m][n][i] = cmp[m][n][i] = 0.f;
 
       for (int kc = 0; kc < nkc; ++kc) {
         if (!mbar_wait_bounded(&full[s], ph, abort_flag, args.err)) return;
@@ -134,39 +147,49 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
         for (int i = 0; i < kb_per_warp; ++i) {
           const int kb = cw * kb_per_warp + i;
           if (kb >= kb_per_stage) break;
-          const int kglob = kc * KC + kb * 32 + 8 * t;
+          const int box = kb >> 1;
+          const int col = ((kb & 1) * 4 + t) * 16;  // byte column of this lane's 8 elements
+          const uint8_t* wb = sb + box * wbox;
+          const uint8_t* xb = sb + NB * wbox + box * xbox;
           uint4 b[NTT];
 #pragma unroll
-          for (int n = 0; n < NTT; ++n) {
-            const int tok = tok0 + n * 8 + g;
-            b[n] = tok < T ? ldg_nc_v4(args.x + (size_t)tok * K + kglob) : make_uint4(0, 0, 0, 0);
-          }
+          for (int n = 0; n < NTT; ++n)
+            b[n] = *reinterpret_cast<const uint4*>(xb + swz128(n * 8 + pg, col));
 #pragma unroll
           for (int m = 0; m < 2; ++m) {
-            const uint4 alo = *reinterpret_cast<const uint4*>(sb + (m * 16 + g) * row_stride + kb * 64 + 16 * t);
-            const uint4 ahi = *reinterpret_cast<const uint4*>(sb + (m * 16 + g + 8) * row_stride + kb * 64 + 16 * t);
+            const uint4 alo = *reinterpret_cast<const uint4*>(wb + swz128(m * 16 + pg, col));
+            const uint4 ahi = *reinterpret_cast<const uint4*>(wb + swz128(m * 16 + pg + 8, col));
 #pragma unroll
             for (int n = 0; n < NTT; ++n) {
-              mma_bf16(acc[m][n], alo.x, ahi.x, alo.y, ahi.y, b[n].x, b[n].y);
-              mma_bf16(acc[m][n], alo.z, ahi.z, alo.w, ahi.w, b[n].z, b[n].w);
+              float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_bf16(tmp, alo.x, ahi.x, alo.y, ahi.y, b[n].x, b[n].y);
+              mma_bf16(tmp, alo.z, ahi.z, alo.w, ahi.w, b[n].z, b[n].w);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float yk = tmp[q] - cmp[m][n][q];
+                const float tk = acc[m][n][q] + yk;
+                cmp[m][n][q] = (tk - acc[m][n][q]) - yk;
+                acc[m][n][q] = tk;
+              }
             }
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == kStages) { s = 0; ph ^= 1; }
+        if (++s == NS) { s = 0; ph ^= 1; }
       }
 
-      // deterministic cross-warp reduction
+      // deterministic cross-warp reduction; red[w][weight row][token], physical indices
       float* r = red + cw * kUnitRows * ntok;
+      const int c0 = pi8(2 * t), c1 = pi8(2 * t + 1);
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
         for (int n = 0; n < NTT; ++n) {
-          r[(m * 16 + g) * ntok + n * 8 + 2 * t] = acc[m][n][0];
-          r[(m * 16 + g) * ntok + n * 8 + 2 * t + 1] = acc[m][n][1];
-          r[(m * 16 + g + 8) * ntok + n * 8 + 2 * t] = acc[m][n][2];
-          r[(m * 16 + g + 8) * ntok + n * 8 + 2 * t + 1] = acc[m][n][3];
+          r[(m * 16 + pg) * ntok + n * 8 + c0] = acc[m][n][0] - cmp[m][n][0];
+          r[(m * 16 + pg) * ntok + n * 8 + c1] = acc[m][n][1] - cmp[m][n][1];
+          r[(m * 16 + pg + 8) * ntok + n * 8 + c0] = acc[m][n][2] - cmp[m][n][2];
+          r[(m * 16 + pg + 8) * ntok + n * 8 + c1] = acc[m][n][3] - cmp[m][n][3];
         }
       if (!group_barrier(cbar, cph, abort_flag, args.err)) return;
       // epilogue: warp = token, lane = row within the unit
@@ -174,9 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
         const int tok = tok0 + j;
         if (tok >= T) break;
         const int row = row0 + lane;
-        float v = 0.f;
+        float v = 0.f, vc = 0.f;  // Kahan over the warps' partials, fixed order
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) v += red[(w * kUnitRows + lane) * ntok + j];
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float yk = red[(w * kUnitRows + lane) * ntok + j] - vc;
+          const float tk = v + yk;
+          vc = (tk - v) - yk;
+          v = tk;
+        }
         const bool valid = row < P.N;
         if (P.out_f32 && valid) P.out_f32[(size_t)tok * P.N + row] = v + (P.bias ? P.bias[row] : 0.f);
         if (P.out_bf16) {
@@ -187,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
             if (P.actq) q = mxfp8_roundtrip(q, mxfp8_block_exp(warp_max(fabsf(q))));
             const int e = f16_block_exp(warp_max(fabsf(q)));
             P.out_h[(size_t)tok * P.N + row] = __float2half_rn(ldexpf(q, -e));
-            if (lane == 0) P.out_s[(size_t)tok * (P.N / 32) + row0 / 32] = (int8_t)e;
+            if (lane == 0) P.out_s[(size_t)tok * exp_pitch(P.N) + row0 / 32] = (int8_t)e;
           }
         }
       }
@@ -197,11 +225,24 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
 }
 
 template <int NTT>
-cudaError_t launch_t(const DenseArgs& a, cudaStream_t s) {
-  const int row_stride = a.KC * 2 + 64;
-  const size_t smem = (size_t)kStages * kUnitRows * row_stride +
-                      (size_t)kConsumerWarps * kUnitRows * 8 * NTT * sizeof(float) +
-                      (2 * kStages + 1) * sizeof(uint64_t) + 16;
+cudaError_t launch_t(DenseArgs& a, const uint16_t* const W[2], const int N[2], const uint16_t* x,
+                     cudaStream_t s) {
+  constexpr int ntok = 8 * NTT;
+  const int target_nb = NTT <= 2 ? 8 : (NTT == 4 ? 4 : 2);
+  const int kt = a.K / 64;
+  a.NB = 1;
+  for (int nb = target_nb; nb >= 1; nb >>= 1)
+    if (kt % nb == 0) { a.NB = nb; break; }
+  const int stage_bytes = a.NB * (kUnitRows * 128 + ntok * 128);
+  a.NS = NTT <= 2 ? 3 : 4;
+  for (int i = 0; i < 2; ++i)
+    if (W[i] && !make_tmap_2d(&a.tw[i], W[i], 2, (uint64_t)a.K, (uint64_t)N[i], (uint64_t)a.K * 2, 64,
+                              kUnitRows, true))
+      return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&a.tx, x, 2, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, ntok, true))
+    return cudaErrorInvalidValue;
+  const size_t smem = (size_t)a.NS * stage_bytes + (size_t)kConsumerWarps * kUnitRows * ntok * sizeof(float) +
+                      (2 * kMaxStages + 1) * sizeof(uint64_t) + 16 + 1024;
   cudaError_t e = cudaFuncSetAttribute(dense_gemv_kernel<NTT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -218,20 +259,19 @@ cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint1
                               int K, uint32_t* err, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   DenseArgs a{};
-  a.p[0] = DenseProblem{W0, N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0};
-  a.p[1] = DenseProblem{W1, N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1};
+  a.p[0] = DenseProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0};
+  a.p[1] = DenseProblem{N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1};
   a.units0 = W0 ? (N0 + kUnitRows - 1) / kUnitRows : 0;
   a.units = a.units0 + (W1 ? (N1 + kUnitRows - 1) / kUnitRows : 0);
-  a.x = x;
   a.T = T;
   a.K = K;
-  a.KC = (K % 512 == 0) ? 512 : (K % 256 == 0) ? 256 : (K % 128 == 0) ? 128 : 64;
   a.err = err;
   if (a.units == 0) return cudaSuccess;
-  if (T <= 8) return launch_t<1>(a, s);
-  if (T <= 16) return launch_t<2>(a, s);
-  if (T <= 32) return launch_t<4>(a, s);
-  return launch_t<8>(a, s);
+  const uint16_t* W[2] = {W0, W1};
+  const int N[2] = {N0, N1};
+  if (T <= 8) return launch_t<1>(a, W, N, x, s);
+  if (T <= 16) return launch_t<2>(a, W, N, x, s);
+  return launch_t<4>(a, W, N, x, s);  // chunks of 32 tokens
 }
 
 }  // namespace k3moe

@@ -7,19 +7,30 @@
 //   down pass: o[r] = D_e a[r]                                  D_e [L][I]
 //
 // HBM-bound: only the selected experts' bytes are read, each once per chunk of up to 8 rows.
-// A persistent CTA walks units = (chunk of rows of one expert, block of 32 output features).
-// A producer warp streams the unit's code rows through a ring of shared-memory stages with
-// per-row bulk copies (TMA engine) and its e8m0 scale rows into a double-buffered unit slot.
+// A persistent CTA walks a contiguous range of units = (chunk of rows of one expert, block of
+// 32 output features); the chunk table gives a unit's expert and rows in one load. A producer
+// warp streams, through the TMA engine:
+//   - the unit's code rows, one 2-D tile (32 rows x 128 bytes = 256 weights, 128-byte
+//     swizzle) per matrix per stage, into a deep ring of shared-memory stages,
+//   - the unit's e8m0 scale rows (one contiguous 1-D copy per matrix) into a double-buffered
+//     unit slot,
+//   - the chunk's activation rows (f16, block-scaled) and block exponents into an activation
+//     slot, reloaded only when the chunk changes.
+// Few large copies matter: the TMA engine takes roughly one copy per ~60 cycles per SM, so
+// per-row copies of a few hundred bytes cannot reach HBM bandwidth while 4-8 KB tiles can.
 // Eight consumer warps split each stage's K. Per 32-weight block a warp converts the codes
 // with the hardware e2m1 -> f16 conversion, multiplies them on the tensor cores (mma.sync
-// m16n8k16, weights on M, rows on N) into a fresh fp32 block sum, and adds that sum scaled by
-// 2^(E-127) (the e8m0 weight scale) times 2^s (the activation block scale). Activations arrive
-// as an f16 copy with one power-of-two exponent per 32 values, so no value overflows f16 and
+// m16n8k16, weights on M, rows on N) into a fresh fp32 block sum, and adds that sum times
+// 2^(E-127) (the e8m0 weight scale) times 2^s (the activation block scale). Activations are
+// an f16 copy with one power-of-two exponent per 32 values, so no value overflows f16 and
 // every bf16 input from 2^-29 of its block maximum upwards converts exactly. A fixed-order
 // shared-memory reduction over the warps keeps results deterministic.
 //
 // GLU unit: M-tile p holds gate rows 8p..8p+7 of the feature block as tile rows 0..7 and the
 // matching up rows as tile rows 8..15, so one thread ends up with gate and up of a feature.
+//
+// Inputs are checked on the device: a chunk whose expert is out of range or a row token
+// outside [0, T) sets the index bit of the error word and the affected rows are skipped.
 #include <cuda_fp16.h>
 
 #include "k3moe_device.cuh"
@@ -30,23 +41,27 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (1 + kConsumerWarps);
-constexpr int kStages = 6;
+constexpr int kMaxStages = 24;
+constexpr int kStageBudget = 96 * 1024;
 
 struct ExpertArgs {
-  const uint8_t* q0;   // GLU: gate codes; down: down codes   [E][N][K/2]
-  const uint8_t* s0;   //                                        [E][N][K/32]
-  const uint8_t* q1;   // GLU: up codes (unused for down)
-  const uint8_t* s1;
+  CUtensorMap tq0;     // GLU: gate codes; down: down codes. 2-D {K/2 bytes, E*N rows}
+  CUtensorMap tq1;     // GLU: up codes
+  const uint8_t* s0;   // scales [E][N][K/32]
+  const uint8_t* s1;   // GLU: up scales
   int N, K;            // output features per expert, reduction length
-  int KCB;             // code bytes per row per stage
+  int IB;              // code bytes per row per stage (tile inner width)
+  int NS;              // ring stages
   const int32_t* plan;
-  const int32_t* offsets;
+  const int4* ctab;
   const int32_t* row_token;  // GLU: B row = token of the sorted row; down: B row = sorted row
-  const __half* bh;    // activations, f16 block-scaled [rows][K]
-  const int8_t* bs;    // activation block exponents [rows][K/32]
+  int brows;           // rows of the activation arrays (GLU: T, down: T*k)
+  int rows_max;        // T*k
+  const __half* bh;    // activations, f16 block-scaled [brows][K]
+  const int8_t* bs;    // activation block exponents [brows][exp_pitch(K)]
   uint16_t* a_out;     // GLU output bf16 [rows][N]
-  __half* ah_out;      // GLU output f16 block-scaled copy
-  int8_t* as_out;
+  __half* ah_out;      // GLU output f16 block-scaled copy [rows][N]
+  int8_t* as_out;      // its exponents [rows][exp_pitch(N)]
   float* o_out;        // down output fp32 [rows][N]
   int E;
   int actq;
@@ -54,28 +69,20 @@ struct ExpertArgs {
 };
 
 struct Unit {
-  int e, r0, nrows, fb;
+  int e, r0, nrows, fb, chunk;
 };
 
-__device__ __forceinline__ Unit decode_unit(const ExpertArgs& A, int u, int fbs) {
-  const int* plan = A.plan;
-  const int D = plan[0];
-  const int* active = plan + 2;
-  const int* cpre = plan + 2 + A.E;
-  const int c = u / fbs;
-  // binary search: largest d with cpre[d] <= c
-  int lo = 0, hi = D - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (cpre[mid] <= c) lo = mid; else hi = mid - 1;
-  }
+__device__ __forceinline__ Unit decode_unit(const ExpertArgs& A, int u, int fbs, bool report) {
   Unit r;
-  r.e = active[lo];
-  const int q = c - cpre[lo];
-  const int beg = A.offsets[r.e], end = A.offsets[r.e + 1];
-  r.r0 = beg + q * kGemvTokens;
-  r.nrows = min(kGemvTokens, end - r.r0);
-  r.fb = u % fbs;
+  r.chunk = u / fbs;
+  r.fb = u - r.chunk * fbs;
+  const int4 c = A.ctab[r.chunk];
+  const bool ok = c.x >= 0 && c.x < A.E && c.y >= 0 && c.z >= 0 && c.z <= kGemvTokens &&
+                  c.y + c.z <= A.rows_max;
+  r.e = ok ? c.x : 0;
+  r.r0 = ok ? c.y : 0;
+  r.nrows = ok ? c.z : 0;
+  if (!ok && report) atomicOr(A.err, kErrIndex);
   return r;
 }
 
@@ -83,26 +90,36 @@ template <bool GLU>
 __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_constant__ ExpertArgs A) {
   constexpr int kRows = GLU ? 2 * kUnitRows : kUnitRows;  // A rows per unit
   constexpr int kMT = GLU ? 4 : 2;                        // M-tiles per unit
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int K = A.K, KCB = A.KCB;
-  const int row_stride = KCB + 16;
-  const int stage_bytes = kRows * row_stride;
-  const int srow = K / 32;                    // scale bytes per row
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int K = A.K, IB = A.IB, NS = A.NS;
+  const bool swz = IB == 128;
+  const int stage_bytes = (kRows * IB + 1023) & ~1023;
+  const int srow = K / 32;                    // scale bytes per weight row
   const int sbytes = kRows * srow;            // scale bytes per unit
   const int sslot = (sbytes + 127) & ~127;
-  uint8_t* stages = smem;
-  uint8_t* sbuf = smem + kStages * stage_bytes;
-  float* red = reinterpret_cast<float*>(sbuf + 2 * sslot);
-  uint64_t* full = reinterpret_cast<uint64_t*>(red + kConsumerWarps * kRows * kGemvTokens);
-  uint64_t* empty = full + kStages;
-  uint64_t* sfull = empty + kStages;
+  const int bpitch = K * 2 + 64;              // f16 activation row pitch in smem
+  const int epitch = exp_pitch(K);            // exponent row pitch (global and smem)
+  const int bslot = kGemvTokens * bpitch + kGemvTokens * epitch;
+  // stages start on a 1024-byte boundary of the shared window (the 128-byte swizzle pattern
+  // is a function of the shared address)
+  uint8_t* stages = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
+  uint8_t* sbuf = stages + NS * stage_bytes;
+  uint8_t* bbuf = sbuf + 2 * sslot;
+  const int8_t* bexp = reinterpret_cast<const int8_t*>(bbuf + kGemvTokens * bpitch);
+  float* red = reinterpret_cast<float*>(bbuf + ((bslot + 127) & ~127));
+  int* bidx = reinterpret_cast<int*>(red + kConsumerWarps * kRows * kGemvTokens);
+  uint64_t* full = reinterpret_cast<uint64_t*>(bidx + kGemvTokens);
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* sfull = empty + kMaxStages;
   uint64_t* sempty = sfull + 2;
-  uint64_t* cbar = sempty + 2;
+  uint64_t* bfull = sempty + 2;
+  uint64_t* bempty = bfull + 1;
+  uint64_t* cbar = bempty + 1;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(cbar + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NS; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
     }
@@ -110,28 +127,52 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
       mbar_init(&sfull[s], 1);
       mbar_init(&sempty[s], kConsumerWarps);
     }
-    mbar_init(cbar, 32 * kConsumerWarps);
+    mbar_init(bfull, 1);
+    mbar_init(bempty, kConsumerWarps);
+    mbar_init(cbar, kConsumerWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
 
   const int fbs = A.N / kUnitRows;
-  const int units = A.plan[1] * fbs;
+  const int C = A.plan[1];
+  const int units = (C > 0 && C <= A.rows_max / kGemvTokens + A.E) ? C * fbs : 0;
   const int ub = (int)(((long long)units * blockIdx.x) / gridDim.x);
   const int ue = (int)(((long long)units * (blockIdx.x + 1)) / gridDim.x);
-  const int nkc = (K / 2) / KCB;
-  const size_t qmat = (size_t)A.N * (K / 2);   // code bytes per expert matrix
+  const int nkc = (K / 2) / IB;
   const size_t smat = (size_t)A.N * srow;      // scale bytes per expert matrix
 
   if (warp == 0) {
-    // ---------------- producer
-    int s = 0, us = 0;
-    uint32_t ph = 0, uph = 0;
+    // ---------------- producer (lane 0 issues; the warp stays converged)
+    int s = 0, us = 0, cur = -1;
+    uint32_t ph = 0, uph = 0, bph = 0;
     bool ok = true;
     for (int u = ub; u < ue && ok; ++u) {
-      const Unit U = decode_unit(A, u, fbs);
+      const Unit U = decode_unit(A, u, fbs, lane == 0);
       const int f0 = U.fb * kUnitRows;
+      if (U.chunk != cur) {  // activation rows of a new chunk
+        if (!mbar_wait_bounded(bempty, bph ^ 1, abort_flag, A.err)) { ok = false; break; }
+        int br = -1;
+        if (lane < U.nrows) {
+          const int r = U.r0 + lane;
+          br = GLU ? A.row_token[r] : r;
+          if (br < 0 || br >= A.brows) {
+            atomicOr(A.err, kErrIndex);
+            br = -1;
+          }
+        }
+        if (lane < kGemvTokens) bidx[lane] = br;
+        const unsigned have = __ballot_sync(0xffffffffu, br >= 0);
+        if (lane == 0) mbar_arrive_expect_tx(bfull, (uint32_t)(__popc(have) * (K * 2 + epitch)));
+        __syncwarp();
+        if (br >= 0) {
+          bulk_g2s(bbuf + lane * bpitch, A.bh + (size_t)br * K, K * 2, bfull);
+          bulk_g2s(bbuf + kGemvTokens * bpitch + lane * epitch, A.bs + (size_t)br * epitch, epitch, bfull);
+        }
+        bph ^= 1;
+        cur = U.chunk;
+      }
       if (!mbar_wait_bounded(&sempty[us], uph ^ 1, abort_flag, A.err)) { ok = false; break; }
       if (lane == 0) {
         mbar_arrive_expect_tx(&sfull[us], (uint32_t)sbytes);
@@ -141,23 +182,22 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
                    kUnitRows * srow, &sfull[us]);
       }
       if (++us == 2) { us = 0; uph ^= 1; }
+      const int y = U.e * A.N + f0;
       for (int kc = 0; kc < nkc; ++kc) {
         if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
-        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(kRows * KCB));
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], (uint32_t)(kRows * IB));
+          uint8_t* dst = stages + s * stage_bytes;
+          tma_load_2d(dst, &A.tq0, kc * IB, y, &full[s]);
+          if (GLU) tma_load_2d(dst + kUnitRows * IB, &A.tq1, kc * IB, y, &full[s]);
+        }
         __syncwarp();
-        uint8_t* dst = stages + s * stage_bytes;
-        const size_t col = (size_t)kc * KCB;
-        bulk_g2s(dst + lane * row_stride, A.q0 + U.e * qmat + (size_t)(f0 + lane) * (K / 2) + col, KCB,
-                 &full[s]);
-        if (GLU)
-          bulk_g2s(dst + (kUnitRows + lane) * row_stride,
-                   A.q1 + U.e * qmat + (size_t)(f0 + lane) * (K / 2) + col, KCB, &full[s]);
-        if (++s == kStages) { s = 0; ph ^= 1; }
+        if (++s == NS) { s = 0; ph ^= 1; }
       }
     }
     if (!ok) {
-      for (int i = 0; i < kStages; ++i) {
-        if (--s < 0) { s = kStages - 1; ph ^= 1; }
+      for (int i = 0; i < NS; ++i) {
+        if (--s < 0) { s = NS - 1; ph ^= 1; }
         volatile int dummy = 0;
         mbar_wait_bounded(&full[s], ph, &dummy, A.err);
       }
@@ -168,18 +208,26 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
   // ---------------- consumers
   const int cw = warp - 1;
   const int g = lane >> 2, t = lane & 3;
-  const int kb_per_stage = KCB / 16;  // 32-weight blocks per stage
+  const int kb_per_stage = IB / 16;  // 32-weight blocks per stage
   const int kb_per_warp = (kb_per_stage + kConsumerWarps - 1) / kConsumerWarps;
-  int s = 0, us = 0;
-  uint32_t ph = 0, uph = 0, cph = 0;
+  int s = 0, us = 0, cur = -1;
+  uint32_t ph = 0, uph = 0, bph = 0, cph = 0;
+  bool bvalid = false, v0 = false, v1 = false;
   for (int u = ub; u < ue; ++u) {
-    const Unit U = decode_unit(A, u, fbs);
+    const Unit U = decode_unit(A, u, fbs, false);
     const int f0 = U.fb * kUnitRows;
-    // B row of this lane's column (tile column g)
-    const bool bvalid = g < U.nrows;
-    const int brow = bvalid ? (GLU ? A.row_token[U.r0 + g] : U.r0 + g) : 0;
-    const __half* bptr = A.bh + (size_t)brow * K;
-    const int8_t* bsp = A.bs + (size_t)brow * (K / 32);
+    if (U.chunk != cur) {
+      if (cur != -1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bempty);
+      }
+      if (!mbar_wait_bounded(bfull, bph, abort_flag, A.err)) return;
+      bph ^= 1;
+      cur = U.chunk;
+      bvalid = bidx[g] >= 0;
+      v0 = bidx[2 * t] >= 0;
+      v1 = bidx[2 * t + 1] >= 0;
+    }
 
     float acc[kMT][4];
 #pragma unroll
@@ -189,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
 
     if (!mbar_wait_bounded(&sfull[us], uph, abort_flag, A.err)) return;
     const uint8_t* sc = sbuf + us * sslot;
+    const uint8_t* brow_s = bbuf + g * bpitch;
 
     for (int kc = 0; kc < nkc; ++kc) {
       if (!mbar_wait_bounded(&full[s], ph, abort_flag, A.err)) return;
@@ -197,22 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
         const int kb = cw * kb_per_warp + i;
         if (kb >= kb_per_stage) break;
         const int KB = kc * kb_per_stage + kb;  // global 32-block index along K
-        uint4 b = make_uint4(0, 0, 0, 0);
-        int bexp = 0;
-        if (bvalid) {
-          b = ldg_nc_v4(bptr + KB * 32 + 8 * t);
-          bexp = bsp[KB];
-        }
-        // activation block scale of tile columns 2t and 2t+1 (held by lanes 8t and 8t+4)
-        const float sc0 = exp2i(__shfl_sync(0xffffffffu, bexp, 8 * t));
-        const float sc1 = exp2i(__shfl_sync(0xffffffffu, bexp, 8 * t + 4));
+        const uint4 b = bvalid ? *reinterpret_cast<const uint4*>(brow_s + KB * 64 + 16 * t)
+                               : make_uint4(0, 0, 0, 0);
+        // activation block scales of tile columns 2t and 2t+1
+        const float sc0 = v0 ? exp2i(bexp[(2 * t) * epitch + KB]) : 0.f;
+        const float sc1 = v1 ? exp2i(bexp[(2 * t + 1) * epitch + KB]) : 0.f;
 #pragma unroll
         for (int m = 0; m < kMT; ++m) {
-          // tile rows g and g+8 -> shared-memory rows
+          // tile rows g and g+8 -> stage rows
           const int rlo = GLU ? (8 * m + g) : (16 * m + g);
           const int rhi = GLU ? (kUnitRows + 8 * m + g) : (16 * m + g + 8);
-          const uint32_t qlo = *reinterpret_cast<const uint32_t*>(sb + rlo * row_stride + kb * 16 + 4 * t);
-          const uint32_t qhi = *reinterpret_cast<const uint32_t*>(sb + rhi * row_stride + kb * 16 + 4 * t);
+          const int clo = kb * 16 + 4 * t;
+          const uint32_t qlo = *reinterpret_cast<const uint32_t*>(sb + (swz ? swz128(rlo, clo) : rlo * IB + clo));
+          const uint32_t qhi = *reinterpret_cast<const uint32_t*>(sb + (swz ? swz128(rhi, clo) : rhi * IB + clo));
           const float slo = e8m0_to_f32(sc[rlo * srow + KB]);
           const float shi = e8m0_to_f32(sc[rhi * srow + KB]);
           float tmp[4] = {0.f, 0.f, 0.f, 0.f};
@@ -228,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-      if (++s == kStages) { s = 0; ph ^= 1; }
+      if (++s == NS) { s = 0; ph ^= 1; }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sempty[us]);
@@ -246,8 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
       r[rhi * kGemvTokens + 2 * t + 1] = acc[m][3];
     }
     if (!group_barrier(cbar, cph, abort_flag, A.err)) return;
-    // epilogue: warp cw handles column (row of the chunk) cw, lane = feature f0 + lane
-    if (cw < U.nrows) {
+    // epilogue: warp cw handles chunk column cw, lane = feature f0 + lane
+    if (bidx[cw] >= 0) {
       const int row = U.r0 + cw;
       if (GLU) {
         float gs = 0.f, us_ = 0.f;
@@ -263,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
         if (A.actq) q = mxfp8_roundtrip(q, mxfp8_block_exp(warp_max(fabsf(q))));
         const int e = f16_block_exp(warp_max(fabsf(q)));
         A.ah_out[(size_t)row * A.N + f0 + lane] = __float2half_rn(ldexpf(q, -e));
-        if (lane == 0) A.as_out[(size_t)row * (A.N / 32) + U.fb] = (int8_t)e;
+        if (lane == 0) A.as_out[(size_t)row * exp_pitch(A.N) + U.fb] = (int8_t)e;
       } else {
         float o = 0.f;
 #pragma unroll
@@ -275,56 +321,86 @@ __global__ void __launch_bounds__(kThreads, 1) expert_gemv_kernel(const __grid_c
   }
 }
 
+struct Geometry {
+  int IB, NS;
+  size_t smem;
+};
+
 template <bool GLU>
-cudaError_t launch_t(const ExpertArgs& a, int units_max, cudaStream_t s) {
+Geometry geometry(int K) {
   constexpr int kRows = GLU ? 2 * kUnitRows : kUnitRows;
-  const int row_stride = a.KCB + 16;
-  const int sbytes = kRows * (a.K / 32);
+  Geometry g;
+  const int rb = K / 2;
+  g.IB = (rb % 128 == 0) ? 128 : (rb % 64 == 0) ? 64 : 32;
+  const int stage_bytes = (kRows * g.IB + 1023) & ~1023;
+  g.NS = kStageBudget / stage_bytes;
+  if (g.NS > kMaxStages) g.NS = kMaxStages;
+  if (g.NS < 2) g.NS = 2;
+  const int sbytes = kRows * (K / 32);
   const int sslot = (sbytes + 127) & ~127;
-  const size_t smem = (size_t)kStages * kRows * row_stride + 2 * (size_t)sslot +
-                      (size_t)kConsumerWarps * kRows * kGemvTokens * sizeof(float) +
-                      (2 * kStages + 5) * sizeof(uint64_t) + 16;
+  const int bslot = kGemvTokens * (K * 2 + 64) + kGemvTokens * exp_pitch(K);
+  g.smem = (size_t)g.NS * stage_bytes + 2 * (size_t)sslot + ((bslot + 127) & ~127) +
+           (size_t)kConsumerWarps * kRows * kGemvTokens * sizeof(float) + kGemvTokens * sizeof(int) +
+           (2 * kMaxStages + 7) * sizeof(uint64_t) + 16 + 1024;  // + alignment slack
+  return g;
+}
+
+template <bool GLU>
+cudaError_t launch_t(ExpertArgs& a, int units_max, cudaStream_t s) {
+  const Geometry g = geometry<GLU>(a.K);
+  a.IB = g.IB;
+  a.NS = g.NS;
   cudaError_t e = cudaFuncSetAttribute(expert_gemv_kernel<GLU>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
   if (e != cudaSuccess) return e;
   int grid = num_sms();
   if (units_max < grid) grid = units_max > 0 ? units_max : 1;
-  expert_gemv_kernel<GLU><<<grid, kThreads, smem, s>>>(a);
+  expert_gemv_kernel<GLU><<<grid, kThreads, g.smem, s>>>(a);
   return cudaGetLastError();
 }
 
-int pick_kcb(int row_bytes) {
-  for (int c : {256, 128, 64, 32, 16})
-    if (row_bytes % c == 0) return c;
-  return 16;
+bool code_map(CUtensorMap* m, const uint8_t* q, int E, int N, int K) {
+  const int IB = ((K / 2) % 128 == 0) ? 128 : ((K / 2) % 64 == 0) ? 64 : 32;
+  return make_tmap_2d(m, q, 1, (uint64_t)(K / 2), (uint64_t)E * N, (uint64_t)(K / 2), (uint32_t)IB,
+                      kUnitRows, IB == 128);
 }
 
 }  // namespace
 
 cudaError_t launch_expert_glu(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
                               const int32_t* offsets, const int32_t* row_token, const __half* zh,
-                              const int8_t* zs, uint16_t* a, __half* ah, int8_t* as, int rows_max,
+                              const int8_t* zs, uint16_t* a, __half* ah, int8_t* as, int T,
                               uint32_t* err, cudaStream_t s) {
+  (void)offsets;
   ExpertArgs A{};
-  A.q0 = w.gate_q; A.s0 = w.gate_s; A.q1 = w.up_q; A.s1 = w.up_s;
-  A.N = d.inter; A.K = d.latent; A.KCB = pick_kcb(d.latent / 2);
-  A.plan = plan; A.offsets = offsets; A.row_token = row_token;
+  if (!code_map(&A.tq0, w.gate_q, d.n_experts, d.inter, d.latent) ||
+      !code_map(&A.tq1, w.up_q, d.n_experts, d.inter, d.latent))
+    return cudaErrorInvalidValue;
+  A.s0 = w.gate_s; A.s1 = w.up_s;
+  A.N = d.inter; A.K = d.latent;
+  A.plan = plan; A.ctab = plan_ctab(const_cast<int32_t*>(plan), d.n_experts);
+  A.row_token = row_token;
+  A.brows = T; A.rows_max = T * d.top_k;
   A.bh = zh; A.bs = zs; A.a_out = a; A.ah_out = ah; A.as_out = as;
   A.E = d.n_experts; A.actq = d.actq; A.err = err;
-  const int chunks_max = rows_max / kGemvTokens + d.n_experts;
+  const int chunks_max = A.rows_max / kGemvTokens + d.n_experts;
   return launch_t<true>(A, chunks_max * (d.inter / kUnitRows), s);
 }
 
 cudaError_t launch_expert_down(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
                                const int32_t* offsets, const __half* ah, const int8_t* as,
-                               float* o_rows, int rows_max, uint32_t* err, cudaStream_t s) {
+                               float* o_rows, int T, uint32_t* err, cudaStream_t s) {
+  (void)offsets;
   ExpertArgs A{};
-  A.q0 = w.down_q; A.s0 = w.down_s;
-  A.N = d.latent; A.K = d.inter; A.KCB = pick_kcb(d.inter / 2);
-  A.plan = plan; A.offsets = offsets; A.row_token = nullptr;
+  if (!code_map(&A.tq0, w.down_q, d.n_experts, d.latent, d.inter)) return cudaErrorInvalidValue;
+  A.s0 = w.down_s;
+  A.N = d.latent; A.K = d.inter;
+  A.plan = plan; A.ctab = plan_ctab(const_cast<int32_t*>(plan), d.n_experts);
+  A.row_token = nullptr;
+  A.brows = T * d.top_k; A.rows_max = T * d.top_k;
   A.bh = ah; A.bs = as; A.o_out = o_rows;
   A.E = d.n_experts; A.actq = d.actq; A.err = err;
-  const int chunks_max = rows_max / kGemvTokens + d.n_experts;
+  const int chunks_max = A.rows_max / kGemvTokens + d.n_experts;
   return launch_t<false>(A, chunks_max * (d.latent / kUnitRows), s);
 }
 

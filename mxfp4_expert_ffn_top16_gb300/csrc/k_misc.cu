@@ -16,20 +16,28 @@ __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __res
   const int t = blockIdx.y;
   const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (t >= T || n >= L) return;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  // Kahan-compensated sum, so the bf16 rounding of c follows the exact sum of the fp32 terms
+  // except within ~1 fp32 ulp of a rounding boundary
+  float s[4] = {0.f, 0.f, 0.f, 0.f}, cc[4] = {0.f, 0.f, 0.f, 0.f};
   for (int j = 0; j < k; ++j) {
     const float wj = w[(size_t)t * k + j];
-    const float4 v = *reinterpret_cast<const float4*>(o + (size_t)slot_row[(size_t)t * k + j] * L + n);
-    acc.x = fmaf(wj, v.x, acc.x);
-    acc.y = fmaf(wj, v.y, acc.y);
-    acc.z = fmaf(wj, v.z, acc.z);
-    acc.w = fmaf(wj, v.w, acc.w);
+    const int r = slot_row[(size_t)t * k + j];
+    if (r < 0 || r >= T * k) continue;  // out-of-range rows contribute nothing
+    const float4 v = *reinterpret_cast<const float4*>(o + (size_t)r * L + n);
+    const float p[4] = {wj * v.x, wj * v.y, wj * v.z, wj * v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float yk = p[q] - cc[q];
+      const float tk = s[q] + yk;
+      cc[q] = (tk - s[q]) - yk;
+      s[q] = tk;
+    }
   }
   ushort4 r;
-  r.x = f32_to_bf16(acc.x);
-  r.y = f32_to_bf16(acc.y);
-  r.z = f32_to_bf16(acc.z);
-  r.w = f32_to_bf16(acc.w);
+  r.x = f32_to_bf16(s[0] - cc[0]);
+  r.y = f32_to_bf16(s[1] - cc[1]);
+  r.z = f32_to_bf16(s[2] - cc[2]);
+  r.w = f32_to_bf16(s[3] - cc[3]);
   *reinterpret_cast<ushort4*>(c + (size_t)t * L + n) = r;
 }
 
@@ -46,7 +54,10 @@ __global__ void act_prep_kernel(const uint16_t* __restrict__ z, int T, int L, in
   if (actq) q = mxfp8_roundtrip(q, mxfp8_block_exp(warp_max(fabsf(q))));
   const int e = f16_block_exp(warp_max(fabsf(q)));
   zh[i] = __float2half_rn(ldexpf(q, -e));
-  if (lane == 0) zs[blk] = (int8_t)e;
+  if (lane == 0) {
+    const long long t = blk / (L / 32), b = blk % (L / 32);
+    zs[t * exp_pitch(L) + b] = (int8_t)e;
+  }
 }
 
 }  // namespace

@@ -123,8 +123,10 @@ __device__ int block_excl_scan(int* cnt, int n, int* tmp) {
   return total;
 }
 
-// Plan from offsets[E+1] held in shared memory: active experts and chunk prefix.
-__device__ void build_plan(const int* off, int E, int32_t* plan, int* tmp, int* flag, int* chunks) {
+// Plan from offsets[E+1] held in shared memory: active experts, chunk prefix, and the chunk
+// table ctab[c] = {expert, first sorted row, rows (<= 8), 0} in expert order.
+__device__ void build_plan(const int* off, int E, int32_t* plan, int4* ctab, int* tmp, int* flag,
+                           int* chunks) {
   const int tid = threadIdx.x;
   const int m = tid < E ? off[tid + 1] - off[tid] : 0;
   if (tid < E) {
@@ -137,6 +139,8 @@ __device__ void build_plan(const int* off, int E, int32_t* plan, int* tmp, int* 
   if (tid < E && m > 0) {
     plan[2 + flag[tid]] = tid;
     plan[2 + E + flag[tid]] = chunks[tid];
+    for (int q = 0; q * kGemvTokens < m; ++q)
+      ctab[chunks[tid] + q] = make_int4(tid, off[tid] + q * kGemvTokens, min(kGemvTokens, m - q * kGemvTokens), 0);
   }
   if (tid == 0) {
     plan[0] = D;
@@ -211,7 +215,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   if (tid <= E) offsets[tid] = cnt[tid];
   __syncthreads();
   // plan reads the offsets before the scatter turns cnt into running bases
-  build_plan(cnt, E, plan, tmp, flag, chunks);
+  build_plan(cnt, E, plan, plan_ctab(plan, E), tmp, flag, chunks);
   __syncthreads();
   if (tid < 32) warp_scatter(idx, 0, T, E, k, cnt, mask, row_token, row_slot, slot_row, err);
 }
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* hist, int nblk, int
     }
   }
   __syncthreads();
-  build_plan(cnt, E, plan, tmp, flag, chunks);
+  build_plan(cnt, E, plan, plan_ctab(plan, E), tmp, flag, chunks);
 }
 
 __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__ idx, int T, int E,
@@ -278,15 +282,34 @@ __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__
   warp_scatter(idx, t0, t1, E, k, base, mask, row_token, row_slot, slot_row, err);
 }
 
+// Plan from caller-supplied offsets. Offsets that are not a non-decreasing sequence from 0
+// to at most rows_max set the index bit of the error word and give an empty plan.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ offsets, int E,
-                                                    int32_t* plan) {
+                                                    int rows_max, int32_t* plan, uint32_t* err) {
   __shared__ int off[kMaxE + 1];
   __shared__ int tmp[1024];
   __shared__ int flag[kMaxE];
   __shared__ int chunks[kMaxE];
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) off[e] = offsets[e];
+  __shared__ int bad;
+  if (threadIdx.x == 0) bad = 0;
   __syncthreads();
-  build_plan(off, E, plan, tmp, flag, chunks);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    off[e] = offsets[e];
+    if (off[e] < 0 || off[e] > rows_max) bad = 1;
+  }
+  __syncthreads();
+  if (threadIdx.x < E && off[threadIdx.x + 1] < off[threadIdx.x]) bad = 1;
+  if (threadIdx.x == 0 && off[0] != 0) bad = 1;
+  __syncthreads();
+  if (bad) {
+    if (threadIdx.x == 0) {
+      plan[0] = 0;
+      plan[1] = 0;
+      atomicOr(err, kErrIndex);
+    }
+    return;
+  }
+  build_plan(off, E, plan, plan_ctab(plan, E), tmp, flag, chunks);
 }
 
 }  // namespace
@@ -314,8 +337,9 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
   return cudaGetLastError();
 }
 
-cudaError_t launch_plan(const int32_t* offsets, int E, int32_t* plan, cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(offsets, E, plan);
+cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,
+                        cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, plan, err);
   return cudaGetLastError();
 }
 

@@ -11,7 +11,7 @@ import torch
 import mxfp4_expert_ffn_top16_gb300 as k3
 import oracle
 import synth
-from k3help import (DEV, REL_L2, LOGIT_ATOL, LOGIT_RTOL, DeviceLayer, bf16_np, dims, up, stream,
+from k3help import (DEV, REL_L2, PER_TOKEN, LOGIT_ATOL, LOGIT_RTOL, DeviceLayer, bf16_np, dims, up, stream,
                     workspace, check_ok, rel_l2_rows, topk_gap_ambiguous)
 
 pytestmark = pytest.mark.gpu
@@ -34,15 +34,18 @@ def test_project(T, N, K):
     x = synth.host_bf16_normal(1, 1, 0, T * K, 1.0).reshape(T, K)
     out = torch.empty((T, N), dtype=torch.int16, device=DEV)
     ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
-    k3.k3moe_project(up(W).data_ptr(), up(x).data_ptr(), T, N, K, out.data_ptr(), ws.data_ptr(), 256,
+    Wd, xd = up(W), up(x)  # keep the device copies alive until the kernels have run
+    k3.k3moe_project(Wd.data_ptr(), xd.data_ptr(), T, N, K, out.data_ptr(), ws.data_ptr(), 256,
                      stream())
     check_ok(ws)
     got = bf16_np(out)
     want_exact, want_b = oracle.dense_proj(W, x)
     want = oracle.bf16_to_f64(want_b)
-    # same bf16 rounding of sums that differ only in fp32 summation order: at most 1 ulp apart
-    ulp = np.abs(want) * 2.0**-7 + 1e-30
-    assert np.all(np.abs(got - want) <= ulp)
+    # bf16 rounding (half an ulp, 2^-9 relative) of an fp32 sum whose error is bounded by
+    # K * 2^-24 * sum |W x| (fp32 accumulation, any order)
+    mag = np.abs(oracle.bf16_to_f64(x)) @ np.abs(oracle.bf16_to_f64(W)).T
+    bound = np.abs(want_exact) * 2.0**-8 + K * 2.0**-24 * mag * 1.01
+    assert np.all(np.abs(got - want_exact) <= bound)
     assert rel_l2_rows(got, want_exact).max() < 4e-3
     assert (got != want).mean() < 0.02
 
@@ -55,8 +58,9 @@ def _expert_ffn(lay, z_np, idx_np, actq=0):
     off, rt, rs, sr = oracle.permute(idx_np, d.n_experts)  # permutation from the host side
     o = torch.empty((T * d.top_k, d.latent), dtype=torch.float32, device=DEV)
     ws, n = workspace(dm, T)
-    k3.k3moe_expert_ffn_mxfp4(dm, lay.weights, up(z_np).data_ptr(), T, up(off).data_ptr(),
-                              up(rt).data_ptr(), o.data_ptr(), ws.data_ptr(), n, stream())
+    zd, offd, rtd = up(z_np), up(off), up(rt)
+    k3.k3moe_expert_ffn_mxfp4(dm, lay.weights, zd.data_ptr(), T, offd.data_ptr(), rtd.data_ptr(),
+                              o.data_ptr(), ws.data_ptr(), n, stream())
     check_ok(ws)
     return o.cpu().numpy().astype(np.float64), (off, rt, rs, sr)
 
@@ -128,12 +132,15 @@ def test_combine():
     sr = rng.permutation(T * d.top_k).astype(np.int32)
     w = rng.dirichlet(np.ones(d.top_k), T).astype(np.float32)
     c = torch.empty((T, d.latent), dtype=torch.int16, device=DEV)
-    k3.k3moe_combine(dims(d), up(o).data_ptr(), up(sr).data_ptr(), up(w).data_ptr(), T, c.data_ptr(),
-                     stream())
+    od, srd, wd = up(o), up(sr), up(w)
+    k3.k3moe_combine(dims(d), od.data_ptr(), srd.data_ptr(), wd.data_ptr(), T, c.data_ptr(), stream())
     torch.cuda.synchronize()
     got = bf16_np(c)
     want = oracle.bf16_to_f64(oracle.combine(o.astype(np.float64), sr, w.astype(np.float64), T, d.top_k))
-    assert np.all(np.abs(got - want) <= np.abs(want) * 2.0**-7 + 1e-30)
+    o64, w64 = o.astype(np.float64), w.astype(np.float64)
+    exact = np.stack([sum(w64[t, j] * o64[sr[t * d.top_k + j]] for j in range(d.top_k)) for t in range(T)])
+    mag = np.stack([sum(abs(w64[t, j] * o64[sr[t * d.top_k + j]]) for j in range(d.top_k)) for t in range(T)])
+    assert np.all(np.abs(got - exact) <= np.abs(exact) * 2.0**-8 + d.top_k * 2.0**-24 * mag * 1.01)
     assert rel_l2_rows(got, want).max() < 1e-3
 
 
@@ -146,7 +153,8 @@ def _forward(lay, x_np, weights=None, dm=None):
     idx = torch.empty((T, d.top_k), dtype=torch.int32, device=DEV)
     w = torch.empty((T, d.top_k), dtype=torch.float32, device=DEV)
     ws, n = workspace(dm, T)
-    k3.k3moe_layer_forward(dm, weights or lay.weights, up(x_np).data_ptr(), T, y.data_ptr(),
+    xd = up(x_np)
+    k3.k3moe_layer_forward(dm, weights or lay.weights, xd.data_ptr(), T, y.data_ptr(),
                            idx.data_ptr(), w.data_ptr(), ws.data_ptr(), n, stream())
     check_ok(ws)
     return bf16_np(y), idx.cpu().numpy(), w.cpu().numpy()
@@ -165,8 +173,14 @@ def _compare_layer(lay, x, y, idx, sample):
     ol = lay.oracle(experts=set(ref_idx.ravel().tolist()))
     ref = ol.forward(x[sample], nthreads=NCPU)
     np.testing.assert_array_equal(ref["idx"], ref_idx)
-    err = rel_l2_rows(y[sample], oracle.bf16_to_f64(ref["y"]))
-    assert err[same].max() <= REL_L2, err
+    want = oracle.bf16_to_f64(ref["y"])
+    err = rel_l2_rows(y[sample], want)
+    got_s, want_s = y[sample][same], want[same]
+    whole = np.linalg.norm(got_s - want_s) / max(np.linalg.norm(want_s), 1e-300)
+    print(f"layer rel L2: whole {whole:.3e}, per token max {err[same].max():.3e}, "
+          f"{int((~same).sum())} boundary-tie tokens")
+    assert whole <= REL_L2, (whole, err)
+    assert err[same].max() <= PER_TOKEN, err
     return err, int((~same).sum())
 
 
@@ -196,10 +210,14 @@ def test_layer_tiny_ragged_and_edge_T():
 
 def test_layer_k3_decode_b1(k3_layer):
     w = synth.WORKLOADS["decode_b1"]
-    x = synth.host_x(w, 0, 3)
-    for t in range(3):
+    n = 6
+    x = synth.host_x(w, 0, n)
+    ys, idxs = [], []
+    for t in range(n):  # one token per call, as in decode
         y, idx, _ = _forward(k3_layer, x[t:t + 1])
-        _compare_layer(k3_layer, x[t:t + 1], y, idx, np.array([0]))
+        ys.append(y[0])
+        idxs.append(idx[0])
+    _compare_layer(k3_layer, x, np.stack(ys), np.stack(idxs), np.arange(n))
 
 
 def test_layer_k3_decode_b64_biased(k3_layer):
@@ -214,7 +232,7 @@ def test_layer_k3_decode_b64_biased(k3_layer):
         y, idx, _ = _forward(k3_layer, x, weights=lw)
         distinct = len(np.unique(idx))
         assert distinct < 64 * 16  # reuse across the batch
-        _compare_layer(k3_layer, x, y, idx, np.array([0, 1, 17, 40, 63]))
+        _compare_layer(k3_layer, x, y, idx, np.array([0, 1, 2, 17, 29, 40, 51, 63]))
     finally:
         k3_layer.bias_host = None
 
@@ -230,6 +248,6 @@ def test_layer_k3_prefill_sampled(k3_layer):
     try:
         x = synth.host_x(w, 0, T)
         y, idx, _ = _forward(k3_layer, x, weights=lw)
-        _compare_layer(k3_layer, x, y, idx, np.array([0, 511, T - 1]))
+        _compare_layer(k3_layer, x, y, idx, np.array([0, 1, 255, 511, 777, T - 1]))
     finally:
         k3_layer.bias_host = None

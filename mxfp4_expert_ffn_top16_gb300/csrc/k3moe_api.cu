@@ -3,6 +3,7 @@
 // kernels; nothing here computes on the host.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -21,6 +22,27 @@ int num_sms() {
     cached[dev] = n;
   }
   return cached[dev];
+}
+
+cudaError_t ensure_smem_attr(const void* fn, size_t bytes) {
+  struct Rec { const void* fn; int dev; size_t bytes; };
+  static Rec recs[64];
+  static int n = 0;
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (recs[i].fn == fn && recs[i].dev == dev && recs[i].bytes >= bytes) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n; ++i)
+    if (recs[i].fn == fn && recs[i].dev == dev) {
+      recs[i].bytes = bytes;
+      return e;
+    }
+  if (n < 64) recs[n++] = Rec{fn, dev, bytes};
+  return e;
 }
 
 static size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -151,11 +173,17 @@ struct ProfScope {
 k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int32_t T, void* ws,
                                 const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s) {
   uint32_t* err = at<uint32_t>(ws, L.err);
-  {
-    ProfScope p(P_TOPK, s);
-    K3_CUDA(launch_topk(at<float>(ws, L.logits), T, d.n_experts, d.top_k, idx, wts, s));
-  }
-  {
+  if (T <= kSmallRouteTokens) {
+    ProfScope p(P_PERMUTE, s);  // top-k, permutation and plan in one block
+    K3_CUDA(launch_route_tail_small(at<float>(ws, L.logits), T, d.n_experts, d.top_k, idx, wts,
+                                    at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.row_token),
+                                    at<int32_t>(ws, L.row_slot), at<int32_t>(ws, L.slot_row),
+                                    at<int32_t>(ws, L.plan), err, s));
+  } else {
+    {
+      ProfScope p(P_TOPK, s);
+      K3_CUDA(launch_topk(at<float>(ws, L.logits), T, d.n_experts, d.top_k, idx, wts, s));
+    }
     ProfScope p(P_PERMUTE, s);
     K3_CUDA(launch_permute(idx, T, d.n_experts, d.top_k, at<int32_t>(ws, L.offsets),
                            at<int32_t>(ws, L.row_token), at<int32_t>(ws, L.row_slot),

@@ -61,6 +61,14 @@ __device__ __forceinline__ int f16_block_exp(float amax) {
   return e < -100 ? -100 : (e > 100 ? 100 : e);
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Kernels of the layer chain are launched so that the next one may start its prologue while
+// this one finishes. pdl_wait() blocks until the preceding grid has completed and its writes
+// are visible; every kernel calls it before its first global memory access. pdl_trigger()
+// lets the following grid launch. Both are no-ops for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ warp reductions
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -145,6 +153,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Byte offset of (row r, byte c) inside a box whose rows are 128 bytes and which was written
 // with the 128-byte swizzle: the 16-byte chunk index is XORed with r mod 8.
 __device__ __forceinline__ int swz128(int r, int c) {
@@ -177,6 +194,18 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t r;
   asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
   return r;
+}
+
+// Four bytes of codes (8 weights, low nibble first) -> four f16x2 registers, byte j -> r[j].
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t (&r)[4]) {
+  asm("{ .reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
 }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {

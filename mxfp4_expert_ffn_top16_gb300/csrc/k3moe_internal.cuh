@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -18,6 +19,12 @@ namespace k3moe {
 // Cached by its arguments. Returns false if the driver entry point or the encoding fails.
 bool make_tmap_2d(CUtensorMap* out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
                   uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+// 3-D view of a row-major [rows][nchunks * chunk] array as {chunk, rows, nchunks}: one box of
+// {chunk, box_rows, box_chunks} lands as box_chunks consecutive [box_rows][chunk] tiles, so a
+// single copy fetches several K-tiles of the same rows.
+bool make_tmap_3d_chunks(CUtensorMap* out, const void* base, int elem_bytes, uint64_t chunk, uint64_t rows,
+                         uint64_t pitch_bytes, uint64_t nchunks, uint32_t box_rows, uint32_t box_chunks,
+                         bool swizzle128);
 
 // ------------------------------------------------------------------ error word
 // Bits of the uint32 error word at offset 0 of the workspace.
@@ -76,6 +83,11 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
                            int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s);
 cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,
                         cudaStream_t s);
+// Top-k + permutation + plan in one block, for T <= kSmallRouteTokens.
+constexpr int kSmallRouteTokens = 64;
+cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                                    int32_t* offsets, int32_t* row_token, int32_t* row_slot,
+                                    int32_t* slot_row, int32_t* plan, uint32_t* err, cudaStream_t s);
 cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,
                             cudaStream_t s);
 cudaError_t launch_expert_glu(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
@@ -89,5 +101,27 @@ cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const f
                            int k, int L, uint16_t* c, cudaStream_t s);
 
 int num_sms();
+
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device,
+// calling the runtime only the first time (or when more is needed), so launches stay cheap.
+cudaError_t ensure_smem_attr(const void* fn, size_t bytes);
+
+// Launch with programmatic stream serialization (the kernel must call pdl_wait() before its
+// first global memory access).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace k3moe

@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   const int KC = 64 * NB;
   const int nkc = K / KC;
@@ -93,14 +95,11 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
       for (int ch = 0; ch < nchunks && ok; ++ch) {
         for (int kc = 0; kc < nkc; ++kc) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
-          if (lane == 0) {
+          if (lane == 0) {  // one copy for the NB weight tiles, one for the NB token tiles
             mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
             uint8_t* dst = stages + s * stage_bytes;
-            for (int b = 0; b < NB; ++b) {
-              const int x = kc * KC + b * 64;
-              tma_load_2d(dst + b * wbox, &args.tw[pi], x, row0, &full[s]);
-              tma_load_2d(dst + NB * wbox + b * xbox, &args.tx, x, ch * ntok, &full[s]);
-            }
+            tma_load_3d(dst, &args.tw[pi], 0, row0, kc * NB, &full[s]);
+            tma_load_3d(dst + NB * wbox, &args.tx, 0, ch * ntok, kc * NB, &full[s]);
           }
           __syncwarp();
           if (++s == NS) { s = 0; ph ^= 1; }
@@ -236,19 +235,18 @@ cudaError_t launch_t(DenseArgs& a, const uint16_t* const W[2], const int N[2], c
   const int stage_bytes = a.NB * (kUnitRows * 128 + ntok * 128);
   a.NS = NTT <= 2 ? 3 : 4;
   for (int i = 0; i < 2; ++i)
-    if (W[i] && !make_tmap_2d(&a.tw[i], W[i], 2, (uint64_t)a.K, (uint64_t)N[i], (uint64_t)a.K * 2, 64,
-                              kUnitRows, true))
+    if (W[i] && !make_tmap_3d_chunks(&a.tw[i], W[i], 2, 64, (uint64_t)N[i], (uint64_t)a.K * 2,
+                                     (uint64_t)kt, kUnitRows, (uint32_t)a.NB, true))
       return cudaErrorInvalidValue;
-  if (!make_tmap_2d(&a.tx, x, 2, (uint64_t)a.K, (uint64_t)a.T, (uint64_t)a.K * 2, 64, ntok, true))
+  if (!make_tmap_3d_chunks(&a.tx, x, 2, 64, (uint64_t)a.T, (uint64_t)a.K * 2, (uint64_t)kt, ntok,
+                           (uint32_t)a.NB, true))
     return cudaErrorInvalidValue;
   const size_t smem = (size_t)a.NS * stage_bytes + (size_t)kConsumerWarps * kUnitRows * ntok * sizeof(float) +
                       (2 * kMaxStages + 1) * sizeof(uint64_t) + 16 + 1024;
-  cudaError_t e = cudaFuncSetAttribute(dense_gemv_kernel<NTT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(dense_gemv_kernel<NTT>), smem);
   if (e != cudaSuccess) return e;
   const int grid = a.units < num_sms() ? a.units : num_sms();
-  dense_gemv_kernel<NTT><<<grid, kThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(dense_gemv_kernel<NTT>, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
 }  // namespace

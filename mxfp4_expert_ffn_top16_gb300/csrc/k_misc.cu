@@ -13,6 +13,8 @@ namespace {
 // ("kimi-k3-mlx", LatentMoE).
 __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_row,
                                const float* __restrict__ w, int T, int k, int L, uint16_t* c) {
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.y;
   const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (t >= T || n >= L) return;
@@ -66,8 +68,7 @@ cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const f
                            int k, int L, uint16_t* c, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   dim3 grid((L / 4 + 127) / 128, T);
-  combine_kernel<<<grid, 128, 0, s>>>(o_rows, slot_row, w, T, k, L, c);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, grid, dim3(128), 0, s, o_rows, slot_row, w, T, k, L, c);
 }
 
 cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,

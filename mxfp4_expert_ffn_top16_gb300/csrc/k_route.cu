@@ -22,13 +22,13 @@ namespace {
 constexpr int kMaxE = 1024;
 constexpr int kMaxPerLane = kMaxE / 32;
 
-__device__ __forceinline__ unsigned long long sort_key(float v, int idx) {
+// Order-preserving 32-bit key of a logit: larger logit -> larger key. -0 equals +0; NaN gets
+// 1, below every number (numbers map to >= 0x007fffff); 0 marks an empty or taken slot.
+__device__ __forceinline__ uint32_t sort_key(float v) {
   uint32_t u = __float_as_uint(v);
-  if (v == 0.0f) u = 0u;                    // -0 == +0
-  uint32_t key;
-  if (v != v) key = 0u;                      // NaN below everything
-  else key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return ((unsigned long long)key << 32) | (uint32_t)(0xffffffffu - (uint32_t)idx);
+  if (v == 0.0f) u = 0u;
+  if (v != v) return 1u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
@@ -44,28 +44,36 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
 // (*sel_idx, *sel_logit) = the j-th largest; returns nothing for lanes >= k.
 __device__ void warp_topk(const float* __restrict__ lg, int E, int k, int lane, int* sel_idx,
                           float* sel_logit) {
-  unsigned long long keys[kMaxPerLane];
+  // slot j of this lane holds expert lane + 32 j; within a lane the lowest j wins ties
+  uint32_t keys[kMaxPerLane];
   const int per = (E + 31) / 32;
 #pragma unroll
   for (int j = 0; j < kMaxPerLane; ++j) {
     const int e = lane + 32 * j;
-    keys[j] = (j < per && e < E) ? sort_key(lg[e], e) : 0ull;
+    keys[j] = (j < per && e < E) ? sort_key(lg[e]) : 0u;
   }
-  unsigned long long best = 0ull;
+  // (key, inverted expert index) of this lane's best remaining slot
+  auto local_best = [&]() -> unsigned long long {
+    uint32_t bk = 0u;
+    int bj = 0;
 #pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j) best = keys[j] > best ? keys[j] : best;
+    for (int j = 0; j < kMaxPerLane; ++j)
+      if (keys[j] > bk) { bk = keys[j]; bj = j; }
+    return bk == 0u ? 0ull
+                    : ((unsigned long long)bk << 32) | (uint32_t)(0xffffffffu - (uint32_t)(lane + 32 * bj));
+  };
+  unsigned long long best = local_best();
   int my_idx = -1;
   for (int r = 0; r < k; ++r) {
     const unsigned long long win = warp_max_u64(best);
     const int widx = (int)(0xffffffffu - (uint32_t)(win & 0xffffffffu));
     if (lane == r) my_idx = widx;
-    if ((widx & 31) == lane) {  // owner removes it and rescans
-      best = 0ull;
+    if ((widx & 31) == lane) {  // owner takes the slot and rescans
+      const int wj = widx >> 5;
 #pragma unroll
-      for (int j = 0; j < kMaxPerLane; ++j) {
-        if (keys[j] == win) keys[j] = 0ull;
-        best = keys[j] > best ? keys[j] : best;
-      }
+      for (int j = 0; j < kMaxPerLane; ++j)
+        if (j == wj) keys[j] = 0u;
+      best = local_best();
     }
   }
   *sel_idx = my_idx;
@@ -190,7 +198,10 @@ __device__ void warp_scatter(const int32_t* __restrict__ idx, int t0, int t1, in
 
 // ---------------------------------------------------------------- single-CTA permutation
 // For T*k small: histogram, scan, scatter and plan in one block of 1024 threads.
-__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __restrict__ idx, int T,
+// With `logits` given, the block first selects the top-k of each token (one warp per token)
+// into idx / w, so decode routing is a single launch.
+__global__ void __launch_bounds__(1024) permute_small_kernel(const float* __restrict__ logits,
+                                                             float* w, int32_t* idx, int T,
                                                              int E, int k, int32_t* offsets,
                                                              int32_t* row_token, int32_t* row_slot,
                                                              int32_t* slot_row, int32_t* plan,
@@ -201,6 +212,18 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* __re
   __shared__ int chunks[kMaxE];
   __shared__ unsigned mask[kMaxE];
   const int tid = threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
+  if (logits) {
+    const int lane = tid & 31;
+    for (int t = tid >> 5; t < T; t += blockDim.x >> 5) {
+      int sel;
+      float l;
+      warp_topk(logits + (size_t)t * E, E, k, lane, &sel, &l);
+      warp_write_topk(sel, l, k, lane, idx + (size_t)t * k, w + (size_t)t * k, nullptr);
+    }
+    __syncthreads();
+  }
   if (tid <= E) cnt[tid] = 0;
   if (tid < E) mask[tid] = 0u;
   __syncthreads();
@@ -326,8 +349,8 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
                            int32_t* row_token, int32_t* row_slot, int32_t* slot_row,
                            int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s) {
   if (T <= kBlockTokens) {
-    permute_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, k, offsets, row_token, row_slot, slot_row,
-                                            plan, err);
+    permute_small_kernel<<<1, 1024, 0, s>>>(nullptr, nullptr, const_cast<int32_t*>(idx), T, E, k,
+                                            offsets, row_token, row_slot, slot_row, plan, err);
     return cudaGetLastError();
   }
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
@@ -335,6 +358,13 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
   scan_kernel<<<1, 1024, 0, s>>>(scratch, nblk, E, offsets, plan);
   scatter_kernel<<<nblk, 32, 0, s>>>(idx, T, E, k, scratch, row_token, row_slot, slot_row, err);
   return cudaGetLastError();
+}
+
+cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
+                                    int32_t* offsets, int32_t* row_token, int32_t* row_slot,
+                                    int32_t* slot_row, int32_t* plan, uint32_t* err, cudaStream_t s) {
+  return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, logits, w, idx, T, E, k, offsets,
+                    row_token, row_slot, slot_row, plan, err);
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,

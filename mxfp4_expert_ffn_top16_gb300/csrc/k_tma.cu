@@ -31,8 +31,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 struct Key {
   const void* base;
-  uint64_t inner, rows, pitch;
-  uint32_t box_inner, box_rows, elem, swz;
+  uint64_t inner, rows, pitch, chunks;  // chunks == 0: 2-D map
+  uint32_t box_inner, box_rows, box_chunks, elem, swz;
   bool operator==(const Key& o) const { return std::memcmp(this, &o, sizeof(Key)) == 0; }
 };
 
@@ -46,6 +46,38 @@ constexpr int kCache = 64;
 Entry g_cache[kCache];
 int g_next = 0;
 std::mutex g_mu;
+
+bool encode_cached(CUtensorMap* out, const Key& k) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < kCache; ++i)
+    if (g_cache[i].used && g_cache[i].key == k) {
+      *out = g_cache[i].map;
+      return true;
+    }
+  auto enc = get_encode();
+  if (!enc) return false;
+  const int rank = k.chunks ? 3 : 2;
+  // dim 0: `inner` contiguous elements; dim 1: rows `pitch` bytes apart; dim 2 (3-D only):
+  // consecutive chunks of `inner` elements along a row (inner * elem bytes apart)
+  cuuint64_t dims[3] = {k.inner, k.rows, k.chunks};
+  cuuint64_t strides[2] = {k.pitch, (cuuint64_t)k.inner * k.elem};
+  cuuint32_t box[3] = {k.box_inner, k.box_rows, k.box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMap m;
+  const CUresult r = enc(&m, k.elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                         (cuuint32_t)rank, const_cast<void*>(k.base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         k.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  Entry& e = g_cache[g_next];
+  g_next = (g_next + 1) % kCache;
+  e.key = k;
+  e.map = m;
+  e.used = true;
+  *out = m;
+  return true;
+}
 
 }  // namespace
 
@@ -61,31 +93,25 @@ bool make_tmap_2d(CUtensorMap* out, const void* base, int elem_bytes, uint64_t i
   k.box_rows = box_rows;
   k.elem = (uint32_t)elem_bytes;
   k.swz = swizzle128 ? 1u : 0u;
-  std::lock_guard<std::mutex> lock(g_mu);
-  for (int i = 0; i < kCache; ++i)
-    if (g_cache[i].used && g_cache[i].key == k) {
-      *out = g_cache[i].map;
-      return true;
-    }
-  auto enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {pitch_bytes};
-  cuuint32_t box[2] = {box_inner, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUtensorMap m;
-  const CUresult r = enc(&m, elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return false;
-  Entry& e = g_cache[g_next];
-  g_next = (g_next + 1) % kCache;
-  e.key = k;
-  e.map = m;
-  e.used = true;
-  *out = m;
-  return true;
+  return encode_cached(out, k);
+}
+
+bool make_tmap_3d_chunks(CUtensorMap* out, const void* base, int elem_bytes, uint64_t chunk, uint64_t rows,
+                         uint64_t pitch_bytes, uint64_t nchunks, uint32_t box_rows, uint32_t box_chunks,
+                         bool swizzle128) {
+  Key k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.inner = chunk;
+  k.rows = rows;
+  k.pitch = pitch_bytes;
+  k.chunks = nchunks;
+  k.box_inner = (uint32_t)chunk;
+  k.box_rows = box_rows;
+  k.box_chunks = box_chunks;
+  k.elem = (uint32_t)elem_bytes;
+  k.swz = swizzle128 ? 1u : 0u;
+  return encode_cached(out, k);
 }
 
 }  // namespace k3moe

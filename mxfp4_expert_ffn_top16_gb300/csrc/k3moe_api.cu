@@ -254,7 +254,7 @@ k3moe_status k3moe_route(const k3moe_dims* dims, const uint16_t* x, int32_t T,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(d, T);
   float* lg = logits ? logits : at<float>(ws, L.logits);
-  K3_CUDA(launch_dense_gemv(w_router, d.n_experts, lg, nullptr, bias, nullptr, 0, nullptr, nullptr,
+  K3_CUDA(launch_dense(w_router, d.n_experts, lg, nullptr, bias, nullptr, 0, nullptr, nullptr,
                             nullptr, 0, x, T, d.hidden, at<uint32_t>(ws, L.err), s));
   K3_CUDA(launch_topk(lg, T, d.n_experts, d.top_k, topk_idx, topk_w, s));
   return K3MOE_OK;
@@ -287,7 +287,7 @@ k3moe_status k3moe_project(const uint16_t* W, const uint16_t* x, int32_t T, int3
   if (!ws || ws_bytes < 256) return K3MOE_E_WORKSPACE;
   if (misaligned(ws)) return K3MOE_E_ALIGN;
   if (T == 0) return K3MOE_OK;
-  K3_CUDA(launch_dense_gemv(W, N, nullptr, out, nullptr, nullptr, 0, nullptr, nullptr, nullptr, 0,
+  K3_CUDA(launch_dense(W, N, nullptr, out, nullptr, nullptr, 0, nullptr, nullptr, nullptr, 0,
                             x, T, K, static_cast<uint32_t*>(ws), static_cast<cudaStream_t>(stream)));
   return K3MOE_OK;
 }
@@ -354,7 +354,7 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
   // router logits and z = bf16(W_in x) (+ its f16 block-scaled copy) in one pass over x
   {
     ProfScope p(P_ROUTER_LATENT, s);
-    K3_CUDA(launch_dense_gemv(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr,
+    K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr,
                               w.router_bias, w.w_in, d.latent, at<uint16_t>(ws, L.z),
                               at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), d.actq, x, T, d.hidden,
                               err, s));
@@ -362,7 +362,7 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
   K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s));
   {
     ProfScope p(P_LATENT_OUT, s);
-    K3_CUDA(launch_dense_gemv(w.w_out, d.hidden, nullptr, y, nullptr, nullptr, 0, nullptr, nullptr,
+    K3_CUDA(launch_dense(w.w_out, d.hidden, nullptr, y, nullptr, nullptr, 0, nullptr, nullptr,
                               nullptr, 0, at<uint16_t>(ws, L.c), T, d.latent, err, s));
   }
   return K3MOE_OK;

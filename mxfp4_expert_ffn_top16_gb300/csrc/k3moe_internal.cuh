@@ -76,6 +76,24 @@ cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint1
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
                               int K, uint32_t* err, cudaStream_t s);
+// Same contract as launch_dense_gemv, on tcgen05 tiles of 128 weight rows x 64 tokens (for
+// many tokens).
+cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
+                              const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
+                              __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
+                              uint32_t* err, cudaStream_t s);
+// Token count from which the dense projections use the tcgen05 tiles.
+constexpr int kUmmaDenseMinTokens = 65;
+inline cudaError_t launch_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
+                                const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
+                                __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
+                                uint32_t* err, cudaStream_t s) {
+  if (T >= kUmmaDenseMinTokens)
+    return launch_umma_dense(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
+                             T, K, err, s);
+  return launch_dense_gemv(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
+                           T, K, err, s);
+}
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s);
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* offsets,

@@ -1,0 +1,240 @@
+// Dense bf16 projections for many tokens (prefill) on the 5th-generation tensor cores:
+// router logits, latent in, latent out ("kimi-k3-mlx", Architecture table: router over 896
+// experts; Stable LatentMoE: 7168 -> 3584 -> 7168 around the routed experts).
+//
+//   out[t][n] = sum_k W[n][k] x[t][k]
+//
+// A persistent CTA walks 128 x 64 output tiles (128 weight rows on M, 64 tokens on N).
+// Warp 0 streams 128 x 64 bf16 tiles of W and 64 x 64 tiles of x through TMA (128-byte
+// swizzle) into a ring of stages. Warp 1 allocates 256 tensor-memory columns (four 64-column
+// accumulator slots) and issues tcgen05.mma kind::f16 (M=128, N=64, K=16, four per stage);
+// each group of 8 stages (512 of K) accumulates into one slot, which is committed to the
+// epilogue. Warps 2-5 (one tensor-memory lane = one weight row per thread) drain every slot
+// into per-thread Kahan-compensated fp32 sums, so the tensor core's own accumulation spans at
+// most 32 MMAs; after the last group they write fp32 + bias (logits), bf16 (z, y) and, for z,
+// the f16 block-scaled copy with one power-of-two exponent per 32 features (in MXFP8 mode of
+// the MXFP8 round trip).
+#include <cuda_fp16.h>
+
+#include "k3moe_device.cuh"
+#include "k3moe_internal.cuh"
+#include "k3moe_umma.cuh"
+
+namespace k3moe {
+namespace {
+
+constexpr int BM = 128, BN = 64, BK = 64, kStages = 6, kGroup = 8, kSlots = 4;
+constexpr int kATile = BM * BK * 2;  // 16 KB
+constexpr int kBTile = BN * BK * 2;  // 8 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = kSlots * BN;
+
+struct UProblem {
+  int N;
+  float* out_f32;
+  const float* bias;
+  uint16_t* out_bf16;
+  __half* out_h;
+  int8_t* out_s;
+  int actq;
+};
+
+struct UDenseArgs {
+  CUtensorMap tw[2];  // W of each problem: {K, N} bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap tx;     // tokens: {K, T} bf16, box {64, 64}, 128-byte swizzle
+  UProblem p[2];
+  int mt0, mtiles, ntiles;
+  int T, K;
+  uint32_t* err;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_constant__ UDenseArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kATile;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBTile);
+  uint64_t* empty = full + kStages;
+  uint64_t* accf = empty + kStages;
+  uint64_t* acce = accf + kSlots;
+  uint64_t* drain = acce + kSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kSlots; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t tmem = *tmem_slot;
+  const int items = a.mtiles * a.ntiles;
+  const int nk = a.K / BK;
+  const int ngroups = (nk + kGroup - 1) / kGroup;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------- TMA producer
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const int mt = it / a.ntiles, nt = it - mt * a.ntiles;
+        const int pi = mt < a.mt0 ? 0 : 1;
+        const int row0 = (pi ? mt - a.mt0 : mt) * BM;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, a.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kATile + kBTile);
+          tma_load_2d(sA + s * kATile, &a.tw[pi], kb * BK, row0, &full[s]);
+          tma_load_2d(sB + s * kBTile, &a.tx, kb * BK, nt * BN, &full[s]);
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int s = 0, slot = 0;
+      uint32_t ph = 0, sph = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        for (int gi = 0; gi < ngroups && ok; ++gi) {
+          if (!mbar_wait_bounded(&acce[slot], sph ^ 1, abort_flag, a.err)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(slot * BN);
+          const int kb1 = min(nk, (gi + 1) * kGroup);
+          for (int kb = gi * kGroup; kb < kb1; ++kb) {
+            if (!mbar_wait_bounded(&full[s], ph, abort_flag, a.err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              umma_bf16(d, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                        (kb != gi * kGroup || k != 0) ? 1u : 0u);
+            umma_commit(&empty[s]);
+            if (++s == kStages) { s = 0; ph ^= 1; }
+          }
+          if (!ok) break;
+          umma_commit(&accf[slot]);
+          if (++slot == kSlots) { slot = 0; sph ^= 1; }
+        }
+      }
+      // every issued MMA has completed before the tensor memory is released
+      umma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(drain, 0, &no_abort, a.err);
+    }
+  } else {  // ---------------- epilogue warps 2..5, lane quadrant = warp % 4
+    const int q = warp & 3;
+    int slot = 0;
+    uint32_t sph = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      const int mt = it / a.ntiles, nt = it - mt * a.ntiles;
+      const int pi = mt < a.mt0 ? 0 : 1;
+      const UProblem& P = a.p[pi];
+      const int row = (pi ? mt - a.mt0 : mt) * BM + q * 32 + lane;  // output feature
+      float sum[BN], cmp[BN];
+#pragma unroll
+      for (int j = 0; j < BN; ++j) sum[j] = cmp[j] = 0.f;
+      for (int gi = 0; gi < ngroups; ++gi) {
+        if (!mbar_wait_bounded(&accf[slot], sph, abort_flag, a.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BN + c), v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float yk = __uint_as_float(v[j]) - cmp[c + j];
+            const float tk = sum[c + j] + yk;
+            cmp[c + j] = (tk - sum[c + j]) - yk;
+            sum[c + j] = tk;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce[slot]);
+        if (++slot == kSlots) { slot = 0; sph ^= 1; }
+      }
+      if (!ok) break;
+      const bool valid = row < P.N;
+      const float bias = (P.bias && valid) ? P.bias[row] : 0.f;
+#pragma unroll
+      for (int j = 0; j < BN; ++j) {
+        const int tok = nt * BN + j;
+        if (tok >= a.T) continue;  // uniform across the warp
+        const float val = sum[j] - cmp[j];
+        if (P.out_f32 && valid) P.out_f32[(size_t)tok * P.N + row] = val + bias;
+        if (P.out_bf16) {
+          const uint16_t vb = f32_to_bf16(val);
+          if (valid) P.out_bf16[(size_t)tok * P.N + row] = vb;
+          if (P.out_h) {  // N multiple of 32: the warp's 32 rows are one block
+            float qv = bf16_to_f32(vb);
+            if (P.actq) qv = mxfp8_roundtrip(qv, mxfp8_block_exp(warp_max(fabsf(qv))));
+            const int e = f16_block_exp(warp_max(fabsf(qv)));
+            P.out_h[(size_t)tok * P.N + row] = __float2half_rn(ldexpf(qv, -e));
+            if (lane == 0) P.out_s[(size_t)tok * exp_pitch(P.N) + row / 32] = (int8_t)e;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kATile + kBTile) + (2 * kStages + 2 * kSlots + 1) * 8 + 16;
+
+}  // namespace
+
+cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
+                              const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
+                              __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
+                              uint32_t* err, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  UDenseArgs a{};
+  a.p[0] = UProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0};
+  a.p[1] = UProblem{N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1};
+  a.mt0 = W0 ? (N0 + BM - 1) / BM : 0;
+  a.mtiles = a.mt0 + (W1 ? (N1 + BM - 1) / BM : 0);
+  a.ntiles = (T + BN - 1) / BN;
+  a.T = T;
+  a.K = K;
+  a.err = err;
+  const uint16_t* W[2] = {W0, W1};
+  const int N[2] = {N0, N1};
+  for (int i = 0; i < 2; ++i)
+    if (W[i] && !make_tmap_2d(&a.tw[i], W[i], 2, (uint64_t)K, (uint64_t)N[i], (uint64_t)K * 2, BK, BM, true))
+      return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&a.tx, x, 2, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK, BN, true))
+    return cudaErrorInvalidValue;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_dense_kernel), kSmem);
+  if (e != cudaSuccess) return e;
+  const int items = a.mtiles * a.ntiles;
+  const int grid = items < num_sms() ? items : num_sms();
+  return launch_pdl(umma_dense_kernel, dim3(grid), dim3(kThreads), kSmem, s, a);
+}
+
+}  // namespace k3moe

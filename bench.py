@@ -104,18 +104,54 @@ def algorithmic(d, T, distinct_experts):
     return dense_w + expert + act, flops
 
 
-def kernel_bytes(name, d, T, distinct, rows):
-    """Algorithmic bytes of one launch of a profiled kernel."""
+def kernel_cost(name, d, T, distinct, rows, actq):
+    """Algorithmic (bytes, flops, tensor dtype) of one launch of a profiled kernel: weights read
+    once per launch, activations read and results written once."""
     L, I, H, E = d.latent, d.inter, d.hidden, d.n_experts
     glu_w = 2 * (d.gate_q_bytes + d.gate_s_bytes)
     down_w = d.down_q_bytes + d.down_s_bytes
-    return {
-        "router_latent_in_gemv": 2 * (E + L) * H + 2 * T * H + 4 * T * E + 2 * T * L * 2,
-        "latent_out_gemv": 2 * H * L + 2 * T * L + 2 * T * H,
-        "expert_glu_gemv": distinct * glu_w + rows * (2 * L + 4 * I),
-        "expert_down_gemv": distinct * down_w + rows * (2 * I + 4 * L),
-        "combine": rows * 4 * L + 2 * T * L,
-    }.get(name)
+    P = 1 if actq else 2  # e4m3 rows per activation row on the tensor-core expert path
+    gemv = T < 65
+    table = {
+        # router logits fp32 + z bf16 (+ its f16 block-scaled copy on the GEMV path)
+        "router_latent_in": (2 * (E + L) * H + 2 * T * H + 4 * T * E + 2 * T * L * (2 if gemv else 1),
+                             2 * T * (E + L) * H, "bf16"),
+        "latent_out": (2 * H * L + 2 * T * L + 2 * T * H, 2 * T * H * L, "bf16"),
+        "expert_glu_gemv": (distinct * glu_w + rows * (2 * L + 4 * I), 4 * rows * L * I, None),
+        "expert_down_gemv": (distinct * down_w + rows * (2 * I + 4 * L), 2 * rows * L * I, None),
+        "expert_act_quant": (rows * 2 * L + P * rows * (L + L // 32), 0, None),
+        "expert_glu_mma": (distinct * glu_w + P * rows * (L + L // 32) + P * rows * (I + I // 32),
+                           4 * rows * L * I, "fp8"),
+        "expert_down_mma": (distinct * down_w + P * rows * (I + I // 32) + 4 * rows * L,
+                            2 * rows * L * I, "fp8"),
+        "combine": (rows * 4 * L + 2 * T * L, 0, None),
+    }
+    return table.get(name, (None, 0, None))
+
+
+def roofline(name, per_launch_ms, cost, pk):
+    """Roofline entry of a kernel: HBM-bound unless its algorithmic flops at the tensor peak of
+    its dtype take longer than its bytes at the copy bandwidth. fp8 (the block-scaled
+    e2m1 x e4m3 MMA rate) = measured bf16 x 2, the nominal dense ratio (4.5 / 2.25 PFLOP/s)."""
+    kb, fl, dt = cost
+    if not kb:
+        return {"bound": "hbm", "kernel": name, "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": None, "traffic": None}
+    t = per_launch_ms / 1e3
+    tensor_peak = pk["bf16_tflops"] * (2.0 if dt == "fp8" else 1.0) if dt else None
+    t_hbm = kb / (pk["hbm_gbs"] * 1e9)
+    t_tc = fl / (tensor_peak * 1e12) if tensor_peak else 0.0
+    if tensor_peak and t_tc > t_hbm:
+        ach = fl / t / 1e12
+        return {"bound": "tensor", "kernel": name, "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": ach / tensor_peak, "traffic": None,
+                "peak_src": pk["src"] + f" bf16 burst{' x 2 (fp8 nominal ratio)' if dt == 'fp8' else ''}",
+                "algorithmic_flops_per_launch": fl, "avg_launch_ms": per_launch_ms}
+    ach = kb / t / 1e9
+    return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": ach / pk["hbm_gbs"], "traffic": None, "peak_src": pk["src"] + " (burst copy)",
+            "algorithmic_bytes_per_launch": kb, "avg_launch_ms": per_launch_ms,
+            "tensor_frac": (fl / t / 1e12 / tensor_peak) if tensor_peak else None}
 
 
 # ---------------------------------------------------------------- CPU oracle sample
@@ -339,8 +375,6 @@ def run_ours(args, w):
     top = max(prof.items(), key=lambda kv: kv[1][0])
     name, (tot_ms, launches) = top
     per_launch_ms = tot_ms / max(1, launches)
-    kb = kernel_bytes(name, d, T, distinct, T * d.top_k)
-    achieved = kb / (per_launch_ms / 1e3) / 1e9 if kb else None
     step_bytes, step_flops = algorithmic(d, T, distinct)
     kernels_per_step = {"permute": 1 if T <= 256 else 3}
     launches_total = sum(n for _, n in prof.values()) + \
@@ -356,15 +390,14 @@ def run_ours(args, w):
                    "router_bias": w.bias, "actq": "mxfp8" if args.actq else "bf16",
                    "l2": "expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 4 copies",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": (achieved / pk["hbm_gbs"]) if achieved else None,
-                     "traffic": None, "peak_src": pk["src"] + " (burst copy)",
-                     "algorithmic_bytes_per_launch": kb, "avg_launch_ms": per_launch_ms},
+        "roofline": roofline(name, per_launch_ms, kernel_cost(name, d, T, distinct, T * d.top_k, args.actq), pk),
         "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
                           "achieved_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
                           "frac_hbm": step_bytes / (ms / args.steps / 1e3) / 1e9 / pk["hbm_gbs"]},
-        "kernels": {n: {"ms_per_launch": (t / c if c else None), "launches": c,
-                        "share": t / sum(v[0] for v in prof.values())} for n, (t, c) in prof.items()},
+        "kernels": {n: dict(ms_per_launch=(t / c if c else None), launches=c,
+                            share=t / sum(v[0] for v in prof.values()),
+                            frac=roofline(n, t / max(1, c), kernel_cost(n, d, T, distinct, T * d.top_k, args.actq),
+                                          pk)["frac"]) for n, (t, c) in prof.items() if c},
         "distinct_experts_last_step": distinct,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * d.hidden * 2,
                 "d2h_bytes_per_step": T * d.hidden * 2},

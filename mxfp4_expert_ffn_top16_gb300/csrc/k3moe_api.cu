@@ -76,6 +76,13 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.o = take(rows * Lw * 4);
   L.c = take(Tt * Lw * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
+  if (umma_expert_ok(d, T)) {
+    const size_t P = d.actq ? 1 : 2;
+    L.bq = take(P * rows * Lw);
+    L.bs = take(P * rows * (size_t)exp_pitch(d.latent));
+    L.aq = take(P * rows * I);
+    L.aqs = take(P * rows * (size_t)exp_pitch(d.inter));
+  }
   L.total = off;
   return L;
 }
@@ -131,11 +138,13 @@ k3moe_status check_weights(const k3moe_weights* w, bool dense, bool experts) {
 
 // ---------------------------------------------------------------- diagnostic profiling
 enum ProfId {
-  P_ROUTER_LATENT = 0, P_TOPK, P_PERMUTE, P_GLU, P_DOWN, P_COMBINE, P_LATENT_OUT, P_COUNT
+  P_ROUTER_LATENT = 0, P_TOPK, P_PERMUTE, P_GLU, P_DOWN, P_COMBINE, P_LATENT_OUT, P_QUANT,
+  P_GLU_MMA, P_DOWN_MMA, P_COUNT
 };
-const char* const kProfNames[P_COUNT] = {"router_latent_in_gemv", "topk", "permute",
+const char* const kProfNames[P_COUNT] = {"router_latent_in", "topk", "permute",
                                          "expert_glu_gemv", "expert_down_gemv", "combine",
-                                         "latent_out_gemv"};
+                                         "latent_out", "expert_act_quant", "expert_glu_mma",
+                                         "expert_down_mma"};
 struct Profiler {
   bool on = false;
   static constexpr int kMax = 65536;
@@ -169,6 +178,40 @@ struct ProfScope {
     if ((expr) != cudaSuccess) return K3MOE_E_CUDA;    \
   } while (0)
 
+// Expert GEMMs for the sorted rows (plan already built): block-scaled tensor-core tiles for
+// many tokens, the GEMV on f16 copies (zh, zs already in ws) otherwise.
+k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const uint16_t* z, int32_t T,
+                              const int32_t* offsets, const int32_t* row_token, float* o_rows, void* ws,
+                              const WsLayout& L, cudaStream_t s) {
+  uint32_t* err = at<uint32_t>(ws, L.err);
+  int32_t* plan = at<int32_t>(ws, L.plan);
+  if (umma_expert_ok(d, T)) {
+    const int P = d.actq ? 1 : 2;
+    {
+      ProfScope p(P_QUANT, s);
+      K3_CUDA(launch_quant_rows(z, row_token, T * d.top_k, T, d.latent, P, at<uint8_t>(ws, L.bq),
+                                at<uint8_t>(ws, L.bs), err, s));
+    }
+    {
+      ProfScope p(P_GLU_MMA, s);
+      K3_CUDA(launch_umma_glu(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T,
+                              at<uint8_t>(ws, L.aq), at<uint8_t>(ws, L.aqs), err, s));
+    }
+    ProfScope p(P_DOWN_MMA, s);
+    K3_CUDA(launch_umma_down(d, w, plan, at<uint8_t>(ws, L.aq), at<uint8_t>(ws, L.aqs), P, T, o_rows, err, s));
+    return K3MOE_OK;
+  }
+  {
+    ProfScope p(P_GLU, s);
+    K3_CUDA(launch_expert_glu(d, w, plan, offsets, row_token, at<__half>(ws, L.zh), at<int8_t>(ws, L.zs),
+                              at<uint16_t>(ws, L.a), at<__half>(ws, L.ah), at<int8_t>(ws, L.as), T, err, s));
+  }
+  ProfScope p(P_DOWN, s);
+  K3_CUDA(launch_expert_down(d, w, plan, offsets, at<__half>(ws, L.ah), at<int8_t>(ws, L.as), o_rows, T, err,
+                             s));
+  return K3MOE_OK;
+}
+
 // Route + permute + experts + combine for T tokens whose logits / z are already in ws.
 k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int32_t T, void* ws,
                                 const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s) {
@@ -190,19 +233,8 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
                            at<int32_t>(ws, L.slot_row), at<int32_t>(ws, L.plan),
                            at<int32_t>(ws, L.perm), err, s));
   }
-  {
-    ProfScope p(P_GLU, s);
-    K3_CUDA(launch_expert_glu(d, w, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.offsets),
-                              at<int32_t>(ws, L.row_token), at<__half>(ws, L.zh),
-                              at<int8_t>(ws, L.zs), at<uint16_t>(ws, L.a), at<__half>(ws, L.ah),
-                              at<int8_t>(ws, L.as), T, err, s));
-  }
-  {
-    ProfScope p(P_DOWN, s);
-    K3_CUDA(launch_expert_down(d, w, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.offsets),
-                               at<__half>(ws, L.ah), at<int8_t>(ws, L.as), at<float>(ws, L.o),
-                               T, err, s));
-  }
+  K3_TRY(run_expert_gemms(d, w, at<uint16_t>(ws, L.z), T, at<int32_t>(ws, L.offsets),
+                          at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s));
   {
     ProfScope p(P_COMBINE, s);
     K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,
@@ -308,13 +340,10 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(d, T);
   uint32_t* err = at<uint32_t>(ws, L.err);
-  K3_CUDA(launch_act_prep(z, T, d.latent, d.actq, at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), s));
+  if (!umma_expert_ok(d, T))
+    K3_CUDA(launch_act_prep(z, T, d.latent, d.actq, at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), s));
   K3_CUDA(launch_plan(expert_offsets, d.n_experts, T * d.top_k, at<int32_t>(ws, L.plan), err, s));
-  K3_CUDA(launch_expert_glu(d, *weights, at<int32_t>(ws, L.plan), expert_offsets, row_token,
-                            at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), at<uint16_t>(ws, L.a),
-                            at<__half>(ws, L.ah), at<int8_t>(ws, L.as), T, err, s));
-  K3_CUDA(launch_expert_down(d, *weights, at<int32_t>(ws, L.plan), expert_offsets,
-                             at<__half>(ws, L.ah), at<int8_t>(ws, L.as), o_rows, T, err, s));
+  K3_TRY(run_expert_gemms(d, *weights, z, T, expert_offsets, row_token, o_rows, ws, L, s));
   return K3MOE_OK;
 }
 
@@ -351,13 +380,14 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
   int32_t* idx = topk_idx_out ? topk_idx_out : at<int32_t>(ws, L.idx);
   float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.wts);
   const k3moe_weights& w = *weights;
-  // router logits and z = bf16(W_in x) (+ its f16 block-scaled copy) in one pass over x
+  // router logits and z = bf16(W_in x) in one pass over x (+ the f16 block-scaled copy of z
+  // that the expert GEMV reads; the tensor-core expert path quantises z itself)
   {
     ProfScope p(P_ROUTER_LATENT, s);
-    K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr,
-                              w.router_bias, w.w_in, d.latent, at<uint16_t>(ws, L.z),
-                              at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), d.actq, x, T, d.hidden,
-                              err, s));
+    const bool f16_copy = !umma_expert_ok(d, T);
+    K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr, w.router_bias, w.w_in,
+                         d.latent, at<uint16_t>(ws, L.z), f16_copy ? at<__half>(ws, L.zh) : nullptr,
+                         f16_copy ? at<int8_t>(ws, L.zs) : nullptr, d.actq, x, T, d.hidden, err, s));
   }
   K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s));
   {

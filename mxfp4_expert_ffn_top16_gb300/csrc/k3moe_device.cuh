@@ -216,6 +216,17 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
   return r;
 }
 
+// Bounded wait by a whole warp: lane 0 polls, the result goes to every lane, and the warp
+// synchronises, so the lanes never part ways on a timeout and all see what lane 0 acquired.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                               uint32_t* err) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait_bounded(bar, parity, abort, err);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
+
 // Barrier over a fixed group of warps (the mbarrier's arrival count = number of warps; lane 0
 // of each warp arrives after the warp synchronises), with the same bounded wait as the
 // pipeline barriers, so a group member that gave up cannot strand the others. `phase` is the
@@ -225,6 +236,16 @@ __device__ __forceinline__ bool group_barrier(uint64_t* bar, uint32_t& phase, vo
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
   const bool ok = mbar_wait_bounded(bar, phase, abort, err);
+  phase ^= 1u;
+  return ok;
+}
+
+// group_barrier with a warp-wide wait (mbar_wait_warp): every lane leaves with the same result.
+__device__ __forceinline__ bool group_barrier_warp(uint64_t* bar, uint32_t& phase, volatile int* abort,
+                                                   uint32_t* err) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait_warp(bar, phase, abort, err);
   phase ^= 1u;
   return ok;
 }

@@ -25,6 +25,12 @@ bool make_tmap_2d(CUtensorMap* out, const void* base, int elem_bytes, uint64_t i
 bool make_tmap_3d_chunks(CUtensorMap* out, const void* base, int elem_bytes, uint64_t chunk, uint64_t rows,
                          uint64_t pitch_bytes, uint64_t nchunks, uint32_t box_rows, uint32_t box_chunks,
                          bool swizzle128);
+// Packed e2m1 codes, `inner` 4-bit codes per row `pitch_bytes` apart (16U4_ALIGN16B): a box of
+// 128 codes x box_rows rows lands as box_rows rows of 128 bytes (each 8 bytes of codes padded to
+// 16), 128-byte swizzle; the copy counts inner/2 bytes per row. `inner` and the pitch must be
+// multiples of 128 codes and 16 bytes.
+bool make_tmap_fp4(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                   uint32_t box_rows);
 
 // ------------------------------------------------------------------ error word
 // Bits of the uint32 error word at offset 0 of the workspace.
@@ -43,6 +49,9 @@ struct WsLayout {
   size_t o;             // fp32 expert outputs per sorted row
   size_t c;             // bf16 combined latent
   size_t perm;          // int32 per-block histograms of the multi-block permutation
+  // block-scaled tensor-core expert path (only when umma_expert_ok): per sorted row, P e4m3
+  // rows of z and of the GLU output with e8m0 scales per 32 (row pitch exp_pitch bytes)
+  size_t bq, bs, aq, aqs;
   size_t total;
 };
 WsLayout ws_layout(const k3moe_dims& d, int64_t T);
@@ -66,8 +75,17 @@ inline __host__ __device__ size_t plan_ctab_offset(int E) { return (plan_ints(E)
 inline __host__ __device__ int4* plan_ctab(int32_t* plan, int E) {
   return reinterpret_cast<int4*>(reinterpret_cast<char*>(plan) + plan_ctab_offset(E));
 }
-inline __host__ __device__ size_t plan_bytes(int E, long long rows) {
+// A second table for the tensor-core expert GEMM follows: entry 0 = {chunks C64, 0, 0, 0},
+// entries 1..C64 = {expert, first sorted row, rows (<= kUmmaChunkRows), 0}.
+constexpr int kUmmaChunkRows = 64;
+inline __host__ __device__ size_t plan_ctab64_offset(int E, long long rows) {
   return plan_ctab_offset(E) + (size_t)(rows / kGemvTokens + E + 1) * 16;
+}
+inline __host__ __device__ int4* plan_ctab64(int32_t* plan, int E, long long rows) {
+  return reinterpret_cast<int4*>(reinterpret_cast<char*>(plan) + plan_ctab64_offset(E, rows));
+}
+inline __host__ __device__ size_t plan_bytes(int E, long long rows) {
+  return plan_ctab64_offset(E, rows) + (size_t)(rows / kUmmaChunkRows + E + 2) * 16;
 }
 
 // ------------------------------------------------------------------ launchers
@@ -115,6 +133,21 @@ cudaError_t launch_expert_glu(const k3moe_dims& d, const k3moe_weights& w, const
 cudaError_t launch_expert_down(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
                                const int32_t* offsets, const __half* ah, const int8_t* as,
                                float* o_rows, int T, uint32_t* err, cudaStream_t s);
+// Block-scaled tensor-core expert GEMMs (many tokens). Usable when latent and inter are
+// multiples of 128 and T >= kUmmaExpertMinTokens. P = 2 (bf16 activations as e4m3 hi + lo) or
+// 1 (MXFP8 activations).
+constexpr int kUmmaExpertMinTokens = 65;
+inline bool umma_expert_ok(const k3moe_dims& d, long long T) {
+  return T >= kUmmaExpertMinTokens && d.latent % 128 == 0 && d.inter % 128 == 0;
+}
+// z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)].
+cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
+                              uint8_t* bq, uint8_t* bs, uint32_t* err, cudaStream_t s);
+cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
+                            const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
+                            cudaStream_t s);
+cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
+                             const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s);
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s);
 

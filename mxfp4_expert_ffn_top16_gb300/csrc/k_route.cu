@@ -131,11 +131,15 @@ __device__ int block_excl_scan(int* cnt, int n, int* tmp) {
   return total;
 }
 
-// Plan from offsets[E+1] held in shared memory: active experts, chunk prefix, and the chunk
-// table ctab[c] = {expert, first sorted row, rows (<= 8), 0} in expert order.
-__device__ void build_plan(const int* off, int E, int32_t* plan, int4* ctab, int* tmp, int* flag,
+// Plan from offsets[E+1] held in shared memory: active experts, chunk prefix, the chunk
+// table ctab[c] = {expert, first sorted row, rows (<= 8), 0} in expert order, and the table of
+// chunks of up to kUmmaChunkRows rows for the tensor-core expert GEMM. rows_max = T * k fixes
+// where the second table sits.
+__device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, int* tmp, int* flag,
                            int* chunks) {
   const int tid = threadIdx.x;
+  int4* ctab = plan_ctab(plan, E);
+  int4* ctab64 = plan_ctab64(plan, E, rows_max);
   const int m = tid < E ? off[tid + 1] - off[tid] : 0;
   if (tid < E) {
     flag[tid] = m > 0 ? 1 : 0;
@@ -155,6 +159,15 @@ __device__ void build_plan(const int* off, int E, int32_t* plan, int4* ctab, int
     plan[1] = C;
     plan[2 + E + D] = C;
   }
+  __syncthreads();
+  if (tid < E) flag[tid] = (m + kUmmaChunkRows - 1) / kUmmaChunkRows;
+  __syncthreads();
+  const int C64 = block_excl_scan(flag, E, tmp);
+  if (tid < E)
+    for (int q = 0; q * kUmmaChunkRows < m; ++q)
+      ctab64[1 + flag[tid] + q] =
+          make_int4(tid, off[tid] + q * kUmmaChunkRows, min(kUmmaChunkRows, m - q * kUmmaChunkRows), 0);
+  if (tid == 0) ctab64[0] = make_int4(C64, 0, 0, 0);
 }
 
 // Scatter of tokens [t0, t1) by one warp, given base[e] = first free row of each expert.
@@ -238,7 +251,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const float* __rest
   if (tid <= E) offsets[tid] = cnt[tid];
   __syncthreads();
   // plan reads the offsets before the scatter turns cnt into running bases
-  build_plan(cnt, E, plan, plan_ctab(plan, E), tmp, flag, chunks);
+  build_plan(cnt, E, T * k, plan, tmp, flag, chunks);
   __syncthreads();
   if (tid < 32) warp_scatter(idx, 0, T, E, k, cnt, mask, row_token, row_slot, slot_row, err);
 }
@@ -262,8 +275,8 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
 
 // One block of 1024 threads: per-expert running sums over token blocks -> offsets, then
 // hist[b][e] becomes the first row of expert e for token block b; plan from offsets.
-__global__ void __launch_bounds__(1024) scan_kernel(int32_t* hist, int nblk, int E, int32_t* offsets,
-                                                    int32_t* plan) {
+__global__ void __launch_bounds__(1024) scan_kernel(int32_t* hist, int nblk, int E, int rows_max,
+                                                    int32_t* offsets, int32_t* plan) {
   __shared__ int cnt[kMaxE + 1];
   __shared__ int tmp[1024];
   __shared__ int flag[kMaxE];
@@ -287,7 +300,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* hist, int nblk, int
     }
   }
   __syncthreads();
-  build_plan(cnt, E, plan, plan_ctab(plan, E), tmp, flag, chunks);
+  build_plan(cnt, E, rows_max, plan, tmp, flag, chunks);
 }
 
 __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__ idx, int T, int E,
@@ -328,11 +341,12 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     if (threadIdx.x == 0) {
       plan[0] = 0;
       plan[1] = 0;
+      plan_ctab64(plan, E, rows_max)[0] = make_int4(0, 0, 0, 0);
       atomicOr(err, kErrIndex);
     }
     return;
   }
-  build_plan(off, E, plan, plan_ctab(plan, E), tmp, flag, chunks);
+  build_plan(off, E, rows_max, plan, tmp, flag, chunks);
 }
 
 }  // namespace
@@ -355,7 +369,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
   }
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
   hist_kernel<<<nblk, 256, 0, s>>>(idx, T, E, k, scratch);
-  scan_kernel<<<1, 1024, 0, s>>>(scratch, nblk, E, offsets, plan);
+  scan_kernel<<<1, 1024, 0, s>>>(scratch, nblk, E, T * k, offsets, plan);
   scatter_kernel<<<nblk, 32, 0, s>>>(idx, T, E, k, scratch, row_token, row_slot, slot_row, err);
   return cudaGetLastError();
 }

@@ -42,6 +42,7 @@ struct Entry {
   bool used;
 };
 
+constexpr uint32_t kElemFp4 = 0x41;
 constexpr int kCache = 64;
 Entry g_cache[kCache];
 int g_next = 0;
@@ -64,7 +65,11 @@ bool encode_cached(CUtensorMap* out, const Key& k) {
   cuuint32_t box[3] = {k.box_inner, k.box_rows, k.box_chunks};
   cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
-  const CUresult r = enc(&m, k.elem == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  // elem 1: bytes; 2: bf16; kElemFp4: e2m1 pairs, 16 codes (8 bytes) per 16-byte unit in shared memory
+  const CUtensorMapDataType dt = k.elem == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : k.elem == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+  const CUresult r = enc(&m, dt,
                          (cuuint32_t)rank, const_cast<void*>(k.base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE,
                          k.swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -93,6 +98,21 @@ bool make_tmap_2d(CUtensorMap* out, const void* base, int elem_bytes, uint64_t i
   k.box_rows = box_rows;
   k.elem = (uint32_t)elem_bytes;
   k.swz = swizzle128 ? 1u : 0u;
+  return encode_cached(out, k);
+}
+
+bool make_tmap_fp4(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                   uint32_t box_rows) {
+  Key k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.inner = inner;
+  k.rows = rows;
+  k.pitch = pitch_bytes;
+  k.box_inner = 128;
+  k.box_rows = box_rows;
+  k.elem = kElemFp4;
+  k.swz = 1u;
   return encode_cached(out, k);
 }
 

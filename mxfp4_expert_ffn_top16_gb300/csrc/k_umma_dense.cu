@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_co
 #pragma unroll
       for (int j = 0; j < BN; ++j) sum[j] = cmp[j] = 0.f;
       for (int gi = 0; gi < ngroups; ++gi) {
-        if (!mbar_wait_bounded(&accf[slot], sph, abort_flag, a.err)) { ok = false; break; }
+        if (!mbar_wait_warp(&accf[slot], sph, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < BN; c += 32) {

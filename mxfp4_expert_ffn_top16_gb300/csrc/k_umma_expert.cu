@@ -1,0 +1,545 @@
+// MXFP4 expert FFN for many tokens on block-scaled 5th-generation tensor cores
+// (tcgen05.mma kind::mxf8f6f4.block_scale): the weights go into the tensor core as e2m1 codes
+// with their e8m0 scales, so no ALU work is spent per weight.
+//
+// "kimi-k3-in-c", MXFP4 experts: 4-bit codes indexing a 16-entry value table, one 8-bit
+// exponent per 32 consecutive weights; "Kimi K3 hardware deep dive", quantisation-aware
+// training: MXFP4 weights with MXFP8 activations. For sorted row r of expert e (token t):
+//   GLU pass:  a[r] = bf16(silu(G_e z_t) * (U_e z_t))          G_e, U_e [I][L]
+//   down pass: o[r] = D_e a[r]                                  D_e [L][I]
+//
+// Activations enter as e4m3 rows with one e8m0 scale per 32 values (P rows per sorted row):
+//   P = 1 (MXFP8 activations): the MXFP8 encoding itself (OCP MX v1.0: shared exponent
+//          floor(log2 amax) - 8, E4M3 elements rounded to nearest even, saturating).
+//   P = 2 (bf16 activations): hi = E4M3 rounding of v / 2^Xh with Xh = floor(log2 amax) - 7
+//          (no saturation: |v| / 2^Xh < 256), lo = v - hi on its own block exponent. bf16 has 8
+//          significant bits and each part carries 4, so hi + lo is the bf16 value exactly for
+//          every element within 2^-13 of its block maximum; below that the error is under
+//          2^-20 of the block maximum. The MMA sees both rows as B columns and the epilogue
+//          adds the two results.
+//
+// Tile: M = 128 weight rows (GLU: 64 gate rows and the 64 up rows of the same features, so
+// lane i and lane i + 64 pair up), N = P x (up to 64) activation rows, K = 128 per pipeline
+// stage (four MMAs of K = 32, each with its scale byte). Work item = (chunk of up to 64 sorted
+// rows of one expert, feature block), feature block fastest: the CTAs working at one time
+// share a chunk's activations and an expert's weights in L2.
+// Warp 0: producer. Its lanes gather each stage's scales with 4-byte cp.async straight into the
+// 32 x 16-byte block that tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l, word w =
+// the four K-block scales of row 32w + l), a few stages ahead; lane 0 then loads the packed
+// e2m1 weight tiles (16U4_ALIGN16B tensor map) and the e4m3 activation tiles, both with the
+// 128-byte swizzle. Warp 1: tensor-memory owner and MMA issuer. Accumulation restarts every
+// kGroup stages in one of three 128-column tensor-memory slots; warps 2-5 (one lane = one
+// weight row) add the slots up in fp32 and run the epilogue; the GLU epilogue transposes
+// through shared memory so each thread quantises one (sorted row, 32-feature block).
+#include <cuda_fp16.h>
+
+#include "k3moe_device.cuh"
+#include "k3moe_internal.cuh"
+#include "k3moe_umma.cuh"
+
+namespace k3moe {
+namespace {
+
+constexpr int BM = 128, BKE = 128;        // weight rows, K elements per stage
+constexpr int kStages = 6;
+constexpr int kATile = BM * BKE;          // bytes in shared memory (e2m1 padded to bytes)
+constexpr int kAPacked = BM * BKE / 2;    // bytes the copy transfers
+constexpr int kBTile = 128 * BKE;         // e4m3, up to 128 rows
+constexpr int kThreads = 192;
+constexpr int kSfSlots = 8;               // scale staging blocks (ring)
+constexpr int kPre = 3;                   // stages the scale gather runs ahead of the tile loads
+constexpr int kGroup = 4;                 // stages per tensor-memory accumulation slot
+constexpr int kAccSlots = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol = kAccSlots * 128;  // scale columns: 8 per staging block (A, then B)
+constexpr int kXPitch = 65;               // GLU exchange row pitch (floats)
+constexpr int kOut = kUmmaChunkRows;      // sorted rows per item (max)
+static_assert(kSfCol + 8 * kSfSlots <= kTmemCols, "tensor memory");
+static_assert(kSfSlots - kPre <= kStages, "scale ring must not hold back the tile ring");
+
+struct UExpertArgs {
+  CUtensorMap ta0;     // GLU: gate codes; down: down codes. {K codes, E*N rows}, box {128, 64|128}
+  CUtensorMap ta1;     // GLU: up codes
+  CUtensorMap tb;      // activation rows, e4m3 {K, P*rows}, box {128, 64*P}
+  const uint8_t* s0;   // weight scales [E][N][K/32]
+  const uint8_t* s1;   // GLU: up scales
+  const uint8_t* sb;   // activation scales [P*rows][exp_pitch(K)]
+  int32_t* plan;
+  int N, K, E;         // output features per expert, reduction length, experts
+  int rows_max;        // sorted rows (T * k)
+  uint8_t* aq;         // GLU: quantised output for the down pass [P*rows][N] e4m3
+  uint8_t* aqs;        //      its scales [P*rows][exp_pitch(N)]
+  float* o_out;        // down: [rows][N] fp32
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void umma_mx(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0; tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+// A e2m1, B e4m3, e8m0 scales, fp32 accumulation, both K-major; scale byte kk of each word.
+__device__ __forceinline__ uint32_t idesc_mx(int N, int kk) {
+  return ((uint32_t)kk << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(BM >> 4) << 24) | ((uint32_t)kk << 29);
+}
+// Descriptor of a 32 x 16-byte scale staging block: no swizzle, 8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+         ((uint64_t)1 << 46);
+}
+
+// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int n>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+}
+
+// Two values -> two E4M3 codes (nearest even, saturating), v0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float v0, float v1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
+  return r;
+}
+// Two E4M3 codes (low byte first) -> their values.
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t pair) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+// v * 2^e for e in [-254, 254] in two exact power-of-two steps.
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+  const int e1 = e / 2;
+  return v * exp2i(e1) * exp2i(e - e1);
+}
+// Block exponent of the hi / lo parts (amax / 2^X in [128, 256)); all-zero block: -127.
+__device__ __forceinline__ int split_block_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  if (!(amax <= 3.4028235e38f)) return 127;
+  const int X = ilog2_floor(amax) - 7;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+template <int P>
+__device__ __forceinline__ int block_exp(float amax) {
+  return P == 1 ? mxfp8_block_exp(amax) : split_block_exp(amax);
+}
+__device__ __forceinline__ float max_in_group4(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+}
+
+// One 32-value block (v, one thread) -> P rows of 32 E4M3 codes (8 words each) and block
+// exponents. P = 2: v is left holding the lo remainders.
+template <int P>
+__device__ __forceinline__ void quant_block32(float (&v)[32], uint32_t (&codes)[P][8], int (&X)[P]) {
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
+    X[p] = p == 0 ? block_exp<P>(am) : split_block_exp(am);
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const uint32_t c01 = e4m3x2(mul_pow2(v[i], -X[p]), mul_pow2(v[i + 1], -X[p]));
+      const uint32_t c23 = e4m3x2(mul_pow2(v[i + 2], -X[p]), mul_pow2(v[i + 3], -X[p]));
+      codes[p][i / 4] = c01 | (c23 << 16);
+      if (P == 2 && p == 0) {  // remainders for the lo row (exact)
+        const float2 h01 = e4m3x2_value(c01), h23 = e4m3x2_value(c23);
+        v[i] -= mul_pow2(h01.x, X[0]);
+        v[i + 1] -= mul_pow2(h01.y, X[0]);
+        v[i + 2] -= mul_pow2(h23.x, X[0]);
+        v[i + 3] -= mul_pow2(h23.y, X[0]);
+      }
+    }
+  }
+}
+
+template <bool GLU, int P>
+__global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_constant__ UExpertArgs A) {
+  constexpr int kFB = GLU ? 64 : 128;  // output features per item
+  constexpr int kBRows = 64 * P;       // activation rows per tile
+  constexpr uint32_t kBTx = kBRows * BKE;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int srow = A.K / 32, spb = exp_pitch(A.K);
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kStages * kATile;
+  uint8_t* stg = sB + kStages * kBTile;                        // kSfSlots x (512 A + 512 B)
+  float* xg = reinterpret_cast<float*>(stg + kSfSlots * 1024);  // GLU: [64][kXPitch]
+  uint64_t* full = reinterpret_cast<uint64_t*>(xg + (GLU ? 64 * kXPitch : 0));
+  uint64_t* empty = full + kStages;
+  uint64_t* accf = empty + kStages;
+  uint64_t* acce = accf + kAccSlots;
+  uint64_t* stgd = acce + kAccSlots;  // [kSfSlots] staging block free again
+  uint64_t* ebar = stgd + kSfSlots;   // epilogue group barrier
+  uint64_t* drain = ebar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < kAccSlots; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
+    }
+    for (int j = 0; j < kSfSlots; ++j) mbar_init(&stgd[j], 1);
+    mbar_init(ebar, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t tmem = *tmem_slot;
+
+  const int4* ctab = plan_ctab64(A.plan, A.E, A.rows_max);
+  const int C = ctab[0].x;
+  const int fbs = A.N / kFB;
+  const int items = (C > 0 && C <= A.rows_max / kUmmaChunkRows + A.E) ? C * fbs : 0;
+  const int nk = A.K / BKE;
+  const int ngroups = (nk + kGroup - 1) / kGroup;
+
+  // item u -> (expert, first sorted row, rows, first feature); false for a corrupt entry
+  auto item_of = [&](int u, int& e, int& r0, int& nr, int& f0) -> bool {
+    const int c = u / fbs, fb = u - c * fbs;
+    const int4 t = ctab[1 + c];
+    const bool ok = t.x >= 0 && t.x < A.E && t.y >= 0 && t.z > 0 && t.z <= kOut && t.y + t.z <= A.rows_max;
+    e = ok ? t.x : 0;
+    r0 = ok ? t.y : 0;
+    nr = ok ? t.z : 0;
+    f0 = fb * kFB;
+    return ok;
+  };
+
+  if (warp == 0) {  // ---------------- producer: scale gather (all lanes) and tile loads (lane 0)
+    // The scales of stage g go to staging block g mod kSfSlots in the layout tcgen05.cp reads:
+    // lane l, word w = the four K-block scales of row 32w + l. The gather runs kPre stages
+    // ahead through cp.async; a stage's tiles are requested once its scales have landed.
+    int pu = blockIdx.x, pkc = 0, pj = 0;
+    uint32_t pjph = 0;
+    int pe = 0, pr0 = 0, pnr = 0, pf0 = 0;
+    if (pu < items) item_of(pu, pe, pr0, pnr, pf0);
+    auto gather = [&]() -> bool {
+      if (pu < items) {
+        if (!mbar_wait_warp(&stgd[pj], pjph ^ 1, abort_flag, A.err)) return false;
+        uint8_t* st = stg + pj * 1024 + lane * 16;
+        const size_t wrow = (size_t)pe * A.N + pf0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int r = 32 * w + lane;
+          const uint8_t* src = (GLU && r >= 64) ? A.s1 + (wrow + r - 64) * srow : A.s0 + (wrow + r) * srow;
+          cp_async4(st + 4 * w, src + 4 * pkc, 4);
+          const bool vb = r < P * pnr;
+          cp_async4(st + 512 + 4 * w, vb ? A.sb + ((size_t)P * pr0 + r) * spb + 4 * pkc : A.sb, vb ? 4u : 0u);
+        }
+        if (++pkc == nk) {
+          pkc = 0;
+          pu += gridDim.x;
+          if (pu < items) item_of(pu, pe, pr0, pnr, pf0);
+        }
+        if (++pj == kSfSlots) { pj = 0; pjph ^= 1; }
+      }
+      cp_async_commit();  // one group per call, possibly empty
+      return true;
+    };
+    bool ok = true;
+    for (int i = 0; i < kPre && ok; ++i) ok = gather();
+    int s = 0;
+    uint32_t ph = 0;
+    for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+      int e, r0, nr, f0;
+      if (!item_of(u, e, r0, nr, f0) && lane == 0) atomicOr(A.err, kErrIndex);
+      const int wrow = e * A.N + f0;
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!gather()) { ok = false; break; }
+        cp_async_wait<kPre>();  // this lane's scale copies for stage (u, kc) have landed
+        fence_async_smem();
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&full[s], kAPacked + kBTx);
+          tma_load_2d(sA + s * kATile, &A.ta0, kc * BKE, wrow, &full[s]);
+          if (GLU) tma_load_2d(sA + s * kATile + 64 * 128, &A.ta1, kc * BKE, wrow, &full[s]);
+          tma_load_2d(sB + s * kBTile, &A.tb, kc * BKE, P * r0, &full[s]);
+        }
+        __syncwarp();
+        if (++s == kStages) { s = 0; ph ^= 1; }
+      }
+    }
+    cp_async_wait<0>();
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------- MMA issuer
+      int s = 0, slot = 0, j = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+        int e, r0, nr, f0;
+        item_of(u, e, r0, nr, f0);
+        int Nc = P * nr;
+        Nc = Nc < 16 ? 16 : ((Nc + 15) & ~15);
+        for (int gi = 0; gi < ngroups && ok; ++gi) {
+          if (!mbar_wait_bounded(&acce[slot], aph ^ 1, abort_flag, A.err)) { ok = false; break; }
+          const uint32_t d = tmem + (uint32_t)(slot * 128);
+          const int kc1 = min(nk, (gi + 1) * kGroup);
+          for (int kc = gi * kGroup; kc < kc1; ++kc) {
+            if (!mbar_wait_bounded(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t tsa = tmem + kSfCol + 8 * j, tsb = tsa + 4;
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa),
+                         "l"(sdesc_sf(smem_u32(stg + j * 1024))));
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb),
+                         "l"(sdesc_sf(smem_u32(stg + j * 1024 + 512))));
+            const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_mx(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_mx(Nc, kk), tsa, tsb,
+                      (kc != gi * kGroup || kk != 0) ? 1u : 0u);
+            umma_commit(&empty[s]);
+            umma_commit(&stgd[j]);
+            if (++s == kStages) { s = 0; ph ^= 1; }
+            if (++j == kSfSlots) j = 0;
+          }
+          if (!ok) break;
+          umma_commit(&accf[slot]);
+          if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
+        }
+      }
+      // every issued MMA has completed before the tensor memory is released
+      umma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(drain, 0, &no_abort, A.err);
+    }
+    __syncwarp();
+  } else {  // ---------------- epilogue warps 2..5, lane quadrant q = warp % 4
+    const int q = warp & 3;
+    const int lrow = q * 32 + lane;         // tile row = tensor-memory lane
+    const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue threads
+    int slot = 0;
+    uint32_t aph = 0, eph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+      int e, r0, nr, f0;
+      item_of(u, e, r0, nr, f0);
+      const int ncols = P * nr;
+      float sum[kOut];
+#pragma unroll
+      for (int i = 0; i < kOut; ++i) sum[i] = 0.f;
+      for (int gi = 0; gi < ngroups; ++gi) {
+        if (!mbar_wait_warp(&accf[slot], aph, abort_flag, A.err)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * 128);
+#pragma unroll
+        for (int c = 0; c < P * kOut / 32; ++c) {
+          if (c * 32 < ncols) {  // warp-uniform
+            uint32_t v[32];
+            tmem_ld32(base + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32 / P; ++i) {
+              float x = __uint_as_float(v[P * i]);
+              if (P == 2) x += __uint_as_float(v[P * i + 1]);
+              sum[c * (32 / P) + i] += x;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce[slot]);
+        if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
+      }
+      if (!ok) break;
+      if (GLU) {
+        // 1. gate rows (lanes 0..63) park their sums; 2. the up row of the same feature forms
+        // a = bf16(silu(gate) * up) in place; 3. every epilogue thread quantises one
+        // (sorted row, 32-feature block) of a into P e4m3 rows for the down pass.
+        if (q < 2) {
+#pragma unroll
+          for (int jr = 0; jr < kOut; ++jr)
+            if (jr < nr) xg[lrow * kXPitch + jr] = sum[jr];
+        }
+        if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
+        if (q >= 2) {
+          float* xr = xg + (lrow - 64) * kXPitch;
+#pragma unroll
+          for (int jr = 0; jr < kOut; ++jr) {
+            if (jr < nr) {
+              const float g = xr[jr];
+              xr[jr] = bf16_to_f32(f32_to_bf16(g / (1.0f + expf(-g)) * sum[jr]));
+            }
+          }
+        }
+        if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
+        const int jr = et & 63, b = et >> 6;
+        if (jr < nr) {
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = xg[(32 * b + i) * kXPitch + jr];
+          uint32_t codes[P][8];
+          int X[P];
+          quant_block32<P>(v, codes, X);
+          const int spo = exp_pitch(A.N);
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            const size_t brow = (size_t)P * (r0 + jr) + p;
+            uint4* dst = reinterpret_cast<uint4*>(A.aq + brow * A.N + f0 + 32 * b);
+            dst[0] = make_uint4(codes[p][0], codes[p][1], codes[p][2], codes[p][3]);
+            dst[1] = make_uint4(codes[p][4], codes[p][5], codes[p][6], codes[p][7]);
+            A.aqs[brow * spo + (f0 + 32 * b) / 32] = (uint8_t)(X[p] + 127);
+          }
+        }
+        if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
+      } else {
+#pragma unroll
+        for (int jr = 0; jr < kOut; ++jr)
+          if (jr < nr) A.o_out[(size_t)(r0 + jr) * A.N + f0 + lrow] = sum[jr];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool GLU, int P>
+size_t smem_bytes() {
+  return 1024 + (size_t)kStages * (kATile + kBTile) + kSfSlots * 1024 + (GLU ? 64 * kXPitch * 4 : 0) +
+         (2 * kStages + 2 * kAccSlots + kSfSlots + 2) * 8 + 16;
+}
+
+template <bool GLU, int P>
+cudaError_t launch_t(UExpertArgs& a, int items_max, cudaStream_t s) {
+  const size_t smem = smem_bytes<GLU, P>();
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_expert_kernel<GLU, P>), smem);
+  if (e != cudaSuccess) return e;
+  int grid = num_sms();
+  if (items_max < grid) grid = items_max > 0 ? items_max : 1;
+  return launch_pdl(umma_expert_kernel<GLU, P>, dim3(grid), dim3(kThreads), smem, s, a);
+}
+
+// z[row_token[r]] (bf16) -> P e4m3 rows with e8m0 block scales per sorted row r. One warp
+// per row; each lane takes 8 consecutive values, four lanes one 32-value block.
+template <int P>
+__global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ z,
+                                                         const int32_t* __restrict__ row_token, int rows,
+                                                         int T, int L, uint8_t* bq, uint8_t* bs,
+                                                         uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;  // warp-uniform
+  int t = row_token[r];
+  if (t < 0 || t >= T) {
+    if (lane == 0) atomicOr(err, kErrIndex);
+    t = 0;
+  }
+  const int sp = exp_pitch(L);
+  for (int base = 0; base < L; base += 256) {
+    const int col = base + 8 * lane;
+    const bool act = col < L;  // L is a multiple of 32: a block is all in or all out
+    float v[8];
+    if (act) {
+      const uint4 w = *reinterpret_cast<const uint4*>(z + (size_t)t * L + col);
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(ww[i] << 16);
+        v[2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    }
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+      const int X = p == 0 ? block_exp<P>(max_in_group4(am)) : split_block_exp(max_in_group4(am));
+      uint32_t codes[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        codes[i] = e4m3x2(mul_pow2(v[2 * i], -X), mul_pow2(v[2 * i + 1], -X));
+        if (P == 2 && p == 0) {  // keep the remainder for the lo row (exact)
+          const float2 h = e4m3x2_value(codes[i]);
+          v[2 * i] -= mul_pow2(h.x, X);
+          v[2 * i + 1] -= mul_pow2(h.y, X);
+        }
+      }
+      if (act) {
+        const size_t row = (size_t)P * r + p;
+        *reinterpret_cast<uint2*>(bq + row * L + col) =
+            make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16));
+        if ((lane & 3) == 0) bs[row * sp + col / 32] = (uint8_t)(X + 127);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
+                              uint8_t* bq, uint8_t* bs, uint32_t* err, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int warps = 8;
+  const dim3 grid((rows + warps - 1) / warps), block(32 * warps);
+  if (P == 1) return launch_pdl(quant_rows_kernel<1>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, err);
+  return launch_pdl(quant_rows_kernel<2>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, err);
+}
+
+cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
+                            const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
+                            cudaStream_t s) {
+  UExpertArgs A{};
+  const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
+  if (!make_tmap_fp4(&A.ta0, w.gate_q, d.latent, wrows, pitch, 64) ||
+      !make_tmap_fp4(&A.ta1, w.up_q, d.latent, wrows, pitch, 64))
+    return cudaErrorInvalidValue;
+  const int rows = T * d.top_k;
+  if (!make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, 64 * P, true))
+    return cudaErrorInvalidValue;
+  A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
+  A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
+  A.aq = aq; A.aqs = aqs; A.err = err;
+  const int items_max = (rows / kUmmaChunkRows + d.n_experts) * (d.inter / 64);
+  return P == 1 ? launch_t<true, 1>(A, items_max, s) : launch_t<true, 2>(A, items_max, s);
+}
+
+cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
+                             const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s) {
+  UExpertArgs A{};
+  if (!make_tmap_fp4(&A.ta0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, 128))
+    return cudaErrorInvalidValue;
+  const int rows = T * d.top_k;
+  if (!make_tmap_2d(&A.tb, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, 64 * P, true))
+    return cudaErrorInvalidValue;
+  A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
+  A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
+  A.o_out = o_rows; A.err = err;
+  const int items_max = (rows / kUmmaChunkRows + d.n_experts) * (d.latent / 128);
+  return P == 1 ? launch_t<false, 1>(A, items_max, s) : launch_t<false, 2>(A, items_max, s);
+}
+
+}  // namespace k3moe

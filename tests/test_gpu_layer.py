@@ -65,11 +65,12 @@ def _expert_ffn(lay, z_np, idx_np, actq=0):
     return o.cpu().numpy().astype(np.float64), (off, rt, rs, sr)
 
 
+# T >= 65 runs the block-scaled tensor-core path, smaller T the GEMV path
+@pytest.mark.parametrize("T", [24, 100])
 @pytest.mark.parametrize("actq", [0, 1])
-def test_expert_ffn_tiny_all_rows(actq):
+def test_expert_ffn_tiny_all_rows(actq, T):
     d = synth.TINY
     lay = DeviceLayer(d, seed=0, actq=actq)
-    T = 24
     z = synth.host_bf16_normal(3, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
     idx = synth.host_topk_sets(4, T, d.n_experts, d.top_k, "zipf")
     o, (off, rt, rs, sr) = _expert_ffn(lay, z, idx, actq)
@@ -79,9 +80,9 @@ def test_expert_ffn_tiny_all_rows(actq):
     assert err.max() <= REL_L2, err.max()
 
 
-def test_expert_ffn_k3_sampled_rows(k3_layer):
+@pytest.mark.parametrize("T", [40, 96])
+def test_expert_ffn_k3_sampled_rows(k3_layer, T):
     d = synth.K3
-    T = 40
     z = synth.host_bf16_normal(7, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
     idx = synth.host_topk_sets(8, T, d.n_experts, d.top_k, "zipf")  # skewed: multi-chunk experts
     o, (off, rt, rs, sr) = _expert_ffn(k3_layer, z, idx)
@@ -93,10 +94,10 @@ def test_expert_ffn_k3_sampled_rows(k3_layer):
         assert rel_l2_rows(o[r], want) <= REL_L2, (r, rel_l2_rows(o[r], want))
 
 
-def test_expert_ffn_invariants_bit_exact():
+@pytest.mark.parametrize("T", [8, 80])
+def test_expert_ffn_invariants_bit_exact(T):
     """All-zero codes give exactly 0; +1 on every up exponent doubles every output exactly."""
     d = synth.TINY
-    T = 8
     z = synth.host_bf16_normal(2, synth.S_X, 0, T * d.latent, 1.0).reshape(T, d.latent)
     idx = synth.host_topk_sets(5, T, d.n_experts, d.top_k, "uniform")
     base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
@@ -109,9 +110,9 @@ def test_expert_ffn_invariants_bit_exact():
     np.testing.assert_array_equal(o2, 2 * o1)
 
 
-def test_expert_ffn_nan_scale_gives_nonfinite():
+@pytest.mark.parametrize("T", [4, 72])
+def test_expert_ffn_nan_scale_gives_nonfinite(T):
     d = synth.TINY
-    T = 4
     base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
     base[0]["down_s"] = base[0]["down_s"].copy()
     base[0]["down_s"][:, 0] = 255
@@ -194,10 +195,21 @@ def test_layer_tiny_every_token(actq):
     assert flips == 0
 
 
+@pytest.mark.parametrize("actq", [0, 1])
+def test_layer_tiny_prefill_every_token(actq):
+    """150 tokens: tensor-core dense projections and block-scaled expert GEMMs."""
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=2, actq=actq)
+    T = 150
+    x = synth.host_bf16_normal(11, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+    y, idx, w = _forward(lay, x)
+    _compare_layer(lay, x, y, idx, np.arange(T))
+
+
 def test_layer_tiny_ragged_and_edge_T():
     d = synth.TINY
     lay = DeviceLayer(d, seed=1, bias=synth.host_f32_normal(1, synth.S_BIAS, 0, d.n_experts, 1.0))
-    for T in (1, 3, 9, 70):
+    for T in (1, 3, 9, 70, 193):
         x = synth.host_bf16_normal(T, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
         y, idx, w = _forward(lay, x)
         _compare_layer(lay, x, y, idx, np.arange(T))

@@ -65,7 +65,8 @@ typedef enum k3moe_status {
   K3MOE_E_MODE = 5,      /* act / actq not supported (act = 1, SiTU-GLU, has no formula) */
   K3MOE_E_CUDA = 6,      /* a CUDA runtime call or launch failed */
   K3MOE_E_TIMEOUT = 7,   /* a device-side bounded wait ran out (see k3moe_check) */
-  K3MOE_E_DEVICE = 8     /* no usable sm_100-family device, or a device-side check failed */
+  K3MOE_E_DEVICE = 8,    /* no usable sm_100-family device, or a device-side check failed */
+  K3MOE_E_SCRATCH = 9    /* request larger than k3moe_route_noalloc's fixed scratch */
 } k3moe_status;
 
 typedef struct k3moe_dims {
@@ -104,6 +105,28 @@ k3moe_status k3moe_route(const k3moe_dims* dims, const uint16_t* x, int32_t T,
                          const uint16_t* w_router, const float* bias, float* logits,
                          int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes,
                          void* stream);
+
+/* k3moe_route without a workspace: the same router logits and top-k (same kernels, same
+ * results as k3moe_route), with the logits kept in a fixed scratch array inside the library.
+ * The paper has no counterpart; this exists for callers that cannot allocate device memory
+ * for a routing decision: a serving process whose device memory is all handed to its own
+ * pool allocator, where cudaMalloc / cudaFree are off limits on the request path because
+ * they can synchronise the whole device and stall every other stream.
+ *   x [T][H] bf16, w_router [E][H] bf16, bias [E] fp32 or NULL, topk_idx [T][k] int32 out,
+ *   topk_w [T][k] fp32 out, as for k3moe_route.
+ *   err_word: optional uint32 device output; cleared by this call, then set nonzero if the
+ *   device detects a fault (a bounded wait that ran out). NULL keeps that word in the scratch.
+ * Limit: T * n_experts <= 65536 (for 896 experts, up to 73 tokens); larger requests return
+ * K3MOE_E_SCRATCH and launch nothing. The scratch is 262,400 bytes, part of the library's
+ * device image, held on every GPU that loads the library until the process exits.
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * The first call on a device looks up the scratch's device address (once, with that device
+ * current); make that first call before any stream capture. All calls share the one scratch
+ * array: calls whose work can overlap on the GPU (different streams, or several host threads)
+ * race on it and must be ordered by the caller. */
+k3moe_status k3moe_route_noalloc(const k3moe_dims* dims, const uint16_t* x, int32_t T,
+                                 const uint16_t* w_router, const float* bias, int32_t* topk_idx,
+                                 float* topk_w, uint32_t* err_word, void* stream);
 
 /* Token-by-expert permutation: histogram over experts, exclusive scan, stable scatter.
  *   topk_idx [T][k] int32 in [0, E): each token's experts, distinct.

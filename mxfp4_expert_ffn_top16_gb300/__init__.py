@@ -23,19 +23,19 @@ _LIBDIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(_LIBDIR, "libk3moe.so")
 
 SOURCES = ["k3moe_api.cu", "k_dense_gemv.cu", "k_expert_gemv.cu", "k_route.cu", "k_misc.cu",
-           "k_tma.cu", "k_umma_dense.cu", "k_umma_expert.cu"]
+           "k_tma.cu", "k_umma_dense.cu", "k_umma_expert.cu", "k3moe_noalloc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-I" + _INCLUDE]
 
 STATUS = {0: "K3MOE_OK", 1: "K3MOE_E_NULL", 2: "K3MOE_E_SHAPE", 3: "K3MOE_E_ALIGN",
           4: "K3MOE_E_WORKSPACE", 5: "K3MOE_E_MODE", 6: "K3MOE_E_CUDA", 7: "K3MOE_E_TIMEOUT",
-          8: "K3MOE_E_DEVICE"}
+          8: "K3MOE_E_DEVICE", 9: "K3MOE_E_SCRATCH"}
 K3MOE_OK = 0
 
 # Exported symbols (kept in step with include/k3moe.h; a CPU test checks both).
 EXPORTS = ["k3moe_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_project",
            "k3moe_expert_ffn_mxfp4", "k3moe_combine", "k3moe_layer_forward", "k3moe_check",
-           "k3moe_status_string", "k3moe_profile", "k3moe_profile_name"]
+           "k3moe_status_string", "k3moe_profile", "k3moe_profile_name", "k3moe_route_noalloc"]
 
 
 def _newer(target: str, deps) -> bool:
@@ -99,6 +99,7 @@ def lib():
             "k3moe_combine": [p, p, p, p, i32, p, p],
             "k3moe_layer_forward": [p, p, p, i32, p, p, p, p, sz, p],
             "k3moe_check": [p, p],
+            "k3moe_route_noalloc": [p, p, i32, p, p, p, p, p, p],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -146,6 +147,13 @@ def k3moe_route(dims, x, T, w_router, bias, logits, topk_idx, topk_w, ws, ws_byt
                 check=True):
     return _ck(lib().k3moe_route(_ref(dims), x, T, w_router, bias, logits, topk_idx, topk_w, ws,
                                  ws_bytes, stream), "k3moe_route", check)
+
+
+def k3moe_route_noalloc(dims, x, T, w_router, bias, topk_idx, topk_w, err_word=None, stream=0,
+                        check=True):
+    """k3moe_route without a workspace (logits in the library's fixed scratch)."""
+    return _ck(lib().k3moe_route_noalloc(_ref(dims), x, T, w_router, bias, topk_idx, topk_w, err_word,
+                                         stream), "k3moe_route_noalloc", check)
 
 
 def k3moe_permute(dims, topk_idx, T, expert_offsets, row_token, row_slot, slot_row, ws, ws_bytes,

@@ -258,6 +258,8 @@ const char* k3moe_status_string(k3moe_status s) {
     case K3MOE_E_CUDA: return "K3MOE_E_CUDA: CUDA call or launch failed";
     case K3MOE_E_TIMEOUT: return "K3MOE_E_TIMEOUT: a device-side bounded wait ran out";
     case K3MOE_E_DEVICE: return "K3MOE_E_DEVICE: device-side check failed";
+    case K3MOE_E_SCRATCH:
+      return "K3MOE_E_SCRATCH: T * n_experts exceeds the 65536 logits of k3moe_route_noalloc's fixed scratch";
   }
   return "K3MOE: unknown status";
 }

@@ -23,11 +23,12 @@
 // stage (four MMAs of K = 32, each with its scale byte). Work item = (chunk of up to 64 sorted
 // rows of one expert, feature block), feature block fastest: the CTAs working at one time
 // share a chunk's activations and an expert's weights in L2.
-// Warp 0: producer. Its lanes gather each stage's scales with 4-byte cp.async straight into the
-// 32 x 16-byte block that tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l, word w =
-// the four K-block scales of row 32w + l), a few stages ahead; lane 0 then loads the packed
-// e2m1 weight tiles (16U4_ALIGN16B tensor map) and the e4m3 activation tiles, both with the
-// 128-byte swizzle. Warp 1: tensor-memory owner and MMA issuer. Accumulation restarts every
+// Warp 0: producer. For each stage its lanes gather the scales with 4-byte cp.async straight
+// into the 32 x 16-byte blocks that tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l,
+// word w = the four K-block scales of row 32w + l), and lane 0 loads the packed e2m1 weight
+// tiles (16U4_ALIGN16B tensor map) and the e4m3 activation tiles, both with the 128-byte
+// swizzle; the stage's full barrier counts the tile bytes and one cp.async arrival per lane.
+// Warp 1: tensor-memory owner and MMA issuer, one commit per stage. Accumulation restarts every
 // kGroup stages in one of three 128-column tensor-memory slots; warps 2-5 (one lane = one
 // weight row) add the slots up in fp32 and run the epilogue; the GLU epilogue transposes
 // through shared memory so each thread quantises one (sorted row, 32-feature block).
@@ -46,16 +47,13 @@ constexpr int kATile = BM * BKE;          // bytes in shared memory (e2m1 padded
 constexpr int kAPacked = BM * BKE / 2;    // bytes the copy transfers
 constexpr int kBTile = 128 * BKE;         // e4m3, up to 128 rows
 constexpr int kThreads = 192;
-constexpr int kSfSlots = 8;               // scale staging blocks (ring)
-constexpr int kPre = 3;                   // stages the scale gather runs ahead of the tile loads
 constexpr int kGroup = 4;                 // stages per tensor-memory accumulation slot
 constexpr int kAccSlots = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = kAccSlots * 128;  // scale columns: 8 per staging block (A, then B)
+constexpr uint32_t kSfCol = kAccSlots * 128;  // scale columns: 8 per stage (A, then B)
 constexpr int kXPitch = 65;               // GLU exchange row pitch (floats)
 constexpr int kOut = kUmmaChunkRows;      // sorted rows per item (max)
-static_assert(kSfCol + 8 * kSfSlots <= kTmemCols, "tensor memory");
-static_assert(kSfSlots - kPre <= kStages, "scale ring must not hold back the tile ring");
+static_assert(kSfCol + 8 * kStages <= kTmemCols, "tensor memory");
 
 struct UExpertArgs {
   CUtensorMap ta0;     // GLU: gate codes; down: down codes. {K codes, E*N rows}, box {128, 64|128}
@@ -97,10 +95,10 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t s
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int n>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory");
+// Arrives on `bar` once every cp.async this thread issued so far has landed (the arrival is
+// part of the barrier's expected count: .noinc).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Two values -> two E4M3 codes (nearest even, saturating), v0 in the low byte.
@@ -172,14 +170,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   const int srow = A.K / 32, spb = exp_pitch(A.K);
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATile;
-  uint8_t* stg = sB + kStages * kBTile;                        // kSfSlots x (512 A + 512 B)
-  float* xg = reinterpret_cast<float*>(stg + kSfSlots * 1024);  // GLU: [64][kXPitch]
+  uint8_t* stg = sB + kStages * kBTile;                       // kStages x (512 A + 512 B)
+  float* xg = reinterpret_cast<float*>(stg + kStages * 1024);  // GLU: [64][kXPitch]
   uint64_t* full = reinterpret_cast<uint64_t*>(xg + (GLU ? 64 * kXPitch : 0));
   uint64_t* empty = full + kStages;
   uint64_t* accf = empty + kStages;
   uint64_t* acce = accf + kAccSlots;
-  uint64_t* stgd = acce + kAccSlots;  // [kSfSlots] staging block free again
-  uint64_t* ebar = stgd + kSfSlots;   // epilogue group barrier
+  uint64_t* ebar = acce + kAccSlots;  // epilogue group barrier
   uint64_t* drain = ebar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -187,14 +184,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], 1 + 32);  // lane 0's expect_tx arrival + one cp.async arrival per lane
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < kAccSlots; ++b) {
       mbar_init(&accf[b], 1);
       mbar_init(&acce[b], 4);
     }
-    for (int j = 0; j < kSfSlots; ++j) mbar_init(&stgd[j], 1);
     mbar_init(ebar, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -231,49 +227,27 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   };
 
   if (warp == 0) {  // ---------------- producer: scale gather (all lanes) and tile loads (lane 0)
-    // The scales of stage g go to staging block g mod kSfSlots in the layout tcgen05.cp reads:
-    // lane l, word w = the four K-block scales of row 32w + l. The gather runs kPre stages
-    // ahead through cp.async; a stage's tiles are requested once its scales have landed.
-    int pu = blockIdx.x, pkc = 0, pj = 0;
-    uint32_t pjph = 0;
-    int pe = 0, pr0 = 0, pnr = 0, pf0 = 0;
-    if (pu < items) item_of(pu, pe, pr0, pnr, pf0);
-    auto gather = [&]() -> bool {
-      if (pu < items) {
-        if (!mbar_wait_warp(&stgd[pj], pjph ^ 1, abort_flag, A.err)) return false;
-        uint8_t* st = stg + pj * 1024 + lane * 16;
-        const size_t wrow = (size_t)pe * A.N + pf0;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const int r = 32 * w + lane;
-          const uint8_t* src = (GLU && r >= 64) ? A.s1 + (wrow + r - 64) * srow : A.s0 + (wrow + r) * srow;
-          cp_async4(st + 4 * w, src + 4 * pkc, 4);
-          const bool vb = r < P * pnr;
-          cp_async4(st + 512 + 4 * w, vb ? A.sb + ((size_t)P * pr0 + r) * spb + 4 * pkc : A.sb, vb ? 4u : 0u);
-        }
-        if (++pkc == nk) {
-          pkc = 0;
-          pu += gridDim.x;
-          if (pu < items) item_of(pu, pe, pr0, pnr, pf0);
-        }
-        if (++pj == kSfSlots) { pj = 0; pjph ^= 1; }
-      }
-      cp_async_commit();  // one group per call, possibly empty
-      return true;
-    };
-    bool ok = true;
-    for (int i = 0; i < kPre && ok; ++i) ok = gather();
     int s = 0;
     uint32_t ph = 0;
+    bool ok = true;
     for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
       int e, r0, nr, f0;
       if (!item_of(u, e, r0, nr, f0) && lane == 0) atomicOr(A.err, kErrIndex);
       const int wrow = e * A.N + f0;
       for (int kc = 0; kc < nk; ++kc) {
-        if (!gather()) { ok = false; break; }
-        cp_async_wait<kPre>();  // this lane's scale copies for stage (u, kc) have landed
-        fence_async_smem();
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
+        // scales of this stage: A rows 32w + lane, B rows 32w + lane (zeros past the chunk)
+        uint8_t* st = stg + s * 1024 + lane * 16;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int r = 32 * w + lane;
+          const uint8_t* src = (GLU && r >= 64) ? A.s1 + ((size_t)wrow + r - 64) * srow
+                                                : A.s0 + ((size_t)wrow + r) * srow;
+          cp_async4(st + 4 * w, src + 4 * kc, 4);
+          const bool vb = r < P * nr;
+          cp_async4(st + 512 + 4 * w, vb ? A.sb + ((size_t)P * r0 + r) * spb + 4 * kc : A.sb, vb ? 4u : 0u);
+        }
+        cp_async_arrive(&full[s]);
         if (lane == 0) {
           mbar_arrive_expect_tx(&full[s], kAPacked + kBTx);
           tma_load_2d(sA + s * kATile, &A.ta0, kc * BKE, wrow, &full[s]);
@@ -284,10 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         if (++s == kStages) { s = 0; ph ^= 1; }
       }
     }
-    cp_async_wait<0>();
+    asm volatile("cp.async.wait_all;" ::: "memory");  // nothing lands after the block has gone
   } else if (warp == 1) {
     if (lane == 0) {  // ---------------- MMA issuer
-      int s = 0, slot = 0, j = 0;
+      int s = 0, slot = 0;
       uint32_t ph = 0, aph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
@@ -301,21 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
           const int kc1 = min(nk, (gi + 1) * kGroup);
           for (int kc = gi * kGroup; kc < kc1; ++kc) {
             if (!mbar_wait_bounded(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
+            fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
             tc_fence_after();
-            const uint32_t tsa = tmem + kSfCol + 8 * j, tsb = tsa + 4;
+            const uint32_t tsa = tmem + kSfCol + 8 * s, tsb = tsa + 4;
             asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa),
-                         "l"(sdesc_sf(smem_u32(stg + j * 1024))));
+                         "l"(sdesc_sf(smem_u32(stg + s * 1024))));
             asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb),
-                         "l"(sdesc_sf(smem_u32(stg + j * 1024 + 512))));
+                         "l"(sdesc_sf(smem_u32(stg + s * 1024 + 512))));
             const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_mx(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_mx(Nc, kk), tsa, tsb,
                       (kc != gi * kGroup || kk != 0) ? 1u : 0u);
-            umma_commit(&empty[s]);
-            umma_commit(&stgd[j]);
+            umma_commit(&empty[s]);  // tiles and scale block of this stage free again
             if (++s == kStages) { s = 0; ph ^= 1; }
-            if (++j == kSfSlots) j = 0;
           }
           if (!ok) break;
           umma_commit(&accf[slot]);
@@ -370,20 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         // 1. gate rows (lanes 0..63) park their sums; 2. the up row of the same feature forms
         // a = bf16(silu(gate) * up) in place; 3. every epilogue thread quantises one
         // (sorted row, 32-feature block) of a into P e4m3 rows for the down pass.
+        // (all kOut columns are handled without a per-row test so the compiler can interleave
+        // them; columns past nr hold unused values and are never stored)
         if (q < 2) {
 #pragma unroll
-          for (int jr = 0; jr < kOut; ++jr)
-            if (jr < nr) xg[lrow * kXPitch + jr] = sum[jr];
+          for (int jr = 0; jr < kOut; ++jr) xg[lrow * kXPitch + jr] = sum[jr];
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
         if (q >= 2) {
           float* xr = xg + (lrow - 64) * kXPitch;
 #pragma unroll
           for (int jr = 0; jr < kOut; ++jr) {
-            if (jr < nr) {
-              const float g = xr[jr];
-              xr[jr] = bf16_to_f32(f32_to_bf16(g / (1.0f + expf(-g)) * sum[jr]));
-            }
+            const float g = xr[jr];  // silu(g) = g / (1 + e^-g); fast forms, ~1e-6 relative
+            xr[jr] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * sum[jr]));
           }
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
@@ -423,8 +395,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
 
 template <bool GLU, int P>
 size_t smem_bytes() {
-  return 1024 + (size_t)kStages * (kATile + kBTile) + kSfSlots * 1024 + (GLU ? 64 * kXPitch * 4 : 0) +
-         (2 * kStages + 2 * kAccSlots + kSfSlots + 2) * 8 + 16;
+  return 1024 + (size_t)kStages * (kATile + kBTile) + kStages * 1024 + (GLU ? 64 * kXPitch * 4 : 0) +
+         (2 * kStages + 2 * kAccSlots + 2) * 8 + 16;
 }
 
 template <bool GLU, int P>

@@ -77,7 +77,7 @@ inline __host__ __device__ int4* plan_ctab(int32_t* plan, int E) {
 }
 // A second table for the tensor-core expert GEMM follows: entry 0 = {chunks C64, 0, 0, 0},
 // entries 1..C64 = {expert, first sorted row, rows (<= kUmmaChunkRows), 0}.
-constexpr int kUmmaChunkRows = 64;
+constexpr int kUmmaChunkRows = 112;
 inline __host__ __device__ size_t plan_ctab64_offset(int E, long long rows) {
   return plan_ctab_offset(E) + (size_t)(rows / kGemvTokens + E + 1) * 16;
 }

@@ -19,16 +19,18 @@
 //          adds the two results.
 //
 // Tile: M = 128 weight rows (GLU: 64 gate rows and the 64 up rows of the same features, so
-// lane i and lane i + 64 pair up), N = P x (up to 64) activation rows, K = 128 per pipeline
-// stage (four MMAs of K = 32, each with its scale byte). Work item = (chunk of up to 64 sorted
+// lane i and lane i + 64 pair up), N = P x (up to 112) activation rows, K = 128 per pipeline
+// stage (four MMAs of K = 32, each with its scale byte). Work item = (chunk of up to 112 sorted
 // rows of one expert, feature block), feature block fastest: the CTAs working at one time
-// share a chunk's activations and an expert's weights in L2.
-// Warp 0: producer. For each stage its lanes gather the scales with 4-byte cp.async straight
-// into the 32 x 16-byte blocks that tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l,
-// word w = the four K-block scales of row 32w + l), and lane 0 loads the packed e2m1 weight
-// tiles (16U4_ALIGN16B tensor map) and the e4m3 activation tiles, both with the 128-byte
-// swizzle; the stage's full barrier counts the tile bytes and one cp.async arrival per lane.
-// Warp 1: tensor-memory owner and MMA issuer, one commit per stage. Accumulation restarts every
+// share a chunk's activations and an expert's weights in L2. Each tcgen05 instruction costs
+// tens of cycles to issue from the single MMA thread, so N is made as large as tensor memory
+// allows (two 224-column accumulators) to keep the tensor pipe, not the issue, the limit.
+// Warp 0 (lane 0) loads the packed e2m1 weight tiles (16U4_ALIGN16B tensor map) and the e4m3
+// activation tiles, both with the 128-byte swizzle. Warps 6 and 7 gather each stage's weight
+// and activation scales with 4-byte cp.async straight into the 32 x 16-byte blocks that
+// tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l, word w = the four K-block scales
+// of row 32w + l); the stage's full barrier counts the tile bytes and one cp.async arrival per
+// gathering lane. Warp 1: tensor-memory owner and MMA issuer, one commit per stage. Accumulation restarts every
 // kGroup stages in one of three 128-column tensor-memory slots; warps 2-5 (one lane = one
 // weight row) add the slots up in fp32 and run the epilogue; the GLU epilogue transposes
 // through shared memory so each thread quantises one (sorted row, 32-feature block).
@@ -42,23 +44,27 @@ namespace k3moe {
 namespace {
 
 constexpr int BM = 128, BKE = 128;        // weight rows, K elements per stage
-constexpr int kStages = 6;
+constexpr int kStages = 4;
 constexpr int kATile = BM * BKE;          // bytes in shared memory (e2m1 padded to bytes)
 constexpr int kAPacked = BM * BKE / 2;    // bytes the copy transfers
-constexpr int kBTile = 128 * BKE;         // e4m3, up to 128 rows
-constexpr int kThreads = 192;
-constexpr int kGroup = 4;                 // stages per tensor-memory accumulation slot
-constexpr int kAccSlots = 3;
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = kAccSlots * 128;  // scale columns: 8 per stage (A, then B)
-constexpr int kXPitch = 65;               // GLU exchange row pitch (floats)
 constexpr int kOut = kUmmaChunkRows;      // sorted rows per item (max)
-static_assert(kSfCol + 8 * kStages <= kTmemCols, "tensor memory");
+constexpr int kNMax = 2 * kOut;           // B rows per tile (P = 2)
+constexpr int kBTile = kNMax * BKE;       // e4m3
+constexpr int kThreads = 256;             // 0 TMA, 1 MMA, 2-5 epilogue, 6-7 scale gather
+constexpr int kGroup = 4;                 // stages per tensor-memory accumulation slot
+constexpr int kAccSlots = 2;
+constexpr int kSfPerStage = 16;           // tensor-memory columns: A 4, B rows 0..127 4, B rows 128.. 4
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol = kAccSlots * kNMax;  // scale columns, kSfPerStage per stage
+constexpr int kStgBytes = 1536;           // per stage: A block, B block rows 0..127, rows 128..255
+constexpr int kXPitch = kOut + 1;         // GLU exchange row pitch (floats)
+static_assert(kSfCol + kSfPerStage * kStages <= kTmemCols, "tensor memory");
+static_assert(kNMax <= 256 && kNMax % 16 == 0, "MMA N");
 
 struct UExpertArgs {
   CUtensorMap ta0;     // GLU: gate codes; down: down codes. {K codes, E*N rows}, box {128, 64|128}
   CUtensorMap ta1;     // GLU: up codes
-  CUtensorMap tb;      // activation rows, e4m3 {K, P*rows}, box {128, 64*P}
+  CUtensorMap tb;      // activation rows, e4m3 {K, P*rows}, box {128, kOut*P}
   const uint8_t* s0;   // weight scales [E][N][K/32]
   const uint8_t* s1;   // GLU: up scales
   const uint8_t* sb;   // activation scales [P*rows][exp_pitch(K)]
@@ -90,10 +96,9 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
          ((uint64_t)1 << 46);
 }
 
-// 4-byte asynchronous copy global -> shared; src_bytes = 0 writes zeros without reading.
-__device__ __forceinline__ void cp_async4(void* dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-               : "memory");
+// 4-byte asynchronous copy global -> shared (shared-window address).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 // Arrives on `bar` once every cp.async this thread issued so far has landed (the arrival is
 // part of the barrier's expected count: .noinc).
@@ -163,15 +168,15 @@ __device__ __forceinline__ void quant_block32(float (&v)[32], uint32_t (&codes)[
 template <bool GLU, int P>
 __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_constant__ UExpertArgs A) {
   constexpr int kFB = GLU ? 64 : 128;  // output features per item
-  constexpr int kBRows = 64 * P;       // activation rows per tile
+  constexpr int kBRows = kOut * P;     // activation rows per tile
   constexpr uint32_t kBTx = kBRows * BKE;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int srow = A.K / 32, spb = exp_pitch(A.K);
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATile;
-  uint8_t* stg = sB + kStages * kBTile;                       // kStages x (512 A + 512 B)
-  float* xg = reinterpret_cast<float*>(stg + kStages * 1024);  // GLU: [64][kXPitch]
+  uint8_t* stg = sB + kStages * kBTile;                            // kStages x kStgBytes
+  float* xg = reinterpret_cast<float*>(stg + kStages * kStgBytes);  // GLU: [64][kXPitch]
   uint64_t* full = reinterpret_cast<uint64_t*>(xg + (GLU ? 64 * kXPitch : 0));
   uint64_t* empty = full + kStages;
   uint64_t* accf = empty + kStages;
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + 32);  // lane 0's expect_tx arrival + one cp.async arrival per lane
+      mbar_init(&full[s], 1 + 64);  // the expect_tx arrival + one cp.async arrival per gathering lane
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < kAccSlots; ++b) {
@@ -226,35 +231,64 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
     return ok;
   };
 
-  if (warp == 0) {  // ---------------- producer: scale gather (all lanes) and tile loads (lane 0)
+  if (warp == 0) {  // ---------------- tile loads
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+        int e, r0, nr, f0;
+        if (!item_of(u, e, r0, nr, f0)) atomicOr(A.err, kErrIndex);
+        const int wrow = e * A.N + f0;
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kAPacked + kBTx);
+          tma_load_2d(sA + s * kATile, &A.ta0, kc * BKE, wrow, &full[s]);
+          if (GLU) tma_load_2d(sA + s * kATile + 64 * 128, &A.ta1, kc * BKE, wrow, &full[s]);
+          tma_load_2d(sB + s * kBTile, &A.tb, kc * BKE, P * r0, &full[s]);
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+      }
+    }
+  } else if (warp >= 6) {  // ---------------- scale gather: warp 6 weight rows, warp 7 activation rows
+    // Activation rows past the chunk are not copied: a B row only affects its own output
+    // column, and those columns are never read.
+    const bool wa = warp == 6;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
       int e, r0, nr, f0;
-      if (!item_of(u, e, r0, nr, f0) && lane == 0) atomicOr(A.err, kErrIndex);
-      const int wrow = e * A.N + f0;
-      for (int kc = 0; kc < nk; ++kc) {
-        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
-        // scales of this stage: A rows 32w + lane, B rows 32w + lane (zeros past the chunk)
-        uint8_t* st = stg + s * 1024 + lane * 16;
+      item_of(u, e, r0, nr, f0);
+      const size_t wrow = (size_t)e * A.N + f0;
+      const uint8_t* src[7];
+      uint32_t dst[7];
+      int n = 0;
+      const uint32_t st_lane = smem_u32(stg) + lane * 16;
+      if (wa) {
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           const int r = 32 * w + lane;
-          const uint8_t* src = (GLU && r >= 64) ? A.s1 + ((size_t)wrow + r - 64) * srow
-                                                : A.s0 + ((size_t)wrow + r) * srow;
-          cp_async4(st + 4 * w, src + 4 * kc, 4);
-          const bool vb = r < P * nr;
-          cp_async4(st + 512 + 4 * w, vb ? A.sb + ((size_t)P * r0 + r) * spb + 4 * kc : A.sb, vb ? 4u : 0u);
+          src[w] = (GLU && r >= 64) ? A.s1 + (wrow + r - 64) * srow : A.s0 + (wrow + r) * srow;
+          dst[w] = st_lane + 4 * w;
         }
+        n = 4;
+      } else {
+#pragma unroll
+        for (int w = 0; w < 7; ++w) {
+          const int rb = 32 * w + lane;  // B row; block rb / 128 of the stage, word (rb / 32) % 4
+          src[w] = A.sb + ((size_t)P * r0 + rb) * spb;
+          dst[w] = st_lane + 512 * (1 + (w >> 2)) + 4 * (w & 3);
+          if (rb < P * nr) n = w + 1;  // rows of this lane that exist: w < n
+        }
+      }
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
+        const uint32_t so = (uint32_t)(s * kStgBytes);
+#pragma unroll
+        for (int w = 0; w < 7; ++w)
+          if (w < n) cp_async4(dst[w] + so, src[w] + 4 * kc);
         cp_async_arrive(&full[s]);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&full[s], kAPacked + kBTx);
-          tma_load_2d(sA + s * kATile, &A.ta0, kc * BKE, wrow, &full[s]);
-          if (GLU) tma_load_2d(sA + s * kATile + 64 * 128, &A.ta1, kc * BKE, wrow, &full[s]);
-          tma_load_2d(sB + s * kBTile, &A.tb, kc * BKE, P * r0, &full[s]);
-        }
-        __syncwarp();
         if (++s == kStages) { s = 0; ph ^= 1; }
       }
     }
@@ -271,17 +305,20 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         Nc = Nc < 16 ? 16 : ((Nc + 15) & ~15);
         for (int gi = 0; gi < ngroups && ok; ++gi) {
           if (!mbar_wait_bounded(&acce[slot], aph ^ 1, abort_flag, A.err)) { ok = false; break; }
-          const uint32_t d = tmem + (uint32_t)(slot * 128);
+          const uint32_t d = tmem + (uint32_t)(slot * kNMax);
           const int kc1 = min(nk, (gi + 1) * kGroup);
           for (int kc = gi * kGroup; kc < kc1; ++kc) {
             if (!mbar_wait_bounded(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
             fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
             tc_fence_after();
-            const uint32_t tsa = tmem + kSfCol + 8 * s, tsb = tsa + 4;
-            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa),
-                         "l"(sdesc_sf(smem_u32(stg + s * 1024))));
-            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb),
-                         "l"(sdesc_sf(smem_u32(stg + s * 1024 + 512))));
+            // scale columns: A (4), then B rows 0..127 (4) and B rows 128..255 (4)
+            const uint32_t tsa = tmem + kSfCol + kSfPerStage * s, tsb = tsa + 4;
+            const uint32_t st0 = smem_u32(stg + s * kStgBytes);
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa), "l"(sdesc_sf(st0)));
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb), "l"(sdesc_sf(st0 + 512)));
+            if (Nc > 128)
+              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb + 4),
+                           "l"(sdesc_sf(st0 + 1024)));
             const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
@@ -318,18 +355,20 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
       for (int gi = 0; gi < ngroups; ++gi) {
         if (!mbar_wait_warp(&accf[slot], aph, abort_flag, A.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * 128);
+        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kNMax);
 #pragma unroll
-        for (int c = 0; c < P * kOut / 32; ++c) {
+        for (int c = 0; c < (P * kOut + 31) / 32; ++c) {
           if (c * 32 < ncols) {  // warp-uniform
             uint32_t v[32];
             tmem_ld32(base + c * 32, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32 / P; ++i) {
-              float x = __uint_as_float(v[P * i]);
-              if (P == 2) x += __uint_as_float(v[P * i + 1]);
-              sum[c * (32 / P) + i] += x;
+              if (c * (32 / P) + i < kOut) {  // compile-time
+                float x = __uint_as_float(v[P * i]);
+                if (P == 2) x += __uint_as_float(v[P * i + 1]);
+                sum[c * (32 / P) + i] += x;
+              }
             }
           }
         }
@@ -340,41 +379,56 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
       }
       if (!ok) break;
       if (GLU) {
-        // 1. gate rows (lanes 0..63) park their sums; 2. the up row of the same feature forms
-        // a = bf16(silu(gate) * up) in place; 3. every epilogue thread quantises one
-        // (sorted row, 32-feature block) of a into P e4m3 rows for the down pass.
-        // (all kOut columns are handled without a per-row test so the compiler can interleave
-        // them; columns past nr hold unused values and are never stored)
+        // 1. the gate row (lanes 0..63) of feature f parks its sums for sorted rows kH.. and the
+        // up row (lanes 64..127) its sums for rows ..kH; 2. each forms a = bf16(silu(gate) * up)
+        // for its other half in place (so all four warps share the work); 3. every epilogue
+        // thread quantises (sorted row, 32-feature block) units of a into P e4m3 rows for the
+        // down pass. All kOut columns are handled without a per-row test so the compiler can
+        // interleave them; columns past nr hold unused values and are never stored.
+        constexpr int kH = kOut / 2;
+        float* xr = xg + (lrow & 63) * kXPitch;
         if (q < 2) {
 #pragma unroll
-          for (int jr = 0; jr < kOut; ++jr) xg[lrow * kXPitch + jr] = sum[jr];
+          for (int jr = kH; jr < kOut; ++jr) xr[jr] = sum[jr];
+        } else {
+#pragma unroll
+          for (int jr = 0; jr < kH; ++jr) xr[jr] = sum[jr];
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
-        if (q >= 2) {
-          float* xr = xg + (lrow - 64) * kXPitch;
+        // silu(g) = g / (1 + e^-g) in the fast forms, ~1e-6 relative, far below bf16 rounding
+        if (q < 2) {
 #pragma unroll
-          for (int jr = 0; jr < kOut; ++jr) {
-            const float g = xr[jr];  // silu(g) = g / (1 + e^-g); fast forms, ~1e-6 relative
+          for (int jr = 0; jr < kH; ++jr) {
+            const float g = sum[jr];
+            xr[jr] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * xr[jr]));
+          }
+        } else {
+#pragma unroll
+          for (int jr = kH; jr < kOut; ++jr) {
+            const float g = xr[jr];
             xr[jr] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * sum[jr]));
           }
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
-        const int jr = et & 63, b = et >> 6;
-        if (jr < nr) {
-          float v[32];
+        // (sorted row, 32-feature block) units: kOut rows x 2 blocks over the 128 threads
+        for (int unit = et; unit < 2 * kOut; unit += 128) {
+          const int jr = unit % kOut, b = unit / kOut;
+          if (jr < nr) {
+            float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = xg[(32 * b + i) * kXPitch + jr];
-          uint32_t codes[P][8];
-          int X[P];
-          quant_block32<P>(v, codes, X);
-          const int spo = exp_pitch(A.N);
+            for (int i = 0; i < 32; ++i) v[i] = xg[(32 * b + i) * kXPitch + jr];
+            uint32_t codes[P][8];
+            int X[P];
+            quant_block32<P>(v, codes, X);
+            const int spo = exp_pitch(A.N);
 #pragma unroll
-          for (int p = 0; p < P; ++p) {
-            const size_t brow = (size_t)P * (r0 + jr) + p;
-            uint4* dst = reinterpret_cast<uint4*>(A.aq + brow * A.N + f0 + 32 * b);
-            dst[0] = make_uint4(codes[p][0], codes[p][1], codes[p][2], codes[p][3]);
-            dst[1] = make_uint4(codes[p][4], codes[p][5], codes[p][6], codes[p][7]);
-            A.aqs[brow * spo + (f0 + 32 * b) / 32] = (uint8_t)(X[p] + 127);
+            for (int p = 0; p < P; ++p) {
+              const size_t brow = (size_t)P * (r0 + jr) + p;
+              uint4* dst = reinterpret_cast<uint4*>(A.aq + brow * A.N + f0 + 32 * b);
+              dst[0] = make_uint4(codes[p][0], codes[p][1], codes[p][2], codes[p][3]);
+              dst[1] = make_uint4(codes[p][4], codes[p][5], codes[p][6], codes[p][7]);
+              A.aqs[brow * spo + (f0 + 32 * b) / 32] = (uint8_t)(X[p] + 127);
+            }
           }
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
@@ -395,7 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
 
 template <bool GLU, int P>
 size_t smem_bytes() {
-  return 1024 + (size_t)kStages * (kATile + kBTile) + kStages * 1024 + (GLU ? 64 * kXPitch * 4 : 0) +
+  return 1024 + (size_t)kStages * (kATile + kBTile) + kStages * kStgBytes + (GLU ? 64 * kXPitch * 4 : 0) +
          (2 * kStages + 2 * kAccSlots + 2) * 8 + 16;
 }
 
@@ -490,7 +544,7 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
       !make_tmap_fp4(&A.ta1, w.up_q, d.latent, wrows, pitch, 64))
     return cudaErrorInvalidValue;
   const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, 64 * P, true))
+  if (!make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, kOut * P, true))
     return cudaErrorInvalidValue;
   A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
   A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
@@ -505,7 +559,7 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
   if (!make_tmap_fp4(&A.ta0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, 128))
     return cudaErrorInvalidValue;
   const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.tb, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, 64 * P, true))
+  if (!make_tmap_2d(&A.tb, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, kOut * P, true))
     return cudaErrorInvalidValue;
   A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
   A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;

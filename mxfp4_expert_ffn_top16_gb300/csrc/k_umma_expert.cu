@@ -30,10 +30,11 @@
 // and activation scales with 4-byte cp.async straight into the 32 x 16-byte blocks that
 // tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l, word w = the four K-block scales
 // of row 32w + l); the stage's full barrier counts the tile bytes and one cp.async arrival per
-// gathering lane. Warp 1: tensor-memory owner and MMA issuer, one commit per stage. Accumulation restarts every
-// kGroup stages in one of three 128-column tensor-memory slots; warps 2-5 (one lane = one
-// weight row) add the slots up in fp32 and run the epilogue; the GLU epilogue transposes
-// through shared memory so each thread quantises one (sorted row, 32-feature block).
+// gathering lane. Warp 1: tensor-memory owner and MMA issuer, one commit per stage.
+// Accumulation restarts every kGroup stages in one of two tensor-memory slots; eight epilogue
+// warps (two per lane quadrant, one lane = one weight row, each half of the sorted rows) add
+// the slots up in fp32 and run the epilogue; the GLU epilogue transposes through shared memory
+// so each thread quantises one (sorted row, 32-feature block).
 #include <cuda_fp16.h>
 
 #include "k3moe_device.cuh"
@@ -50,7 +51,9 @@ constexpr int kAPacked = BM * BKE / 2;    // bytes the copy transfers
 constexpr int kOut = kUmmaChunkRows;      // sorted rows per item (max)
 constexpr int kNMax = 2 * kOut;           // B rows per tile (P = 2)
 constexpr int kBTile = kNMax * BKE;       // e4m3
-constexpr int kThreads = 256;             // 0 TMA, 1 MMA, 2-5 epilogue, 6-7 scale gather
+constexpr int kThreads = 384;             // 0 TMA, 1 MMA, 2-9 epilogue, 10-11 scale gather
+constexpr int kEpiWarps = 8;
+constexpr int kGather0 = 2 + kEpiWarps;   // first scale-gather warp
 constexpr int kGroup = 4;                 // stages per tensor-memory accumulation slot
 constexpr int kAccSlots = 2;
 constexpr int kSfPerStage = 16;           // tensor-memory columns: A 4, B rows 0..127 4, B rows 128.. 4
@@ -194,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
     }
     for (int b = 0; b < kAccSlots; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 4);
+      mbar_init(&acce[b], kEpiWarps);
     }
-    mbar_init(ebar, 4);
+    mbar_init(ebar, kEpiWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -250,10 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         }
       }
     }
-  } else if (warp >= 6) {  // ---------------- scale gather: warp 6 weight rows, warp 7 activation rows
+  } else if (warp >= kGather0) {  // ---------------- scale gather: weight rows, then activation rows
     // Activation rows past the chunk are not copied: a B row only affects its own output
     // column, and those columns are never read.
-    const bool wa = warp == 6;
+    const bool wa = warp == kGather0;
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -293,81 +296,89 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
       }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // nothing lands after the block has gone
-  } else if (warp == 1) {
-    if (lane == 0) {  // ---------------- MMA issuer
-      int s = 0, slot = 0;
-      uint32_t ph = 0, aph = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
-        int e, r0, nr, f0;
-        item_of(u, e, r0, nr, f0);
-        int Nc = P * nr;
-        Nc = Nc < 16 ? 16 : ((Nc + 15) & ~15);
-        for (int gi = 0; gi < ngroups && ok; ++gi) {
-          if (!mbar_wait_bounded(&acce[slot], aph ^ 1, abort_flag, A.err)) { ok = false; break; }
-          const uint32_t d = tmem + (uint32_t)(slot * kNMax);
-          const int kc1 = min(nk, (gi + 1) * kGroup);
-          for (int kc = gi * kGroup; kc < kc1; ++kc) {
-            if (!mbar_wait_bounded(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
+  } else if (warp == 1) {  // ---------------- MMA issue: the whole warp runs the loop, one lane issues
+    int s = 0, slot = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+      int e, r0, nr, f0;
+      item_of(u, e, r0, nr, f0);
+      int Nc = P * nr;
+      Nc = Nc < 16 ? 16 : ((Nc + 15) & ~15);
+      for (int gi = 0; gi < ngroups && ok; ++gi) {
+        if (!mbar_wait_warp(&acce[slot], aph ^ 1, abort_flag, A.err)) { ok = false; break; }
+        const uint32_t d = tmem + (uint32_t)(slot * kNMax);
+        const int kc1 = min(nk, (gi + 1) * kGroup);
+        for (int kc = gi * kGroup; kc < kc1; ++kc) {
+          if (!mbar_wait_warp(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
+          // scale columns: A (4), then B rows 0..127 (4) and B rows 128..255 (4)
+          const uint32_t tsa = tmem + kSfCol + kSfPerStage * s, tsb = tsa + 4;
+          const uint32_t st0 = smem_u32(stg + s * kStgBytes);
+          const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
+          if (elect_one()) {
             fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
             tc_fence_after();
-            // scale columns: A (4), then B rows 0..127 (4) and B rows 128..255 (4)
-            const uint32_t tsa = tmem + kSfCol + kSfPerStage * s, tsb = tsa + 4;
-            const uint32_t st0 = smem_u32(stg + s * kStgBytes);
             asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa), "l"(sdesc_sf(st0)));
             asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb), "l"(sdesc_sf(st0 + 512)));
             if (Nc > 128)
               asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb + 4),
                            "l"(sdesc_sf(st0 + 1024)));
-            const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_mx(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_mx(Nc, kk), tsa, tsb,
                       (kc != gi * kGroup || kk != 0) ? 1u : 0u);
             umma_commit(&empty[s]);  // tiles and scale block of this stage free again
-            if (++s == kStages) { s = 0; ph ^= 1; }
           }
-          if (!ok) break;
-          umma_commit(&accf[slot]);
-          if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
+          __syncwarp();
+          if (++s == kStages) { s = 0; ph ^= 1; }
         }
+        if (!ok) break;
+        if (elect_one()) umma_commit(&accf[slot]);
+        __syncwarp();
+        if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
       }
-      // every issued MMA has completed before the tensor memory is released
+    }
+    // every issued MMA has completed before the tensor memory is released
+    if (elect_one()) {
       umma_commit(drain);
       volatile int no_abort = 0;
       mbar_wait_bounded(drain, 0, &no_abort, A.err);
     }
     __syncwarp();
-  } else {  // ---------------- epilogue warps 2..5, lane quadrant q = warp % 4
-    const int q = warp & 3;
-    const int lrow = q * 32 + lane;         // tile row = tensor-memory lane
-    const int et = (warp - 2) * 32 + lane;  // 0..127 over the epilogue threads
+  } else {  // ---------------- epilogue warps 2..9: lane quadrant q = warp % 4, row half h
+    constexpr int kHalf = kOut / 2;       // sorted rows per epilogue warp
+    constexpr int kQ = kHalf / 2;         // GLU exchange split within a half
+    const int eq = warp - 2, q = warp & 3, h = eq >> 2;
+    const int lrow = q * 32 + lane;       // tile row = tensor-memory lane
+    const int et = eq * 32 + lane;        // 0..255 over the epilogue threads
+    const int j0 = h * kHalf;             // first sorted row of this warp's half
     int slot = 0;
     uint32_t aph = 0, eph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
       int e, r0, nr, f0;
       item_of(u, e, r0, nr, f0);
-      const int ncols = P * nr;
-      float sum[kOut];
+      const int ncols = P * (nr - j0);    // live accumulator columns of this half (may be <= 0)
+      float sum[kHalf];
 #pragma unroll
-      for (int i = 0; i < kOut; ++i) sum[i] = 0.f;
+      for (int i = 0; i < kHalf; ++i) sum[i] = 0.f;
       for (int gi = 0; gi < ngroups; ++gi) {
         if (!mbar_wait_warp(&accf[slot], aph, abort_flag, A.err)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t base = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kNMax);
+        const uint32_t base =
+            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kNMax + P * j0);
 #pragma unroll
-        for (int c = 0; c < (P * kOut + 31) / 32; ++c) {
-          if (c * 32 < ncols) {  // warp-uniform
-            uint32_t v[32];
-            tmem_ld32(base + c * 32, v);
+        for (int c = 0; c < (P * kHalf + 15) / 16; ++c) {
+          if (c * 16 < ncols) {  // warp-uniform
+            uint32_t v[16];
+            tmem_ld16(base + c * 16, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32 / P; ++i) {
-              if (c * (32 / P) + i < kOut) {  // compile-time
+            for (int i = 0; i < 16 / P; ++i) {
+              if (c * (16 / P) + i < kHalf) {  // compile-time
                 float x = __uint_as_float(v[P * i]);
                 if (P == 2) x += __uint_as_float(v[P * i + 1]);
-                sum[c * (32 / P) + i] += x;
+                sum[c * (16 / P) + i] += x;
               }
             }
           }
@@ -379,39 +390,38 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
       }
       if (!ok) break;
       if (GLU) {
-        // 1. the gate row (lanes 0..63) of feature f parks its sums for sorted rows kH.. and the
-        // up row (lanes 64..127) its sums for rows ..kH; 2. each forms a = bf16(silu(gate) * up)
-        // for its other half in place (so all four warps share the work); 3. every epilogue
-        // thread quantises (sorted row, 32-feature block) units of a into P e4m3 rows for the
-        // down pass. All kOut columns are handled without a per-row test so the compiler can
-        // interleave them; columns past nr hold unused values and are never stored.
-        constexpr int kH = kOut / 2;
-        float* xr = xg + (lrow & 63) * kXPitch;
+        // 1. within each half of the sorted rows, the gate row (lanes 0..63) of feature f parks
+        // its sums for the half's upper kQ rows and the up row (lanes 64..127) its sums for the
+        // lower kQ rows; 2. each forms a = bf16(silu(gate) * up) for its other quarter in place;
+        // 3. every epilogue thread quantises one (sorted row, 32-feature block) of a into P
+        // e4m3 rows for the down pass. All rows are handled without a per-row test so the
+        // compiler can interleave them; rows past nr hold unused values and are never stored.
+        float* xr = xg + (lrow & 63) * kXPitch + j0;
         if (q < 2) {
 #pragma unroll
-          for (int jr = kH; jr < kOut; ++jr) xr[jr] = sum[jr];
+          for (int i = kQ; i < kHalf; ++i) xr[i] = sum[i];
         } else {
 #pragma unroll
-          for (int jr = 0; jr < kH; ++jr) xr[jr] = sum[jr];
+          for (int i = 0; i < kQ; ++i) xr[i] = sum[i];
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
         // silu(g) = g / (1 + e^-g) in the fast forms, ~1e-6 relative, far below bf16 rounding
         if (q < 2) {
 #pragma unroll
-          for (int jr = 0; jr < kH; ++jr) {
-            const float g = sum[jr];
-            xr[jr] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * xr[jr]));
+          for (int i = 0; i < kQ; ++i) {
+            const float g = sum[i];
+            xr[i] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * xr[i]));
           }
         } else {
 #pragma unroll
-          for (int jr = kH; jr < kOut; ++jr) {
-            const float g = xr[jr];
-            xr[jr] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * sum[jr]));
+          for (int i = kQ; i < kHalf; ++i) {
+            const float g = xr[i];
+            xr[i] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * sum[i]));
           }
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
-        // (sorted row, 32-feature block) units: kOut rows x 2 blocks over the 128 threads
-        for (int unit = et; unit < 2 * kOut; unit += 128) {
+        // (sorted row, 32-feature block) units: kOut rows x 2 blocks over the 256 threads
+        for (int unit = et; unit < 2 * kOut; unit += 32 * kEpiWarps) {
           const int jr = unit % kOut, b = unit / kOut;
           if (jr < nr) {
             float v[32];
@@ -434,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
       } else {
 #pragma unroll
-        for (int jr = 0; jr < kOut; ++jr)
-          if (jr < nr) A.o_out[(size_t)(r0 + jr) * A.N + f0 + lrow] = sum[jr];
+        for (int i = 0; i < kHalf; ++i)
+          if (j0 + i < nr) A.o_out[(size_t)(r0 + j0 + i) * A.N + f0 + lrow] = sum[i];
       }
     }
   }

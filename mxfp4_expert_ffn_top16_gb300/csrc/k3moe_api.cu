@@ -76,7 +76,7 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.o = take(rows * Lw * 4);
   L.c = take(Tt * Lw * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
-  if (umma_expert_ok(d, T)) {
+  if (umma_expert_ok(d)) {
     const size_t P = d.actq ? 1 : 2;
     L.bq = take(P * rows * Lw);
     L.bs = take(P * rows * (size_t)exp_pitch(d.latent));
@@ -185,7 +185,7 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
                               const WsLayout& L, cudaStream_t s) {
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* plan = at<int32_t>(ws, L.plan);
-  if (umma_expert_ok(d, T)) {
+  if (umma_expert_ok(d)) {
     const int P = d.actq ? 1 : 2;
     {
       ProfScope p(P_QUANT, s);
@@ -342,7 +342,7 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights*
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const WsLayout L = ws_layout(d, T);
   uint32_t* err = at<uint32_t>(ws, L.err);
-  if (!umma_expert_ok(d, T))
+  if (!umma_expert_ok(d))
     K3_CUDA(launch_act_prep(z, T, d.latent, d.actq, at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), s));
   K3_CUDA(launch_plan(expert_offsets, d.n_experts, T * d.top_k, at<int32_t>(ws, L.plan), err, s));
   K3_TRY(run_expert_gemms(d, *weights, z, T, expert_offsets, row_token, o_rows, ws, L, s));
@@ -386,7 +386,7 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
   // that the expert GEMV reads; the tensor-core expert path quantises z itself)
   {
     ProfScope p(P_ROUTER_LATENT, s);
-    const bool f16_copy = !umma_expert_ok(d, T);
+    const bool f16_copy = !umma_expert_ok(d);
     K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr, w.router_bias, w.w_in,
                          d.latent, at<uint16_t>(ws, L.z), f16_copy ? at<__half>(ws, L.zh) : nullptr,
                          f16_copy ? at<int8_t>(ws, L.zs) : nullptr, d.actq, x, T, d.hidden, err, s));

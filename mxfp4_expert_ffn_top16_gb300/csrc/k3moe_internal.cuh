@@ -133,13 +133,13 @@ cudaError_t launch_expert_glu(const k3moe_dims& d, const k3moe_weights& w, const
 cudaError_t launch_expert_down(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
                                const int32_t* offsets, const __half* ah, const int8_t* as,
                                float* o_rows, int T, uint32_t* err, cudaStream_t s);
-// Block-scaled tensor-core expert GEMMs (many tokens). Usable when latent and inter are
-// multiples of 128 and T >= kUmmaExpertMinTokens. P = 2 (bf16 activations as e4m3 hi + lo) or
-// 1 (MXFP8 activations).
+// Block-scaled tensor-core expert GEMMs. Usable when latent and inter are multiples of 128
+// (otherwise the expert GEMV runs). P = 2 (bf16 activations as e4m3 hi + lo) or 1 (MXFP8
+// activations). Items are chunks of up to kUmmaChunkRows sorted rows from
+// kUmmaExpertMinTokens tokens on, of up to kGemvTokens rows below.
 constexpr int kUmmaExpertMinTokens = 65;
-inline bool umma_expert_ok(const k3moe_dims& d, long long T) {
-  return T >= kUmmaExpertMinTokens && d.latent % 128 == 0 && d.inter % 128 == 0;
-}
+inline bool umma_expert_ok(const k3moe_dims& d) { return d.latent % 128 == 0 && d.inter % 128 == 0; }
+inline int umma_chunk_rows(long long T) { return T >= kUmmaExpertMinTokens ? kUmmaChunkRows : kGemvTokens; }
 // z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)].
 cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
                               uint8_t* bq, uint8_t* bs, uint32_t* err, cudaStream_t s);

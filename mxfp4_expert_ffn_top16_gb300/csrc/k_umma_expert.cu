@@ -45,29 +45,37 @@ namespace k3moe {
 namespace {
 
 constexpr int BM = 128, BKE = 128;        // weight rows, K elements per stage
-constexpr int kStages = 4;
 constexpr int kATile = BM * BKE;          // bytes in shared memory (e2m1 padded to bytes)
 constexpr int kAPacked = BM * BKE / 2;    // bytes the copy transfers
-constexpr int kOut = kUmmaChunkRows;      // sorted rows per item (max)
-constexpr int kNMax = 2 * kOut;           // B rows per tile (P = 2)
-constexpr int kBTile = kNMax * BKE;       // e4m3
 constexpr int kThreads = 384;             // 0 TMA, 1 MMA, 2-9 epilogue, 10-11 scale gather
 constexpr int kEpiWarps = 8;
 constexpr int kGather0 = 2 + kEpiWarps;   // first scale-gather warp
 constexpr int kGroup = 4;                 // stages per tensor-memory accumulation slot
 constexpr int kAccSlots = 2;
 constexpr int kSfPerStage = 16;           // tensor-memory columns: A 4, B rows 0..127 4, B rows 128.. 4
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = kAccSlots * kNMax;  // scale columns, kSfPerStage per stage
 constexpr int kStgBytes = 1536;           // per stage: A block, B block rows 0..127, rows 128..255
-constexpr int kXPitch = kOut + 1;         // GLU exchange row pitch (floats)
-static_assert(kSfCol + kSfPerStage * kStages <= kTmemCols, "tensor memory");
-static_assert(kNMax <= 256 && kNMax % 16 == 0, "MMA N");
+
+// Shapes by chunk size R (sorted rows per item): R = kUmmaChunkRows (many tokens: N up to 224,
+// four deep stages) or R = kGemvTokens (few tokens: N up to 16, small activation tiles, so
+// eleven stages keep enough weight bytes in flight to stream at HBM speed).
+template <int R>
+struct Cfg {
+  static constexpr int kOut = R;                  // sorted rows per item (max)
+  static constexpr int kNMax = 2 * R;             // B rows per tile (P = 2)
+  static constexpr int kBTile = kNMax * BKE;      // e4m3
+  static constexpr int kStages = R == kGemvTokens ? 11 : 4;
+  static constexpr int kXPitch = R + 1;           // GLU exchange row pitch (floats)
+  static constexpr uint32_t kSfCol = kAccSlots * kNMax;  // scale columns, kSfPerStage per stage
+  static constexpr uint32_t kTmemCols = R == kGemvTokens ? 256 : 512;
+  static_assert(R == kGemvTokens || R == kUmmaChunkRows, "chunk size");
+  static_assert(kSfCol + kSfPerStage * kStages <= kTmemCols, "tensor memory");
+  static_assert(kNMax <= 256 && kNMax % 16 == 0, "MMA N");
+};
 
 struct UExpertArgs {
   CUtensorMap ta0;     // GLU: gate codes; down: down codes. {K codes, E*N rows}, box {128, 64|128}
   CUtensorMap ta1;     // GLU: up codes
-  CUtensorMap tb;      // activation rows, e4m3 {K, P*rows}, box {128, kOut*P}
+  CUtensorMap tb;      // activation rows, e4m3 {K, P*rows}, box {128, R*P}
   const uint8_t* s0;   // weight scales [E][N][K/32]
   const uint8_t* s1;   // GLU: up scales
   const uint8_t* sb;   // activation scales [P*rows][exp_pitch(K)]
@@ -168,8 +176,12 @@ __device__ __forceinline__ void quant_block32(float (&v)[32], uint32_t (&codes)[
   }
 }
 
-template <bool GLU, int P>
+template <bool GLU, int P, int R>
 __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_constant__ UExpertArgs A) {
+  using CF = Cfg<R>;
+  constexpr int kOut = CF::kOut, kNMax = CF::kNMax, kBTile = CF::kBTile, kStages = CF::kStages;
+  constexpr int kXPitch = CF::kXPitch;
+  constexpr uint32_t kSfCol = CF::kSfCol, kTmemCols = CF::kTmemCols;
   constexpr int kFB = GLU ? 64 : 128;  // output features per item
   constexpr int kBRows = kOut * P;     // activation rows per tile
   constexpr uint32_t kBTx = kBRows * BKE;
@@ -215,17 +227,25 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
 
-  const int4* ctab = plan_ctab64(A.plan, A.E, A.rows_max);
-  const int C = ctab[0].x;
+  // chunk table of the plan for this chunk size (entries {expert, first row, rows, 0})
+  const int4* ctab;
+  int C;
+  if (R == kUmmaChunkRows) {
+    ctab = plan_ctab64(A.plan, A.E, A.rows_max) + 1;
+    C = ctab[-1].x;
+  } else {
+    ctab = plan_ctab(A.plan, A.E);
+    C = A.plan[1];
+  }
   const int fbs = A.N / kFB;
-  const int items = (C > 0 && C <= A.rows_max / kUmmaChunkRows + A.E) ? C * fbs : 0;
+  const int items = (C > 0 && C <= A.rows_max / R + A.E) ? C * fbs : 0;
   const int nk = A.K / BKE;
   const int ngroups = (nk + kGroup - 1) / kGroup;
 
   // item u -> (expert, first sorted row, rows, first feature); false for a corrupt entry
   auto item_of = [&](int u, int& e, int& r0, int& nr, int& f0) -> bool {
     const int c = u / fbs, fb = u - c * fbs;
-    const int4 t = ctab[1 + c];
+    const int4 t = ctab[c];
     const bool ok = t.x >= 0 && t.x < A.E && t.y >= 0 && t.z > 0 && t.z <= kOut && t.y + t.z <= A.rows_max;
     e = ok ? t.x : 0;
     r0 = ok ? t.y : 0;
@@ -457,21 +477,30 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   }
 }
 
-template <bool GLU, int P>
-size_t smem_bytes() {
-  return 1024 + (size_t)kStages * (kATile + kBTile) + kStages * kStgBytes + (GLU ? 64 * kXPitch * 4 : 0) +
-         (2 * kStages + 2 * kAccSlots + 2) * 8 + 16;
+template <bool GLU, int R>
+constexpr size_t smem_bytes() {
+  using CF = Cfg<R>;
+  return 1024 + (size_t)CF::kStages * (kATile + CF::kBTile) + CF::kStages * kStgBytes +
+         (GLU ? 64 * CF::kXPitch * 4 : 0) + (2 * CF::kStages + 2 * kAccSlots + 2) * 8 + 16;
 }
+static_assert(smem_bytes<true, kGemvTokens>() <= 227 * 1024 && smem_bytes<true, kUmmaChunkRows>() <= 227 * 1024,
+              "shared memory");
 
-template <bool GLU, int P>
+template <bool GLU, int P, int R>
 cudaError_t launch_t(UExpertArgs& a, int items_max, cudaStream_t s) {
-  const size_t smem = smem_bytes<GLU, P>();
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_expert_kernel<GLU, P>), smem);
+  const size_t smem = smem_bytes<GLU, R>();
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_expert_kernel<GLU, P, R>), smem);
   if (e != cudaSuccess) return e;
   int grid = num_sms();
   if (items_max < grid) grid = items_max > 0 ? items_max : 1;
-  return launch_pdl(umma_expert_kernel<GLU, P>, dim3(grid), dim3(kThreads), smem, s, a);
+  return launch_pdl(umma_expert_kernel<GLU, P, R>, dim3(grid), dim3(kThreads), smem, s, a);
+}
+
+template <bool GLU>
+cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t s) {
+  if (R == kGemvTokens)
+    return P == 1 ? launch_t<GLU, 1, kGemvTokens>(a, items_max, s) : launch_t<GLU, 2, kGemvTokens>(a, items_max, s);
+  return P == 1 ? launch_t<GLU, 1, kUmmaChunkRows>(a, items_max, s) : launch_t<GLU, 2, kUmmaChunkRows>(a, items_max, s);
 }
 
 // z[row_token[r]] (bf16) -> P e4m3 rows with e8m0 block scales per sorted row r. One warp
@@ -548,34 +577,36 @@ cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int r
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
                             cudaStream_t s) {
+  const int R = umma_chunk_rows(T);
   UExpertArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
   if (!make_tmap_fp4(&A.ta0, w.gate_q, d.latent, wrows, pitch, 64) ||
       !make_tmap_fp4(&A.ta1, w.up_q, d.latent, wrows, pitch, 64))
     return cudaErrorInvalidValue;
   const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, kOut * P, true))
+  if (!make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, R * P, true))
     return cudaErrorInvalidValue;
   A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
   A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.err = err;
-  const int items_max = (rows / kUmmaChunkRows + d.n_experts) * (d.inter / 64);
-  return P == 1 ? launch_t<true, 1>(A, items_max, s) : launch_t<true, 2>(A, items_max, s);
+  const int items_max = (rows / R + d.n_experts) * (d.inter / 64);
+  return launch_pr<true>(A, P, R, items_max, s);
 }
 
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s) {
+  const int R = umma_chunk_rows(T);
   UExpertArgs A{};
   if (!make_tmap_fp4(&A.ta0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, 128))
     return cudaErrorInvalidValue;
   const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.tb, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, kOut * P, true))
+  if (!make_tmap_2d(&A.tb, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, R * P, true))
     return cudaErrorInvalidValue;
   A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
   A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
   A.o_out = o_rows; A.err = err;
-  const int items_max = (rows / kUmmaChunkRows + d.n_experts) * (d.latent / 128);
-  return P == 1 ? launch_t<false, 1>(A, items_max, s) : launch_t<false, 2>(A, items_max, s);
+  const int items_max = (rows / R + d.n_experts) * (d.latent / 128);
+  return launch_pr<false>(A, P, R, items_max, s);
 }
 
 }  // namespace k3moe

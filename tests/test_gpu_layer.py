@@ -80,6 +80,19 @@ def test_expert_ffn_tiny_all_rows(actq, T):
     assert err.max() <= REL_L2, err.max()
 
 
+@pytest.mark.parametrize("T", [5, 70])
+def test_expert_ffn_gemv_path_all_rows(T):
+    """inter = 192 is not a multiple of 128, so the expert GEMV runs instead of the MMA path."""
+    d = synth.Dims(hidden=256, latent=128, inter=192, n_experts=32, top_k=4)
+    lay = DeviceLayer(d, seed=5)
+    z = synth.host_bf16_normal(6, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
+    idx = synth.host_topk_sets(7, T, d.n_experts, d.top_k, "zipf")
+    o, (off, rt, rs, sr) = _expert_ffn(lay, z, idx)
+    ol = lay.oracle()
+    want = np.stack([ol.expert_row(int(idx[rt[r], rs[r]]), z[rt[r]])[0] for r in range(T * d.top_k)])
+    assert rel_l2_rows(o, want).max() <= REL_L2
+
+
 @pytest.mark.parametrize("T", [40, 96])
 def test_expert_ffn_k3_sampled_rows(k3_layer, T):
     d = synth.K3

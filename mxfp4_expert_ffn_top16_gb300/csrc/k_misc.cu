@@ -11,36 +11,45 @@ namespace {
 // c[t][n] = bf16(sum_{j<k} w[t][j] * o[slot_row[t*k+j]][n]), fp32, j ascending.
 // Routed outputs are combined in latent space before the projection back to the residual
 // ("kimi-k3-mlx", LatentMoE).
+// Two values per thread; the k rows and weights are loaded before any is summed, so all of a
+// thread's loads are in flight together (few tokens leave this kernel latency-bound).
+constexpr int kMaxTopK = 32;
 __global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_row,
                                const float* __restrict__ w, int T, int k, int L, uint16_t* c) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
-  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
   if (t >= T || n >= L) return;
-  // Kahan-compensated sum, so the bf16 rounding of c follows the exact sum of the fp32 terms
-  // except within ~1 fp32 ulp of a rounding boundary
-  float s[4] = {0.f, 0.f, 0.f, 0.f}, cc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    const float wj = w[(size_t)t * k + j];
-    const int r = slot_row[(size_t)t * k + j];
-    if (r < 0 || r >= T * k) continue;  // out-of-range rows contribute nothing
-    const float4 v = *reinterpret_cast<const float4*>(o + (size_t)r * L + n);
-    const float p[4] = {wj * v.x, wj * v.y, wj * v.z, wj * v.w};
+  int rr[kMaxTopK];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+  for (int j = 0; j < kMaxTopK; ++j) rr[j] = j < k ? slot_row[(size_t)t * k + j] : -1;
+  float2 v[kMaxTopK];
+  float wj[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    const bool ok = j < k && rr[j] >= 0 && rr[j] < T * k;  // out-of-range rows contribute nothing
+    v[j] = ok ? *reinterpret_cast<const float2*>(o + (size_t)rr[j] * L + n) : make_float2(0.f, 0.f);
+    wj[j] = ok ? w[(size_t)t * k + j] : 0.f;
+    if (!ok) rr[j] = -1;
+  }
+  // Kahan-compensated sum in slot order, so the bf16 rounding of c follows the exact sum of
+  // the fp32 terms except within ~1 fp32 ulp of a rounding boundary
+  float s[2] = {0.f, 0.f}, cc[2] = {0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    if (rr[j] < 0) continue;
+    const float p[2] = {wj[j] * v[j].x, wj[j] * v[j].y};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
       const float yk = p[q] - cc[q];
       const float tk = s[q] + yk;
       cc[q] = (tk - s[q]) - yk;
       s[q] = tk;
     }
   }
-  ushort4 r;
-  r.x = f32_to_bf16(s[0] - cc[0]);
-  r.y = f32_to_bf16(s[1] - cc[1]);
-  r.z = f32_to_bf16(s[2] - cc[2]);
-  r.w = f32_to_bf16(s[3] - cc[3]);
-  *reinterpret_cast<ushort4*>(c + (size_t)t * L + n) = r;
+  const uint32_t packed = (uint32_t)f32_to_bf16(s[0] - cc[0]) | ((uint32_t)f32_to_bf16(s[1] - cc[1]) << 16);
+  *reinterpret_cast<uint32_t*>(c + (size_t)t * L + n) = packed;
 }
 
 // One warp per (token, block of 32 values): optional MXFP8 round trip, then an f16 copy
@@ -67,7 +76,8 @@ __global__ void act_prep_kernel(const uint16_t* __restrict__ z, int T, int L, in
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  dim3 grid((L / 4 + 127) / 128, T);
+  if (k > kMaxTopK) return cudaErrorInvalidValue;
+  dim3 grid((L / 2 + 127) / 128, T);
   return launch_pdl(combine_kernel, grid, dim3(128), 0, s, o_rows, slot_row, w, T, k, L, c);
 }
 

@@ -113,20 +113,32 @@ __global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int 
 }
 
 // ---------------------------------------------------------------- block-level building blocks
-// Exclusive scan of cnt[0..n) in shared memory (n <= blockDim.x); returns the total.
+// Exclusive scan of cnt[0..n) in shared memory (n <= blockDim.x, blockDim.x a multiple of 32);
+// returns the total. Warp shuffles within each warp, one warp over the warp totals: three
+// block barriers in all.
 __device__ int block_excl_scan(int* cnt, int n, int* tmp) {
-  const int tid = threadIdx.x;
-  int v = tid < n ? cnt[tid] : 0;
-  tmp[tid] = v;
-  __syncthreads();
-  for (int o = 1; o < (int)blockDim.x; o <<= 1) {
-    const int add = tid >= o ? tmp[tid - o] : 0;
-    __syncthreads();
-    tmp[tid] += add;
-    __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  const int v = tid < n ? cnt[tid] : 0;
+  int x = v;  // inclusive scan within the warp
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
-  const int total = tmp[blockDim.x - 1];
-  if (tid < n) cnt[tid] = tmp[tid] - v;
+  if (lane == 31) tmp[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < nw ? tmp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    tmp[lane] = w;  // inclusive totals of warps 0..lane
+  }
+  __syncthreads();
+  const int total = tmp[nw - 1];
+  if (tid < n) cnt[tid] = (wid > 0 ? tmp[wid - 1] : 0) + x - v;
   __syncthreads();
   return total;
 }

@@ -104,6 +104,24 @@ def algorithmic(d, T, distinct_experts):
     return dense_w + expert + act, flops
 
 
+def measured_traffic(workload, kernel):
+    """DRAM bytes per launch of a kernel from the committed ncu capture (profiles/traffic.json),
+    or None when there is none or the kernel's sources have changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        h = hashlib.sha256()
+        for p in t["source_files"]:
+            with open(os.path.join(ROOT, p), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != t["source_sha256"]:
+            return None
+        return t["workloads"][workload][kernel]["traffic"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def kernel_cost(name, d, T, distinct, rows, actq):
     """Algorithmic (bytes, flops, tensor dtype) of one launch of a profiled kernel: weights read
     once per launch, activations read and results written once."""
@@ -155,11 +173,13 @@ def roofline(name, per_launch_ms, cost, pk):
 
 
 # ---------------------------------------------------------------- CPU oracle sample
-def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads):
+def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads, pool=None):
     """Times the oracle on (token, slot) units: each unit is one routed expert row through the
     oracle (gate/up, GLU, down; ~33M MACs) plus 1/k of that token's dense work (router, latent
-    in and latent out rows), i.e. 1/k of a token. Units run on `nthreads` host threads.
-    Returns (tokens/s, units timed, seconds)."""
+    in and latent out rows), i.e. 1/k of a token. Units run on `nthreads` host threads. With
+    `pool`, steps cycle through the first `pool` units only (the oracle decodes the weights on
+    every call, so a repeated unit costs the same; fewer experts are generated on the host).
+    Returns (layer, run_step)."""
     import oracle
     import synth
 
@@ -172,6 +192,8 @@ def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads)
         for j in range(k):
             e = int(idx_sample[t, j])
             units.append((t, j, e))
+    if pool:
+        units = units[:max(units_per_step, pool)]
     need = {e for (_, _, e) in units[: units_per_step * steps]}
     for e in need:
         experts[e] = synth.host_expert(d, layer_seed, e)
@@ -221,7 +243,7 @@ def run_reference(args, w):
     step1(0)
     per_unit_s = time.perf_counter() - t0
     budget = 150.0 / max(1, args.steps + args.warmup)
-    units = max(1, min(nth * 4, int(budget * nth / per_unit_s)))
+    units = max(1, min(nth * 64, int(budget * nth / per_unit_s)))
     units = max(1, (units // nth) * nth) if units >= nth else units
     _, step = cpu_sample(w, 0, x, idx, units, args.steps + args.warmup, nth)
     for s in range(args.warmup):
@@ -230,15 +252,17 @@ def run_reference(args, w):
     for s in range(args.steps):
         step(args.warmup + s)
     el = time.perf_counter() - t0
+    nl = max(1, int(getattr(w, "layers", 1) or 1))
     tokens = args.steps * units / d.top_k
-    val = tokens / el
-    sample = (f"{units} (token, expert-slot) units per step = {units / d.top_k:.3g} tokens of the "
-              f"{w.name} workload (expert row + 1/{d.top_k} of the token's dense rows each)")
+    val = tokens / el / nl  # through the whole stack of layers
+    sample = (f"{units} (token, expert-slot) units per step = {units / d.top_k:.3g} tokens through one "
+              f"layer of the {w.name} workload (expert row + 1/{d.top_k} of the token's dense rows each; "
+              f"tokens/s divided by its {nl} layer(s))")
     out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic (seeded)",
-           "config": {"workload": w.name, "tokens_per_step": w.tokens},
+           "config": {"workload": w.name, "tokens_per_step": w.tokens, "layers": nl},
            "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": nth, "kind": "oracle",
                             "sample": sample},
            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -266,34 +290,57 @@ def run_ours(args, w):
     T = w.tokens
     E = d.n_experts
 
-    # --- layer: one expert store, DENSE_COPIES copies of the dense weights
+    # --- layers: one layer = one expert store with DENSE_COPIES copies of its dense weights;
+    # a stack of n layers (independent seeded weights, run back to back) = n stores, one dense
+    # set each (together already far larger than L2)
     t_setup = time.time()
+    nl = max(1, int(getattr(w, "layers", 1) or 1))
     sizes = {"gate_q": E * d.gate_q_bytes, "gate_s": E * d.gate_s_bytes, "up_q": E * d.gate_q_bytes,
              "up_s": E * d.gate_s_bytes, "down_q": E * d.down_q_bytes, "down_s": E * d.down_s_bytes}
-    ex = {n: torch.empty(b, dtype=torch.uint8, device=dev) for n, b in sizes.items()}
+    dims = k3.Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, 0, args.actq)
+    if nl > 1:
+        keep = []
+        wts = []
+        for layer in range(nl):
+            exl = {n: torch.empty(b, dtype=torch.uint8, device=dev) for n, b in sizes.items()}
+            ddl = {"w_router": torch.empty(E * d.hidden, dtype=torch.int16, device=dev),
+                   "w_in": torch.empty(d.latent * d.hidden, dtype=torch.int16, device=dev),
+                   "w_out": torch.empty(d.hidden * d.latent, dtype=torch.int16, device=dev)}
+            pl = {n: t.data_ptr() for n, t in exl.items()}
+            pl.update({n: t.data_ptr() for n, t in ddl.items()})
+            synth.dev_fill_layer(d, layer, pl, sh)
+            bl = synth.router_bias(w, layer)
+            bt = None if bl is None else torch.from_numpy(bl).to(dev)
+            keep.append((exl, ddl, bt))
+            wts.append(k3.Weights(ddl["w_router"].data_ptr(), None if bt is None else bt.data_ptr(),
+                                  ddl["w_in"].data_ptr(), ddl["w_out"].data_ptr(),
+                                  *[exl[n].data_ptr() for n in ("gate_q", "gate_s", "up_q", "up_s",
+                                                                "down_q", "down_s")]))
+    ex = {n: torch.empty(b if nl == 1 else 0, dtype=torch.uint8, device=dev) for n, b in sizes.items()}
     dense = []
-    for c in range(DENSE_COPIES):
+    for c in range(DENSE_COPIES if nl == 1 else 0):
         dd = {"w_router": torch.empty(E * d.hidden, dtype=torch.int16, device=dev),
               "w_in": torch.empty(d.latent * d.hidden, dtype=torch.int16, device=dev),
               "w_out": torch.empty(d.hidden * d.latent, dtype=torch.int16, device=dev)}
         dense.append(dd)
-    ptrs = {n: t.data_ptr() for n, t in ex.items()}
-    ptrs.update({n: t.data_ptr() for n, t in dense[0].items()})
-    synth.dev_fill_layer(d, 0, ptrs, sh)
-    for c in range(1, DENSE_COPIES):
-        for n in dense[c]:
-            dense[c][n].copy_(dense[0][n])
     bias_np = synth.router_bias(w)
-    bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
-    dims = k3.Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, 0, args.actq)
-    wts = [k3.Weights(dd["w_router"].data_ptr(), None if bias is None else bias.data_ptr(),
-                      dd["w_in"].data_ptr(), dd["w_out"].data_ptr(),
-                      *[ex[n].data_ptr() for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q",
-                                                   "down_s")]) for dd in dense]
+    if nl == 1:
+        ptrs = {n: t.data_ptr() for n, t in ex.items()}
+        ptrs.update({n: t.data_ptr() for n, t in dense[0].items()})
+        synth.dev_fill_layer(d, 0, ptrs, sh)
+        for c in range(1, DENSE_COPIES):
+            for n in dense[c]:
+                dense[c][n].copy_(dense[0][n])
+        bias = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
+        wts = [k3.Weights(dd["w_router"].data_ptr(), None if bias is None else bias.data_ptr(),
+                          dd["w_in"].data_ptr(), dd["w_out"].data_ptr(),
+                          *[ex[n].data_ptr() for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q",
+                                                       "down_s")]) for dd in dense]
     nx = w.x_count
     x = torch.empty((nx, d.hidden), dtype=torch.int16, device=dev)
     synth.dev_fill_x(w, x.data_ptr(), cuda_stream=sh)
     y = torch.empty((T, d.hidden), dtype=torch.int16, device=dev)
+    hbuf = [torch.empty((T, d.hidden), dtype=torch.int16, device=dev) for _ in range(2 if nl > 1 else 0)]
     idx = torch.empty((T, d.top_k), dtype=torch.int32, device=dev)
     nbytes = k3.k3moe_workspace_size(dims, T)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
@@ -303,8 +350,17 @@ def run_ours(args, w):
 
     def step(i, xp=None, yp=None):
         xi = xp if xp is not None else x[(i % nsteps_x) * T:].data_ptr()
-        k3.k3moe_layer_forward(dims, wts[i % DENSE_COPIES], xi, T, yp or y.data_ptr(),
-                               idx.data_ptr(), None, ws.data_ptr(), nbytes, sh)
+        yo = yp or y.data_ptr()
+        if nl == 1:
+            k3.k3moe_layer_forward(dims, wts[i % DENSE_COPIES], xi, T, yo, idx.data_ptr(), None,
+                                   ws.data_ptr(), nbytes, sh)
+            return
+        # every layer takes the step's tokens (chaining the synthetic layers' outputs would
+        # overflow within a few layers: the random experts amplify the activations)
+        for layer in range(nl):
+            dst = yo if layer == nl - 1 else hbuf[layer % 2].data_ptr()
+            k3.k3moe_layer_forward(dims, wts[layer], xi, T, dst, idx.data_ptr(), None, ws.data_ptr(),
+                                   nbytes, sh)
 
     def barrier():
         torch.cuda.synchronize()
@@ -376,6 +432,7 @@ def run_ours(args, w):
     name, (tot_ms, launches) = top
     per_launch_ms = tot_ms / max(1, launches)
     step_bytes, step_flops = algorithmic(d, T, distinct)
+    step_bytes, step_flops = step_bytes * nl, step_flops * nl  # every layer of the stack
     kernels_per_step = {"permute": 1 if T <= 256 else 3}
     launches_total = sum(n for _, n in prof.values()) + \
         (kernels_per_step["permute"] - 1) * prof.get("permute", (0, 0))[1]
@@ -387,10 +444,13 @@ def run_ours(args, w):
         "data": "synthetic (seeded SplitMix64; bf16 ~N(0,1) tokens, ~N(0,0.02) dense, U{0..15} codes, U{120..127} e8m0)",
         "config": {"workload": w.name, "tokens_per_step": T, "hidden": d.hidden, "latent": d.latent,
                    "inter": d.inter, "n_experts": d.n_experts, "top_k": d.top_k,
-                   "router_bias": w.bias, "actq": "mxfp8" if args.actq else "bf16",
-                   "l2": "expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 4 copies",
+                   "router_bias": w.bias, "actq": "mxfp8" if args.actq else "bf16", "layers": nl,
+                   "l2": ("expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 4 copies"
+                          if nl == 1 else f"{nl} layers with independent weights ({nl * 15.7:.0f} GB of experts) run back to "
+                          "back on the same tokens; fresh tokens per step"),
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline(name, per_launch_ms, kernel_cost(name, d, T, distinct, T * d.top_k, args.actq), pk),
+        # (traffic filled in below from the committed capture of this workload, bf16 mode only)
         "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
                           "achieved_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
                           "frac_hbm": step_bytes / (ms / args.steps / 1e3) / 1e9 / pk["hbm_gbs"]},
@@ -406,26 +466,31 @@ def run_ours(args, w):
         "setup_s": setup_s,
     }
     out["gpu_launches"] = int(launches_total)
+    if not args.actq and not args.experts:
+        out["roofline"]["traffic"] = measured_traffic(w.name, name)
     if rank == 0 and not args.no_cpu_baseline:
         nth = os.cpu_count() or 1
         xs_np = synth.host_x(w, 0, min(T, 8) if T > 1 else 16)
         import oracle
         wr, _, _ = synth.host_dense(d, 0)
         isamp = oracle.select_topk(oracle.router_logits_np(xs_np, wr, bias_np), d.top_k)
-        units = nth * 2
-        steps_cpu = 3
-        _, cstep = cpu_sample(w, 0, xs_np, isamp, units, steps_cpu + 1, nth)
+        # bounded sample: about 10 s of oracle work, calibrated on one step of nth units
+        units = nth
+        _, cstep = cpu_sample(w, 0, xs_np, isamp, units, 64, nth, pool=2 * nth)
+        t0 = time.perf_counter()
         cstep(0)
+        per_step = max(1e-3, time.perf_counter() - t0)
+        steps_cpu = int(max(1, min(400, 10.0 / per_step)))
         t0 = time.perf_counter()
         for s in range(steps_cpu):
             cstep(1 + s)
         el = time.perf_counter() - t0
         out["cpu_baseline"] = {
-            "value": steps_cpu * units / d.top_k / el, "unit": "tokens/s", "cores": nth,
+            "value": steps_cpu * units / d.top_k / el / nl, "unit": "tokens/s", "cores": nth,
             "kind": "oracle",
             "sample": f"{steps_cpu * units} (token, expert-slot) units = {steps_cpu * units / d.top_k:.2f} "
-                      f"tokens of {w.name}; each unit = one expert row + 1/{d.top_k} of the token's "
-                      f"dense rows, {el:.1f} s on {nth} threads"}
+                      f"tokens through one layer of {w.name} (tokens/s divided by its {nl} layer(s)); each "
+                      f"unit = one expert row + 1/{d.top_k} of the token's dense rows, {el:.1f} s on {nth} threads"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist is not None:
@@ -441,9 +506,15 @@ def main():
     ap.add_argument("--workload", default="decode_b1")
     ap.add_argument("--actq", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="profiling aid: the same workload with fewer experts (fits an ncu capture); "
+                         "not a bench configuration")
     args = ap.parse_args()
+    import dataclasses
     import synth
     w = synth.WORKLOADS[args.workload]
+    if args.experts:
+        w = dataclasses.replace(w, dims=dataclasses.replace(w.dims, n_experts=args.experts))
     default_steps = {"decode_b1": 1000, "decode_b64": 200, "prefill_4k": 20, "prefill_32k": 4}
     if args.steps is None:
         args.steps = default_steps.get(w.name, 20)

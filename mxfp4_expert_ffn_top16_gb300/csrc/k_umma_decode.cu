@@ -1,0 +1,407 @@
+// MXFP4 expert FFN for decode (chunks of up to 8 sorted rows) on block-scaled tensor cores,
+// with the operands placed so that each MMA carries as many weight bytes as possible.
+//
+// "kimi-k3-in-c", MXFP4 experts: 4-bit codes into a 16-entry table, one 8-bit exponent per 32
+// consecutive weights. For sorted row r of expert e (token t):
+//   GLU pass:  a[r] = bf16(silu(G_e z_t) * (U_e z_t))          G_e, U_e [I][L]
+//   down pass: o[r] = D_e a[r]                                  D_e [L][I]
+//
+// At decode sizes the layer streams the selected experts' weights once; every tcgen05 or TMA
+// instruction costs tens of cycles to issue from one thread, so the weights sit on the N side
+// of tcgen05.mma.kind::mxf8f6f4.block_scale (N = 256 weight rows per MMA, e2m1 through a
+// 16U4_ALIGN16B tensor map) and the activation rows on the M side (M = 128, e4m3 with e8m0
+// scales, P rows per sorted row as in the many-token kernel: P = 2 splits a bf16 value exactly
+// into e4m3 hi + lo, P = 1 is MXFP8). Only the first 8 * P of the 128 M rows carry data: each
+// stage loads just those rows (2 KB), the stages' activation tiles sit 2 KB apart, and an
+// MMA's remaining rows read whatever follows in shared memory. Row m of the result depends
+// only on row m of A, so those accumulator rows are never read.
+//
+// Work item = (chunk of up to 8 sorted rows of one expert, feature block): GLU items take 128
+// features (B rows 0..127 gate, 128..255 up), down items 256 features. K = 128 per stage.
+// Warp 0 (lane 0) loads the weight and activation tiles; warps 2 and 3 gather the stage's
+// scales with cp.async into the 32 x 16-byte blocks tcgen05.cp.32x128b.warpx4 copies to tensor
+// memory (lane l, word w = the four K-block scales of row 32w + l); warp 1 issues (one elected
+// lane of the converged warp). One 256-column accumulator per item; warps 4 and 8 (tensor-memory
+// lanes 0..31) each drain half its columns, add the hi and lo rows, and run the epilogue.
+#include <cuda_fp16.h>
+
+#include "k3moe_device.cuh"
+#include "k3moe_internal.cuh"
+#include "k3moe_umma.cuh"
+
+namespace k3moe {
+namespace {
+
+constexpr int BKE = 128;                  // K per stage
+constexpr int kNW = 256;                  // weight rows per item (MMA N)
+constexpr int kMA = 128;                  // MMA M
+constexpr int kRows = kGemvTokens;        // sorted rows per chunk (8)
+constexpr int kStages = 5;
+constexpr int kBTile = kNW * BKE;         // weight tile in shared memory (e2m1 padded to bytes)
+constexpr int kBPacked = kNW * BKE / 2;   // bytes the weight copies transfer
+constexpr int kATile = 2 * kRows * BKE;   // activation rows a stage loads (at most 16 x 128 B)
+constexpr int kASlack = kMA * BKE - kATile;  // the MMA reads 128 rows from a tile's start
+constexpr int kStgBytes = 1536;           // per stage: A scale block, B rows 0..127, B rows 128..255
+constexpr int kThreads = 288;             // warps 0 TMA, 1 MMA, 2-3 gather, 4 and 8 epilogue
+constexpr int kEpiWarp0 = 4, kEpiWarp1 = 8;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol = kNW;          // 12 columns per stage: A 4, B 8
+static_assert(kSfCol + 12 * kStages <= kTmemCols, "tensor memory");
+
+struct UDecodeArgs {
+  CUtensorMap tw0;     // GLU: gate codes, box {128, 128}; down: down codes, box {128, 256}
+  CUtensorMap tw1;     // GLU: up codes, box {128, 128}
+  CUtensorMap ta;      // activation rows e4m3 {K, P*rows}, box {128, 8*P}
+  const uint8_t* s0;   // weight scales [E][N][K/32]
+  const uint8_t* s1;   // GLU: up scales
+  const uint8_t* sb;   // activation scales [P*rows][exp_pitch(K)]
+  int32_t* plan;
+  int N, K, E;         // output features per expert, reduction length, experts
+  int rows_max;        // T * k
+  uint8_t* aq;         // GLU: quantised output [P*rows][N] e4m3
+  uint8_t* aqs;        //      its scales [P*rows][exp_pitch(N)]
+  float* o_out;        // down: [rows][N] fp32
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void umma_mx(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                        uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0; tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+// A e4m3, B e2m1, e8m0 scales, fp32 accumulation, both K-major, M = 128, N = 256; scale byte kk.
+__device__ __forceinline__ uint32_t idesc_dec(int kk) {
+  return ((uint32_t)kk << 4) | (0u << 7) | (5u << 10) | ((uint32_t)(kNW >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(kMA >> 4) << 24) | ((uint32_t)kk << 29);
+}
+__device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
+  return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+         ((uint64_t)1 << 46);
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint32_t e4m3x2(float v0, float v1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
+  return r;
+}
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t pair) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+  const int e1 = e / 2;
+  return v * exp2i(e1) * exp2i(e - e1);
+}
+__device__ __forceinline__ int split_block_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  if (!(amax <= 3.4028235e38f)) return 127;
+  const int X = ilog2_floor(amax) - 7;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+// 32 values of one thread -> P rows of 32 E4M3 codes with their block exponents (P = 1: MXFP8;
+// P = 2: hi and lo, v left holding the lo remainders).
+template <int P>
+__device__ __forceinline__ void quant32(float* v, uint32_t (&codes)[P][8], int (&X)[P]) {
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) am = fmaxf(am, fabsf(v[i]));
+    X[p] = (P == 1) ? mxfp8_block_exp(am) : split_block_exp(am);
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+      const uint32_t c01 = e4m3x2(mul_pow2(v[i], -X[p]), mul_pow2(v[i + 1], -X[p]));
+      const uint32_t c23 = e4m3x2(mul_pow2(v[i + 2], -X[p]), mul_pow2(v[i + 3], -X[p]));
+      codes[p][i / 4] = c01 | (c23 << 16);
+      if (P == 2 && p == 0) {
+        const float2 h01 = e4m3x2_value(c01), h23 = e4m3x2_value(c23);
+        v[i] -= mul_pow2(h01.x, X[0]);
+        v[i + 1] -= mul_pow2(h01.y, X[0]);
+        v[i + 2] -= mul_pow2(h23.x, X[0]);
+        v[i + 3] -= mul_pow2(h23.y, X[0]);
+      }
+    }
+  }
+}
+
+template <bool GLU, int P>
+__global__ void __launch_bounds__(kThreads, 1) umma_decode_kernel(const __grid_constant__ UDecodeArgs A) {
+  constexpr int kFeat = GLU ? kNW / 2 : kNW;  // output features per item
+  constexpr int kARows = kRows * P;           // activation rows a stage loads
+  constexpr uint32_t kATx = kARows * BKE;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int srow = A.K / 32, spb = exp_pitch(A.K);
+  uint8_t* sB = smem;                                  // kStages x kBTile
+  uint8_t* sA = sB + kStages * kBTile;                 // kStages x kATile + kASlack
+  uint8_t* stg = sA + kStages * kATile + kASlack;      // kStages x kStgBytes
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg + kStages * kStgBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* accf = empty + kStages;
+  uint64_t* acce = accf + 1;
+  uint64_t* drain = acce + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1 + 64);  // the expect_tx arrival + one cp.async arrival per gathering lane
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accf, 1);
+    mbar_init(acce, 2);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  pdl_trigger();
+  const uint32_t tmem = *tmem_slot;
+
+  const int4* ctab = plan_ctab(A.plan, A.E);
+  const int C = A.plan[1];
+  const int fbs = A.N / kFeat;
+  const int items = (C > 0 && C <= A.rows_max / kRows + A.E) ? C * fbs : 0;
+  const int nk = A.K / BKE;
+
+  auto item_of = [&](int u, int& e, int& r0, int& nr, int& f0) -> bool {
+    const int c = u / fbs, fb = u - c * fbs;
+    const int4 t = ctab[c];
+    const bool ok = t.x >= 0 && t.x < A.E && t.y >= 0 && t.z > 0 && t.z <= kRows && t.y + t.z <= A.rows_max;
+    e = ok ? t.x : 0;
+    r0 = ok ? t.y : 0;
+    nr = ok ? t.z : 0;
+    f0 = fb * kFeat;
+    return ok;
+  };
+
+  if (warp == 0) {  // ---------------- tile loads
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+        int e, r0, nr, f0;
+        if (!item_of(u, e, r0, nr, f0)) atomicOr(A.err, kErrIndex);
+        const int wrow = e * A.N + f0;
+        for (int kc = 0; kc < nk; ++kc) {
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
+          mbar_arrive_expect_tx(&full[s], kBPacked + kATx);
+          if (GLU) {
+            tma_load_2d(sB + s * kBTile, &A.tw0, kc * BKE, wrow, &full[s]);
+            tma_load_2d(sB + s * kBTile + (kNW / 2) * 128, &A.tw1, kc * BKE, wrow, &full[s]);
+          } else {
+            tma_load_2d(sB + s * kBTile, &A.tw0, kc * BKE, wrow, &full[s]);
+          }
+          tma_load_2d(sA + s * kATile, &A.ta, kc * BKE, P * r0, &full[s]);
+          if (++s == kStages) { s = 0; ph ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 2 || warp == 3) {  // ---------------- scale gather
+    // warp 2: activation rows (lanes < 8P, word 0) and weight rows 0..127; warp 3: weight rows
+    // 128..255 (GLU: the up rows)
+    const bool w2 = warp == 2;
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+      int e, r0, nr, f0;
+      item_of(u, e, r0, nr, f0);
+      const size_t wrow = (size_t)e * A.N + f0;
+      const uint8_t* ws[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int r = 32 * w + lane + (w2 ? 0 : 128);  // weight row of the item
+        ws[w] = (GLU && r >= kNW / 2) ? A.s1 + (wrow + r - kNW / 2) * srow : A.s0 + (wrow + r) * srow;
+      }
+      const bool act = w2 && lane < P * nr;
+      const uint8_t* as = A.sb + ((size_t)P * r0 + (act ? lane : 0)) * spb;
+      const uint32_t st_lane = smem_u32(stg) + lane * 16;
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
+        const uint32_t so = st_lane + (uint32_t)(s * kStgBytes);
+        if (act) cp_async4(so, as + 4 * kc);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) cp_async4(so + 512 * (w2 ? 1 : 2) + 4 * w, ws[w] + 4 * kc);
+        cp_async_arrive(&full[s]);
+        if (++s == kStages) { s = 0; ph ^= 1; }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // nothing lands after the block has gone
+  } else if (warp == 1) {  // ---------------- MMA issue (converged warp, one elected lane)
+    int s = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+      if (!mbar_wait_warp(acce, aph ^ 1, abort_flag, A.err)) { ok = false; break; }
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!mbar_wait_warp(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
+        const uint32_t tsa = tmem + kSfCol + 12 * s, tsb = tsa + 4;
+        const uint32_t st0 = smem_u32(stg + s * kStgBytes);
+        const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
+        if (elect_one()) {
+          fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
+          tc_fence_after();
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa), "l"(sdesc_sf(st0)));
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb), "l"(sdesc_sf(st0 + 512)));
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb + 4), "l"(sdesc_sf(st0 + 1024)));
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            umma_mx(tmem, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_dec(kk), tsa, tsb,
+                    (kc | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[s]);
+        }
+        __syncwarp();
+        if (++s == kStages) { s = 0; ph ^= 1; }
+      }
+      if (!ok) break;
+      if (elect_one()) umma_commit(accf);
+      __syncwarp();
+      aph ^= 1;
+    }
+    if (elect_one()) {  // every issued MMA has completed before the tensor memory is released
+      umma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(drain, 0, &no_abort, A.err);
+    }
+    __syncwarp();
+  } else if (warp == kEpiWarp0 || warp == kEpiWarp1) {  // ---------------- epilogue (lanes 0..31)
+    // Accumulator lane m = activation row m (sorted row m / P, part m % P); column n = weight
+    // row n of the item. This warp takes columns [h * 128, h * 128 + 128): for the GLU the gate
+    // columns of its 64 features and the matching up columns.
+    const int h = warp == kEpiWarp1 ? 1 : 0;
+    uint32_t aph = 0;
+    for (int u = blockIdx.x; u < items; u += gridDim.x) {
+      int e, r0, nr, f0;
+      item_of(u, e, r0, nr, f0);
+      if (!mbar_wait_warp(accf, aph, abort_flag, A.err)) break;
+      aph ^= 1;
+      tc_fence_after();
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int col = GLU ? (c < 2 ? 64 * h + 32 * c : kNW / 2 + 64 * h + 32 * (c - 2)) : 128 * h + 32 * c;
+        uint32_t r[32];
+        tmem_ld32(tmem + (uint32_t)col, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[32 * c + i] = __uint_as_float(r[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce);  // the accumulator may be overwritten now
+      if (P == 2) {  // lane 2j holds the hi part of sorted row j, lane 2j + 1 the lo part
+#pragma unroll
+        for (int i = 0; i < 128; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 1);
+      }
+      const int jr = lane / P;
+      const bool mine = (lane % P) == 0 && jr < nr;
+      if (GLU) {
+        // v[0..63] gate, v[64..127] up of features f0 + 64h + i; one 32-feature block at a time
+        const int spo = exp_pitch(A.N);
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          float a[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float g = v[32 * b + i];  // silu(g) = g / (1 + e^-g), fast forms (~1e-6 relative)
+            a[i] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * v[64 + 32 * b + i]));
+          }
+          if (mine) {
+            uint32_t codes[P][8];
+            int X[P];
+            quant32<P>(a, codes, X);
+            const int f = f0 + 64 * h + 32 * b;
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+              const size_t brow = (size_t)P * (r0 + jr) + p;
+              uint4* dst = reinterpret_cast<uint4*>(A.aq + brow * A.N + f);
+              dst[0] = make_uint4(codes[p][0], codes[p][1], codes[p][2], codes[p][3]);
+              dst[1] = make_uint4(codes[p][4], codes[p][5], codes[p][6], codes[p][7]);
+              A.aqs[brow * spo + f / 32] = (uint8_t)(X[p] + 127);
+            }
+          }
+        }
+      } else if (mine) {
+        float4* dst = reinterpret_cast<float4*>(A.o_out + (size_t)(r0 + jr) * A.N + f0 + 128 * h);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kBTile + kATile + kStgBytes) + kASlack + (2 * kStages + 3) * 8 + 16;
+static_assert(kSmem <= 227 * 1024, "shared memory");
+
+template <bool GLU, int P>
+cudaError_t launch_t(UDecodeArgs& a, int items_max, cudaStream_t s) {
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_decode_kernel<GLU, P>), kSmem);
+  if (e != cudaSuccess) return e;
+  int grid = num_sms();
+  if (items_max < grid) grid = items_max > 0 ? items_max : 1;
+  return launch_pdl(umma_decode_kernel<GLU, P>, dim3(grid), dim3(kThreads), kSmem, s, a);
+}
+
+}  // namespace
+
+cudaError_t launch_umma_decode_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
+                                   const uint8_t* bq, const uint8_t* bs, int P, int T, uint8_t* aq,
+                                   uint8_t* aqs, uint32_t* err, cudaStream_t s) {
+  UDecodeArgs A{};
+  const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
+  if (!make_tmap_fp4(&A.tw0, w.gate_q, d.latent, wrows, pitch, kNW / 2) ||
+      !make_tmap_fp4(&A.tw1, w.up_q, d.latent, wrows, pitch, kNW / 2))
+    return cudaErrorInvalidValue;
+  const int rows = T * d.top_k;
+  if (!make_tmap_2d(&A.ta, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, kRows * P,
+                    true))
+    return cudaErrorInvalidValue;
+  A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
+  A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
+  A.aq = aq; A.aqs = aqs; A.err = err;
+  const int items_max = (rows / kRows + d.n_experts) * (d.inter / (kNW / 2));
+  return P == 1 ? launch_t<true, 1>(A, items_max, s) : launch_t<true, 2>(A, items_max, s);
+}
+
+cudaError_t launch_umma_decode_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
+                                    const uint8_t* aq, const uint8_t* aqs, int P, int T, float* o_rows,
+                                    uint32_t* err, cudaStream_t s) {
+  UDecodeArgs A{};
+  if (!make_tmap_fp4(&A.tw0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, kNW))
+    return cudaErrorInvalidValue;
+  const int rows = T * d.top_k;
+  if (!make_tmap_2d(&A.ta, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, kRows * P, true))
+    return cudaErrorInvalidValue;
+  A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
+  A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
+  A.o_out = o_rows; A.err = err;
+  const int items_max = (rows / kRows + d.n_experts) * (d.latent / kNW);
+  return P == 1 ? launch_t<false, 1>(A, items_max, s) : launch_t<false, 2>(A, items_max, s);
+}
+
+}  // namespace k3moe

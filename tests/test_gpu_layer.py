@@ -93,15 +93,15 @@ def test_expert_ffn_gemv_path_all_rows(T):
     assert rel_l2_rows(o, want).max() <= REL_L2
 
 
-@pytest.mark.parametrize("T", [40, 96])
-def test_expert_ffn_k3_sampled_rows(k3_layer, T):
+@pytest.mark.parametrize("T,actq", [(40, 0), (40, 1), (96, 0), (96, 1)])
+def test_expert_ffn_k3_sampled_rows(k3_layer, T, actq):
     d = synth.K3
     z = synth.host_bf16_normal(7, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
     idx = synth.host_topk_sets(8, T, d.n_experts, d.top_k, "zipf")  # skewed: multi-chunk experts
-    o, (off, rt, rs, sr) = _expert_ffn(k3_layer, z, idx)
+    o, (off, rt, rs, sr) = _expert_ffn(k3_layer, z, idx, actq)
     rng = np.random.default_rng(0)
     rows = sorted(set(rng.choice(T * d.top_k, 12, replace=False).tolist()) | {0, T * d.top_k - 1})
-    ol = k3_layer.oracle(experts={int(idx[rt[r], rs[r]]) for r in rows})
+    ol = k3_layer.oracle(experts={int(idx[rt[r], rs[r]]) for r in rows}, actq=actq)
     for r in rows:
         want = ol.expert_row(int(idx[rt[r], rs[r]]), z[rt[r]])[0]
         assert rel_l2_rows(o[r], want) <= REL_L2, (r, rel_l2_rows(o[r], want))

@@ -503,8 +503,9 @@ cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t 
   return P == 1 ? launch_t<GLU, 1, kUmmaChunkRows>(a, items_max, s) : launch_t<GLU, 2, kUmmaChunkRows>(a, items_max, s);
 }
 
-// z[row_token[r]] (bf16) -> P e4m3 rows with e8m0 block scales per sorted row r. One warp
-// per row; each lane takes 8 consecutive values, four lanes one 32-value block.
+// z[row_token[r]] (bf16) -> P e4m3 rows with e8m0 block scales per sorted row r. One warp per
+// (sorted row, 256-value segment), so every load of a launch is in flight at once; each lane
+// takes 8 consecutive values, four lanes one 32-value block.
 template <int P>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ z,
                                                          const int32_t* __restrict__ row_token, int rows,
@@ -513,52 +514,52 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (r >= rows) return;  // warp-uniform
+  const int segs = (L + 255) / 256;
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (wid >= (long long)rows * segs) return;  // warp-uniform
+  const int r = (int)(wid / segs), base = (int)(wid % segs) * 256;
   int t = row_token[r];
   if (t < 0 || t >= T) {
-    if (lane == 0) atomicOr(err, kErrIndex);
+    if (lane == 0 && base == 0) atomicOr(err, kErrIndex);
     t = 0;
   }
   const int sp = exp_pitch(L);
-  for (int base = 0; base < L; base += 256) {
-    const int col = base + 8 * lane;
-    const bool act = col < L;  // L is a multiple of 32: a block is all in or all out
-    float v[8];
-    if (act) {
-      const uint4 w = *reinterpret_cast<const uint4*>(z + (size_t)t * L + col);
-      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  const int col = base + 8 * lane;
+  const bool act = col < L;  // L is a multiple of 32: a block is all in or all out
+  float v[8];
+  if (act) {
+    const uint4 w = *reinterpret_cast<const uint4*>(z + (size_t)t * L + col);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[2 * i] = __uint_as_float(ww[i] << 16);
-        v[2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = 0.f;
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(ww[i] << 16);
+      v[2 * i + 1] = __uint_as_float(ww[i] & 0xffff0000u);
     }
+  } else {
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-      float am = 0.f;
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
-      const int X = p == 0 ? block_exp<P>(max_in_group4(am)) : split_block_exp(max_in_group4(am));
-      uint32_t codes[4];
+  for (int p = 0; p < P; ++p) {
+    float am = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        codes[i] = e4m3x2(mul_pow2(v[2 * i], -X), mul_pow2(v[2 * i + 1], -X));
-        if (P == 2 && p == 0) {  // keep the remainder for the lo row (exact)
-          const float2 h = e4m3x2_value(codes[i]);
-          v[2 * i] -= mul_pow2(h.x, X);
-          v[2 * i + 1] -= mul_pow2(h.y, X);
-        }
+    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+    const int X = p == 0 ? block_exp<P>(max_in_group4(am)) : split_block_exp(max_in_group4(am));
+    uint32_t codes[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      codes[i] = e4m3x2(mul_pow2(v[2 * i], -X), mul_pow2(v[2 * i + 1], -X));
+      if (P == 2 && p == 0) {  // keep the remainder for the lo row (exact)
+        const float2 h = e4m3x2_value(codes[i]);
+        v[2 * i] -= mul_pow2(h.x, X);
+        v[2 * i + 1] -= mul_pow2(h.y, X);
       }
-      if (act) {
-        const size_t row = (size_t)P * r + p;
-        *reinterpret_cast<uint2*>(bq + row * L + col) =
-            make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16));
-        if ((lane & 3) == 0) bs[row * sp + col / 32] = (uint8_t)(X + 127);
-      }
+    }
+    if (act) {
+      const size_t row = (size_t)P * r + p;
+      *reinterpret_cast<uint2*>(bq + row * L + col) =
+          make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16));
+      if ((lane & 3) == 0) bs[row * sp + col / 32] = (uint8_t)(X + 127);
     }
   }
 }
@@ -569,7 +570,8 @@ cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int r
                               uint8_t* bq, uint8_t* bs, uint32_t* err, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int warps = 8;
-  const dim3 grid((rows + warps - 1) / warps), block(32 * warps);
+  const long long units = (long long)rows * ((L + 255) / 256);
+  const dim3 grid((unsigned)((units + warps - 1) / warps)), block(32 * warps);
   if (P == 1) return launch_pdl(quant_rows_kernel<1>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, err);
   return launch_pdl(quant_rows_kernel<2>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, err);
 }

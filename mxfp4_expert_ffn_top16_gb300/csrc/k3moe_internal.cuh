@@ -119,7 +119,7 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
                            int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s);
 cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,
                         cudaStream_t s);
-// Top-k + permutation + plan in one block, for T <= kSmallRouteTokens.
+// Top-k (one block per token), then permutation + plan in one block, for T <= kSmallRouteTokens.
 constexpr int kSmallRouteTokens = 64;
 cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                                     int32_t* offsets, int32_t* row_token, int32_t* row_slot,

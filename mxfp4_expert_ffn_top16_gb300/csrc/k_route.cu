@@ -7,8 +7,7 @@
 // and their weights are the softmax over the kept logits, which equals softmax over all
 // logits renormalised over the kept ones.
 //
-// Top-k: one warp per token, each lane holding E/32 logits as order-preserving 64-bit keys
-// (float key, then inverted index) in registers; k rounds of a warp max.
+// Top-k: one CTA per token, a radix select over order-preserving 32-bit keys of the logits.
 // Permutation: rows grouped by expert, token order inside an expert (the order a stable
 // counting sort gives). Histogram -> exclusive scan -> scatter; the scatter walks tokens in
 // chunks of 32 (one per lane) and ranks a (token, expert) pair inside its chunk with a
@@ -20,7 +19,6 @@ namespace k3moe {
 namespace {
 
 constexpr int kMaxE = 1024;
-constexpr int kMaxPerLane = kMaxE / 32;
 
 // Order-preserving 32-bit key of a logit: larger logit -> larger key. -0 equals +0; NaN gets
 // 1, below every number (numbers map to >= 0x007fffff); 0 marks an empty or taken slot.
@@ -31,85 +29,132 @@ __device__ __forceinline__ uint32_t sort_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+// One CTA of 256 threads routes one token. Radix select over the 32-bit keys, one 8-bit digit
+// per pass (a shared histogram, then one warp finds the digit holding the k-th largest key),
+// gives the k-th largest key; keys above it are kept, and of the keys equal to it the
+// lowest-indexed ones (ranked by a block count in index order). One warp sorts the kept
+// experts by index and writes them with the softmax weights over their logits.
+constexpr int kTopkThreads = 256;
+constexpr int kTopkKeys = kMaxE / kTopkThreads;  // keys per thread
+__global__ void __launch_bounds__(kTopkThreads) topk_block_kernel(const float* __restrict__ logits, int T, int E,
+                                                                  int k, int32_t* idx, float* w) {
+  __shared__ int hist[256];
+  __shared__ int s_digit, s_above, s_nsel;
+  __shared__ int wcnt[kTopkKeys][kTopkThreads / 32];
+  __shared__ int sel_e[32];
+  __shared__ float sel_l[32];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x;
+  if (t >= T) return;  // block-uniform
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const unsigned lt = (1u << lane) - 1u;
+  const float* lg = logits + (size_t)t * E;
+  uint32_t key[kTopkKeys];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w > v ? w : v;
+  for (int i = 0; i < kTopkKeys; ++i) {
+    const int e = tid + kTopkThreads * i;
+    key[i] = e < E ? sort_key(lg[e]) : 0u;  // 0 = no expert (below every key, even NaN's)
   }
-  return v;
-}
-
-// One warp selects the top-k of one token's logits row. Lanes j < k end with
-// (*sel_idx, *sel_logit) = the j-th largest; returns nothing for lanes >= k.
-__device__ void warp_topk(const float* __restrict__ lg, int E, int k, int lane, int* sel_idx,
-                          float* sel_logit) {
-  // slot j of this lane holds expert lane + 32 j; within a lane the lowest j wins ties
-  uint32_t keys[kMaxPerLane];
-  const int per = (E + 31) / 32;
+  if (tid == 0) s_nsel = 0;
+  uint32_t thr = 0u, pmask = 0u;
+  int need = k;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    hist[tid] = 0;
+    __syncthreads();
 #pragma unroll
-  for (int j = 0; j < kMaxPerLane; ++j) {
-    const int e = lane + 32 * j;
-    keys[j] = (j < per && e < E) ? sort_key(lg[e]) : 0u;
+    for (int i = 0; i < kTopkKeys; ++i)
+      if (key[i] != 0u && (key[i] & pmask) == thr) atomicAdd(&hist[(key[i] >> shift) & 255], 1);
+    __syncthreads();
+    if (wid == 0) {  // digits in descending order: lane l covers 255 - 8l .. 248 - 8l
+      int c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[255 - 8 * lane - j];
+        sum += c[j];
+      }
+      int inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+      }
+      int run = inc - sum;
+      if (run < need && need <= inc) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (run < need && need <= run + c[j]) {
+            s_digit = 255 - 8 * lane - j;
+            s_above = run;
+          }
+          run += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    thr |= (uint32_t)s_digit << shift;
+    pmask |= 255u << shift;
+    need -= s_above;
   }
-  // (key, inverted expert index) of this lane's best remaining slot
-  auto local_best = [&]() -> unsigned long long {
-    uint32_t bk = 0u;
-    int bj = 0;
+  // thr is the k-th largest key; take `need` of the keys equal to it, lowest index first
+  int rank_in_warp[kTopkKeys];
 #pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j)
-      if (keys[j] > bk) { bk = keys[j]; bj = j; }
-    return bk == 0u ? 0ull
-                    : ((unsigned long long)bk << 32) | (uint32_t)(0xffffffffu - (uint32_t)(lane + 32 * bj));
-  };
-  unsigned long long best = local_best();
-  int my_idx = -1;
-  for (int r = 0; r < k; ++r) {
-    const unsigned long long win = warp_max_u64(best);
-    const int widx = (int)(0xffffffffu - (uint32_t)(win & 0xffffffffu));
-    if (lane == r) my_idx = widx;
-    if ((widx & 31) == lane) {  // owner takes the slot and rescans
-      const int wj = widx >> 5;
+  for (int i = 0; i < kTopkKeys; ++i) {
+    const unsigned b = __ballot_sync(0xffffffffu, key[i] == thr);
+    rank_in_warp[i] = __popc(b & lt);
+    if (lane == 0) wcnt[i][wid] = __popc(b);
+  }
+  __syncthreads();
+  int before = 0;
 #pragma unroll
-      for (int j = 0; j < kMaxPerLane; ++j)
-        if (j == wj) keys[j] = 0u;
-      best = local_best();
+  for (int i = 0; i < kTopkKeys; ++i) {
+    int bw = 0, tot = 0;
+#pragma unroll
+    for (int x = 0; x < kTopkThreads / 32; ++x) {
+      bw += x < wid ? wcnt[i][x] : 0;
+      tot += wcnt[i][x];
+    }
+    const bool sel = key[i] > thr || (key[i] == thr && before + bw + rank_in_warp[i] < need);
+    if (sel) {
+      const int slot = atomicAdd(&s_nsel, 1);
+      const int e = tid + kTopkThreads * i;
+      sel_e[slot] = e;
+      sel_l[slot] = lg[e];
+    }
+    before += tot;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    int e = lane < k ? sel_e[lane] : 0x7fffffff;
+    float l = lane < k ? sel_l[lane] : 0.f;
+    // bitonic sort by expert index, ascending
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const int pe = __shfl_xor_sync(0xffffffffu, e, stride);
+        const float pl = __shfl_xor_sync(0xffffffffu, l, stride);
+        const bool up = (lane & size) == 0 || size == 32;
+        const bool lower = (lane & stride) == 0;
+        if (lower == up ? pe < e : pe > e) {
+          e = pe;
+          l = pl;
+        }
+      }
+    }
+    float lmax = lane < k ? l : -3.402823466e38f;
+    lmax = warp_max(lmax);
+    const float ex = lane < k ? expf(l - lmax) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+      idx[(size_t)t * k + lane] = e;
+      w[(size_t)t * k + lane] = ex / sum;
     }
   }
-  *sel_idx = my_idx;
-  *sel_logit = (lane < k && my_idx >= 0) ? lg[my_idx] : 0.0f;
-}
-
-// Writes one token's k indices in ascending order with their renormalised weights.
-__device__ void warp_write_topk(int sel, float l, int k, int lane, int32_t* idx_row, float* w_row,
-                                int* smem_idx_row) {
-  const bool act = lane < k;
-  const float lmax = __shfl_sync(0xffffffffu, l, 0);  // lane 0 holds the largest
-  const float ex = act ? expf(l - lmax) : 0.0f;
-  float sum = ex;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  int rank = 0;
-  for (int j = 0; j < k; ++j) {
-    const int other = __shfl_sync(0xffffffffu, sel, j);
-    rank += (act && other < sel) ? 1 : 0;
-  }
-  if (act) {
-    idx_row[rank] = sel;
-    w_row[rank] = ex / sum;
-    if (smem_idx_row) smem_idx_row[rank] = sel;
-  }
-}
-
-__global__ void topk_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* idx,
-                            float* w) {
-  const int lane = threadIdx.x & 31;
-  const int tok = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (tok >= T) return;
-  int sel;
-  float l;
-  warp_topk(logits + (size_t)tok * E, E, k, lane, &sel, &l);
-  warp_write_topk(sel, l, k, lane, idx + (size_t)tok * k, w + (size_t)tok * k, nullptr);
 }
 
 // ---------------------------------------------------------------- block-level building blocks
@@ -186,34 +231,53 @@ __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, i
 __device__ void warp_scatter(const int32_t* __restrict__ idx, int t0, int t1, int E, int k,
                              int* base, unsigned* mask, int32_t* row_token, int32_t* row_slot,
                              int32_t* slot_row, uint32_t* err) {
+  constexpr int kHalfK = 16;  // a token's slots are handled 16 at a time (k <= 32)
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   for (int c0 = t0; c0 < t1; c0 += 32) {
     const int t = c0 + lane;
     const bool v = t < t1;
-    for (int j = 0; j < k; ++j) {
-      const int e = v ? idx[(size_t)t * k + j] : -1;
-      if (v && (e < 0 || e >= E)) atomicOr(err, kErrIndex);
-      if (v && e >= 0 && e < E) atomicOr(&mask[e], 1u << lane);
+    // slots j0..j0+15 of this lane's token, read in one go (-1: none or out of range)
+    auto load = [&](int j0, int (&ev)[kHalfK], bool report) {
+#pragma unroll
+      for (int q = 0; q < kHalfK; ++q) {
+        const int j = j0 + q;
+        const int e = (v && j < k) ? idx[(size_t)t * k + j] : -1;
+        if (report && v && j < k && (e < 0 || e >= E)) atomicOr(err, kErrIndex);
+        ev[q] = (e >= 0 && e < E) ? e : -1;
+      }
+    };
+    int ev[kHalfK];
+    for (int j0 = 0; j0 < k; j0 += kHalfK) {
+      load(j0, ev, true);
+#pragma unroll
+      for (int q = 0; q < kHalfK; ++q)
+        if (ev[q] >= 0) atomicOr(&mask[ev[q]], 1u << lane);
     }
     __syncwarp();
-    for (int j = 0; j < k; ++j) {
-      const int e = v ? idx[(size_t)t * k + j] : -1;
-      if (v && e >= 0 && e < E) {
-        const int r = base[e] + __popc(mask[e] & lt);
-        row_token[r] = t;
-        row_slot[r] = j;
-        slot_row[(size_t)t * k + j] = r;
+    for (int j0 = 0; j0 < k; j0 += kHalfK) {
+      load(j0, ev, false);
+#pragma unroll
+      for (int q = 0; q < kHalfK; ++q) {
+        if (ev[q] >= 0) {
+          const int r = base[ev[q]] + __popc(mask[ev[q]] & lt);
+          row_token[r] = t;
+          row_slot[r] = j0 + q;
+          slot_row[(size_t)t * k + j0 + q] = r;
+        }
       }
     }
     __syncwarp();
-    for (int j = 0; j < k; ++j) {
-      const int e = v ? idx[(size_t)t * k + j] : -1;
-      if (v && e >= 0 && e < E) {
-        const unsigned m = mask[e];
-        if ((m & lt) == 0u) {  // lowest lane holding e advances its base and clears
-          base[e] += __popc(m);
-          mask[e] = 0u;
+    for (int j0 = 0; j0 < k; j0 += kHalfK) {
+      load(j0, ev, false);
+#pragma unroll
+      for (int q = 0; q < kHalfK; ++q) {
+        if (ev[q] >= 0) {
+          const unsigned m = mask[ev[q]];
+          if ((m & lt) == 0u) {  // lowest lane holding e advances its base and clears
+            base[ev[q]] += __popc(m);
+            mask[ev[q]] = 0u;
+          }
         }
       }
     }
@@ -222,38 +286,31 @@ __device__ void warp_scatter(const int32_t* __restrict__ idx, int t0, int t1, in
 }
 
 // ---------------------------------------------------------------- single-CTA permutation
-// For T*k small: histogram, scan, scatter and plan in one block of 1024 threads.
-// With `logits` given, the block first selects the top-k of each token (one warp per token)
-// into idx / w, so decode routing is a single launch.
-__global__ void __launch_bounds__(1024) permute_small_kernel(const float* __restrict__ logits,
-                                                             float* w, int32_t* idx, int T,
-                                                             int E, int k, int32_t* offsets,
-                                                             int32_t* row_token, int32_t* row_slot,
-                                                             int32_t* slot_row, int32_t* plan,
-                                                             uint32_t* err) {
+// For T * k small: histogram, scan, scatter and plan in one block of 1024 threads (the indices
+// pass through shared memory when T * k <= kSmallIdx).
+constexpr int kSmallIdx = 2048;
+__global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* idx, int T, int E, int k,
+                                                             int32_t* offsets, int32_t* row_token,
+                                                             int32_t* row_slot, int32_t* slot_row,
+                                                             int32_t* plan, uint32_t* err) {
   __shared__ int cnt[kMaxE + 1];
   __shared__ int tmp[1024];
   __shared__ int flag[kMaxE];
   __shared__ int chunks[kMaxE];
   __shared__ unsigned mask[kMaxE];
+  __shared__ int s_idx[kSmallIdx];
   const int tid = threadIdx.x;
   pdl_wait();
   pdl_trigger();
-  if (logits) {
-    const int lane = tid & 31;
-    for (int t = tid >> 5; t < T; t += blockDim.x >> 5) {
-      int sel;
-      float l;
-      warp_topk(logits + (size_t)t * E, E, k, lane, &sel, &l);
-      warp_write_topk(sel, l, k, lane, idx + (size_t)t * k, w + (size_t)t * k, nullptr);
-    }
-    __syncthreads();
-  }
+  const bool in_smem = T * k <= kSmallIdx;
+  if (in_smem)
+    for (int i = tid; i < T * k; i += blockDim.x) s_idx[i] = idx[i];
   if (tid <= E) cnt[tid] = 0;
   if (tid < E) mask[tid] = 0u;
   __syncthreads();
+  const int32_t* ix = in_smem ? s_idx : idx;
   for (int i = tid; i < T * k; i += blockDim.x) {
-    const int e = idx[i];
+    const int e = ix[i];
     if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
   }
   __syncthreads();
@@ -265,7 +322,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const float* __rest
   // plan reads the offsets before the scatter turns cnt into running bases
   build_plan(cnt, E, T * k, plan, tmp, flag, chunks);
   __syncthreads();
-  if (tid < 32) warp_scatter(idx, 0, T, E, k, cnt, mask, row_token, row_slot, slot_row, err);
+  if (tid < 32) warp_scatter(ix, 0, T, E, k, cnt, mask, row_token, row_slot, slot_row, err);
 }
 
 // ---------------------------------------------------------------- multi-CTA permutation
@@ -366,17 +423,14 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  const int warps = 8;
-  topk_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, T, E, k, idx, w);
-  return cudaGetLastError();
+  return launch_pdl(topk_block_kernel, dim3(T), dim3(kTopkThreads), 0, s, logits, T, E, k, idx, w);
 }
 
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* offsets,
                            int32_t* row_token, int32_t* row_slot, int32_t* slot_row,
                            int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s) {
   if (T <= kBlockTokens) {
-    permute_small_kernel<<<1, 1024, 0, s>>>(nullptr, nullptr, const_cast<int32_t*>(idx), T, E, k,
-                                            offsets, row_token, row_slot, slot_row, plan, err);
+    permute_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, k, offsets, row_token, row_slot, slot_row, plan, err);
     return cudaGetLastError();
   }
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
@@ -389,7 +443,9 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
 cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                                     int32_t* offsets, int32_t* row_token, int32_t* row_slot,
                                     int32_t* slot_row, int32_t* plan, uint32_t* err, cudaStream_t s) {
-  return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, logits, w, idx, T, E, k, offsets,
+  cudaError_t e = launch_pdl(topk_block_kernel, dim3(T), dim3(kTopkThreads), 0, s, logits, T, E, k, idx, w);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)idx, T, E, k, offsets,
                     row_token, row_slot, slot_row, plan, err);
 }
 

@@ -150,12 +150,12 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s);
 // Decode (T < kUmmaExpertMinTokens): the same GEMMs with the weights on the MMA's N side (256
 // weight rows per MMA, 8-row chunks). The down pass needs latent % 256 == 0.
-cudaError_t launch_umma_decode_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                                   const uint8_t* bq, const uint8_t* bs, int P, int T, uint8_t* aq,
-                                   uint8_t* aqs, uint32_t* err, cudaStream_t s);
-cudaError_t launch_umma_decode_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                                    const uint8_t* aq, const uint8_t* aqs, int P, int T, float* o_rows,
-                                    uint32_t* err, cudaStream_t s);
+cudaError_t launch_umma_wn_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
+                               const uint8_t* bq, const uint8_t* bs, int P, int T, uint8_t* aq,
+                               uint8_t* aqs, uint32_t* err, cudaStream_t s);
+cudaError_t launch_umma_wn_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
+                                const uint8_t* aq, const uint8_t* aqs, int P, int T, float* o_rows,
+                                uint32_t* err, cudaStream_t s);
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s);
 

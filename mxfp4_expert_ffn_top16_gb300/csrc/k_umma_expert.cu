@@ -580,7 +580,7 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
                             cudaStream_t s) {
   const int R = umma_chunk_rows(T);
-  if (R == kGemvTokens) return launch_umma_decode_glu(d, w, plan, bq, bs, P, T, aq, aqs, err, s);
+  if (R == kGemvTokens) return launch_umma_wn_glu(d, w, plan, bq, bs, P, T, aq, aqs, err, s);
   UExpertArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
   if (!make_tmap_fp4(&A.ta0, w.gate_q, d.latent, wrows, pitch, 64) ||
@@ -600,7 +600,7 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s) {
   const int R = umma_chunk_rows(T);
   if (R == kGemvTokens && d.latent % 256 == 0)
-    return launch_umma_decode_down(d, w, plan, aq, aqs, P, T, o_rows, err, s);
+    return launch_umma_wn_down(d, w, plan, aq, aqs, P, T, o_rows, err, s);
   UExpertArgs A{};
   if (!make_tmap_fp4(&A.ta0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, 128))
     return cudaErrorInvalidValue;

@@ -48,7 +48,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = kNW;          // 12 columns per stage: A 4, B 8
 static_assert(kSfCol + 12 * kStages <= kTmemCols, "tensor memory");
 
-struct UDecodeArgs {
+struct UWnArgs {
   CUtensorMap tw0;     // GLU: gate codes, box {128, 128}; down: down codes, box {128, 256}
   CUtensorMap tw1;     // GLU: up codes, box {128, 128}
   CUtensorMap ta;      // activation rows e4m3 {K, P*rows}, box {128, 8*P}
@@ -134,7 +134,7 @@ __device__ __forceinline__ void quant32(float* v, uint32_t (&codes)[P][8], int (
 }
 
 template <bool GLU, int P>
-__global__ void __launch_bounds__(kThreads, 1) umma_decode_kernel(const __grid_constant__ UDecodeArgs A) {
+__global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_constant__ UWnArgs A) {
   constexpr int kFeat = GLU ? kNW / 2 : kNW;  // output features per item
   constexpr int kARows = kRows * P;           // activation rows a stage loads
   constexpr uint32_t kATx = kARows * BKE;
@@ -359,20 +359,20 @@ constexpr size_t kSmem = 1024 + (size_t)kStages * (kBTile + kATile + kStgBytes) 
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
 template <bool GLU, int P>
-cudaError_t launch_t(UDecodeArgs& a, int items_max, cudaStream_t s) {
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_decode_kernel<GLU, P>), kSmem);
+cudaError_t launch_t(UWnArgs& a, int items_max, cudaStream_t s) {
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_wn_kernel<GLU, P>), kSmem);
   if (e != cudaSuccess) return e;
   int grid = num_sms();
   if (items_max < grid) grid = items_max > 0 ? items_max : 1;
-  return launch_pdl(umma_decode_kernel<GLU, P>, dim3(grid), dim3(kThreads), kSmem, s, a);
+  return launch_pdl(umma_wn_kernel<GLU, P>, dim3(grid), dim3(kThreads), kSmem, s, a);
 }
 
 }  // namespace
 
-cudaError_t launch_umma_decode_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                                   const uint8_t* bq, const uint8_t* bs, int P, int T, uint8_t* aq,
-                                   uint8_t* aqs, uint32_t* err, cudaStream_t s) {
-  UDecodeArgs A{};
+cudaError_t launch_umma_wn_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
+                               const uint8_t* bq, const uint8_t* bs, int P, int T, uint8_t* aq,
+                               uint8_t* aqs, uint32_t* err, cudaStream_t s) {
+  UWnArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
   if (!make_tmap_fp4(&A.tw0, w.gate_q, d.latent, wrows, pitch, kNW / 2) ||
       !make_tmap_fp4(&A.tw1, w.up_q, d.latent, wrows, pitch, kNW / 2))
@@ -388,10 +388,10 @@ cudaError_t launch_umma_decode_glu(const k3moe_dims& d, const k3moe_weights& w, 
   return P == 1 ? launch_t<true, 1>(A, items_max, s) : launch_t<true, 2>(A, items_max, s);
 }
 
-cudaError_t launch_umma_decode_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                                    const uint8_t* aq, const uint8_t* aqs, int P, int T, float* o_rows,
-                                    uint32_t* err, cudaStream_t s) {
-  UDecodeArgs A{};
+cudaError_t launch_umma_wn_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
+                                const uint8_t* aq, const uint8_t* aqs, int P, int T, float* o_rows,
+                                uint32_t* err, cudaStream_t s) {
+  UWnArgs A{};
   if (!make_tmap_fp4(&A.tw0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, kNW))
     return cudaErrorInvalidValue;
   const int rows = T * d.top_k;

@@ -65,11 +65,16 @@ def _expert_ffn(lay, z_np, idx_np, actq=0):
     return o.cpu().numpy().astype(np.float64), (off, rt, rs, sr)
 
 
-# T >= 65 runs the block-scaled tensor-core path, smaller T the GEMV path
-@pytest.mark.parametrize("T", [24, 100])
+# T >= 65 runs the tensor-core kernel with the weights on the MMA's M side (chunks of up to 112
+# sorted rows); smaller T the one with the weights on N (chunks of up to 8), whose down pass needs
+# latent % 256 == 0 (latent = 128 keeps the M-side kernel for it).
+WIDE = synth.Dims(hidden=256, latent=256, inter=256, n_experts=16, top_k=4)
+
+
+@pytest.mark.parametrize("dname,T", [("tiny", 24), ("tiny", 100), ("wide", 7), ("wide", 200)])
 @pytest.mark.parametrize("actq", [0, 1])
-def test_expert_ffn_tiny_all_rows(actq, T):
-    d = synth.TINY
+def test_expert_ffn_tiny_all_rows(actq, dname, T):
+    d = synth.TINY if dname == "tiny" else WIDE
     lay = DeviceLayer(d, seed=0, actq=actq)
     z = synth.host_bf16_normal(3, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
     idx = synth.host_topk_sets(4, T, d.n_experts, d.top_k, "zipf")
@@ -107,10 +112,10 @@ def test_expert_ffn_k3_sampled_rows(k3_layer, T, actq):
         assert rel_l2_rows(o[r], want) <= REL_L2, (r, rel_l2_rows(o[r], want))
 
 
-@pytest.mark.parametrize("T", [8, 80])
-def test_expert_ffn_invariants_bit_exact(T):
+@pytest.mark.parametrize("dname,T", [("tiny", 8), ("tiny", 80), ("wide", 80)])
+def test_expert_ffn_invariants_bit_exact(dname, T):
     """All-zero codes give exactly 0; +1 on every up exponent doubles every output exactly."""
-    d = synth.TINY
+    d = synth.TINY if dname == "tiny" else WIDE
     z = synth.host_bf16_normal(2, synth.S_X, 0, T * d.latent, 1.0).reshape(T, d.latent)
     idx = synth.host_topk_sets(5, T, d.n_experts, d.top_k, "uniform")
     base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
@@ -123,9 +128,9 @@ def test_expert_ffn_invariants_bit_exact(T):
     np.testing.assert_array_equal(o2, 2 * o1)
 
 
-@pytest.mark.parametrize("T", [4, 72])
-def test_expert_ffn_nan_scale_gives_nonfinite(T):
-    d = synth.TINY
+@pytest.mark.parametrize("dname,T", [("tiny", 4), ("tiny", 72), ("wide", 72)])
+def test_expert_ffn_nan_scale_gives_nonfinite(dname, T):
+    d = synth.TINY if dname == "tiny" else WIDE
     base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
     base[0]["down_s"] = base[0]["down_s"].copy()
     base[0]["down_s"][:, 0] = 255

@@ -142,6 +142,9 @@ def kernel_cost(name, d, T, distinct, rows, actq):
                            4 * rows * L * I, "fp8"),
         "expert_down_mma": (distinct * down_w + P * rows * (I + I // 32) + 4 * rows * L,
                             2 * rows * L * I, "fp8"),
+        # both passes in one launch (decode): the GLU output is written and read back once
+        "expert_ffn_mma": (distinct * (glu_w + down_w) + P * rows * (L + L // 32) +
+                           2 * P * rows * (I + I // 32) + 4 * rows * L, 6 * rows * L * I, "fp8"),
         "combine": (rows * 4 * L + 2 * T * L, 0, None),
     }
     return table.get(name, (None, 0, None))

@@ -82,6 +82,7 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
     L.bs = take(P * rows * (size_t)exp_pitch(d.latent));
     L.aq = take(P * rows * I);
     L.aqs = take(P * rows * (size_t)exp_pitch(d.inter));
+    L.chunk_done = take((size_t)plan_chunks_max(d, T) * 4);
   }
   L.total = off;
   return L;
@@ -139,12 +140,12 @@ k3moe_status check_weights(const k3moe_weights* w, bool dense, bool experts) {
 // ---------------------------------------------------------------- diagnostic profiling
 enum ProfId {
   P_ROUTER_LATENT = 0, P_TOPK, P_PERMUTE, P_GLU, P_DOWN, P_COMBINE, P_LATENT_OUT, P_QUANT,
-  P_GLU_MMA, P_DOWN_MMA, P_COUNT
+  P_GLU_MMA, P_DOWN_MMA, P_FFN_MMA, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"router_latent_in", "topk", "permute",
                                          "expert_glu_gemv", "expert_down_gemv", "combine",
                                          "latent_out", "expert_act_quant", "expert_glu_mma",
-                                         "expert_down_mma"};
+                                         "expert_down_mma", "expert_ffn_mma"};
 struct Profiler {
   bool on = false;
   static constexpr int kMax = 65536;
@@ -187,18 +188,34 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
   int32_t* plan = at<int32_t>(ws, L.plan);
   if (umma_expert_ok(d)) {
     const int P = d.actq ? 1 : 2;
+    int* cnt = at<int>(ws, L.chunk_done);
     {
       ProfScope p(P_QUANT, s);
       K3_CUDA(launch_quant_rows(z, row_token, T * d.top_k, T, d.latent, P, at<uint8_t>(ws, L.bq),
-                                at<uint8_t>(ws, L.bs), err, s));
+                                at<uint8_t>(ws, L.bs), cnt, plan_chunks_max(d, T), err, s));
+    }
+    uint8_t* aq = at<uint8_t>(ws, L.aq);
+    uint8_t* aqs = at<uint8_t>(ws, L.aqs);
+    if (T < kUmmaExpertMinTokens) {
+      // decode: weights on the MMA's N side; both passes in one launch when latent % 256 == 0
+      const bool both = d.latent % 256 == 0;
+      {
+        ProfScope p(both ? P_FFN_MMA : P_GLU_MMA, s);
+        K3_CUDA(launch_umma_wn(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T, aq, aqs, both,
+                               o_rows, cnt, err, s));
+      }
+      if (!both) {
+        ProfScope p(P_DOWN_MMA, s);
+        K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s));
+      }
+      return K3MOE_OK;
     }
     {
       ProfScope p(P_GLU_MMA, s);
-      K3_CUDA(launch_umma_glu(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T,
-                              at<uint8_t>(ws, L.aq), at<uint8_t>(ws, L.aqs), err, s));
+      K3_CUDA(launch_umma_glu(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T, aq, aqs, err, s));
     }
     ProfScope p(P_DOWN_MMA, s);
-    K3_CUDA(launch_umma_down(d, w, plan, at<uint8_t>(ws, L.aq), at<uint8_t>(ws, L.aqs), P, T, o_rows, err, s));
+    K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s));
     return K3MOE_OK;
   }
   {

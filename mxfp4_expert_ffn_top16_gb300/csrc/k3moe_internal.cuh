@@ -52,6 +52,7 @@ struct WsLayout {
   // block-scaled tensor-core expert path (only when umma_expert_ok): per sorted row, P e4m3
   // rows of z and of the GLU output with e8m0 scales per 32 (row pitch exp_pitch bytes)
   size_t bq, bs, aq, aqs;
+  size_t chunk_done;    // int per chunk: GLU items finished (decode kernel running both passes)
   size_t total;
 };
 WsLayout ws_layout(const k3moe_dims& d, int64_t T);
@@ -141,21 +142,23 @@ constexpr int kUmmaExpertMinTokens = 65;
 inline bool umma_expert_ok(const k3moe_dims& d) { return d.latent % 128 == 0 && d.inter % 128 == 0; }
 inline int umma_chunk_rows(long long T) { return T >= kUmmaExpertMinTokens ? kUmmaChunkRows : kGemvTokens; }
 // z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)].
+// Also clears the ncnt counters at cnt (the decode kernel's per-chunk GLU completion counts).
 cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
-                              uint8_t* bq, uint8_t* bs, uint32_t* err, cudaStream_t s);
+                              uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s);
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
                             cudaStream_t s);
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s);
 // Decode (T < kUmmaExpertMinTokens): the same GEMMs with the weights on the MMA's N side (256
-// weight rows per MMA, 8-row chunks). The down pass needs latent % 256 == 0.
-cudaError_t launch_umma_wn_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                               const uint8_t* bq, const uint8_t* bs, int P, int T, uint8_t* aq,
-                               uint8_t* aqs, uint32_t* err, cudaStream_t s);
-cudaError_t launch_umma_wn_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                                const uint8_t* aq, const uint8_t* aqs, int P, int T, float* o_rows,
-                                uint32_t* err, cudaStream_t s);
+// weight rows per MMA, 8-row chunks): the GLU pass, and with_down (needs latent % 256 == 0) the
+// down pass in the same launch. chunk_done: plan_chunks_max ints, zero at launch.
+cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
+                           const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, bool with_down,
+                           float* o_rows, int* chunk_done, uint32_t* err, cudaStream_t s);
+inline int plan_chunks_max(const k3moe_dims& d, long long T) {
+  return (int)(T * d.top_k / kGemvTokens + d.n_experts + 1);
+}
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s);
 

@@ -509,10 +509,12 @@ cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t 
 template <int P>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ z,
                                                          const int32_t* __restrict__ row_token, int rows,
-                                                         int T, int L, uint8_t* bq, uint8_t* bs,
-                                                         uint32_t* err) {
+                                                         int T, int L, uint8_t* bq, uint8_t* bs, int* cnt,
+                                                         int ncnt, uint32_t* err) {
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
   const int lane = threadIdx.x & 31;
   const int segs = (L + 255) / 256;
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -567,20 +569,20 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 }  // namespace
 
 cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
-                              uint8_t* bq, uint8_t* bs, uint32_t* err, cudaStream_t s) {
+                              uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int warps = 8;
   const long long units = (long long)rows * ((L + 255) / 256);
   const dim3 grid((unsigned)((units + warps - 1) / warps)), block(32 * warps);
-  if (P == 1) return launch_pdl(quant_rows_kernel<1>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, err);
-  return launch_pdl(quant_rows_kernel<2>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, err);
+  if (P == 1)
+    return launch_pdl(quant_rows_kernel<1>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
+  return launch_pdl(quant_rows_kernel<2>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
 }
 
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
                             cudaStream_t s) {
   const int R = umma_chunk_rows(T);
-  if (R == kGemvTokens) return launch_umma_wn_glu(d, w, plan, bq, bs, P, T, aq, aqs, err, s);
   UExpertArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
   if (!make_tmap_fp4(&A.ta0, w.gate_q, d.latent, wrows, pitch, 64) ||
@@ -599,8 +601,6 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s) {
   const int R = umma_chunk_rows(T);
-  if (R == kGemvTokens && d.latent % 256 == 0)
-    return launch_umma_wn_down(d, w, plan, aq, aqs, P, T, o_rows, err, s);
   UExpertArgs A{};
   if (!make_tmap_fp4(&A.ta0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, 128))
     return cudaErrorInvalidValue;

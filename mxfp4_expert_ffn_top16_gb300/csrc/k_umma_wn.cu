@@ -23,6 +23,14 @@
 // memory (lane l, word w = the four K-block scales of row 32w + l); warp 1 issues (one elected
 // lane of the converged warp). One 256-column accumulator per item; warps 4 and 8 (tensor-memory
 // lanes 0..31) each drain half its columns, add the hi and lo rows, and run the epilogue.
+//
+// One launch can run both passes: the GLU items, then the down items, dealt round-robin over
+// persistent CTAs in that order, so an SM that has no third GLU item starts on down items while
+// the others finish theirs. A down item needs the GLU output of its whole chunk: each epilogue
+// warp counts its finished GLU items per chunk in global memory (release), and the down item's
+// loaders wait (acquire, bounded) until the chunk is complete before reading its activations.
+// Every CTA runs its GLU items before any down item, and all CTAs are resident at once (one per
+// SM, grid <= SMs), so every awaited GLU item is running or done and the waits end.
 #include <cuda_fp16.h>
 
 #include "k3moe_device.cuh"
@@ -48,21 +56,50 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = kNW;          // 12 columns per stage: A 4, B 8
 static_assert(kSfCol + 12 * kStages <= kTmemCols, "tensor memory");
 
-struct UWnArgs {
+struct WnPass {
   CUtensorMap tw0;     // GLU: gate codes, box {128, 128}; down: down codes, box {128, 256}
   CUtensorMap tw1;     // GLU: up codes, box {128, 128}
   CUtensorMap ta;      // activation rows e4m3 {K, P*rows}, box {128, 8*P}
   const uint8_t* s0;   // weight scales [E][N][K/32]
   const uint8_t* s1;   // GLU: up scales
   const uint8_t* sb;   // activation scales [P*rows][exp_pitch(K)]
+  int N, K;            // output features per expert, reduction length
+};
+
+struct UWnArgs {
+  WnPass pass[2];      // [0] GLU, [1] down
+  int npass;           // 1: the GLU pass only; 2: GLU then down
   int32_t* plan;
-  int N, K, E;         // output features per expert, reduction length, experts
+  int E;               // experts
   int rows_max;        // T * k
-  uint8_t* aq;         // GLU: quantised output [P*rows][N] e4m3
-  uint8_t* aqs;        //      its scales [P*rows][exp_pitch(N)]
-  float* o_out;        // down: [rows][N] fp32
+  uint8_t* aq;         // GLU output [P*rows][inter] e4m3 (the down pass's activations)
+  uint8_t* aqs;        //   its scales [P*rows][exp_pitch(inter)]
+  float* o_out;        // down output [rows][latent] fp32
+  int* chunk_done;     // GLU items finished per chunk, times 2 (one count per epilogue warp); zeroed
   uint32_t* err;
 };
+
+// Waits (bounded) until the chunk's GLU output is complete; acquire, then the async proxy may
+// read it.
+__device__ __forceinline__ bool wait_chunk(const int* cnt, int target, volatile int* abort, uint32_t* err) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= target) break;
+    if ((i & 15u) == 15u) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
 
 __device__ __forceinline__ void umma_mx(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
                                         uint32_t sfb, uint32_t acc) {
@@ -133,14 +170,12 @@ __device__ __forceinline__ void quant32(float* v, uint32_t (&codes)[P][8], int (
   }
 }
 
-template <bool GLU, int P>
+template <int P>
 __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_constant__ UWnArgs A) {
-  constexpr int kFeat = GLU ? kNW / 2 : kNW;  // output features per item
   constexpr int kARows = kRows * P;           // activation rows a stage loads
   constexpr uint32_t kATx = kARows * BKE;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  const int srow = A.K / 32, spb = exp_pitch(A.K);
   uint8_t* sB = smem;                                  // kStages x kBTile
   uint8_t* sA = sB + kStages * kBTile;                 // kStages x kATile + kASlack
   uint8_t* stg = sA + kStages * kATile + kASlack;      // kStages x kStgBytes
@@ -176,19 +211,30 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   const int4* ctab = plan_ctab(A.plan, A.E);
-  const int C = A.plan[1];
-  const int fbs = A.N / kFeat;
-  const int items = (C > 0 && C <= A.rows_max / kRows + A.E) ? C * fbs : 0;
-  const int nk = A.K / BKE;
+  const int C0 = A.plan[1];
+  const int C = (C0 > 0 && C0 <= A.rows_max / kRows + A.E) ? C0 : 0;
+  const int fbs_g = A.pass[0].N / (kNW / 2), fbs_d = A.pass[1].N / kNW;
+  const int items_g = C * fbs_g;
+  const int items = items_g + (A.npass == 2 ? C * fbs_d : 0);
+  const int glu_target = 2 * fbs_g;  // epilogue-warp arrivals that complete a chunk
 
-  auto item_of = [&](int u, int& e, int& r0, int& nr, int& f0) -> bool {
-    const int c = u / fbs, fb = u - c * fbs;
-    const int4 t = ctab[c];
+  // item u: GLU items first (chunk-major), then down items
+  struct Item {
+    bool glu;
+    int c, e, r0, nr, f0;
+  };
+  auto item_of = [&](int u, Item& it) -> bool {
+    it.glu = u < items_g;
+    const int fbs = it.glu ? fbs_g : fbs_d;
+    const int v = it.glu ? u : u - items_g;
+    it.c = v / fbs;
+    const int fb = v - it.c * fbs;
+    const int4 t = ctab[it.c];
     const bool ok = t.x >= 0 && t.x < A.E && t.y >= 0 && t.z > 0 && t.z <= kRows && t.y + t.z <= A.rows_max;
-    e = ok ? t.x : 0;
-    r0 = ok ? t.y : 0;
-    nr = ok ? t.z : 0;
-    f0 = fb * kFeat;
+    it.e = ok ? t.x : 0;
+    it.r0 = ok ? t.y : 0;
+    it.nr = ok ? t.z : 0;
+    it.f0 = fb * (it.glu ? kNW / 2 : kNW);
     return ok;
   };
 
@@ -198,19 +244,23 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
       uint32_t ph = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
-        int e, r0, nr, f0;
-        if (!item_of(u, e, r0, nr, f0)) atomicOr(A.err, kErrIndex);
-        const int wrow = e * A.N + f0;
+        Item it;
+        if (!item_of(u, it)) atomicOr(A.err, kErrIndex);
+        const WnPass& W = A.pass[it.glu ? 0 : 1];
+        const int wrow = it.e * W.N + it.f0;
+        const int nk = W.K / BKE;
+        // a down item's activations are the GLU output of its chunk
+        if (!it.glu && !wait_chunk(A.chunk_done + it.c, glu_target, abort_flag, A.err)) break;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kBPacked + kATx);
-          if (GLU) {
-            tma_load_2d(sB + s * kBTile, &A.tw0, kc * BKE, wrow, &full[s]);
-            tma_load_2d(sB + s * kBTile + (kNW / 2) * 128, &A.tw1, kc * BKE, wrow, &full[s]);
+          if (it.glu) {
+            tma_load_2d(sB + s * kBTile, &W.tw0, kc * BKE, wrow, &full[s]);
+            tma_load_2d(sB + s * kBTile + (kNW / 2) * 128, &W.tw1, kc * BKE, wrow, &full[s]);
           } else {
-            tma_load_2d(sB + s * kBTile, &A.tw0, kc * BKE, wrow, &full[s]);
+            tma_load_2d(sB + s * kBTile, &W.tw0, kc * BKE, wrow, &full[s]);
           }
-          tma_load_2d(sA + s * kATile, &A.ta, kc * BKE, P * r0, &full[s]);
+          tma_load_2d(sA + s * kATile, &W.ta, kc * BKE, P * it.r0, &full[s]);
           if (++s == kStages) { s = 0; ph ^= 1; }
         }
       }
@@ -223,18 +273,27 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     uint32_t ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
-      int e, r0, nr, f0;
-      item_of(u, e, r0, nr, f0);
-      const size_t wrow = (size_t)e * A.N + f0;
+      Item it;
+      item_of(u, it);
+      const WnPass& W = A.pass[it.glu ? 0 : 1];
+      const int srow = W.K / 32, spb = exp_pitch(W.K), nk = W.K / BKE;
+      const size_t wrow = (size_t)it.e * W.N + it.f0;
       const uint8_t* ws[4];
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const int r = 32 * w + lane + (w2 ? 0 : 128);  // weight row of the item
-        ws[w] = (GLU && r >= kNW / 2) ? A.s1 + (wrow + r - kNW / 2) * srow : A.s0 + (wrow + r) * srow;
+        ws[w] = (it.glu && r >= kNW / 2) ? W.s1 + (wrow + r - kNW / 2) * srow : W.s0 + (wrow + r) * srow;
       }
-      const bool act = w2 && lane < P * nr;
-      const uint8_t* as = A.sb + ((size_t)P * r0 + (act ? lane : 0)) * spb;
+      const bool act = w2 && lane < P * it.nr;
+      const uint8_t* as = W.sb + ((size_t)P * it.r0 + (act ? lane : 0)) * spb;
       const uint32_t st_lane = smem_u32(stg) + lane * 16;
+      if (!it.glu && w2) {  // the activation scales come from this chunk's GLU items
+        int good = 1;
+        if (lane == 0) good = wait_chunk(A.chunk_done + it.c, glu_target, abort_flag, A.err) ? 1 : 0;
+        good = __shfl_sync(0xffffffffu, good, 0);
+        __syncwarp();
+        if (!good) { ok = false; break; }
+      }
       for (int kc = 0; kc < nk; ++kc) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
         const uint32_t so = st_lane + (uint32_t)(s * kStgBytes);
@@ -251,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+      const int nk = A.pass[u < items_g ? 0 : 1].K / BKE;
       if (!mbar_wait_warp(acce, aph ^ 1, abort_flag, A.err)) { ok = false; break; }
       for (int kc = 0; kc < nk; ++kc) {
         if (!mbar_wait_warp(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
@@ -290,15 +350,16 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     const int h = warp == kEpiWarp1 ? 1 : 0;
     uint32_t aph = 0;
     for (int u = blockIdx.x; u < items; u += gridDim.x) {
-      int e, r0, nr, f0;
-      item_of(u, e, r0, nr, f0);
+      Item it;
+      item_of(u, it);
       if (!mbar_wait_warp(accf, aph, abort_flag, A.err)) break;
       aph ^= 1;
       tc_fence_after();
       float v[128];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int col = GLU ? (c < 2 ? 64 * h + 32 * c : kNW / 2 + 64 * h + 32 * (c - 2)) : 128 * h + 32 * c;
+        const int col =
+            it.glu ? (c < 2 ? 64 * h + 32 * c : kNW / 2 + 64 * h + 32 * (c - 2)) : 128 * h + 32 * c;
         uint32_t r[32];
         tmem_ld32(tmem + (uint32_t)col, r);
         tmem_ld_wait();
@@ -313,10 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
         for (int i = 0; i < 128; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], 1);
       }
       const int jr = lane / P;
-      const bool mine = (lane % P) == 0 && jr < nr;
-      if (GLU) {
+      const bool mine = (lane % P) == 0 && jr < it.nr;
+      if (it.glu) {
         // v[0..63] gate, v[64..127] up of features f0 + 64h + i; one 32-feature block at a time
-        const int spo = exp_pitch(A.N);
+        const int N = A.pass[0].N, spo = exp_pitch(N);
 #pragma unroll
         for (int b = 0; b < 2; ++b) {
           float a[32];
@@ -329,19 +390,27 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
             uint32_t codes[P][8];
             int X[P];
             quant32<P>(a, codes, X);
-            const int f = f0 + 64 * h + 32 * b;
+            const int f = it.f0 + 64 * h + 32 * b;
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-              const size_t brow = (size_t)P * (r0 + jr) + p;
-              uint4* dst = reinterpret_cast<uint4*>(A.aq + brow * A.N + f);
+              const size_t brow = (size_t)P * (it.r0 + jr) + p;
+              uint4* dst = reinterpret_cast<uint4*>(A.aq + brow * N + f);
               dst[0] = make_uint4(codes[p][0], codes[p][1], codes[p][2], codes[p][3]);
               dst[1] = make_uint4(codes[p][4], codes[p][5], codes[p][6], codes[p][7]);
               A.aqs[brow * spo + f / 32] = (uint8_t)(X[p] + 127);
             }
           }
         }
+        if (A.npass == 2) {  // publish this warp's part of the chunk's GLU output (release)
+          __syncwarp();
+          if (lane == 0) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            __threadfence();
+            atomicAdd(A.chunk_done + it.c, 1);
+          }
+        }
       } else if (mine) {
-        float4* dst = reinterpret_cast<float4*>(A.o_out + (size_t)(r0 + jr) * A.N + f0 + 128 * h);
+        float4* dst = reinterpret_cast<float4*>(A.o_out + (size_t)(it.r0 + jr) * A.pass[1].N + it.f0 + 128 * h);
 #pragma unroll
         for (int i = 0; i < 32; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
@@ -358,50 +427,48 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
 constexpr size_t kSmem = 1024 + (size_t)kStages * (kBTile + kATile + kStgBytes) + kASlack + (2 * kStages + 3) * 8 + 16;
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
-template <bool GLU, int P>
+template <int P>
 cudaError_t launch_t(UWnArgs& a, int items_max, cudaStream_t s) {
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_wn_kernel<GLU, P>), kSmem);
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_wn_kernel<P>), kSmem);
   if (e != cudaSuccess) return e;
-  int grid = num_sms();
+  int grid = num_sms();  // one CTA per SM (the shared memory allows no second): all resident
   if (items_max < grid) grid = items_max > 0 ? items_max : 1;
-  return launch_pdl(umma_wn_kernel<GLU, P>, dim3(grid), dim3(kThreads), kSmem, s, a);
+  return launch_pdl(umma_wn_kernel<P>, dim3(grid), dim3(kThreads), kSmem, s, a);
 }
 
 }  // namespace
 
-cudaError_t launch_umma_wn_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                               const uint8_t* bq, const uint8_t* bs, int P, int T, uint8_t* aq,
-                               uint8_t* aqs, uint32_t* err, cudaStream_t s) {
+cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
+                           const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, bool with_down,
+                           float* o_rows, int* chunk_done, uint32_t* err, cudaStream_t s) {
   UWnArgs A{};
+  const int rows = T * d.top_k;
+  WnPass& G = A.pass[0];
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
-  if (!make_tmap_fp4(&A.tw0, w.gate_q, d.latent, wrows, pitch, kNW / 2) ||
-      !make_tmap_fp4(&A.tw1, w.up_q, d.latent, wrows, pitch, kNW / 2))
+  if (!make_tmap_fp4(&G.tw0, w.gate_q, d.latent, wrows, pitch, kNW / 2) ||
+      !make_tmap_fp4(&G.tw1, w.up_q, d.latent, wrows, pitch, kNW / 2) ||
+      !make_tmap_2d(&G.ta, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, kRows * P, true))
     return cudaErrorInvalidValue;
-  const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.ta, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, kRows * P,
-                    true))
-    return cudaErrorInvalidValue;
-  A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
-  A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
-  A.aq = aq; A.aqs = aqs; A.err = err;
-  const int items_max = (rows / kRows + d.n_experts) * (d.inter / (kNW / 2));
-  return P == 1 ? launch_t<true, 1>(A, items_max, s) : launch_t<true, 2>(A, items_max, s);
-}
-
-cudaError_t launch_umma_wn_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan,
-                                const uint8_t* aq, const uint8_t* aqs, int P, int T, float* o_rows,
-                                uint32_t* err, cudaStream_t s) {
-  UWnArgs A{};
-  if (!make_tmap_fp4(&A.tw0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, kNW))
-    return cudaErrorInvalidValue;
-  const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.ta, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, kRows * P, true))
-    return cudaErrorInvalidValue;
-  A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
-  A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
-  A.o_out = o_rows; A.err = err;
-  const int items_max = (rows / kRows + d.n_experts) * (d.latent / kNW);
-  return P == 1 ? launch_t<false, 1>(A, items_max, s) : launch_t<false, 2>(A, items_max, s);
+  G.s0 = w.gate_s; G.s1 = w.up_s; G.sb = bs;
+  G.N = d.inter; G.K = d.latent;
+  int items_max = (rows / kRows + d.n_experts) * (d.inter / (kNW / 2));
+  A.npass = 1;
+  if (with_down) {
+    WnPass& D = A.pass[1];
+    if (!make_tmap_fp4(&D.tw0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, kNW) ||
+        !make_tmap_2d(&D.ta, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, kRows * P, true))
+      return cudaErrorInvalidValue;
+    D.s0 = w.down_s; D.sb = aqs;
+    D.N = d.latent; D.K = d.inter;
+    items_max += (rows / kRows + d.n_experts) * (d.latent / kNW);
+    A.npass = 2;
+  } else {
+    A.pass[1].N = kNW;  // unused; keeps the item arithmetic defined
+    A.pass[1].K = BKE;
+  }
+  A.plan = plan; A.E = d.n_experts; A.rows_max = rows;
+  A.aq = aq; A.aqs = aqs; A.o_out = o_rows; A.chunk_done = chunk_done; A.err = err;
+  return P == 1 ? launch_t<1>(A, items_max, s) : launch_t<2>(A, items_max, s);
 }
 
 }  // namespace k3moe

@@ -67,14 +67,18 @@ def _expert_ffn(lay, z_np, idx_np, actq=0):
 
 # T >= 65 runs the tensor-core kernel with the weights on the MMA's M side (chunks of up to 112
 # sorted rows); smaller T the one with the weights on N (chunks of up to 8), whose down pass needs
-# latent % 256 == 0 (latent = 128 keeps the M-side kernel for it).
+# latent % 256 == 0 (latent = 128 keeps the M-side kernel for it). DEEP has eight K stages per
+# item and fewer items than SMs.
 WIDE = synth.Dims(hidden=256, latent=256, inter=256, n_experts=16, top_k=4)
+DEEP = synth.Dims(hidden=256, latent=1024, inter=1024, n_experts=8, top_k=2)
+DIMS = {"tiny": synth.TINY, "wide": WIDE, "deep": DEEP}
 
 
-@pytest.mark.parametrize("dname,T", [("tiny", 24), ("tiny", 100), ("wide", 7), ("wide", 200)])
+@pytest.mark.parametrize("dname,T", [("tiny", 24), ("tiny", 100), ("wide", 7), ("wide", 200), ("deep", 3),
+                                     ("deep", 20)])
 @pytest.mark.parametrize("actq", [0, 1])
 def test_expert_ffn_tiny_all_rows(actq, dname, T):
-    d = synth.TINY if dname == "tiny" else WIDE
+    d = DIMS[dname]
     lay = DeviceLayer(d, seed=0, actq=actq)
     z = synth.host_bf16_normal(3, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
     idx = synth.host_topk_sets(4, T, d.n_experts, d.top_k, "zipf")
@@ -112,10 +116,10 @@ def test_expert_ffn_k3_sampled_rows(k3_layer, T, actq):
         assert rel_l2_rows(o[r], want) <= REL_L2, (r, rel_l2_rows(o[r], want))
 
 
-@pytest.mark.parametrize("dname,T", [("tiny", 8), ("tiny", 80), ("wide", 80)])
+@pytest.mark.parametrize("dname,T", [("tiny", 8), ("tiny", 80), ("wide", 80), ("deep", 5)])
 def test_expert_ffn_invariants_bit_exact(dname, T):
     """All-zero codes give exactly 0; +1 on every up exponent doubles every output exactly."""
-    d = synth.TINY if dname == "tiny" else WIDE
+    d = DIMS[dname]
     z = synth.host_bf16_normal(2, synth.S_X, 0, T * d.latent, 1.0).reshape(T, d.latent)
     idx = synth.host_topk_sets(5, T, d.n_experts, d.top_k, "uniform")
     base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
@@ -128,9 +132,9 @@ def test_expert_ffn_invariants_bit_exact(dname, T):
     np.testing.assert_array_equal(o2, 2 * o1)
 
 
-@pytest.mark.parametrize("dname,T", [("tiny", 4), ("tiny", 72), ("wide", 72)])
+@pytest.mark.parametrize("dname,T", [("tiny", 4), ("tiny", 72), ("wide", 72), ("deep", 4)])
 def test_expert_ffn_nan_scale_gives_nonfinite(dname, T):
-    d = synth.TINY if dname == "tiny" else WIDE
+    d = DIMS[dname]
     base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
     base[0]["down_s"] = base[0]["down_s"].copy()
     base[0]["down_s"][:, 0] = 255

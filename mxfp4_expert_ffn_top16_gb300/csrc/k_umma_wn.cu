@@ -13,8 +13,8 @@
 // scales, P rows per sorted row as in the many-token kernel: P = 2 splits a bf16 value exactly
 // into e4m3 hi + lo, P = 1 is MXFP8). Only the first 8 * P of the 128 M rows carry data: each
 // stage loads just those rows (2 KB), the stages' activation tiles sit 2 KB apart, and an
-// MMA's remaining rows read whatever follows in shared memory. Row m of the result depends
-// only on row m of A, so those accumulator rows are never read.
+// MMA's remaining rows read whatever follows in shared memory (the later tiles, then the weight
+// tiles). Row m of the result depends only on row m of A, so those accumulator rows are never read.
 //
 // Work item = (chunk of up to 8 sorted rows of one expert, feature block): GLU items take 128
 // features (B rows 0..127 gate, 128..255 up), down items 256 features. K = 128 per stage.
@@ -48,7 +48,6 @@ constexpr int kStages = 5;
 constexpr int kBTile = kNW * BKE;         // weight tile in shared memory (e2m1 padded to bytes)
 constexpr int kBPacked = kNW * BKE / 2;   // bytes the weight copies transfer
 constexpr int kATile = 2 * kRows * BKE;   // activation rows a stage loads (at most 16 x 128 B)
-constexpr int kASlack = kMA * BKE - kATile;  // the MMA reads 128 rows from a tile's start
 constexpr int kStgBytes = 1536;           // per stage: A scale block, B rows 0..127, B rows 128..255
 constexpr int kThreads = 288;             // warps 0 TMA, 1 MMA, 2-3 gather, 4 and 8 epilogue
 constexpr int kEpiWarp0 = 4, kEpiWarp1 = 8;
@@ -176,9 +175,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
   constexpr uint32_t kATx = kARows * BKE;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sB = smem;                                  // kStages x kBTile
-  uint8_t* sA = sB + kStages * kBTile;                 // kStages x kATile + kASlack
-  uint8_t* stg = sA + kStages * kATile + kASlack;      // kStages x kStgBytes
+  // The activation tiles come first: an MMA reads 128 rows (16 KB) from a tile's start, and what
+  // follows the last tile is the weight tiles, still inside this block's shared memory.
+  uint8_t* sA = smem;                                  // kStages x kATile
+  uint8_t* sB = sA + kStages * kATile;                 // kStages x kBTile
+  uint8_t* stg = sB + kStages * kBTile;                // kStages x kStgBytes
   uint64_t* full = reinterpret_cast<uint64_t*>(stg + kStages * kStgBytes);
   uint64_t* empty = full + kStages;
   uint64_t* accf = empty + kStages;
@@ -424,7 +425,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
   }
 }
 
-constexpr size_t kSmem = 1024 + (size_t)kStages * (kBTile + kATile + kStgBytes) + kASlack + (2 * kStages + 3) * 8 + 16;
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kBTile + kATile + kStgBytes) + (2 * kStages + 3) * 8 + 16;
+static_assert((size_t)kStages * kATile + kBTile >= (size_t)(kStages - 1) * kATile + kMA * BKE,
+              "an MMA's 128-row read of the last activation tile stays inside shared memory");
+static_assert(kATile % 1024 == 0 && (kStages * kATile) % 1024 == 0, "128-byte swizzle alignment");
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
 template <int P>

@@ -111,13 +111,14 @@ def measured_traffic(workload, kernel):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
+        e = t["workloads"][workload][kernel]
         h = hashlib.sha256()
-        for p in t["source_files"]:
+        for p in e["source_files"]:
             with open(os.path.join(ROOT, p), "rb") as f:
                 h.update(f.read())
-        if h.hexdigest() != t["source_sha256"]:
+        if h.hexdigest() != e["source_sha256"]:
             return None
-        return t["workloads"][workload][kernel]["traffic"]
+        return e["traffic"]
     except (OSError, KeyError, ValueError):
         return None
 

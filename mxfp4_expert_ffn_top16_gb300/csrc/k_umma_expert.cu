@@ -26,15 +26,15 @@
 // tens of cycles to issue from the single MMA thread, so N is made as large as tensor memory
 // allows (two 224-column accumulators) to keep the tensor pipe, not the issue, the limit.
 // Warp 0 (lane 0) loads the packed e2m1 weight tiles (16U4_ALIGN16B tensor map) and the e4m3
-// activation tiles, both with the 128-byte swizzle. Warps 6 and 7 gather each stage's weight
+// activation tiles, both with the 128-byte swizzle. Warps 10 and 11 gather each stage's weight
 // and activation scales with 4-byte cp.async straight into the 32 x 16-byte blocks that
 // tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l, word w = the four K-block scales
 // of row 32w + l); the stage's full barrier counts the tile bytes and one cp.async arrival per
 // gathering lane. Warp 1: tensor-memory owner and MMA issuer, one commit per stage.
-// Accumulation restarts every kGroup stages in one of two tensor-memory slots; eight epilogue
-// warps (two per lane quadrant, one lane = one weight row, each half of the sorted rows) add
-// the slots up in fp32 and run the epilogue; the GLU epilogue transposes through shared memory
-// so each thread quantises one (sorted row, 32-feature block).
+// Each item accumulates its whole K in one of two tensor-memory slots, so the epilogue of one
+// item overlaps the MMAs of the next; eight epilogue warps (two per lane quadrant, one lane = one
+// weight row, each half of the sorted rows) drain it and run the epilogue; the GLU epilogue
+// transposes through shared memory so each thread quantises one (sorted row, 32-feature block).
 #include <cuda_fp16.h>
 
 #include "k3moe_device.cuh"
@@ -50,7 +50,6 @@ constexpr int kAPacked = BM * BKE / 2;    // bytes the copy transfers
 constexpr int kThreads = 384;             // 0 TMA, 1 MMA, 2-9 epilogue, 10-11 scale gather
 constexpr int kEpiWarps = 8;
 constexpr int kGather0 = 2 + kEpiWarps;   // first scale-gather warp
-constexpr int kGroup = 4;                 // stages per tensor-memory accumulation slot
 constexpr int kAccSlots = 2;
 constexpr int kSfPerStage = 16;           // tensor-memory columns: A 4, B rows 0..127 4, B rows 128.. 4
 constexpr int kStgBytes = 1536;           // per stage: A block, B block rows 0..127, rows 128..255
@@ -240,7 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   const int fbs = A.N / kFB;
   const int items = (C > 0 && C <= A.rows_max / R + A.E) ? C * fbs : 0;
   const int nk = A.K / BKE;
-  const int ngroups = (nk + kGroup - 1) / kGroup;
 
   // item u -> (expert, first sorted row, rows, first feature); false for a corrupt entry
   auto item_of = [&](int u, int& e, int& r0, int& nr, int& f0) -> bool {
@@ -325,38 +323,35 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
       item_of(u, e, r0, nr, f0);
       int Nc = P * nr;
       Nc = Nc < 16 ? 16 : ((Nc + 15) & ~15);
-      for (int gi = 0; gi < ngroups && ok; ++gi) {
-        if (!mbar_wait_warp(&acce[slot], aph ^ 1, abort_flag, A.err)) { ok = false; break; }
-        const uint32_t d = tmem + (uint32_t)(slot * kNMax);
-        const int kc1 = min(nk, (gi + 1) * kGroup);
-        for (int kc = gi * kGroup; kc < kc1; ++kc) {
-          if (!mbar_wait_warp(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
-          // scale columns: A (4), then B rows 0..127 (4) and B rows 128..255 (4)
-          const uint32_t tsa = tmem + kSfCol + kSfPerStage * s, tsb = tsa + 4;
-          const uint32_t st0 = smem_u32(stg + s * kStgBytes);
-          const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
-          if (elect_one()) {
-            fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
-            tc_fence_after();
-            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa), "l"(sdesc_sf(st0)));
-            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb), "l"(sdesc_sf(st0 + 512)));
-            if (Nc > 128)
-              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb + 4),
-                           "l"(sdesc_sf(st0 + 1024)));
+      if (!mbar_wait_warp(&acce[slot], aph ^ 1, abort_flag, A.err)) { ok = false; break; }
+      const uint32_t d = tmem + (uint32_t)(slot * kNMax);
+      for (int kc = 0; kc < nk; ++kc) {
+        if (!mbar_wait_warp(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
+        // scale columns: A (4), then B rows 0..127 (4) and B rows 128..255 (4)
+        const uint32_t tsa = tmem + kSfCol + kSfPerStage * s, tsb = tsa + 4;
+        const uint32_t st0 = smem_u32(stg + s * kStgBytes);
+        const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
+        if (elect_one()) {
+          fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
+          tc_fence_after();
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa), "l"(sdesc_sf(st0)));
+          asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb), "l"(sdesc_sf(st0 + 512)));
+          if (Nc > 128)
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsb + 4),
+                         "l"(sdesc_sf(st0 + 1024)));
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              umma_mx(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_mx(Nc, kk), tsa, tsb,
-                      (kc != gi * kGroup || kk != 0) ? 1u : 0u);
-            umma_commit(&empty[s]);  // tiles and scale block of this stage free again
-          }
-          __syncwarp();
-          if (++s == kStages) { s = 0; ph ^= 1; }
+          for (int kk = 0; kk < 4; ++kk)
+            umma_mx(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_mx(Nc, kk), tsa, tsb,
+                    (kc | kk) != 0 ? 1u : 0u);
+          umma_commit(&empty[s]);  // tiles and scale block of this stage free again
         }
-        if (!ok) break;
-        if (elect_one()) umma_commit(&accf[slot]);
         __syncwarp();
-        if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
+        if (++s == kStages) { s = 0; ph ^= 1; }
       }
+      if (!ok) break;
+      if (elect_one()) umma_commit(&accf[slot]);
+      __syncwarp();
+      if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
     }
     // every issued MMA has completed before the tensor memory is released
     if (elect_one()) {
@@ -382,33 +377,30 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
       float sum[kHalf];
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) sum[i] = 0.f;
-      for (int gi = 0; gi < ngroups; ++gi) {
-        if (!mbar_wait_warp(&accf[slot], aph, abort_flag, A.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t base =
-            tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kNMax + P * j0);
+      if (!mbar_wait_warp(&accf[slot], aph, abort_flag, A.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t base =
+          tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kNMax + P * j0);
 #pragma unroll
-        for (int c = 0; c < (P * kHalf + 15) / 16; ++c) {
-          if (c * 16 < ncols) {  // warp-uniform
-            uint32_t v[16];
-            tmem_ld16(base + c * 16, v);
-            tmem_ld_wait();
+      for (int c = 0; c < (P * kHalf + 15) / 16; ++c) {
+        if (c * 16 < ncols) {  // warp-uniform
+          uint32_t v[16];
+          tmem_ld16(base + c * 16, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16 / P; ++i) {
-              if (c * (16 / P) + i < kHalf) {  // compile-time
-                float x = __uint_as_float(v[P * i]);
-                if (P == 2) x += __uint_as_float(v[P * i + 1]);
-                sum[c * (16 / P) + i] += x;
-              }
+          for (int i = 0; i < 16 / P; ++i) {
+            if (c * (16 / P) + i < kHalf) {  // compile-time
+              float x = __uint_as_float(v[P * i]);
+              if (P == 2) x += __uint_as_float(v[P * i + 1]);
+              sum[c * (16 / P) + i] += x;
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce[slot]);
-        if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
       }
-      if (!ok) break;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[slot]);
+      if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
       if (GLU) {
         // 1. within each half of the sorted rows, the gate row (lanes 0..63) of feature f parks
         // its sums for the half's upper kQ rows and the up row (lanes 64..127) its sums for the

@@ -76,6 +76,7 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.o = take(rows * Lw * 4);
   L.c = take(Tt * Lw * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
+  L.route_done = take(4);
   if (umma_expert_ok(d)) {
     const size_t P = d.actq ? 1 : 2;
     L.bq = take(P * rows * Lw);
@@ -234,11 +235,11 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
                                 const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s) {
   uint32_t* err = at<uint32_t>(ws, L.err);
   if (T <= kSmallRouteTokens) {
-    ProfScope p(P_PERMUTE, s);  // top-k, permutation and plan in one block
+    ProfScope p(P_PERMUTE, s);  // top-k, then permutation and plan (one kernel for a few tokens)
     K3_CUDA(launch_route_tail_small(at<float>(ws, L.logits), T, d.n_experts, d.top_k, idx, wts,
                                     at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.row_token),
                                     at<int32_t>(ws, L.row_slot), at<int32_t>(ws, L.slot_row),
-                                    at<int32_t>(ws, L.plan), err, s));
+                                    at<int32_t>(ws, L.plan), at<int>(ws, L.route_done), err, s));
   } else {
     {
       ProfScope p(P_TOPK, s);

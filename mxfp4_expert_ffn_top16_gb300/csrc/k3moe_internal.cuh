@@ -49,6 +49,7 @@ struct WsLayout {
   size_t o;             // fp32 expert outputs per sorted row
   size_t c;             // bf16 combined latent
   size_t perm;          // int32 per-block histograms of the multi-block permutation
+  size_t route_done;    // int: top-k blocks finished (a few tokens); back to zero after each launch
   // block-scaled tensor-core expert path (only when umma_expert_ok): per sorted row, P e4m3
   // rows of z and of the GLU output with e8m0 scales per 32 (row pitch exp_pitch bytes)
   size_t bq, bs, aq, aqs;
@@ -122,9 +123,10 @@ cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* pl
                         cudaStream_t s);
 // Top-k (one block per token), then permutation + plan in one block, for T <= kSmallRouteTokens.
 constexpr int kSmallRouteTokens = 64;
+// done: a workspace counter that is zero between launches (the workspace starts zeroed).
 cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                                     int32_t* offsets, int32_t* row_token, int32_t* row_slot,
-                                    int32_t* slot_row, int32_t* plan, uint32_t* err, cudaStream_t s);
+                                    int32_t* slot_row, int32_t* plan, int* done, uint32_t* err, cudaStream_t s);
 cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,
                             cudaStream_t s);
 cudaError_t launch_expert_glu(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,

@@ -36,17 +36,12 @@ __device__ __forceinline__ uint32_t sort_key(float v) {
 // experts by index and writes them with the softmax weights over their logits.
 constexpr int kTopkThreads = 256;
 constexpr int kTopkKeys = kMaxE / kTopkThreads;  // keys per thread
-__global__ void __launch_bounds__(kTopkThreads) topk_block_kernel(const float* __restrict__ logits, int T, int E,
-                                                                  int k, int32_t* idx, float* w) {
+__device__ void block_topk(const float* __restrict__ logits, int t, int E, int k, int32_t* idx, float* w) {
   __shared__ int hist[256];
   __shared__ int s_digit, s_above, s_nsel;
   __shared__ int wcnt[kTopkKeys][kTopkThreads / 32];
   __shared__ int sel_e[32];
   __shared__ float sel_l[32];
-  pdl_wait();
-  pdl_trigger();
-  const int t = blockIdx.x;
-  if (t >= T) return;  // block-uniform
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const unsigned lt = (1u << lane) - 1u;
   const float* lg = logits + (size_t)t * E;
@@ -155,6 +150,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_block_kernel(const float* _
       w[(size_t)t * k + lane] = ex / sum;
     }
   }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_block_kernel(const float* __restrict__ logits, int T, int E,
+                                                                  int k, int32_t* idx, float* w) {
+  pdl_wait();
+  pdl_trigger();
+  if (blockIdx.x >= T) return;  // block-uniform
+  block_topk(logits, blockIdx.x, E, k, idx, w);
 }
 
 // ---------------------------------------------------------------- block-level building blocks
@@ -325,6 +328,116 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* idx,
   if (tid < 32) warp_scatter(ix, 0, T, E, k, cnt, mask, row_token, row_slot, slot_row, err);
 }
 
+// ---------------------------------------------------------------- a few tokens: top-k + permutation
+// For T * k <= kTinyRows: each block selects one token's experts; the block that finishes last
+// (a counter in the workspace, release/acquire through fences) builds the permutation and the
+// plan, so decode pays for one kernel here instead of two.
+constexpr int kTinyRows = 64;
+
+// rows r = t * k + j (r < R <= kTinyRows), experts idx[r]: sorted rows grouped by expert, token
+// order inside an expert; the same outputs as the histogram / scan / scatter path. All threads
+// of the block take part.
+__device__ void block_route_tiny(const int32_t* idx, int T, int E, int k, int rows_max, int32_t* offsets,
+                                 int32_t* row_token, int32_t* row_slot, int32_t* slot_row, int32_t* plan,
+                                 uint32_t* err) {
+  __shared__ uint32_t s_key[kTinyRows];
+  __shared__ int s_e[kTinyRows], s_start[kTinyRows], s_run[kTinyRows + 1], s_chunks[kTinyRows];
+  const int tid = threadIdx.x;
+  const int R = T * k;
+  // key = expert * kTinyRows + row: in key order, rows go by expert, then by row (token order)
+  bool valid = false;
+  if (tid < R) {
+    const int e = __ldcg(idx + tid);
+    valid = e >= 0 && e < E;
+    if (!valid) {
+      atomicOr(err, kErrIndex);
+      slot_row[tid] = -1;  // contributes nothing to the combine
+    }
+    s_key[tid] = valid ? (uint32_t)e * kTinyRows + (uint32_t)tid : 0xffffffffu;
+  }
+  const int nvalid = __syncthreads_count(valid);
+  if (valid) {
+    const uint32_t key = s_key[tid];
+    int p = 0;  // rank among the keys (distinct)
+    for (int x = 0; x < R; ++x) p += s_key[x] < key ? 1 : 0;
+    const int t = tid / k;
+    row_token[p] = t;
+    row_slot[p] = tid - t * k;
+    slot_row[tid] = p;
+    s_e[p] = (int)(key / kTinyRows);
+  }
+  __syncthreads();
+  if (tid < nvalid) s_start[tid] = (tid == 0 || s_e[tid] != s_e[tid - 1]) ? 1 : 0;
+  // offsets[e] = rows of experts below e
+  for (int e = tid; e <= E; e += blockDim.x) {
+    int lo = 0, hi = nvalid;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (s_e[mid] < e) lo = mid + 1; else hi = mid;
+    }
+    offsets[e] = lo;
+  }
+  __syncthreads();
+  // runs of one expert = the active experts, in expert order
+  int D = 0;
+  for (int x = 0; x < nvalid; ++x) D += s_start[x];
+  if (tid < nvalid && s_start[tid]) {
+    int i = 0;
+    for (int x = 0; x < tid; ++x) i += s_start[x];
+    s_run[i] = tid;
+  }
+  if (tid == 0) s_run[D] = nvalid;
+  __syncthreads();
+  if (tid < D) s_chunks[tid] = (s_run[tid + 1] - s_run[tid] + kGemvTokens - 1) / kGemvTokens;
+  __syncthreads();
+  if (tid < D) {
+    int C0 = 0;
+    for (int x = 0; x < tid; ++x) C0 += s_chunks[x];
+    const int p0 = s_run[tid], m = s_run[tid + 1] - p0, e = s_e[p0];
+    int4* ctab = plan_ctab(plan, E);
+    plan[2 + tid] = e;
+    plan[2 + E + tid] = C0;
+    for (int q = 0; q * kGemvTokens < m; ++q)
+      ctab[C0 + q] = make_int4(e, p0 + q * kGemvTokens, min(kGemvTokens, m - q * kGemvTokens), 0);
+    plan_ctab64(plan, E, rows_max)[1 + tid] = make_int4(e, p0, m, 0);  // m <= kTinyRows: one chunk
+    if (tid == D - 1) {
+      plan[0] = D;
+      plan[1] = C0 + s_chunks[tid];
+      plan[2 + E + D] = C0 + s_chunks[tid];
+      plan_ctab64(plan, E, rows_max)[0] = make_int4(D, 0, 0, 0);
+    }
+  }
+  if (D == 0 && tid == 0) {
+    plan[0] = 0;
+    plan[1] = 0;
+    plan[2 + E] = 0;
+    plan_ctab64(plan, E, rows_max)[0] = make_int4(0, 0, 0, 0);
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads) route_tiny_kernel(const float* __restrict__ logits, int T, int E,
+                                                                  int k, int32_t* idx, float* w, int32_t* offsets,
+                                                                  int32_t* row_token, int32_t* row_slot,
+                                                                  int32_t* slot_row, int32_t* plan, int* done,
+                                                                  uint32_t* err) {
+  __shared__ int s_last;
+  pdl_wait();
+  pdl_trigger();
+  block_topk(logits, blockIdx.x, E, k, idx, w);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this token's indices are visible before it is counted
+    const int last = atomicAdd(done, 1) == T - 1;
+    if (last) {
+      *done = 0;  // ready for the next launch
+      __threadfence();
+    }
+    s_last = last;
+  }
+  __syncthreads();
+  if (s_last) block_route_tiny(idx, T, E, k, T * k, offsets, row_token, row_slot, slot_row, plan, err);
+}
+
 // ---------------------------------------------------------------- multi-CTA permutation
 constexpr int kBlockTokens = 256;
 
@@ -442,7 +555,10 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
 
 cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                                     int32_t* offsets, int32_t* row_token, int32_t* row_slot,
-                                    int32_t* slot_row, int32_t* plan, uint32_t* err, cudaStream_t s) {
+                                    int32_t* slot_row, int32_t* plan, int* done, uint32_t* err, cudaStream_t s) {
+  if (T * k <= kTinyRows)
+    return launch_pdl(route_tiny_kernel, dim3(T), dim3(kTopkThreads), 0, s, logits, T, E, k, idx, w, offsets,
+                      row_token, row_slot, slot_row, plan, done, err);
   cudaError_t e = launch_pdl(topk_block_kernel, dim3(T), dim3(kTopkThreads), 0, s, logits, T, E, k, idx, w);
   if (e != cudaSuccess) return e;
   return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)idx, T, E, k, offsets,

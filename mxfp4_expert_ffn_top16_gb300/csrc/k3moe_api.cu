@@ -182,34 +182,42 @@ struct ProfScope {
 
 // Expert GEMMs for the sorted rows (plan already built): block-scaled tensor-core tiles for
 // many tokens, the GEMV on f16 copies (zh, zs already in ws) otherwise.
+// z_rows_ready: (decode, tensor-core path) the dense kernel already wrote z as P E4M3 rows per
+// token into bq / bs, and the routing kernel cleared the chunk counters.
 k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const uint16_t* z, int32_t T,
                               const int32_t* offsets, const int32_t* row_token, float* o_rows, void* ws,
-                              const WsLayout& L, cudaStream_t s) {
+                              const WsLayout& L, cudaStream_t s, bool z_rows_ready = false) {
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* plan = at<int32_t>(ws, L.plan);
   if (umma_expert_ok(d)) {
     const int P = d.actq ? 1 : 2;
     int* cnt = at<int>(ws, L.chunk_done);
-    {
-      ProfScope p(P_QUANT, s);
-      K3_CUDA(launch_quant_rows(z, row_token, T * d.top_k, T, d.latent, P, at<uint8_t>(ws, L.bq),
-                                at<uint8_t>(ws, L.bs), cnt, plan_chunks_max(d, T), err, s));
-    }
     uint8_t* aq = at<uint8_t>(ws, L.aq);
     uint8_t* aqs = at<uint8_t>(ws, L.aqs);
     if (T < kUmmaExpertMinTokens) {
-      // decode: weights on the MMA's N side; both passes in one launch when latent % 256 == 0
+      // decode: z as P E4M3 rows per token (the expert kernel gathers a chunk's rows by token),
+      // weights on the MMA's N side; both passes in one launch when latent % 256 == 0
+      if (!z_rows_ready) {
+        ProfScope p(P_QUANT, s);
+        K3_CUDA(launch_quant_rows(z, nullptr, T, T, d.latent, P, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs),
+                                  cnt, plan_chunks_max(d, T), err, s));
+      }
       const bool both = d.latent % 256 == 0;
       {
         ProfScope p(both ? P_FFN_MMA : P_GLU_MMA, s);
-        K3_CUDA(launch_umma_wn(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T, aq, aqs, both,
-                               o_rows, cnt, err, s));
+        K3_CUDA(launch_umma_wn(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), row_token, P, T, aq,
+                               aqs, both, o_rows, cnt, err, s));
       }
       if (!both) {
         ProfScope p(P_DOWN_MMA, s);
         K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s));
       }
       return K3MOE_OK;
+    }
+    {  // many tokens: z gathered into P E4M3 rows per sorted row
+      ProfScope p(P_QUANT, s);
+      K3_CUDA(launch_quant_rows(z, row_token, T * d.top_k, T, d.latent, P, at<uint8_t>(ws, L.bq),
+                                at<uint8_t>(ws, L.bs), cnt, 0, err, s));
     }
     {
       ProfScope p(P_GLU_MMA, s);
@@ -239,7 +247,9 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
     K3_CUDA(launch_route_tail_small(at<float>(ws, L.logits), T, d.n_experts, d.top_k, idx, wts,
                                     at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.row_token),
                                     at<int32_t>(ws, L.row_slot), at<int32_t>(ws, L.slot_row),
-                                    at<int32_t>(ws, L.plan), at<int>(ws, L.route_done), err, s));
+                                    at<int32_t>(ws, L.plan), at<int>(ws, L.route_done),
+                                    umma_expert_ok(d) ? at<int>(ws, L.chunk_done) : nullptr,
+                                    umma_expert_ok(d) ? plan_chunks_max(d, T) : 0, err, s));
   } else {
     {
       ProfScope p(P_TOPK, s);
@@ -251,8 +261,11 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
                            at<int32_t>(ws, L.slot_row), at<int32_t>(ws, L.plan),
                            at<int32_t>(ws, L.perm), err, s));
   }
+  // (decode, tensor-core experts: the dense kernel wrote z's E4M3 rows, the routing cleared the
+  // chunk counters)
   K3_TRY(run_expert_gemms(d, w, at<uint16_t>(ws, L.z), T, at<int32_t>(ws, L.offsets),
-                          at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s));
+                          at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s,
+                          T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && umma_expert_ok(d)));
   {
     ProfScope p(P_COMBINE, s);
     K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,
@@ -401,13 +414,17 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
   float* wts = topk_w_out ? topk_w_out : at<float>(ws, L.wts);
   const k3moe_weights& w = *weights;
   // router logits and z = bf16(W_in x) in one pass over x (+ the f16 block-scaled copy of z
-  // that the expert GEMV reads; the tensor-core expert path quantises z itself)
+  // that the expert GEMV reads, or for decode on tensor cores z's E4M3 rows per token)
   {
     ProfScope p(P_ROUTER_LATENT, s);
     const bool f16_copy = !umma_expert_ok(d);
+    // decode on the tensor-core experts: z also as P E4M3 rows per token for the expert kernel
+    const bool rows = !f16_copy && T <= kSmallRouteTokens && T < kUmmaExpertMinTokens;
     K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr, w.router_bias, w.w_in,
                          d.latent, at<uint16_t>(ws, L.z), f16_copy ? at<__half>(ws, L.zh) : nullptr,
-                         f16_copy ? at<int8_t>(ws, L.zs) : nullptr, d.actq, x, T, d.hidden, err, s));
+                         f16_copy ? at<int8_t>(ws, L.zs) : nullptr, d.actq, x, T, d.hidden, err, s,
+                         rows ? at<uint8_t>(ws, L.bq) : nullptr, rows ? at<uint8_t>(ws, L.bs) : nullptr,
+                         d.actq ? 1 : 2));
   }
   K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s));
   {

@@ -54,6 +54,37 @@ __device__ __forceinline__ int mxfp8_block_exp(float amax) {
   return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 
+// Two values -> two E4M3 codes (nearest even, saturating), v0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float v0, float v1) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
+  return r;
+}
+// Two E4M3 codes (low byte first) -> their values.
+__device__ __forceinline__ float2 e4m3x2_value(uint32_t pair) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair));
+  return __half22float2(*reinterpret_cast<__half2*>(&h2));
+}
+// v * 2^e for e in [-254, 254] in two exact power-of-two steps.
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+  const int e1 = e / 2;
+  return v * exp2i(e1) * exp2i(e - e1);
+}
+// Block exponent of the hi / lo parts of a bf16 value split into two E4M3 rows
+// (amax / 2^X in [128, 256)); all-zero block: -127.
+__device__ __forceinline__ int split_block_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  if (!(amax <= 3.4028235e38f)) return 127;
+  const int X = ilog2_floor(amax) - 7;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+// Exponent of the first E4M3 row of a block: P = 1 MXFP8, P = 2 the hi part of the split.
+template <int P>
+__device__ __forceinline__ int block_exp(float amax) {
+  return P == 1 ? mxfp8_block_exp(amax) : split_block_exp(amax);
+}
+
 // f16 block exponent: the power of two that brings a block's amax into [2^14, 2^15).
 __device__ __forceinline__ int f16_block_exp(float amax) {
   if (!(amax > 0.0f) || !(amax <= 3.4028235e38f)) return 0;

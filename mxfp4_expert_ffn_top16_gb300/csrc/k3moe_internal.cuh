@@ -95,7 +95,8 @@ inline __host__ __device__ size_t plan_bytes(int E, long long rows) {
 cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
-                              int K, uint32_t* err, cudaStream_t s);
+                              int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q = nullptr,
+                              uint8_t* out1_qs = nullptr, int q1P = 0);
 // Same contract as launch_dense_gemv, on tcgen05 tiles of 128 weight rows x 64 tokens (for
 // many tokens).
 cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
@@ -104,15 +105,18 @@ cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint1
                               uint32_t* err, cudaStream_t s);
 // Token count from which the dense projections use the tcgen05 tiles.
 constexpr int kUmmaDenseMinTokens = 65;
+// out1_q / out1_qs / q1P (token-at-a-time path, T < kUmmaDenseMinTokens, only): problem 1's bf16
+// outputs also as q1P E4M3 rows per token with e8m0 scales per 32, for the decode expert kernel.
 inline cudaError_t launch_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                                 const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                                 __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
-                                uint32_t* err, cudaStream_t s) {
+                                uint32_t* err, cudaStream_t s, uint8_t* out1_q = nullptr,
+                                uint8_t* out1_qs = nullptr, int q1P = 0) {
   if (T >= kUmmaDenseMinTokens)
     return launch_umma_dense(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
                              T, K, err, s);
   return launch_dense_gemv(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
-                           T, K, err, s);
+                           T, K, err, s, out1_q, out1_qs, q1P);
 }
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s);
@@ -123,10 +127,12 @@ cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* pl
                         cudaStream_t s);
 // Top-k (one block per token), then permutation + plan in one block, for T <= kSmallRouteTokens.
 constexpr int kSmallRouteTokens = 64;
-// done: a workspace counter that is zero between launches (the workspace starts zeroed).
+// done: a workspace counter that is zero between launches (the workspace starts zeroed). Also
+// clears the ncnt counters at cnt (the decode expert kernel's per-chunk GLU completion counts).
 cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                                     int32_t* offsets, int32_t* row_token, int32_t* row_slot,
-                                    int32_t* slot_row, int32_t* plan, int* done, uint32_t* err, cudaStream_t s);
+                                    int32_t* slot_row, int32_t* plan, int* done, int* cnt, int ncnt,
+                                    uint32_t* err, cudaStream_t s);
 cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,
                             cudaStream_t s);
 cudaError_t launch_expert_glu(const k3moe_dims& d, const k3moe_weights& w, const int32_t* plan,
@@ -143,8 +149,9 @@ cudaError_t launch_expert_down(const k3moe_dims& d, const k3moe_weights& w, cons
 constexpr int kUmmaExpertMinTokens = 65;
 inline bool umma_expert_ok(const k3moe_dims& d) { return d.latent % 128 == 0 && d.inter % 128 == 0; }
 inline int umma_chunk_rows(long long T) { return T >= kUmmaExpertMinTokens ? kUmmaChunkRows : kGemvTokens; }
-// z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)].
-// Also clears the ncnt counters at cnt (the decode kernel's per-chunk GLU completion counts).
+// z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)]
+// (row_token null: row r is token r). Also clears the ncnt counters at cnt (the decode kernel's
+// per-chunk GLU completion counts).
 cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
                               uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s);
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
@@ -155,9 +162,12 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
 // Decode (T < kUmmaExpertMinTokens): the same GEMMs with the weights on the MMA's N side (256
 // weight rows per MMA, 8-row chunks): the GLU pass, and with_down (needs latent % 256 == 0) the
 // down pass in the same launch. chunk_done: plan_chunks_max ints, zero at launch.
-cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
-                           const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, bool with_down,
-                           float* o_rows, int* chunk_done, uint32_t* err, cudaStream_t s);
+// zq / zqs: the latent activations as P E4M3 rows per token [T][P][L] with e8m0 scales
+// [T][P][exp_pitch(L)]; the kernel gathers a chunk's rows through row_token.
+cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* zq,
+                           const uint8_t* zqs, const int32_t* row_token, int P, int T, uint8_t* aq,
+                           uint8_t* aqs, bool with_down, float* o_rows, int* chunk_done, uint32_t* err,
+                           cudaStream_t s);
 inline int plan_chunks_max(const k3moe_dims& d, long long T) {
   return (int)(T * d.top_k / kGemvTokens + d.n_experts + 1);
 }

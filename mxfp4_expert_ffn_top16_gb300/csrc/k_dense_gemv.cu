@@ -39,6 +39,9 @@ struct DenseProblem {
   __half* out_h;
   int8_t* out_s;
   int actq;
+  uint8_t* out_q;   // optional: the bf16 outputs as qP E4M3 rows per token [T][qP][N] ...
+  uint8_t* out_qs;  // ... with e8m0 block exponents [T][qP][exp_pitch(N)]
+  int qP;           // 1: MXFP8; 2: bf16 split exactly into hi + lo
 };
 
 struct DenseArgs {
@@ -216,6 +219,21 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
             P.out_h[(size_t)tok * P.N + row] = __float2half_rn(ldexpf(q, -e));
             if (lane == 0) P.out_s[(size_t)tok * exp_pitch(P.N) + row0 / 32] = (int8_t)e;
           }
+          if (P.out_q) {  // the same blocks of 32 features, as E4M3 rows for the tensor cores
+            const float q = bf16_to_f32(vb);
+            const int sp = exp_pitch(P.N);
+            const size_t qr = (size_t)tok * P.qP;
+            const int X0 = P.qP == 1 ? mxfp8_block_exp(warp_max(fabsf(q))) : split_block_exp(warp_max(fabsf(q)));
+            const uint32_t c0 = e4m3x2(mul_pow2(q, -X0), 0.f) & 0xffu;
+            P.out_q[qr * P.N + row] = (uint8_t)c0;
+            if (lane == 0) P.out_qs[qr * sp + row0 / 32] = (uint8_t)(X0 + 127);
+            if (P.qP == 2) {  // lo = the exact remainder v - hi, on its own block exponent
+              const float rem = q - mul_pow2(e4m3x2_value(c0).x, X0);
+              const int X1 = split_block_exp(warp_max(fabsf(rem)));
+              P.out_q[(qr + 1) * P.N + row] = (uint8_t)(e4m3x2(mul_pow2(rem, -X1), 0.f) & 0xffu);
+              if (lane == 0) P.out_qs[(qr + 1) * sp + row0 / 32] = (uint8_t)(X1 + 127);
+            }
+          }
         }
       }
       if (!group_barrier(cbar, cph, abort_flag, args.err)) return;
@@ -254,11 +272,12 @@ cudaError_t launch_t(DenseArgs& a, const uint16_t* const W[2], const int N[2], c
 cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
-                              int K, uint32_t* err, cudaStream_t s) {
+                              int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q, uint8_t* out1_qs, int q1P) {
   if (T <= 0) return cudaSuccess;
   DenseArgs a{};
-  a.p[0] = DenseProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0};
-  a.p[1] = DenseProblem{N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1};
+  a.p[0] = DenseProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0, nullptr, nullptr, 0};
+  a.p[1] = DenseProblem{N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1, out1_q, out1_qs, q1P};
+  if (out1_q && (!out1_bf16 || N1 % 32 != 0 || (q1P != 1 && q1P != 2))) return cudaErrorInvalidValue;
   a.units0 = W0 ? (N0 + kUnitRows - 1) / kUnitRows : 0;
   a.units = a.units0 + (W1 ? (N1 + kUnitRows - 1) / kUnitRows : 0);
   a.T = T;

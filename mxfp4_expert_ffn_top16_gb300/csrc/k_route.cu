@@ -295,7 +295,7 @@ constexpr int kSmallIdx = 2048;
 __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* idx, int T, int E, int k,
                                                              int32_t* offsets, int32_t* row_token,
                                                              int32_t* row_slot, int32_t* slot_row,
-                                                             int32_t* plan, uint32_t* err) {
+                                                             int32_t* plan, int* zcnt, int nzcnt, uint32_t* err) {
   __shared__ int cnt[kMaxE + 1];
   __shared__ int tmp[1024];
   __shared__ int flag[kMaxE];
@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* idx,
   const int tid = threadIdx.x;
   pdl_wait();
   pdl_trigger();
+  for (int i = tid; i < nzcnt; i += blockDim.x) zcnt[i] = 0;  // the decode expert kernel's counters
   const bool in_smem = T * k <= kSmallIdx;
   if (in_smem)
     for (int i = tid; i < T * k; i += blockDim.x) s_idx[i] = idx[i];
@@ -419,10 +420,12 @@ __global__ void __launch_bounds__(kTopkThreads) route_tiny_kernel(const float* _
                                                                   int k, int32_t* idx, float* w, int32_t* offsets,
                                                                   int32_t* row_token, int32_t* row_slot,
                                                                   int32_t* slot_row, int32_t* plan, int* done,
-                                                                  uint32_t* err) {
+                                                                  int* cnt, int ncnt, uint32_t* err) {
   __shared__ int s_last;
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
   block_topk(logits, blockIdx.x, E, k, idx, w);
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -543,7 +546,8 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
                            int32_t* row_token, int32_t* row_slot, int32_t* slot_row,
                            int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s) {
   if (T <= kBlockTokens) {
-    permute_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, k, offsets, row_token, row_slot, slot_row, plan, err);
+    permute_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, k, offsets, row_token, row_slot, slot_row, plan, nullptr,
+                                            0, err);
     return cudaGetLastError();
   }
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
@@ -555,14 +559,15 @@ cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* off
 
 cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                                     int32_t* offsets, int32_t* row_token, int32_t* row_slot,
-                                    int32_t* slot_row, int32_t* plan, int* done, uint32_t* err, cudaStream_t s) {
+                                    int32_t* slot_row, int32_t* plan, int* done, int* cnt, int ncnt,
+                                    uint32_t* err, cudaStream_t s) {
   if (T * k <= kTinyRows)
     return launch_pdl(route_tiny_kernel, dim3(T), dim3(kTopkThreads), 0, s, logits, T, E, k, idx, w, offsets,
-                      row_token, row_slot, slot_row, plan, done, err);
+                      row_token, row_slot, slot_row, plan, done, cnt, ncnt, err);
   cudaError_t e = launch_pdl(topk_block_kernel, dim3(T), dim3(kTopkThreads), 0, s, logits, T, E, k, idx, w);
   if (e != cudaSuccess) return e;
   return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)idx, T, E, k, offsets,
-                    row_token, row_slot, slot_row, plan, err);
+                    row_token, row_slot, slot_row, plan, cnt, ncnt, err);
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,

@@ -116,34 +116,6 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Two values -> two E4M3 codes (nearest even, saturating), v0 in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float v0, float v1) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
-  return r;
-}
-// Two E4M3 codes (low byte first) -> their values.
-__device__ __forceinline__ float2 e4m3x2_value(uint32_t pair) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair));
-  return __half22float2(*reinterpret_cast<__half2*>(&h2));
-}
-// v * 2^e for e in [-254, 254] in two exact power-of-two steps.
-__device__ __forceinline__ float mul_pow2(float v, int e) {
-  const int e1 = e / 2;
-  return v * exp2i(e1) * exp2i(e - e1);
-}
-// Block exponent of the hi / lo parts (amax / 2^X in [128, 256)); all-zero block: -127.
-__device__ __forceinline__ int split_block_exp(float amax) {
-  if (!(amax > 0.0f)) return -127;
-  if (!(amax <= 3.4028235e38f)) return 127;
-  const int X = ilog2_floor(amax) - 7;
-  return X < -127 ? -127 : (X > 127 ? 127 : X);
-}
-template <int P>
-__device__ __forceinline__ int block_exp(float amax) {
-  return P == 1 ? mxfp8_block_exp(amax) : split_block_exp(amax);
-}
 __device__ __forceinline__ float max_in_group4(float v) {
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
   return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
@@ -512,7 +484,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (wid >= (long long)rows * segs) return;  // warp-uniform
   const int r = (int)(wid / segs), base = (int)(wid % segs) * 256;
-  int t = row_token[r];
+  int t = row_token ? row_token[r] : r;
   if (t < 0 || t >= T) {
     if (lane == 0 && base == 0) atomicOr(err, kErrIndex);
     t = 0;

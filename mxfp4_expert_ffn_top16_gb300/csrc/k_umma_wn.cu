@@ -58,10 +58,11 @@ static_assert(kSfCol + 12 * kStages <= kTmemCols, "tensor memory");
 struct WnPass {
   CUtensorMap tw0;     // GLU: gate codes, box {128, 128}; down: down codes, box {128, 256}
   CUtensorMap tw1;     // GLU: up codes, box {128, 128}
-  CUtensorMap ta;      // activation rows e4m3 {K, P*rows}, box {128, 8*P}
+  CUtensorMap ta;      // down: activation rows e4m3 {K, P*rows}, box {128, 8*P}
   const uint8_t* s0;   // weight scales [E][N][K/32]
   const uint8_t* s1;   // GLU: up scales
-  const uint8_t* sb;   // activation scales [P*rows][exp_pitch(K)]
+  const uint8_t* sa;   // GLU: activation rows per token [T][P][K] e4m3 (gathered by row_token)
+  const uint8_t* sb;   // activation scales: GLU [T][P][exp_pitch(K)] per token; down [P*rows][...]
   int N, K;            // output features per expert, reduction length
 };
 
@@ -69,6 +70,8 @@ struct UWnArgs {
   WnPass pass[2];      // [0] GLU, [1] down
   int npass;           // 1: the GLU pass only; 2: GLU then down
   int32_t* plan;
+  const int32_t* row_token;  // sorted row -> token
+  int ntok;            // tokens (T)
   int E;               // experts
   int rows_max;        // T * k
   uint8_t* aq;         // GLU output [P*rows][inter] e4m3 (the down pass's activations)
@@ -117,31 +120,14 @@ __device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
          ((uint64_t)1 << 46);
 }
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ uint32_t e4m3x2(float v0, float v1) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(v1), "f"(v0));
-  return r;
-}
-__device__ __forceinline__ float2 e4m3x2_value(uint32_t pair) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)pair));
-  return __half22float2(*reinterpret_cast<__half2*>(&h2));
-}
-__device__ __forceinline__ float mul_pow2(float v, int e) {
-  const int e1 = e / 2;
-  return v * exp2i(e1) * exp2i(e - e1);
-}
-__device__ __forceinline__ int split_block_exp(float amax) {
-  if (!(amax > 0.0f)) return -127;
-  if (!(amax <= 3.4028235e38f)) return 127;
-  const int X = ilog2_floor(amax) - 7;
-  return X < -127 ? -127 : (X > 127 ? 127 : X);
 }
 // 32 values of one thread -> P rows of 32 E4M3 codes with their block exponents (P = 1: MXFP8;
 // P = 2: hi and lo, v left holding the lo remainders).
@@ -254,22 +240,26 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
         if (!it.glu && !wait_chunk(A.chunk_done + it.c, glu_target, abort_flag, A.err)) break;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], kBPacked + kATx);
-          if (it.glu) {
+          if (it.glu) {  // the gather warps copy the GLU activation rows
+            mbar_arrive_expect_tx(&full[s], kBPacked);
             tma_load_2d(sB + s * kBTile, &W.tw0, kc * BKE, wrow, &full[s]);
             tma_load_2d(sB + s * kBTile + (kNW / 2) * 128, &W.tw1, kc * BKE, wrow, &full[s]);
           } else {
+            mbar_arrive_expect_tx(&full[s], kBPacked + kATx);
             tma_load_2d(sB + s * kBTile, &W.tw0, kc * BKE, wrow, &full[s]);
+            tma_load_2d(sA + s * kATile, &W.ta, kc * BKE, P * it.r0, &full[s]);
           }
-          tma_load_2d(sA + s * kATile, &W.ta, kc * BKE, P * it.r0, &full[s]);
           if (++s == kStages) { s = 0; ph ^= 1; }
         }
       }
     }
   } else if (warp == 2 || warp == 3) {  // ---------------- scale gather
     // warp 2: activation rows (lanes < 8P, word 0) and weight rows 0..127; warp 3: weight rows
-    // 128..255 (GLU: the up rows)
+    // 128..255 (GLU: the up rows). For GLU items the two warps also copy the activation tile:
+    // 8P rows x 128 bytes per stage, 16 bytes per copy, into the 128-byte swizzled layout the
+    // MMA reads (16-byte unit j of row m at unit j ^ (m & 7)); rows past the chunk are left out.
     const bool w2 = warp == 2;
+    const int gl = lane + (w2 ? 0 : 32);  // 0..63 over the two warps
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -286,8 +276,29 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
         ws[w] = (it.glu && r >= kNW / 2) ? W.s1 + (wrow + r - kNW / 2) * srow : W.s0 + (wrow + r) * srow;
       }
       const bool act = w2 && lane < P * it.nr;
-      const uint8_t* as = W.sb + ((size_t)P * it.r0 + (act ? lane : 0)) * spb;
+      // token of a sorted row (checked: a bad one reads token 0 and sets the error word)
+      auto token = [&](int r) -> size_t {
+        const int t = __ldg(A.row_token + r);
+        if (t >= 0 && t < A.ntok) return (size_t)t;
+        atomicOr(A.err, kErrIndex);
+        return 0;
+      };
+      // activation row m = lane (scales): a sorted row of the down pass, a token's row of the GLU
+      const size_t arow = !act ? 0 : it.glu ? token(it.r0 + lane / P) * P + lane % P : (size_t)P * it.r0 + lane;
+      const uint8_t* as = W.sb + arow * spb;
       const uint32_t st_lane = smem_u32(stg) + lane * 16;
+      // GLU activation tile: units gl and gl + 64 (row m = unit / 8, 16-byte column j = unit % 8)
+      const uint8_t* asrc[2];
+      uint32_t adst[2];
+      bool aon[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int unit = gl + 64 * h, m = unit >> 3, j = unit & 7;
+        aon[h] = it.glu && m < P * it.nr;
+        const size_t tr = aon[h] ? token(it.r0 + m / P) * P + m % P : 0;
+        asrc[h] = W.sa + tr * W.K + 16 * j;
+        adst[h] = smem_u32(sA) + (uint32_t)(m * 128 + ((j ^ (m & 7)) << 4));
+      }
       if (!it.glu && w2) {  // the activation scales come from this chunk's GLU items
         int good = 1;
         if (lane == 0) good = wait_chunk(A.chunk_done + it.c, glu_target, abort_flag, A.err) ? 1 : 0;
@@ -298,6 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
       for (int kc = 0; kc < nk; ++kc) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
         const uint32_t so = st_lane + (uint32_t)(s * kStgBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          if (aon[h]) cp_async16(adst[h] + (uint32_t)(s * kATile), asrc[h] + (size_t)kc * BKE);
         if (act) cp_async4(so, as + 4 * kc);
 #pragma unroll
         for (int w = 0; w < 4; ++w) cp_async4(so + 512 * (w2 ? 1 : 2) + 4 * w, ws[w] + 4 * kc);
@@ -442,18 +456,18 @@ cudaError_t launch_t(UWnArgs& a, int items_max, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
-                           const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, bool with_down,
-                           float* o_rows, int* chunk_done, uint32_t* err, cudaStream_t s) {
+cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* zq,
+                           const uint8_t* zqs, const int32_t* row_token, int P, int T, uint8_t* aq,
+                           uint8_t* aqs, bool with_down, float* o_rows, int* chunk_done, uint32_t* err,
+                           cudaStream_t s) {
   UWnArgs A{};
   const int rows = T * d.top_k;
   WnPass& G = A.pass[0];
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
   if (!make_tmap_fp4(&G.tw0, w.gate_q, d.latent, wrows, pitch, kNW / 2) ||
-      !make_tmap_fp4(&G.tw1, w.up_q, d.latent, wrows, pitch, kNW / 2) ||
-      !make_tmap_2d(&G.ta, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, kRows * P, true))
+      !make_tmap_fp4(&G.tw1, w.up_q, d.latent, wrows, pitch, kNW / 2))
     return cudaErrorInvalidValue;
-  G.s0 = w.gate_s; G.s1 = w.up_s; G.sb = bs;
+  G.s0 = w.gate_s; G.s1 = w.up_s; G.sa = zq; G.sb = zqs;
   G.N = d.inter; G.K = d.latent;
   int items_max = (rows / kRows + d.n_experts) * (d.inter / (kNW / 2));
   A.npass = 1;
@@ -470,7 +484,7 @@ cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t*
     A.pass[1].N = kNW;  // unused; keeps the item arithmetic defined
     A.pass[1].K = BKE;
   }
-  A.plan = plan; A.E = d.n_experts; A.rows_max = rows;
+  A.plan = plan; A.row_token = row_token; A.ntok = T; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.o_out = o_rows; A.chunk_done = chunk_done; A.err = err;
   return P == 1 ? launch_t<1>(A, items_max, s) : launch_t<2>(A, items_max, s);
 }

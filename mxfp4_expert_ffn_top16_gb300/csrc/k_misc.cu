@@ -11,45 +11,55 @@ namespace {
 // c[t][n] = bf16(sum_{j<k} w[t][j] * o[slot_row[t*k+j]][n]), fp32, j ascending.
 // Routed outputs are combined in latent space before the projection back to the residual
 // ("kimi-k3-mlx", LatentMoE).
-// Two values per thread; the k rows and weights are loaded before any is summed, so all of a
-// thread's loads are in flight together (few tokens leave this kernel latency-bound).
+// Four values per thread (16-byte loads); the k rows and weights are loaded before any is
+// summed, so all of a thread's loads are in flight together: HBM-bound for many tokens (the
+// fp32 rows are read once, with the streaming hint), latency-bound for a few. KB >= k bounds the
+// unrolled slot loop.
 constexpr int kMaxTopK = 32;
-__global__ void combine_kernel(const float* __restrict__ o, const int32_t* __restrict__ slot_row,
-                               const float* __restrict__ w, int T, int k, int L, uint16_t* c) {
+constexpr int kCombineThreads = 128;
+template <int KB>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ o,
+                                                                  const int32_t* __restrict__ slot_row,
+                                                                  const float* __restrict__ w, int T, int k,
+                                                                  int L, uint16_t* c) {
   pdl_wait();
   pdl_trigger();
   const int t = blockIdx.y;
-  const int n = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
+  const int n = (blockIdx.x * kCombineThreads + threadIdx.x) * 4;
   if (t >= T || n >= L) return;
-  int rr[kMaxTopK];
+  int rr[KB];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) rr[j] = j < k ? slot_row[(size_t)t * k + j] : -1;
-  float2 v[kMaxTopK];
-  float wj[kMaxTopK];
+  for (int j = 0; j < KB; ++j) {
+    rr[j] = j < k ? __ldg(slot_row + (size_t)t * k + j) : -1;
+    if (rr[j] >= T * k) rr[j] = -1;  // out-of-range rows contribute nothing
+  }
+  float4 v[KB];
+  float wj[KB];
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    const bool ok = j < k && rr[j] >= 0 && rr[j] < T * k;  // out-of-range rows contribute nothing
-    v[j] = ok ? *reinterpret_cast<const float2*>(o + (size_t)rr[j] * L + n) : make_float2(0.f, 0.f);
-    wj[j] = ok ? w[(size_t)t * k + j] : 0.f;
-    if (!ok) rr[j] = -1;
+  for (int j = 0; j < KB; ++j) {
+    const bool ok = rr[j] >= 0;
+    v[j] = ok ? __ldcs(reinterpret_cast<const float4*>(o + (size_t)rr[j] * L + n)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    wj[j] = ok ? __ldg(w + (size_t)t * k + j) : 0.f;
   }
   // Kahan-compensated sum in slot order, so the bf16 rounding of c follows the exact sum of
   // the fp32 terms except within ~1 fp32 ulp of a rounding boundary
-  float s[2] = {0.f, 0.f}, cc[2] = {0.f, 0.f};
+  float s[4] = {0.f, 0.f, 0.f, 0.f}, cc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
+  for (int j = 0; j < KB; ++j) {
     if (rr[j] < 0) continue;
-    const float p[2] = {wj[j] * v[j].x, wj[j] * v[j].y};
+    const float p[4] = {wj[j] * v[j].x, wj[j] * v[j].y, wj[j] * v[j].z, wj[j] * v[j].w};
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
+    for (int q = 0; q < 4; ++q) {
       const float yk = p[q] - cc[q];
       const float tk = s[q] + yk;
       cc[q] = (tk - s[q]) - yk;
       s[q] = tk;
     }
   }
-  const uint32_t packed = (uint32_t)f32_to_bf16(s[0] - cc[0]) | ((uint32_t)f32_to_bf16(s[1] - cc[1]) << 16);
-  *reinterpret_cast<uint32_t*>(c + (size_t)t * L + n) = packed;
+  uint2 packed;
+  packed.x = (uint32_t)f32_to_bf16(s[0] - cc[0]) | ((uint32_t)f32_to_bf16(s[1] - cc[1]) << 16);
+  packed.y = (uint32_t)f32_to_bf16(s[2] - cc[2]) | ((uint32_t)f32_to_bf16(s[3] - cc[3]) << 16);
+  *reinterpret_cast<uint2*>(c + (size_t)t * L + n) = packed;
 }
 
 // One warp per (token, block of 32 values): optional MXFP8 round trip, then an f16 copy
@@ -76,9 +86,11 @@ __global__ void act_prep_kernel(const uint16_t* __restrict__ z, int T, int L, in
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
-  if (k > kMaxTopK) return cudaErrorInvalidValue;
-  dim3 grid((L / 2 + 127) / 128, T);
-  return launch_pdl(combine_kernel, grid, dim3(128), 0, s, o_rows, slot_row, w, T, k, L, c);
+  if (k > kMaxTopK || L % 4) return cudaErrorInvalidValue;
+  dim3 grid((L / 4 + kCombineThreads - 1) / kCombineThreads, T);
+  if (k <= 16)
+    return launch_pdl(combine_kernel<16>, grid, dim3(kCombineThreads), 0, s, o_rows, slot_row, w, T, k, L, c);
+  return launch_pdl(combine_kernel<kMaxTopK>, grid, dim3(kCombineThreads), 0, s, o_rows, slot_row, w, T, k, L, c);
 }
 
 cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,

@@ -242,6 +242,24 @@ def test_layer_tiny_ragged_and_edge_T():
                                   check=False) in (k3.K3MOE_OK, 1)
 
 
+# Whole layer on shapes other than the tiny one: DEEP (several K stages per expert item, fewer
+# items than SMs) and HIDE (a residual wider than the latent, 64 experts), decode token counts.
+HIDE = synth.Dims(hidden=1536, latent=512, inter=256, n_experts=64, top_k=4)
+
+
+@pytest.mark.parametrize("dname,T", [("deep", 1), ("deep", 5), ("deep", 40), ("hide", 1), ("hide", 9),
+                                     ("hide", 64)])
+def test_layer_other_dims_every_token(dname, T):
+    d = {"deep": DEEP, "hide": HIDE}[dname]
+    lay = DeviceLayer(d, seed=4)
+    x = synth.host_bf16_normal(5, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+    y, idx, w = _forward(lay, x)
+    _compare_layer(lay, x, y, idx, np.arange(T))
+    y2, idx2, w2 = _forward(lay, x)  # a rerun gives the same bits
+    np.testing.assert_array_equal(y2, y)
+    np.testing.assert_array_equal(idx2, idx)
+
+
 def test_layer_k3_decode_b1(k3_layer):
     w = synth.WORKLOADS["decode_b1"]
     n = 6

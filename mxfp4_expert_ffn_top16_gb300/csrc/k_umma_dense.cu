@@ -4,13 +4,16 @@
 //
 //   out[t][n] = sum_k W[n][k] x[t][k]
 //
-// A persistent CTA walks 128 x 64 output tiles (128 weight rows on M, 64 tokens on N).
-// Warp 0 streams 128 x 64 bf16 tiles of W and 64 x 64 tiles of x through TMA (128-byte
-// swizzle) into a ring of stages. Warp 1 allocates 256 tensor-memory columns (four 64-column
-// accumulator slots) and issues tcgen05.mma kind::f16 (M=128, N=64, K=16, four per stage);
-// each group of 8 stages (512 of K) accumulates into one slot, which is committed to the
-// epilogue. Warps 2-5 (one tensor-memory lane = one weight row per thread) drain every slot
-// into per-thread Kahan-compensated fp32 sums, so the tensor core's own accumulation spans at
+// A persistent CTA walks 128 x BN output tiles (128 weight rows on M, BN tokens on N; BN = 256
+// for many tokens: 48 KB of operands per 4.2 MFLOP stage, twice the flops per byte from L2 of
+// BN = 64, which is kept for a few hundred tokens, where 256-token tiles would leave SMs idle).
+// Warp 0 streams 128 x 64 bf16 tiles of W and BN x 64 tiles of x through TMA (128-byte
+// swizzle) into a ring of stages. Warp 1 allocates the tensor memory (BN-column accumulator
+// slots) and issues tcgen05.mma kind::f16 (M=128, N=BN, K=16, four per stage); each group of 8
+// stages (512 of K) accumulates into one slot, which is committed to the epilogue. The
+// epilogue warps (lane quadrant = warp % 4; with BN = 256 two warps per quadrant, half of the
+// columns each; one tensor-memory lane = one weight row per thread) drain every slot into
+// per-thread fp32 sums added in group order, so the tensor core's own accumulation spans at
 // most 32 MMAs; after the last group they write fp32 + bias (logits), bf16 (z, y) and, for z,
 // the f16 block-scaled copy with one power-of-two exponent per 32 features (in MXFP8 mode of
 // the MXFP8 round trip).
@@ -23,11 +26,21 @@
 namespace k3moe {
 namespace {
 
-constexpr int BM = 128, BN = 64, BK = 64, kStages = 6, kGroup = 8, kSlots = 4;
+constexpr int BM = 128, BK = 64, kGroup = 8, kGroupM = 16;
 constexpr int kATile = BM * BK * 2;  // 16 KB
-constexpr int kBTile = BN * BK * 2;  // 8 KB
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = kSlots * BN;
+template <int BN>
+struct Tile {
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kSlots = BN == 256 ? 2 : 4;
+  static constexpr int kBTile = BN * BK * 2;
+  static constexpr int kEpiWarps = BN == 256 ? 8 : 4;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kEpiCols = BN / (kEpiWarps / 4);  // accumulator columns (tokens) per epilogue warp
+  static constexpr uint32_t kTmemCols = kSlots * BN;
+  static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "tensor memory");
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * (kATile + kBTile) + (2 * kStages + 2 * kSlots + 1) * 8 + 16;
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+};
 
 struct UProblem {
   int N;
@@ -48,7 +61,12 @@ struct UDenseArgs {
   uint32_t* err;
 };
 
-__global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_constant__ UDenseArgs a) {
+template <int BN>
+__global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const __grid_constant__ UDenseArgs a) {
+  using TL = Tile<BN>;
+  constexpr int kStages = TL::kStages, kSlots = TL::kSlots, kBTile = TL::kBTile, kEpiWarps = TL::kEpiWarps,
+                kEpiCols = TL::kEpiCols;
+  constexpr uint32_t kTmemCols = TL::kTmemCols;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sA = smem;
@@ -69,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_co
     }
     for (int b = 0; b < kSlots; ++b) {
       mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 4);
+      mbar_init(&acce[b], kEpiWarps);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -87,6 +105,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_co
   const uint32_t tmem = *tmem_slot;
   const int items = a.mtiles * a.ntiles;
   const int nk = a.K / BK;
+  // item -> (weight tile, token tile), in groups of kGroupM weight tiles: the CTAs in flight
+  // share a few weight tiles and a few token tiles, so both are reused from L2 even when the
+  // tokens do not fit in it
+  auto tile_of = [&](int it, int& mt, int& nt) {
+    const int g = it / (kGroupM * a.ntiles), r = it - g * kGroupM * a.ntiles;
+    const int gm = min(kGroupM, a.mtiles - g * kGroupM);
+    nt = r / gm;
+    mt = g * kGroupM + (r - nt * gm);
+  };
   const int ngroups = (nk + kGroup - 1) / kGroup;
 
   if (warp == 0) {
@@ -95,7 +122,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_co
       uint32_t ph = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const int mt = it / a.ntiles, nt = it - mt * a.ntiles;
+        int mt, nt;
+        tile_of(it, mt, nt);
         const int pi = mt < a.mt0 ? 0 : 1;
         const int row0 = (pi ? mt - a.mt0 : mt) * BM;
         for (int kb = 0; kb < nk; ++kb) {
@@ -140,34 +168,30 @@ __global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_co
       volatile int no_abort = 0;
       mbar_wait_bounded(drain, 0, &no_abort, a.err);
     }
-  } else {  // ---------------- epilogue warps 2..5, lane quadrant = warp % 4
-    const int q = warp & 3;
+  } else {  // ---------------- epilogue warps 2..9: lane quadrant = warp % 4, column half h
+    const int q = warp & 3, h = (warp - 2) >> 2;
     int slot = 0;
     uint32_t sph = 0;
     bool ok = true;
     for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-      const int mt = it / a.ntiles, nt = it - mt * a.ntiles;
+      int mt, nt;
+      tile_of(it, mt, nt);
       const int pi = mt < a.mt0 ? 0 : 1;
       const UProblem& P = a.p[pi];
       const int row = (pi ? mt - a.mt0 : mt) * BM + q * 32 + lane;  // output feature
-      float sum[BN], cmp[BN];
+      float sum[kEpiCols];
 #pragma unroll
-      for (int j = 0; j < BN; ++j) sum[j] = cmp[j] = 0.f;
+      for (int j = 0; j < kEpiCols; ++j) sum[j] = 0.f;
       for (int gi = 0; gi < ngroups; ++gi) {
         if (!mbar_wait_warp(&accf[slot], sph, abort_flag, a.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < kEpiCols; c += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BN + c), v);
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * BN + h * kEpiCols + c), v);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float yk = __uint_as_float(v[j]) - cmp[c + j];
-            const float tk = sum[c + j] + yk;
-            cmp[c + j] = (tk - sum[c + j]) - yk;
-            sum[c + j] = tk;
-          }
+          for (int j = 0; j < 32; ++j) sum[c + j] += __uint_as_float(v[j]);
         }
         tc_fence_before();
         __syncwarp();
@@ -178,10 +202,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_co
       const bool valid = row < P.N;
       const float bias = (P.bias && valid) ? P.bias[row] : 0.f;
 #pragma unroll
-      for (int j = 0; j < BN; ++j) {
-        const int tok = nt * BN + j;
+      for (int j = 0; j < kEpiCols; ++j) {
+        const int tok = nt * BN + h * kEpiCols + j;
         if (tok >= a.T) continue;  // uniform across the warp
-        const float val = sum[j] - cmp[j];
+        const float val = sum[j];
         if (P.out_f32 && valid) P.out_f32[(size_t)tok * P.N + row] = val + bias;
         if (P.out_bf16) {
           const uint16_t vb = f32_to_bf16(val);
@@ -205,7 +229,22 @@ __global__ void __launch_bounds__(kThreads, 1) umma_dense_kernel(const __grid_co
   }
 }
 
-constexpr size_t kSmem = 1024 + (size_t)kStages * (kATile + kBTile) + (2 * kStages + 2 * kSlots + 1) * 8 + 16;
+template <int BN>
+cudaError_t launch_bn(UDenseArgs& a, const uint16_t* const W[2], const int N[2], const uint16_t* x, int T, int K,
+                      cudaStream_t s) {
+  a.ntiles = (T + BN - 1) / BN;
+  for (int i = 0; i < 2; ++i)
+    if (W[i] && !make_tmap_2d(&a.tw[i], W[i], 2, (uint64_t)K, (uint64_t)N[i], (uint64_t)K * 2, BK, BM, true))
+      return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&a.tx, x, 2, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK, BN, true))
+    return cudaErrorInvalidValue;
+  constexpr size_t smem = Tile<BN>::kSmem;
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_dense_kernel<BN>), smem);
+  if (e != cudaSuccess) return e;
+  const int items = a.mtiles * a.ntiles;
+  const int grid = items < num_sms() ? items : num_sms();
+  return launch_pdl(umma_dense_kernel<BN>, dim3(grid), dim3(Tile<BN>::kThreads), smem, s, a);
+}
 
 }  // namespace
 
@@ -219,22 +258,17 @@ cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint1
   a.p[1] = UProblem{N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1};
   a.mt0 = W0 ? (N0 + BM - 1) / BM : 0;
   a.mtiles = a.mt0 + (W1 ? (N1 + BM - 1) / BM : 0);
-  a.ntiles = (T + BN - 1) / BN;
   a.T = T;
   a.K = K;
   a.err = err;
   const uint16_t* W[2] = {W0, W1};
   const int N[2] = {N0, N1};
-  for (int i = 0; i < 2; ++i)
-    if (W[i] && !make_tmap_2d(&a.tw[i], W[i], 2, (uint64_t)K, (uint64_t)N[i], (uint64_t)K * 2, BK, BM, true))
-      return cudaErrorInvalidValue;
-  if (!make_tmap_2d(&a.tx, x, 2, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK, BN, true))
-    return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_dense_kernel), kSmem);
-  if (e != cudaSuccess) return e;
-  const int items = a.mtiles * a.ntiles;
-  const int grid = items < num_sms() ? items : num_sms();
-  return launch_pdl(umma_dense_kernel, dim3(grid), dim3(kThreads), kSmem, s, a);
+  // rounds of items over the SMs times the cost of one item (a 256-token tile ~ two 64-token ones)
+  const long long g = num_sms();
+  const long long r64 = ((long long)a.mtiles * ((T + 63) / 64) + g - 1) / g;
+  const long long r256 = ((long long)a.mtiles * ((T + 255) / 256) + g - 1) / g;
+  if (2 * r256 < r64) return launch_bn<256>(a, W, N, x, T, K, s);
+  return launch_bn<64>(a, W, N, x, T, K, s);
 }
 
 }  // namespace k3moe

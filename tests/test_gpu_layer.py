@@ -28,7 +28,8 @@ def k3_layer():
 
 
 # ------------------------------------------------------------------ projection
-@pytest.mark.parametrize("T,N,K", [(1, 3584, 7168), (5, 128, 256), (64, 7168, 3584), (200, 192, 320)])
+@pytest.mark.parametrize("T,N,K", [(1, 3584, 7168), (5, 128, 256), (64, 7168, 3584), (200, 192, 320),
+                                   (2500, 1024, 1088)])
 def test_project(T, N, K):
     W = synth.host_bf16_normal(1, 3, 0, N * K, 0.02).reshape(N, K)
     x = synth.host_bf16_normal(1, 1, 0, T * K, 1.0).reshape(T, K)

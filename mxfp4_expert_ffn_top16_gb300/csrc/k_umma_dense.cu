@@ -210,12 +210,14 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const
         if (P.out_bf16) {
           const uint16_t vb = f32_to_bf16(val);
           if (valid) P.out_bf16[(size_t)tok * P.N + row] = vb;
-          if (P.out_h) {  // N multiple of 32: the warp's 32 rows are one block
+          if (P.out_h) {  // N multiple of 32: the warp's 32 rows are one block, all valid or none
             float qv = bf16_to_f32(vb);
             if (P.actq) qv = mxfp8_roundtrip(qv, mxfp8_block_exp(warp_max(fabsf(qv))));
             const int e = f16_block_exp(warp_max(fabsf(qv)));
-            P.out_h[(size_t)tok * P.N + row] = __float2half_rn(ldexpf(qv, -e));
-            if (lane == 0) P.out_s[(size_t)tok * exp_pitch(P.N) + row / 32] = (int8_t)e;
+            if (valid) {
+              P.out_h[(size_t)tok * P.N + row] = __float2half_rn(ldexpf(qv, -e));
+              if (lane == 0) P.out_s[(size_t)tok * exp_pitch(P.N) + row / 32] = (int8_t)e;
+            }
           }
         }
       }

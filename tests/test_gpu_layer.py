@@ -29,7 +29,7 @@ def k3_layer():
 
 # ------------------------------------------------------------------ projection
 @pytest.mark.parametrize("T,N,K", [(1, 3584, 7168), (5, 128, 256), (64, 7168, 3584), (200, 192, 320),
-                                   (2500, 1024, 1088)])
+                                   (2500, 1024, 1088), (2300, 1152, 320)])
 def test_project(T, N, K):
     W = synth.host_bf16_normal(1, 3, 0, N * K, 0.02).reshape(N, K)
     x = synth.host_bf16_normal(1, 1, 0, T * K, 1.0).reshape(T, K)
@@ -244,14 +244,17 @@ def test_layer_tiny_ragged_and_edge_T():
 
 
 # Whole layer on shapes other than the tiny one: DEEP (several K stages per expert item, fewer
-# items than SMs) and HIDE (a residual wider than the latent, 64 experts), decode token counts.
+# items than SMs), HIDE (a residual wider than the latent, 64 experts) and ODD.
+# ODD: latent and inter not multiples of 128 (the expert GEMV, the f16 block-scaled copy of z,
+# and a last 128-row tile of W_in that is partly past its end).
 HIDE = synth.Dims(hidden=1536, latent=512, inter=256, n_experts=64, top_k=4)
+ODD = synth.Dims(hidden=256, latent=192, inter=192, n_experts=16, top_k=4)
 
 
 @pytest.mark.parametrize("dname,T", [("deep", 1), ("deep", 5), ("deep", 40), ("hide", 1), ("hide", 9),
-                                     ("hide", 64)])
+                                     ("hide", 64), ("odd", 3), ("odd", 70), ("odd", 300)])
 def test_layer_other_dims_every_token(dname, T):
-    d = {"deep": DEEP, "hide": HIDE}[dname]
+    d = {"deep": DEEP, "hide": HIDE, "odd": ODD}[dname]
     lay = DeviceLayer(d, seed=4)
     x = synth.host_bf16_normal(5, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
     y, idx, w = _forward(lay, x)

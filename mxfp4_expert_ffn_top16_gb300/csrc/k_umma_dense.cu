@@ -200,25 +200,40 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const
       }
       if (!ok) break;
       const bool valid = row < P.N;
-      const float bias = (P.bias && valid) ? P.bias[row] : 0.f;
+      // outputs of this warp: tokens tok0 .. tok0 + ntok - 1, one loop per output kind (the
+      // executed code per item stays small: the MMA and TMA warps' loops stay in the
+      // instruction cache)
+      const int tok0 = nt * BN + h * kEpiCols;
+      const int ntok = min(kEpiCols, a.T - tok0);
+      if (P.out_h) {  // f16 block-scaled copy (+ bf16): N multiple of 32, the warp's rows are one block
 #pragma unroll
-      for (int j = 0; j < kEpiCols; ++j) {
-        const int tok = nt * BN + h * kEpiCols + j;
-        if (tok >= a.T) continue;  // uniform across the warp
-        const float val = sum[j];
-        if (P.out_f32 && valid) P.out_f32[(size_t)tok * P.N + row] = val + bias;
-        if (P.out_bf16) {
-          const uint16_t vb = f32_to_bf16(val);
+        for (int j = 0; j < kEpiCols; ++j) {
+          if (j >= ntok) continue;  // uniform across the warp
+          const int tok = tok0 + j;
+          const uint16_t vb = f32_to_bf16(sum[j]);
           if (valid) P.out_bf16[(size_t)tok * P.N + row] = vb;
-          if (P.out_h) {  // N multiple of 32: the warp's 32 rows are one block, all valid or none
-            float qv = bf16_to_f32(vb);
-            if (P.actq) qv = mxfp8_roundtrip(qv, mxfp8_block_exp(warp_max(fabsf(qv))));
-            const int e = f16_block_exp(warp_max(fabsf(qv)));
-            if (valid) {
-              P.out_h[(size_t)tok * P.N + row] = __float2half_rn(ldexpf(qv, -e));
-              if (lane == 0) P.out_s[(size_t)tok * exp_pitch(P.N) + row / 32] = (int8_t)e;
-            }
+          float qv = bf16_to_f32(vb);
+          if (P.actq) qv = mxfp8_roundtrip(qv, mxfp8_block_exp(warp_max(fabsf(qv))));
+          const int e = f16_block_exp(warp_max(fabsf(qv)));
+          if (valid) {
+            P.out_h[(size_t)tok * P.N + row] = __float2half_rn(ldexpf(qv, -e));
+            if (lane == 0) P.out_s[(size_t)tok * exp_pitch(P.N) + row / 32] = (int8_t)e;
           }
+        }
+      } else if (valid && P.out_f32) {  // router logits + bias
+        const float bias = P.bias ? P.bias[row] : 0.f;
+        float* dst = P.out_f32 + (size_t)tok0 * P.N + row;
+#pragma unroll
+        for (int j = 0; j < kEpiCols; ++j) {
+          if (j < ntok) *dst = sum[j] + bias;
+          dst += P.N;
+        }
+      } else if (valid && P.out_bf16) {
+        uint16_t* dst = P.out_bf16 + (size_t)tok0 * P.N + row;
+#pragma unroll
+        for (int j = 0; j < kEpiCols; ++j) {
+          if (j < ntok) *dst = f32_to_bf16(sum[j]);
+          dst += P.N;
         }
       }
     }

@@ -33,7 +33,8 @@ def build(force: bool = False) -> str:
 
 class Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("hidden", "latent", "inter", "n_experts", "top_k", "act", "actq")]
+                ("hidden", "latent", "inter", "n_experts", "top_k", "act", "actq", "n_shared",
+                 "shared_inter")]
 
 
 class Weights(ctypes.Structure):
@@ -41,7 +42,8 @@ class Weights(ctypes.Structure):
                 ("w_in", ctypes.c_void_p), ("w_out", ctypes.c_void_p),
                 ("gate_q", ctypes.c_void_p), ("gate_s", ctypes.c_void_p),
                 ("up_q", ctypes.c_void_p), ("up_s", ctypes.c_void_p),
-                ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p)]
+                ("down_q", ctypes.c_void_p), ("down_s", ctypes.c_void_p),
+                ("w_sgate", ctypes.c_void_p), ("w_sup", ctypes.c_void_p), ("w_sdown", ctypes.c_void_p)]
 
 
 _lib = None
@@ -79,6 +81,8 @@ def lib():
         L.k3o_expert_row.argtypes = [p, p, i, p, p, p]
         L.k3o_expert_row.restype = i
         L.k3o_combine_token.argtypes = [i, i, p, p, p, p]
+        L.k3o_shared_ffn.argtypes = [p, p, p, p, p]
+        L.k3o_shared_ffn.restype = i
         L.k3o_layer_forward.argtypes = [p, p, p, i, p, p, p, p, p, p, i]
         L.k3o_layer_forward.restype = i
         L.k3o_max_threads.restype = i
@@ -156,8 +160,8 @@ def mx_weight(q_row, s_row, j) -> float:
     return lib().k3o_mx_weight(q_row.ctypes.data, s_row.ctypes.data, j)
 
 
-def make_dims(d, act=0, actq=0) -> Dims:
-    return Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, act, actq)
+def make_dims(d, act=0, actq=0, n_shared=0, shared_inter=0) -> Dims:
+    return Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, act, actq, n_shared, shared_inter)
 
 
 def expert_params(d) -> int:
@@ -253,9 +257,15 @@ class Layer:
     """A layer for the oracle: dense weights (bf16 bits) plus the experts that may be
     selected ({e: {gate_q, gate_s, up_q, up_s, down_q, down_s}})."""
 
-    def __init__(self, d, w_router, w_in, w_out, experts: dict, bias=None, act=0, actq=0):
+    def __init__(self, d, w_router, w_in, w_out, experts: dict, bias=None, act=0, actq=0, shared=None):
+        """shared: None, or (w_sgate [S][H], w_sup [S][H], w_sdown [H][S], n_shared) bf16 bits,
+        the n_shared experts stacked along S."""
         self.d = d
-        self.dims = make_dims(d, act, actq)
+        ns, si = 0, 0
+        if shared is not None:
+            ns = shared[3]
+            si = shared[0].shape[0] // ns
+        self.dims = make_dims(d, act, actq, ns, si)
         self.wr = _c(w_router, np.uint16)
         self.wi = _c(w_in, np.uint16)
         self.wo = _c(w_out, np.uint16)
@@ -268,6 +278,20 @@ class Layer:
         self.w.w_in = self.wi.ctypes.data
         self.w.w_out = self.wo.ctypes.data
         self.et.fill(self.w)
+        self.shared = None
+        if shared is not None:
+            self.shared = [_c(a, np.uint16) for a in shared[:3]]
+            self.w.w_sgate, self.w.w_sup, self.w.w_sdown = (a.ctypes.data for a in self.shared)
+
+    def shared_ffn(self, x_row):
+        """The shared experts on one token: (s double [H], stacked GLU outputs bf16 [S])."""
+        x = _c(x_row, np.uint16)
+        s = np.empty(self.d.hidden, np.float64)
+        a = np.empty(max(1, self.dims.n_shared * self.dims.shared_inter), np.uint16)
+        if lib().k3o_shared_ffn(ctypes.byref(self.dims), ctypes.byref(self.w), x.ctypes.data,
+                                s.ctypes.data, a.ctypes.data) != 0:
+            raise ValueError("oracle: unsupported activation")
+        return s, a
 
     def expert_row(self, e, z_row):
         z = _c(z_row, np.uint16)

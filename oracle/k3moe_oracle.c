@@ -25,6 +25,12 @@
  *  - One shared latent-in W_in [L][H] and latent-out W_out [H][L] per layer; the combine
  *    runs in latent space before W_out.
  *  - bf16 round-to-nearest-even at z, at the GLU output a, at the combine c and at y.
+ *  - Shared experts ("kimi-k3-mlx", Architecture table and LatentMoE: n_shared always-on
+ *    experts per token that work on the H-wide residual, not in the latent space; the
+ *    weights outside the routed experts are bf16, Quantisation tiers): each is a bf16 GLU
+ *    FFN with the routed experts' activation, s_j = D_j bf16(silu(G_j x) * (U_j x)); their
+ *    width is not on the pages (a parameter). The shared outputs are added to W_out c before
+ *    the one rounding of y: y = bf16(W_out c + sum_j s_j).
  * Arithmetic: every sum in double; decode is scalar, element by element.
  */
 #include <math.h>
@@ -39,6 +45,8 @@ typedef struct {
   int32_t hidden, latent, inter, n_experts, top_k;
   int32_t act;   /* 0 = SiLU-GLU */
   int32_t actq;  /* 0 = bf16 activations, 1 = MXFP8 activations */
+  int32_t n_shared;      /* always-on shared experts (0 = none) */
+  int32_t shared_inter;  /* intermediate width of each shared expert */
 } k3o_dims;
 
 /* Expert tensors are passed as tables of n_experts pointers (NULL for an expert that is
@@ -54,6 +62,11 @@ typedef struct {
   const uint8_t* const* up_s;
   const uint8_t* const* down_q; /* per expert [L][I/2] */
   const uint8_t* const* down_s; /* per expert [L][I/32] */
+  /* shared experts, stacked: expert j owns rows [j*Is, (j+1)*Is) of gate/up and the same
+   * columns of down (Is = shared_inter, S = n_shared * Is) */
+  const uint16_t* w_sgate;    /* [S][H] bf16 */
+  const uint16_t* w_sup;      /* [S][H] bf16 */
+  const uint16_t* w_sdown;    /* [H][S] bf16 */
 } k3o_weights;
 
 /* ------------------------------------------------------------------ number formats */
@@ -348,6 +361,39 @@ int k3o_expert_row(const k3o_dims* d, const k3o_weights* w, int e, const uint16_
   return 0;
 }
 
+/* The shared experts on one token x (bf16, [H]): s = sum_j D_j bf16(silu(G_j x) * (U_j x))
+ * (double, [H]); `a_out` (optional, [S]) receives the stacked GLU outputs as bf16. Each expert
+ * is summed on its own, in expert order. Returns 0, or -1 for an unsupported act. */
+int k3o_shared_ffn(const k3o_dims* d, const k3o_weights* w, const uint16_t* x, double* s,
+                   uint16_t* a_out) {
+  const int H = d->hidden, Is = d->shared_inter;
+  if (d->act != 0) return -1;
+  double* a = (double*)malloc(sizeof(double) * (size_t)(Is > 0 ? Is : 1));
+  for (int h = 0; h < H; ++h) s[h] = 0.0;
+  for (int j = 0; j < d->n_shared; ++j) {
+    for (int i = 0; i < Is; ++i) {
+      const size_t r = (size_t)j * Is + i;
+      double g = 0.0, u = 0.0;
+      for (int k = 0; k < H; ++k) {
+        const double xk = k3o_bf16_to_double(x[k]);
+        g += k3o_bf16_to_double(w->w_sgate[r * H + k]) * xk;
+        u += k3o_bf16_to_double(w->w_sup[r * H + k]) * xk;
+      }
+      const uint16_t ab = k3o_bf16_from_double(k3o_silu(g) * u);
+      if (a_out) a_out[r] = ab;
+      a[i] = k3o_bf16_to_double(ab);
+    }
+    const size_t S = (size_t)d->n_shared * Is;
+    for (int h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int i = 0; i < Is; ++i) acc += k3o_bf16_to_double(w->w_sdown[(size_t)h * S + (size_t)j * Is + i]) * a[i];
+      s[h] += acc;
+    }
+  }
+  free(a);
+  return 0;
+}
+
 /* Routing-weighted combine of one token in latent space: c = bf16(sum_j w_j * o_j),
  * j ascending. */
 void k3o_combine_token(int L, int k, const double* const* o_rows, const double* w, uint16_t* c,
@@ -362,7 +408,8 @@ void k3o_combine_token(int L, int k, const double* const* o_rows, const double* 
 
 /* Whole layer for T tokens, tokens independent (OpenMP over tokens when nthreads > 1):
  *   logits -> top-k (on the double logits) -> weights -> z = bf16(W_in x)
- *   -> per slot: expert row -> combine c = bf16(sum w o) -> y = bf16(W_out c).
+ *   -> per slot: expert row -> combine c = bf16(sum w o) -> y = bf16(W_out c + s), with s the
+ *   shared experts' output on x (0 when n_shared = 0).
  * Outputs (any may be NULL except y): idx [T][k], wts [T][k], logits [T][E],
  * z [T][L], c [T][L], y [T][H]. Returns 0, or -1 for an unsupported mode or a selected
  * expert whose tensors were not supplied. */
@@ -371,6 +418,8 @@ int k3o_layer_forward(const k3o_dims* d, const k3o_weights* w, const uint16_t* x
                       uint16_t* z_out, uint16_t* c_out, int nthreads) {
   const int H = d->hidden, L = d->latent, E = d->n_experts, k = d->top_k;
   if (d->act != 0 || d->actq < 0 || d->actq > 1) return -1;
+  if (d->n_shared < 0 || (d->n_shared > 0 && (d->shared_inter <= 0 || !w->w_sgate || !w->w_sup || !w->w_sdown)))
+    return -1;
   int bad = 0;
 #ifdef _OPENMP
   if (nthreads < 1) nthreads = 1;
@@ -401,7 +450,16 @@ int k3o_layer_forward(const k3o_dims* d, const k3o_weights* w, const uint16_t* x
       orow[j] = o + (size_t)j * L;
     }
     k3o_combine_token(L, k, orow, wt, c, NULL);
-    k3o_dense_proj(w->w_out, c, 1, H, L, NULL, y + (size_t)t * H);
+    double* yo = (double*)malloc(sizeof(double) * (size_t)H);
+    k3o_dense_proj(w->w_out, c, 1, H, L, yo, NULL);
+    if (d->n_shared > 0) {
+      double* sh = (double*)malloc(sizeof(double) * (size_t)H);
+      k3o_shared_ffn(d, w, xt, sh, NULL);
+      for (int h = 0; h < H; ++h) yo[h] += sh[h];
+      free(sh);
+    }
+    for (int h = 0; h < H; ++h) y[(size_t)t * H + h] = k3o_bf16_from_double(yo[h]);
+    free(yo);
     if (idx_out) memcpy(idx_out + (size_t)t * k, id, sizeof(int32_t) * (size_t)k);
     if (w_out) memcpy(w_out + (size_t)t * k, wt, sizeof(double) * (size_t)k);
     if (logits_out) memcpy(logits_out + (size_t)t * E, lg, sizeof(double) * (size_t)E);

@@ -30,6 +30,7 @@ _DEV_LIB = os.path.join(_LIBDIR, "libk3synth_dev.so")
 S_X, S_W_ROUTER, S_W_IN, S_W_OUT = 1, 2, 3, 4
 S_GATE_Q, S_GATE_S, S_UP_Q, S_UP_S, S_DOWN_Q, S_DOWN_S = 5, 6, 7, 8, 9, 10
 S_BIAS, S_PERM, S_IDX = 11, 12, 13
+S_SGATE, S_SUP, S_SDOWN = 14, 15, 16
 
 SIGMA_X = 1.0       # tokens ~N(0, 1)
 SIGMA_W = 0.02      # router and latent projections ~N(0, 0.02)
@@ -284,6 +285,24 @@ def dev_fill_layer(d: Dims, seed: int, ptrs: dict, cuda_stream=0):
     dev_uniform_u8(seed, S_GATE_S, 0, E * d.gate_s_bytes, E8M0_LO, E8M0_HI, ptrs["gate_s"], cuda_stream)
     dev_uniform_u8(seed, S_UP_S, 0, E * d.gate_s_bytes, E8M0_LO, E8M0_HI, ptrs["up_s"], cuda_stream)
     dev_uniform_u8(seed, S_DOWN_S, 0, E * d.down_s_bytes, E8M0_LO, E8M0_HI, ptrs["down_s"], cuda_stream)
+
+
+def host_shared(d: Dims, n_shared: int, shared_inter: int, seed: int):
+    """Shared experts stacked along S = n_shared * shared_inter, bf16 bits: gate [S][H],
+    up [S][H], down [H][S]."""
+    S, H = n_shared * shared_inter, d.hidden
+    g = host_bf16_normal(seed, S_SGATE, 0, S * H, SIGMA_W).reshape(S, H)
+    u = host_bf16_normal(seed, S_SUP, 0, S * H, SIGMA_W).reshape(S, H)
+    dn = host_bf16_normal(seed, S_SDOWN, 0, H * S, SIGMA_W).reshape(H, S)
+    return g, u, dn
+
+
+def dev_fill_shared(d: Dims, n_shared: int, shared_inter: int, seed: int, ptrs: dict, cuda_stream=0):
+    """Device copy of host_shared: ``ptrs`` maps w_sgate, w_sup, w_sdown to device addresses."""
+    S, H = n_shared * shared_inter, d.hidden
+    dev_bf16_normal(seed, S_SGATE, 0, S * H, SIGMA_W, ptrs["w_sgate"], cuda_stream)
+    dev_bf16_normal(seed, S_SUP, 0, S * H, SIGMA_W, ptrs["w_sup"], cuda_stream)
+    dev_bf16_normal(seed, S_SDOWN, 0, H * S, SIGMA_W, ptrs["w_sdown"], cuda_stream)
 
 
 def dev_fill_x(w: Workload, ptr, first: int = 0, count: int | None = None, cuda_stream=0):

@@ -93,14 +93,15 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- algorithmic work
-def algorithmic(d, T, distinct_experts):
+def algorithmic(d, T, distinct_experts, shared_width=0):
     """Bytes and flops one layer step must move / compute (dense weights once, each selected
-    expert's bytes once, activations of the step)."""
-    dense_w = 2 * (d.n_experts * d.hidden + 2 * d.latent * d.hidden)
+    expert's bytes once, activations of the step; shared_width = n_shared x shared_inter, the
+    stacked bf16 shared experts, read once)."""
+    dense_w = 2 * (d.n_experts * d.hidden + 2 * d.latent * d.hidden) + 2 * 3 * shared_width * d.hidden
     act = 2 * T * d.hidden * 2 + T * d.n_experts * 4
     expert = distinct_experts * d.expert_bytes
     flops = 2 * T * (d.n_experts * d.hidden + 2 * d.latent * d.hidden) + \
-        2 * T * d.top_k * 3 * d.latent * d.inter
+        2 * T * d.top_k * 3 * d.latent * d.inter + 2 * T * 3 * shared_width * d.hidden
     return dense_w + expert + act, flops
 
 
@@ -123,14 +124,14 @@ def measured_traffic(workload, kernel):
         return None
 
 
-def kernel_cost(name, d, T, distinct, rows, actq):
+def kernel_cost(name, d, T, distinct, rows, actq, shared_width=0):
     """Algorithmic (bytes, flops, tensor dtype) of one launch of a profiled kernel: weights read
     once per launch, activations read and results written once."""
     L, I, H, E = d.latent, d.inter, d.hidden, d.n_experts
     glu_w = 2 * (d.gate_q_bytes + d.gate_s_bytes)
     down_w = d.down_q_bytes + d.down_s_bytes
     P = 1 if actq else 2  # e4m3 rows per activation row on the tensor-core expert path
-    gemv = T < 65
+    gemv = T < 33  # token-at-a-time dense projections below 33 tokens
     table = {
         # router logits fp32 + z bf16 (+ its f16 block-scaled copy on the GEMV path)
         "router_latent_in": (2 * (E + L) * H + 2 * T * H + 4 * T * E + 2 * T * L * (2 if gemv else 1),
@@ -147,6 +148,10 @@ def kernel_cost(name, d, T, distinct, rows, actq):
         "expert_ffn_mma": (distinct * (glu_w + down_w) + P * rows * (L + L // 32) +
                            2 * P * rows * (I + I // 32) + 4 * rows * L, 6 * rows * L * I, "fp8"),
         "combine": (rows * 4 * L + 2 * T * L, 0, None),
+        # gate + up (fp32 out), GLU, down (fp32 out); S = n_shared x shared_inter
+        "shared_experts": (2 * 3 * shared_width * H + 2 * T * H + 2 * 4 * T * shared_width +
+                           (2 + 8) * T * shared_width + 2 * T * shared_width + 4 * T * H,
+                           6 * T * shared_width * H, "bf16"),
     }
     return table.get(name, (None, 0, None))
 
@@ -301,7 +306,13 @@ def run_ours(args, w):
     nl = max(1, int(getattr(w, "layers", 1) or 1))
     sizes = {"gate_q": E * d.gate_q_bytes, "gate_s": E * d.gate_s_bytes, "up_q": E * d.gate_q_bytes,
              "up_s": E * d.gate_s_bytes, "down_q": E * d.down_q_bytes, "down_s": E * d.down_s_bytes}
-    dims = k3.Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, 0, args.actq)
+    ns, si = (2, args.shared_inter) if args.shared_inter else (0, 0)
+    S = ns * si
+    dims = k3.Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, 0, args.actq, ns, si)
+    shw = {n: torch.empty(S * d.hidden, dtype=torch.int16, device=dev) for n in ("w_sgate", "w_sup", "w_sdown")}
+    if S:
+        synth.dev_fill_shared(d, ns, si, 0, {n: t.data_ptr() for n, t in shw.items()}, sh)
+    shp = [shw[n].data_ptr() if S else None for n in ("w_sgate", "w_sup", "w_sdown")]
     if nl > 1:
         keep = []
         wts = []
@@ -319,7 +330,7 @@ def run_ours(args, w):
             wts.append(k3.Weights(ddl["w_router"].data_ptr(), None if bt is None else bt.data_ptr(),
                                   ddl["w_in"].data_ptr(), ddl["w_out"].data_ptr(),
                                   *[exl[n].data_ptr() for n in ("gate_q", "gate_s", "up_q", "up_s",
-                                                                "down_q", "down_s")]))
+                                                                "down_q", "down_s")], *shp))
     ex = {n: torch.empty(b if nl == 1 else 0, dtype=torch.uint8, device=dev) for n, b in sizes.items()}
     dense = []
     for c in range(DENSE_COPIES if nl == 1 else 0):
@@ -339,7 +350,7 @@ def run_ours(args, w):
         wts = [k3.Weights(dd["w_router"].data_ptr(), None if bias is None else bias.data_ptr(),
                           dd["w_in"].data_ptr(), dd["w_out"].data_ptr(),
                           *[ex[n].data_ptr() for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q",
-                                                       "down_s")]) for dd in dense]
+                                                       "down_s")], *shp) for dd in dense]
     nx = w.x_count
     x = torch.empty((nx, d.hidden), dtype=torch.int16, device=dev)
     synth.dev_fill_x(w, x.data_ptr(), cuda_stream=sh)
@@ -435,7 +446,7 @@ def run_ours(args, w):
     top = max(prof.items(), key=lambda kv: kv[1][0])
     name, (tot_ms, launches) = top
     per_launch_ms = tot_ms / max(1, launches)
-    step_bytes, step_flops = algorithmic(d, T, distinct)
+    step_bytes, step_flops = algorithmic(d, T, distinct, S)
     step_bytes, step_flops = step_bytes * nl, step_flops * nl  # every layer of the stack
     kernels_per_step = {"permute": 1 if T <= 256 else 3}
     launches_total = sum(n for _, n in prof.values()) + \
@@ -452,15 +463,17 @@ def run_ours(args, w):
                    "l2": ("expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 4 copies"
                           if nl == 1 else f"{nl} layers with independent weights ({nl * 15.7:.0f} GB of experts) run back to "
                           "back on the same tokens; fresh tokens per step"),
-                   "parallelism": f"replicas x{world}"},
-        "roofline": roofline(name, per_launch_ms, kernel_cost(name, d, T, distinct, T * d.top_k, args.actq), pk),
+                   "parallelism": f"replicas x{world}",
+                   "shared_experts": (f"{ns} x {si} bf16 (width a parameter; not in the headline configuration)"
+                                      if S else "none")},
+        "roofline": roofline(name, per_launch_ms, kernel_cost(name, d, T, distinct, T * d.top_k, args.actq, S), pk),
         # (traffic filled in below from the committed capture of this workload, bf16 mode only)
         "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
                           "achieved_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
                           "frac_hbm": step_bytes / (ms / args.steps / 1e3) / 1e9 / pk["hbm_gbs"]},
         "kernels": {n: dict(ms_per_launch=(t / c if c else None), launches=c,
                             share=t / sum(v[0] for v in prof.values()),
-                            frac=roofline(n, t / max(1, c), kernel_cost(n, d, T, distinct, T * d.top_k, args.actq),
+                            frac=roofline(n, t / max(1, c), kernel_cost(n, d, T, distinct, T * d.top_k, args.actq, S),
                                           pk)["frac"]) for n, (t, c) in prof.items() if c},
         "distinct_experts_last_step": distinct,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * d.hidden * 2,
@@ -510,6 +523,9 @@ def main():
     ap.add_argument("--workload", default="decode_b1")
     ap.add_argument("--actq", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shared-inter", type=int, default=0,
+                    help="also run two always-on bf16 shared experts of this width (their width is not "
+                         "on the pages; the headline metric is the routed layer without them)")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling aid: the same workload with fewer experts (fits an ncu capture); "
                          "not a bench configuration")

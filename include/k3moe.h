@@ -19,7 +19,10 @@
  *   o_tj   = D_e bf16(silu(G_e z_t) * (U_e z_t))  for e = S_t[j], MXFP4 G,U [I][L], D [L][I]
  *                                                                             (k3moe_expert_ffn_mxfp4)
  *   c_t    = bf16(sum_j w_j o_tj)              combine in latent space           (k3moe_combine)
- *   y_t    = bf16(W_out c_t)                   latent out, [H][L]                (k3moe_project)
+ *   s_t    = sum_j D_j bf16(silu(G_j x_t) * (U_j x_t))   the n_shared always-on shared experts,
+ *            bf16 G,U [Is][H], D [H][Is], on the residual ("kimi-k3-mlx", Architecture table:
+ *            shared experts beside the routed ones, outside the latent space); 0 if none
+ *   y_t    = bf16(W_out c_t + s_t)             latent out, [H][L], one rounding   (k3moe_project)
  * k3moe_layer_forward runs all of it. In MXFP8 mode (actq = 1) z and the GLU output go
  * through an MXFP8 round trip (E4M3 elements, one E8M0 scale per 32, OCP MX v1.0) before
  * they enter an expert matrix.
@@ -77,6 +80,9 @@ typedef struct k3moe_dims {
   int32_t top_k;     /* k (K3: 16) */
   int32_t act;       /* 0 = SiLU-GLU silu(gate) * up, fp32; 1 = SiTU-GLU -> K3MOE_E_MODE */
   int32_t actq;      /* 0 = bf16 activations; 1 = MXFP8 activations (E4M3 + E8M0 per 32) */
+  int32_t n_shared;     /* always-on shared experts per token, 0..8 (K3: 2; 0 = none) */
+  int32_t shared_inter; /* intermediate width of each shared expert (not on the pages; a
+                           parameter); n_shared * shared_inter must be a multiple of 64 */
 } k3moe_dims;
 
 typedef struct k3moe_weights {
@@ -90,6 +96,12 @@ typedef struct k3moe_weights {
   const uint8_t* up_s;        /* [E][I][L/32] */
   const uint8_t* down_q;      /* [E][L][I/2] */
   const uint8_t* down_s;      /* [E][L][I/32] */
+  /* Shared experts (used when n_shared > 0, else ignored), stacked: shared expert j owns rows
+   * [j*Is, (j+1)*Is) of gate and up and the same columns of down (Is = shared_inter,
+   * S = n_shared * Is). */
+  const uint16_t* w_shared_gate; /* [S][H] bf16 */
+  const uint16_t* w_shared_up;   /* [S][H] bf16 */
+  const uint16_t* w_shared_down; /* [H][S] bf16 */
 } k3moe_weights;
 
 /* Bytes of device workspace that every call below needs for up to `max_tokens` tokens.

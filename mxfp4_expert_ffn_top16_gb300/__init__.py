@@ -70,13 +70,14 @@ def build(force: bool = False, jobs: int = 8) -> str:
 
 class Dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
-                ("hidden", "latent", "inter", "n_experts", "top_k", "act", "actq")]
+                ("hidden", "latent", "inter", "n_experts", "top_k", "act", "actq", "n_shared",
+                 "shared_inter")]
 
 
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_router", "router_bias", "w_in", "w_out", "gate_q", "gate_s", "up_q", "up_s",
-                 "down_q", "down_s")]
+                 "down_q", "down_s", "w_shared_gate", "w_shared_up", "w_shared_down")]
 
 
 _lib = None

@@ -77,6 +77,13 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.c = take(Tt * Lw * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
   L.route_done = take(4);
+  {  // shared experts: gate and up (fp32), GLU output (bf16) [T][S], their output (fp32) [T][H]
+    const size_t S = (size_t)d.n_shared * (size_t)d.shared_inter;
+    L.sg = take(Tt * S * 4);
+    L.su = take(Tt * S * 4);
+    L.sa = take(Tt * S * 2);
+    L.ss = take(d.n_shared > 0 ? Tt * (size_t)d.hidden * 4 : 0);
+  }
   if (umma_expert_ok(d)) {
     const size_t P = d.actq ? 1 : 2;
     L.bq = take(P * rows * Lw);
@@ -110,6 +117,10 @@ k3moe_status check_dims(const k3moe_dims* d) {
   if (d->top_k < 1 || d->top_k > 32 || d->top_k > d->n_experts) return K3MOE_E_SHAPE;
   if (d->act != 0) return K3MOE_E_MODE;
   if (d->actq != 0 && d->actq != 1) return K3MOE_E_MODE;
+  if (d->n_shared < 0 || d->n_shared > 8) return K3MOE_E_SHAPE;
+  if (d->n_shared > 0 && (d->shared_inter <= 0 || ((int64_t)d->n_shared * d->shared_inter) % 64 ||
+                          (int64_t)d->n_shared * d->shared_inter > (1 << 20)))
+    return K3MOE_E_SHAPE;
   return K3MOE_OK;
 }
 
@@ -138,15 +149,25 @@ k3moe_status check_weights(const k3moe_weights* w, bool dense, bool experts) {
   return K3MOE_OK;
 }
 
+k3moe_status check_shared(const k3moe_dims& d, const k3moe_weights* w) {
+  if (d.n_shared == 0) return K3MOE_OK;
+  const void* p[3] = {w->w_shared_gate, w->w_shared_up, w->w_shared_down};
+  for (const void* q : p) {
+    if (!q) return K3MOE_E_NULL;
+    if (misaligned(q)) return K3MOE_E_ALIGN;
+  }
+  return K3MOE_OK;
+}
+
 // ---------------------------------------------------------------- diagnostic profiling
 enum ProfId {
   P_ROUTER_LATENT = 0, P_TOPK, P_PERMUTE, P_GLU, P_DOWN, P_COMBINE, P_LATENT_OUT, P_QUANT,
-  P_GLU_MMA, P_DOWN_MMA, P_FFN_MMA, P_COUNT
+  P_GLU_MMA, P_DOWN_MMA, P_FFN_MMA, P_SHARED, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"router_latent_in", "topk", "permute",
                                          "expert_glu_gemv", "expert_down_gemv", "combine",
                                          "latent_out", "expert_act_quant", "expert_glu_mma",
-                                         "expert_down_mma", "expert_ffn_mma"};
+                                         "expert_down_mma", "expert_ffn_mma", "shared_experts"};
 struct Profiler {
   bool on = false;
   static constexpr int kMax = 65536;
@@ -265,7 +286,8 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
   // chunk counters)
   K3_TRY(run_expert_gemms(d, w, at<uint16_t>(ws, L.z), T, at<int32_t>(ws, L.offsets),
                           at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s,
-                          T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && umma_expert_ok(d)));
+                          T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens &&
+                              umma_expert_ok(d)));
   {
     ProfScope p(P_COMBINE, s);
     K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,
@@ -401,6 +423,7 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
   K3_TRY(check_dims(dims));
   const k3moe_dims& d = *dims;
   K3_TRY(check_weights(weights, true, true));
+  K3_TRY(check_shared(d, weights));
   if (T < 0) return K3MOE_E_SHAPE;
   if (!x || !y) return K3MOE_E_NULL;
   if (misaligned(x) || misaligned(y) || misaligned(topk_idx_out) || misaligned(topk_w_out))
@@ -419,7 +442,7 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
     ProfScope p(P_ROUTER_LATENT, s);
     const bool f16_copy = !umma_expert_ok(d);
     // decode on the tensor-core experts: z also as P E4M3 rows per token for the expert kernel
-    const bool rows = !f16_copy && T <= kSmallRouteTokens && T < kUmmaExpertMinTokens;
+    const bool rows = !f16_copy && T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens;
     K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr, w.router_bias, w.w_in,
                          d.latent, at<uint16_t>(ws, L.z), f16_copy ? at<__half>(ws, L.zh) : nullptr,
                          f16_copy ? at<int8_t>(ws, L.zs) : nullptr, d.actq, x, T, d.hidden, err, s,
@@ -427,10 +450,22 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
                          d.actq ? 1 : 2));
   }
   K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s));
-  {
+  // shared experts on the residual: g, u = G x, U x (fp32); a = bf16(silu(g) u); s = D a (fp32)
+  const int S = d.n_shared * d.shared_inter;
+  if (S > 0) {
+    ProfScope p(P_SHARED, s);
+    K3_CUDA(launch_dense(w.w_shared_gate, S, at<float>(ws, L.sg), nullptr, nullptr, w.w_shared_up, S, nullptr,
+                         nullptr, nullptr, 0, x, T, d.hidden, err, s, nullptr, nullptr, 0, nullptr,
+                         at<float>(ws, L.su)));
+    K3_CUDA(launch_glu(at<float>(ws, L.sg), at<float>(ws, L.su), (long long)T * S, at<uint16_t>(ws, L.sa), s));
+    K3_CUDA(launch_dense(w.w_shared_down, d.hidden, at<float>(ws, L.ss), nullptr, nullptr, nullptr, 0, nullptr,
+                         nullptr, nullptr, 0, at<uint16_t>(ws, L.sa), T, S, err, s));
+  }
+  {  // y = bf16(W_out c + s)
     ProfScope p(P_LATENT_OUT, s);
     K3_CUDA(launch_dense(w.w_out, d.hidden, nullptr, y, nullptr, nullptr, 0, nullptr, nullptr,
-                              nullptr, 0, at<uint16_t>(ws, L.c), T, d.latent, err, s));
+                         nullptr, 0, at<uint16_t>(ws, L.c), T, d.latent, err, s, nullptr, nullptr, 0,
+                         S > 0 ? at<float>(ws, L.ss) : nullptr));
   }
   return K3MOE_OK;
 }

@@ -42,6 +42,7 @@ struct DenseProblem {
   uint8_t* out_q;   // optional: the bf16 outputs as qP E4M3 rows per token [T][qP][N] ...
   uint8_t* out_qs;  // ... with e8m0 block exponents [T][qP][exp_pitch(N)]
   int qP;           // 1: MXFP8; 2: bf16 split exactly into hi + lo
+  const float* add; // optional [T][N] fp32 added to the sums before the outputs are formed
 };
 
 struct DenseArgs {
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
           v = tk;
         }
         const bool valid = row < P.N;
+        if (P.add && valid) v += P.add[(size_t)tok * P.N + row];
         if (P.out_f32 && valid) P.out_f32[(size_t)tok * P.N + row] = v + (P.bias ? P.bias[row] : 0.f);
         if (P.out_bf16) {
           const uint16_t vb = f32_to_bf16(v);
@@ -272,11 +274,12 @@ cudaError_t launch_t(DenseArgs& a, const uint16_t* const W[2], const int N[2], c
 cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
-                              int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q, uint8_t* out1_qs, int q1P) {
+                              int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q, uint8_t* out1_qs, int q1P,
+                              const float* add0, float* out1_f32) {
   if (T <= 0) return cudaSuccess;
   DenseArgs a{};
-  a.p[0] = DenseProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0, nullptr, nullptr, 0};
-  a.p[1] = DenseProblem{N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1, out1_q, out1_qs, q1P};
+  a.p[0] = DenseProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0, nullptr, nullptr, 0, add0};
+  a.p[1] = DenseProblem{N1, out1_f32, nullptr, out1_bf16, out1_h, out1_s, actq1, out1_q, out1_qs, q1P, nullptr};
   if (out1_q && (!out1_bf16 || N1 % 32 != 0 || (q1P != 1 && q1P != 2))) return cudaErrorInvalidValue;
   a.units0 = W0 ? (N0 + kUnitRows - 1) / kUnitRows : 0;
   a.units = a.units0 + (W1 ? (N1 + kUnitRows - 1) / kUnitRows : 0);

@@ -62,6 +62,23 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
   *reinterpret_cast<uint2*>(c + (size_t)t * L + n) = packed;
 }
 
+// Shared experts' GLU: a = bf16(silu(g) * up), silu(g) = g / (1 + e^-g) in the same fast forms
+// as the routed experts' epilogue (~1e-6 relative, far below the bf16 rounding). Four
+// elements per thread (16-byte loads); n is a multiple of 4.
+__global__ void glu_kernel(const float4* __restrict__ g, const float4* __restrict__ u, long long n4,
+                           uint2* __restrict__ a) {
+  pdl_wait();
+  pdl_trigger();
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+    const float4 gv = g[i], uv = u[i];
+    const float gg[4] = {gv.x, gv.y, gv.z, gv.w}, uu[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t b[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) b[q] = f32_to_bf16(__fdividef(gg[q], 1.0f + __expf(-gg[q])) * uu[q]);
+    a[i] = make_uint2(b[0] | (b[1] << 16), b[2] | (b[3] << 16));
+  }
+}
+
 // One warp per (token, block of 32 values): optional MXFP8 round trip, then an f16 copy
 // scaled by 2^-e with e chosen from the block maximum, and the exponent e.
 __global__ void act_prep_kernel(const uint16_t* __restrict__ z, int T, int L, int actq, __half* zh,
@@ -91,6 +108,16 @@ cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const f
   if (k <= 16)
     return launch_pdl(combine_kernel<16>, grid, dim3(kCombineThreads), 0, s, o_rows, slot_row, w, T, k, L, c);
   return launch_pdl(combine_kernel<kMaxTopK>, grid, dim3(kCombineThreads), 0, s, o_rows, slot_row, w, T, k, L, c);
+}
+
+cudaError_t launch_glu(const float* g, const float* u, long long n, uint16_t* a, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (n % 4) return cudaErrorInvalidValue;
+  const long long n4 = n / 4;
+  long long blocks = (n4 + 255) / 256;
+  if (blocks > 16LL * num_sms()) blocks = 16LL * num_sms();
+  return launch_pdl(glu_kernel, dim3((unsigned)blocks), dim3(256), 0, s, reinterpret_cast<const float4*>(g),
+                    reinterpret_cast<const float4*>(u), n4, reinterpret_cast<uint2*>(a));
 }
 
 cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* zh, int8_t* zs,

@@ -50,6 +50,7 @@ struct UProblem {
   __half* out_h;
   int8_t* out_s;
   int actq;
+  const float* add;  // optional [T][N] fp32 added to the sums before the outputs are formed
 };
 
 struct UDenseArgs {
@@ -228,6 +229,20 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const
           if (j < ntok) *dst = sum[j] + bias;
           dst += P.N;
         }
+      } else if (valid && P.out_bf16 && P.add) {  // y = bf16(W c + add): one rounding of the total
+        uint16_t* dst = P.out_bf16 + (size_t)tok0 * P.N + row;
+        const float* ad = P.add + (size_t)tok0 * P.N + row;
+#pragma unroll
+        for (int j0 = 0; j0 < kEpiCols; j0 += 16) {  // 16 loads in flight before their stores
+          float av[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) av[i] = j0 + i < ntok ? __ldg(ad + (size_t)(j0 + i) * P.N) : 0.f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (j0 + i < ntok) *dst = f32_to_bf16(sum[j0 + i] + av[i]);
+            dst += P.N;
+          }
+        }
       } else if (valid && P.out_bf16) {
         uint16_t* dst = P.out_bf16 + (size_t)tok0 * P.N + row;
 #pragma unroll
@@ -268,11 +283,13 @@ cudaError_t launch_bn(UDenseArgs& a, const uint16_t* const W[2], const int N[2],
 cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
-                              uint32_t* err, cudaStream_t s) {
+                              uint32_t* err, cudaStream_t s, const float* add0, float* out1_f32) {
   if (T <= 0) return cudaSuccess;
+  // one output kind per problem: fp32 (+ bias), bf16 (+ add), or bf16 + the f16 block-scaled copy
+  if ((out0_f32 && (out0_bf16 || add0)) || (out1_f32 && (out1_bf16 || out1_h))) return cudaErrorInvalidValue;
   UDenseArgs a{};
-  a.p[0] = UProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0};
-  a.p[1] = UProblem{N1, nullptr, nullptr, out1_bf16, out1_h, out1_s, actq1};
+  a.p[0] = UProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0, add0};
+  a.p[1] = UProblem{N1, out1_f32, nullptr, out1_bf16, out1_h, out1_s, actq1, nullptr};
   a.mt0 = W0 ? (N0 + BM - 1) / BM : 0;
   a.mtiles = a.mt0 + (W1 ? (N1 + BM - 1) / BM : 0);
   a.T = T;

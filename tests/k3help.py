@@ -42,16 +42,20 @@ def bf16_np(t: torch.Tensor) -> np.ndarray:
     return oracle.bf16_to_f64(t.cpu().numpy().view(np.uint16))
 
 
-def dims(d: synth.Dims, actq=0, act=0) -> k3.Dims:
-    return k3.Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, act, actq)
+def dims(d: synth.Dims, actq=0, act=0, shared=None) -> k3.Dims:
+    ns, si = shared or (0, 0)
+    return k3.Dims(d.hidden, d.latent, d.inter, d.n_experts, d.top_k, act, actq, ns, si)
 
 
 class DeviceLayer:
     """A whole layer resident on the GPU. Small layers are generated on the host and copied;
     K3-sized ones are generated on the device (byte-identical generator)."""
 
-    def __init__(self, d: synth.Dims, seed=0, bias=None, actq=0, host_fill=None, experts=None):
-        self.d, self.seed, self.actq = d, seed, actq
+    def __init__(self, d: synth.Dims, seed=0, bias=None, actq=0, host_fill=None, experts=None, shared=None,
+                 zero_out=False):
+        """shared: (n_shared, shared_inter) or None; zero_out: W_out = 0, so that y is the shared
+        experts' output alone."""
+        self.d, self.seed, self.actq, self.shared, self.zero_out = d, seed, actq, shared, zero_out
         E = d.n_experts
         if host_fill is None:
             host_fill = E * d.expert_bytes < 64 << 20
@@ -77,18 +81,36 @@ class DeviceLayer:
             for n, b in sizes.items():
                 self.t[n] = torch.empty(b, dtype=torch.uint8, device=DEV)
             synth.dev_fill_layer(d, seed, {n: v.data_ptr() for n, v in self.t.items()}, stream())
+        if zero_out:
+            self.t["w_out"].zero_()
+        self.shared_host = None
+        sp = [None, None, None]
+        if shared is not None:
+            ns, si = shared
+            S = ns * si
+            if host_fill:
+                self.shared_host = synth.host_shared(d, ns, si, seed)
+                for i, n in enumerate(("w_sgate", "w_sup", "w_sdown")):
+                    self.t[n] = up(self.shared_host[i])
+            else:
+                for n in ("w_sgate", "w_sup", "w_sdown"):
+                    self.t[n] = torch.empty(S * d.hidden * 2, dtype=torch.uint8, device=DEV)
+                synth.dev_fill_shared(d, ns, si, seed, {n: self.t[n].data_ptr() for n in ("w_sgate", "w_sup", "w_sdown")},
+                                      stream())
+            sp = [self.t[n].data_ptr() for n in ("w_sgate", "w_sup", "w_sdown")]
         self.bias_host = None if bias is None else np.ascontiguousarray(bias, np.float32)
         self.t["bias"] = None if bias is None else up(self.bias_host)
-        self.dims = dims(d, actq)
+        self.dims = dims(d, actq, shared=shared)
         self.weights = k3.Weights(self.t["w_router"].data_ptr(),
                                   None if bias is None else self.t["bias"].data_ptr(),
                                   self.t["w_in"].data_ptr(), self.t["w_out"].data_ptr(),
-                                  *[self.t[n].data_ptr() for n in NAMES])
+                                  *[self.t[n].data_ptr() for n in NAMES], *sp)
 
     def dense(self):
         if self.dense_host is None:
             self.dense_host = synth.host_dense(self.d, self.seed)
-        return self.dense_host
+        wr, wi, wo = self.dense_host
+        return (wr, wi, np.zeros_like(wo)) if self.zero_out else (wr, wi, wo)
 
     def expert_host(self, e):
         if e not in self._experts_host:
@@ -99,8 +121,13 @@ class DeviceLayer:
         ids = range(self.d.n_experts) if experts is None else experts
         ex = {int(e): self.expert_host(int(e)) for e in ids}
         wr, wi, wo = self.dense()
+        sh = None
+        if self.shared is not None:
+            if self.shared_host is None:
+                self.shared_host = synth.host_shared(self.d, *self.shared, self.seed)
+            sh = (*self.shared_host, self.shared[0])
         return oracle.Layer(self.d, wr, wi, wo, ex, bias=self.bias_host,
-                            actq=self.actq if actq is None else actq)
+                            actq=self.actq if actq is None else actq, shared=sh)
 
 
 def workspace(dm: k3.Dims, T: int) -> tuple[torch.Tensor, int]:

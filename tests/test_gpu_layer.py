@@ -264,6 +264,40 @@ def test_layer_other_dims_every_token(dname, T):
     np.testing.assert_array_equal(idx2, idx)
 
 
+# Two always-on shared experts beside the routed ones (width 64 on the tiny shape, 3072 on K3).
+# With W_out = 0 the output is the shared experts' alone, y = bf16(s); otherwise
+# y = bf16(W_out c + s). T = 3 runs the token-at-a-time projections, T = 150 the tensor-core ones.
+@pytest.mark.parametrize("T", [3, 150])
+@pytest.mark.parametrize("zero_out", [True, False])
+def test_layer_shared_experts_every_token(T, zero_out):
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=3, shared=(2, 64), zero_out=zero_out)
+    x = synth.host_bf16_normal(9, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+    y, idx, w = _forward(lay, x)
+    _compare_layer(lay, x, y, idx, np.arange(T))
+    if zero_out:
+        assert np.count_nonzero(y) > 0.9 * y.size
+
+
+@pytest.mark.parametrize("T,sample", [(1, [0]), (64, [0, 31, 63]), (300, [0, 150, 299])])
+def test_layer_k3_shared_experts_alone(T, sample):
+    """K3 shapes, two shared experts of width 3072, W_out = 0: y = bf16(s) on sampled tokens."""
+    d = synth.K3
+    lay = DeviceLayer(d, seed=1, shared=(2, 3072), zero_out=True)
+    try:
+        x = synth.host_bf16_normal(12, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+        y, idx, w = _forward(lay, x)
+        ol = lay.oracle(experts=[])
+        for t in sample:
+            s, _ = ol.shared_ffn(x[t])
+            want = oracle.bf16_to_f64(oracle.bf16_from_f64(s))
+            err = rel_l2_rows(y[t], want)
+            assert err <= REL_L2, (t, err)
+    finally:
+        del lay
+        torch.cuda.empty_cache()
+
+
 def test_layer_k3_decode_b1(k3_layer):
     w = synth.WORKLOADS["decode_b1"]
     n = 6

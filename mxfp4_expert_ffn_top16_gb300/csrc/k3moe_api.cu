@@ -77,12 +77,11 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.c = take(Tt * Lw * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
   L.route_done = take(4);
-  {  // shared experts: gate and up (fp32), GLU output (bf16) [T][S], their output (fp32) [T][H]
+  {  // shared experts: gate and up (fp32), GLU output (bf16) [T][S]
     const size_t S = (size_t)d.n_shared * (size_t)d.shared_inter;
     L.sg = take(Tt * S * 4);
     L.su = take(Tt * S * 4);
     L.sa = take(Tt * S * 2);
-    L.ss = take(d.n_shared > 0 ? Tt * (size_t)d.hidden * 4 : 0);
   }
   if (umma_expert_ok(d)) {
     const size_t P = d.actq ? 1 : 2;
@@ -450,22 +449,19 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
                          d.actq ? 1 : 2));
   }
   K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s));
-  // shared experts on the residual: g, u = G x, U x (fp32); a = bf16(silu(g) u); s = D a (fp32)
+  // shared experts on the residual: g, u = G x, U x (fp32); a = bf16(silu(g) u)
   const int S = d.n_shared * d.shared_inter;
   if (S > 0) {
     ProfScope p(P_SHARED, s);
     K3_CUDA(launch_dense(w.w_shared_gate, S, at<float>(ws, L.sg), nullptr, nullptr, w.w_shared_up, S, nullptr,
-                         nullptr, nullptr, 0, x, T, d.hidden, err, s, nullptr, nullptr, 0, nullptr,
-                         at<float>(ws, L.su)));
+                         nullptr, nullptr, 0, x, T, d.hidden, err, s, nullptr, nullptr, 0, at<float>(ws, L.su)));
     K3_CUDA(launch_glu(at<float>(ws, L.sg), at<float>(ws, L.su), (long long)T * S, at<uint16_t>(ws, L.sa), s));
-    K3_CUDA(launch_dense(w.w_shared_down, d.hidden, at<float>(ws, L.ss), nullptr, nullptr, nullptr, 0, nullptr,
-                         nullptr, nullptr, 0, at<uint16_t>(ws, L.sa), T, S, err, s));
   }
-  {  // y = bf16(W_out c + s)
+  {  // y = bf16(W_out c + D a): the shared experts' down projection is a second K segment
     ProfScope p(P_LATENT_OUT, s);
     K3_CUDA(launch_dense(w.w_out, d.hidden, nullptr, y, nullptr, nullptr, 0, nullptr, nullptr,
-                         nullptr, 0, at<uint16_t>(ws, L.c), T, d.latent, err, s, nullptr, nullptr, 0,
-                         S > 0 ? at<float>(ws, L.ss) : nullptr));
+                         nullptr, 0, at<uint16_t>(ws, L.c), T, d.latent, err, s, nullptr, nullptr, 0, nullptr,
+                         S > 0 ? w.w_shared_down : nullptr, S > 0 ? at<uint16_t>(ws, L.sa) : nullptr, S));
   }
   return K3MOE_OK;
 }

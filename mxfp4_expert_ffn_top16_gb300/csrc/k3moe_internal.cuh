@@ -50,7 +50,7 @@ struct WsLayout {
   size_t c;             // bf16 combined latent
   size_t perm;          // int32 per-block histograms of the multi-block permutation
   size_t route_done;    // int: top-k blocks finished (a few tokens); back to zero after each launch
-  size_t sg, su, sa, ss; // shared experts: gate, up (fp32) and GLU output (bf16) [T][S]; output fp32 [T][H]
+  size_t sg, su, sa;    // shared experts: gate, up (fp32) and GLU output (bf16) [T][S]
   // block-scaled tensor-core expert path (only when umma_expert_ok): per sorted row, P e4m3
   // rows of z and of the GLU output with e8m0 scales per 32 (row pitch exp_pitch bytes)
   size_t bq, bs, aq, aqs;
@@ -97,31 +97,31 @@ cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint1
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
                               int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q = nullptr,
-                              uint8_t* out1_qs = nullptr, int q1P = 0, const float* add0 = nullptr,
-                              float* out1_f32 = nullptr);
+                              uint8_t* out1_qs = nullptr, int q1P = 0, float* out1_f32 = nullptr,
+                              const uint16_t* W0b = nullptr, const uint16_t* xb = nullptr, int Kb = 0);
 // Same contract as launch_dense_gemv (less the E4M3 rows), on tcgen05 tiles (for many tokens).
 cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
-                              uint32_t* err, cudaStream_t s, const float* add0 = nullptr,
-                              float* out1_f32 = nullptr);
+                              uint32_t* err, cudaStream_t s, float* out1_f32 = nullptr,
+                              const uint16_t* W0b = nullptr, const uint16_t* xb = nullptr, int Kb = 0);
 // Token count from which the dense projections use the tcgen05 tiles.
 constexpr int kUmmaDenseMinTokens = 33;
 // out1_q / out1_qs / q1P (token-at-a-time path, T < kUmmaDenseMinTokens, only): problem 1's bf16
 // outputs also as q1P E4M3 rows per token with e8m0 scales per 32, for the decode expert kernel.
-// add0: fp32 [T][N0] added to problem 0's sums before its outputs are formed (one rounding of
-// the total). out1_f32: problem 1's sums in fp32.
+// out1_f32: problem 1's sums in fp32. W0b / xb / Kb: a second K segment of problem 0 (with no
+// problem 1): out0 = W0 x + W0b xb, W0b [N0][Kb], xb [T][Kb], one rounding of the total.
 inline cudaError_t launch_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                                 const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                                 __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
                                 uint32_t* err, cudaStream_t s, uint8_t* out1_q = nullptr,
-                                uint8_t* out1_qs = nullptr, int q1P = 0, const float* add0 = nullptr,
-                                float* out1_f32 = nullptr) {
+                                uint8_t* out1_qs = nullptr, int q1P = 0, float* out1_f32 = nullptr,
+                                const uint16_t* W0b = nullptr, const uint16_t* xb = nullptr, int Kb = 0) {
   if (T >= kUmmaDenseMinTokens)
     return launch_umma_dense(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
-                             T, K, err, s, add0, out1_f32);
+                             T, K, err, s, out1_f32, W0b, xb, Kb);
   return launch_dense_gemv(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
-                           T, K, err, s, out1_q, out1_qs, q1P, add0, out1_f32);
+                           T, K, err, s, out1_q, out1_qs, q1P, out1_f32, W0b, xb, Kb);
 }
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s);

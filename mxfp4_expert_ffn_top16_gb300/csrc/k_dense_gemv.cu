@@ -42,7 +42,6 @@ struct DenseProblem {
   uint8_t* out_q;   // optional: the bf16 outputs as qP E4M3 rows per token [T][qP][N] ...
   uint8_t* out_qs;  // ... with e8m0 block exponents [T][qP][exp_pitch(N)]
   int qP;           // 1: MXFP8; 2: bf16 split exactly into hi + lo
-  const float* add; // optional [T][N] fp32 added to the sums before the outputs are formed
 };
 
 struct DenseArgs {
@@ -51,6 +50,10 @@ struct DenseArgs {
   DenseProblem p[2];
   int units0, units;   // units of problem 0, total units
   int T, K, NB, NS;    // tokens, reduction length, tiles per stage along K, stages
+  // optional second K segment of problem 0 (a single problem): out = W x + W2 x2; its nkc1
+  // K steps follow the first K / (64 NB)
+  CUtensorMap tw2, tx2;
+  int nkc1;
   uint32_t* err;
 };
 
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
   pdl_trigger();
 
   const int KC = 64 * NB;
-  const int nkc = K / KC;
+  const int nkc0 = K / KC, nkc = nkc0 + args.nkc1;
   const int nchunks = (T + ntok - 1) / ntok;
 
   if (warp == 0) {
@@ -102,8 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
           if (lane == 0) {  // one copy for the NB weight tiles, one for the NB token tiles
             mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
             uint8_t* dst = stages + s * stage_bytes;
-            tma_load_3d(dst, &args.tw[pi], 0, row0, kc * NB, &full[s]);
-            tma_load_3d(dst + NB * wbox, &args.tx, 0, ch * ntok, kc * NB, &full[s]);
+            const bool seg2 = kc >= nkc0;  // second K segment (problem 0 only)
+            tma_load_3d(dst, seg2 ? &args.tw2 : &args.tw[pi], 0, row0, (seg2 ? kc - nkc0 : kc) * NB, &full[s]);
+            tma_load_3d(dst + NB * wbox, seg2 ? &args.tx2 : &args.tx, 0, ch * ntok, (seg2 ? kc - nkc0 : kc) * NB,
+                        &full[s]);
           }
           __syncwarp();
           if (++s == NS) { s = 0; ph ^= 1; }
@@ -209,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
           v = tk;
         }
         const bool valid = row < P.N;
-        if (P.add && valid) v += P.add[(size_t)tok * P.N + row];
         if (P.out_f32 && valid) P.out_f32[(size_t)tok * P.N + row] = v + (P.bias ? P.bias[row] : 0.f);
         if (P.out_bf16) {
           const uint16_t vb = f32_to_bf16(v);
@@ -245,13 +249,19 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
 
 template <int NTT>
 cudaError_t launch_t(DenseArgs& a, const uint16_t* const W[2], const int N[2], const uint16_t* x,
-                     cudaStream_t s) {
+                     const uint16_t* W2, const uint16_t* x2, int K2, cudaStream_t s) {
   constexpr int ntok = 8 * NTT;
   const int target_nb = NTT <= 2 ? 8 : (NTT == 4 ? 4 : 2);
-  const int kt = a.K / 64;
+  const int kt = a.K / 64, kt2 = K2 / 64;
   a.NB = 1;
   for (int nb = target_nb; nb >= 1; nb >>= 1)
-    if (kt % nb == 0) { a.NB = nb; break; }
+    if (kt % nb == 0 && kt2 % nb == 0) { a.NB = nb; break; }
+  a.nkc1 = kt2 / a.NB;
+  if (kt2 > 0 && (!make_tmap_3d_chunks(&a.tw2, W2, 2, 64, (uint64_t)N[0], (uint64_t)K2 * 2, (uint64_t)kt2,
+                                       kUnitRows, (uint32_t)a.NB, true) ||
+                  !make_tmap_3d_chunks(&a.tx2, x2, 2, 64, (uint64_t)a.T, (uint64_t)K2 * 2, (uint64_t)kt2, ntok,
+                                       (uint32_t)a.NB, true)))
+    return cudaErrorInvalidValue;
   const int stage_bytes = a.NB * (kUnitRows * 128 + ntok * 128);
   a.NS = NTT <= 2 ? 3 : 4;
   for (int i = 0; i < 2; ++i)
@@ -275,11 +285,12 @@ cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint1
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
                               int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q, uint8_t* out1_qs, int q1P,
-                              const float* add0, float* out1_f32) {
+                              float* out1_f32, const uint16_t* W0b, const uint16_t* xb, int Kb) {
   if (T <= 0) return cudaSuccess;
+  if (W0b && (W1 || !xb || Kb <= 0 || Kb % 64)) return cudaErrorInvalidValue;
   DenseArgs a{};
-  a.p[0] = DenseProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0, nullptr, nullptr, 0, add0};
-  a.p[1] = DenseProblem{N1, out1_f32, nullptr, out1_bf16, out1_h, out1_s, actq1, out1_q, out1_qs, q1P, nullptr};
+  a.p[0] = DenseProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0, nullptr, nullptr, 0};
+  a.p[1] = DenseProblem{N1, out1_f32, nullptr, out1_bf16, out1_h, out1_s, actq1, out1_q, out1_qs, q1P};
   if (out1_q && (!out1_bf16 || N1 % 32 != 0 || (q1P != 1 && q1P != 2))) return cudaErrorInvalidValue;
   a.units0 = W0 ? (N0 + kUnitRows - 1) / kUnitRows : 0;
   a.units = a.units0 + (W1 ? (N1 + kUnitRows - 1) / kUnitRows : 0);
@@ -289,9 +300,10 @@ cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint1
   if (a.units == 0) return cudaSuccess;
   const uint16_t* W[2] = {W0, W1};
   const int N[2] = {N0, N1};
-  if (T <= 8) return launch_t<1>(a, W, N, x, s);
-  if (T <= 16) return launch_t<2>(a, W, N, x, s);
-  return launch_t<4>(a, W, N, x, s);  // chunks of 32 tokens
+  const int K2 = W0b ? Kb : 0;
+  if (T <= 8) return launch_t<1>(a, W, N, x, W0b, xb, K2, s);
+  if (T <= 16) return launch_t<2>(a, W, N, x, W0b, xb, K2, s);
+  return launch_t<4>(a, W, N, x, W0b, xb, K2, s);  // chunks of 32 tokens
 }
 
 }  // namespace k3moe

@@ -50,7 +50,6 @@ struct UProblem {
   __half* out_h;
   int8_t* out_s;
   int actq;
-  const float* add;  // optional [T][N] fp32 added to the sums before the outputs are formed
 };
 
 struct UDenseArgs {
@@ -59,6 +58,10 @@ struct UDenseArgs {
   UProblem p[2];
   int mt0, mtiles, ntiles;
   int T, K;
+  // optional second K segment of problem 0 (a single problem): out = W x + W2 x2, W2 {K2, N0},
+  // x2 {K2, T}; its K steps follow the first nk0
+  CUtensorMap tw2, tx2;
+  int nk0, K2;
   uint32_t* err;
 };
 
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
   const int items = a.mtiles * a.ntiles;
-  const int nk = a.K / BK;
+  const int nk = a.K / BK + a.K2 / BK;
   // item -> (weight tile, token tile), in groups of kGroupM weight tiles: the CTAs in flight
   // share a few weight tiles and a few token tiles, so both are reused from L2 even when the
   // tokens do not fit in it
@@ -130,8 +133,13 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const
         for (int kb = 0; kb < nk; ++kb) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, a.err)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], kATile + kBTile);
-          tma_load_2d(sA + s * kATile, &a.tw[pi], kb * BK, row0, &full[s]);
-          tma_load_2d(sB + s * kBTile, &a.tx, kb * BK, nt * BN, &full[s]);
+          if (kb < a.nk0) {
+            tma_load_2d(sA + s * kATile, &a.tw[pi], kb * BK, row0, &full[s]);
+            tma_load_2d(sB + s * kBTile, &a.tx, kb * BK, nt * BN, &full[s]);
+          } else {  // second K segment (problem 0 only)
+            tma_load_2d(sA + s * kATile, &a.tw2, (kb - a.nk0) * BK, row0, &full[s]);
+            tma_load_2d(sB + s * kBTile, &a.tx2, (kb - a.nk0) * BK, nt * BN, &full[s]);
+          }
           if (++s == kStages) { s = 0; ph ^= 1; }
         }
       }
@@ -229,20 +237,6 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const
           if (j < ntok) *dst = sum[j] + bias;
           dst += P.N;
         }
-      } else if (valid && P.out_bf16 && P.add) {  // y = bf16(W c + add): one rounding of the total
-        uint16_t* dst = P.out_bf16 + (size_t)tok0 * P.N + row;
-        const float* ad = P.add + (size_t)tok0 * P.N + row;
-#pragma unroll
-        for (int j0 = 0; j0 < kEpiCols; j0 += 16) {  // 16 loads in flight before their stores
-          float av[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) av[i] = j0 + i < ntok ? __ldg(ad + (size_t)(j0 + i) * P.N) : 0.f;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            if (j0 + i < ntok) *dst = f32_to_bf16(sum[j0 + i] + av[i]);
-            dst += P.N;
-          }
-        }
       } else if (valid && P.out_bf16) {
         uint16_t* dst = P.out_bf16 + (size_t)tok0 * P.N + row;
 #pragma unroll
@@ -263,12 +257,15 @@ __global__ void __launch_bounds__(Tile<BN>::kThreads, 1) umma_dense_kernel(const
 
 template <int BN>
 cudaError_t launch_bn(UDenseArgs& a, const uint16_t* const W[2], const int N[2], const uint16_t* x, int T, int K,
-                      cudaStream_t s) {
+                      const uint16_t* W2, const uint16_t* x2, cudaStream_t s) {
   a.ntiles = (T + BN - 1) / BN;
   for (int i = 0; i < 2; ++i)
     if (W[i] && !make_tmap_2d(&a.tw[i], W[i], 2, (uint64_t)K, (uint64_t)N[i], (uint64_t)K * 2, BK, BM, true))
       return cudaErrorInvalidValue;
   if (!make_tmap_2d(&a.tx, x, 2, (uint64_t)K, (uint64_t)T, (uint64_t)K * 2, BK, BN, true))
+    return cudaErrorInvalidValue;
+  if (a.K2 > 0 && (!make_tmap_2d(&a.tw2, W2, 2, (uint64_t)a.K2, (uint64_t)N[0], (uint64_t)a.K2 * 2, BK, BM, true) ||
+                   !make_tmap_2d(&a.tx2, x2, 2, (uint64_t)a.K2, (uint64_t)T, (uint64_t)a.K2 * 2, BK, BN, true)))
     return cudaErrorInvalidValue;
   constexpr size_t smem = Tile<BN>::kSmem;
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_dense_kernel<BN>), smem);
@@ -283,13 +280,17 @@ cudaError_t launch_bn(UDenseArgs& a, const uint16_t* const W[2], const int N[2],
 cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
-                              uint32_t* err, cudaStream_t s, const float* add0, float* out1_f32) {
+                              uint32_t* err, cudaStream_t s, float* out1_f32, const uint16_t* W0b,
+                              const uint16_t* xb, int Kb) {
   if (T <= 0) return cudaSuccess;
-  // one output kind per problem: fp32 (+ bias), bf16 (+ add), or bf16 + the f16 block-scaled copy
-  if ((out0_f32 && (out0_bf16 || add0)) || (out1_f32 && (out1_bf16 || out1_h))) return cudaErrorInvalidValue;
+  // one output kind per problem: fp32 (+ bias), bf16, or bf16 + the f16 block-scaled copy
+  if ((out0_f32 && out0_bf16) || (out1_f32 && (out1_bf16 || out1_h))) return cudaErrorInvalidValue;
+  if (W0b && (W1 || !xb || Kb <= 0 || Kb % BK)) return cudaErrorInvalidValue;
   UDenseArgs a{};
-  a.p[0] = UProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0, add0};
-  a.p[1] = UProblem{N1, out1_f32, nullptr, out1_bf16, out1_h, out1_s, actq1, nullptr};
+  a.p[0] = UProblem{N0, out0_f32, bias0, out0_bf16, nullptr, nullptr, 0};
+  a.p[1] = UProblem{N1, out1_f32, nullptr, out1_bf16, out1_h, out1_s, actq1};
+  a.nk0 = K / BK;
+  a.K2 = W0b ? Kb : 0;
   a.mt0 = W0 ? (N0 + BM - 1) / BM : 0;
   a.mtiles = a.mt0 + (W1 ? (N1 + BM - 1) / BM : 0);
   a.T = T;
@@ -301,8 +302,8 @@ cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint1
   const long long g = num_sms();
   const long long r64 = ((long long)a.mtiles * ((T + 63) / 64) + g - 1) / g;
   const long long r256 = ((long long)a.mtiles * ((T + 255) / 256) + g - 1) / g;
-  if (2 * r256 < r64) return launch_bn<256>(a, W, N, x, T, K, s);
-  return launch_bn<64>(a, W, N, x, T, K, s);
+  if (2 * r256 < r64) return launch_bn<256>(a, W, N, x, T, K, W0b, xb, s);
+  return launch_bn<64>(a, W, N, x, T, K, W0b, xb, s);
 }
 
 }  // namespace k3moe

@@ -83,3 +83,29 @@ def test_null_misaligned_and_small_workspace_rejected(L):
     # SiTU-GLU has no formula on the pages: refused
     assert k3.k3moe_layer_forward(dims(act=1), w, good, 1, good, None, None, good, 1 << 30,
                                   check=False) == 5
+
+
+def test_shared_expert_dims_and_workspace(L):
+    """Shared experts: n_shared in 0..8, n_shared * shared_inter a positive multiple of 64; their
+    buffers ([T][S] gate and up fp32, GLU output bf16) grow the workspace by 10 * T * S bytes at
+    most (plus alignment)."""
+    T = 64
+    base = k3.k3moe_workspace_size(dims(), T)
+    with_sh = k3.k3moe_workspace_size(dims(n_shared=2, shared_inter=3072), T)
+    S = 2 * 3072
+    assert 10 * T * S <= with_sh - base <= 10 * T * S + 3 * 256
+    out = ctypes.c_size_t(0)
+    for kw in (dict(n_shared=9, shared_inter=64), dict(n_shared=-1, shared_inter=64),
+               dict(n_shared=2, shared_inter=0), dict(n_shared=3, shared_inter=20)):
+        assert L.k3moe_workspace_size(ctypes.byref(dims(**kw)), 4, ctypes.byref(out)) == 2, kw
+    assert L.k3moe_workspace_size(ctypes.byref(dims(n_shared=1, shared_inter=64)), 4, ctypes.byref(out)) == 0
+
+
+def test_shared_expert_weights_checked(L):
+    good = 0x10000
+    d = dims(n_shared=2, shared_inter=64)
+    w = k3.Weights(good, None, good, good, good, good, good, good, good, good)
+    # shared pointers missing
+    assert k3.k3moe_layer_forward(d, w, good, 1, good, None, None, good, 1 << 30, check=False) == 1
+    w.w_shared_gate, w.w_shared_up, w.w_shared_down = good, good + 4, good
+    assert k3.k3moe_layer_forward(d, w, good, 1, good, None, None, good, 1 << 30, check=False) == 3

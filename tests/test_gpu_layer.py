@@ -268,10 +268,10 @@ def test_layer_other_dims_every_token(dname, T):
 # With W_out = 0 the output is the shared experts' alone, y = bf16(s); otherwise
 # y = bf16(W_out c + s). T = 3 runs the token-at-a-time projections, T = 150 the tensor-core ones.
 @pytest.mark.parametrize("T", [3, 150])
-@pytest.mark.parametrize("zero_out", [True, False])
-def test_layer_shared_experts_every_token(T, zero_out):
+@pytest.mark.parametrize("zero_out,actq", [(True, 0), (False, 0), (False, 1)])
+def test_layer_shared_experts_every_token(T, zero_out, actq):
     d = synth.TINY
-    lay = DeviceLayer(d, seed=3, shared=(2, 64), zero_out=zero_out)
+    lay = DeviceLayer(d, seed=3, shared=(2, 64), zero_out=zero_out, actq=actq)
     x = synth.host_bf16_normal(9, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
     y, idx, w = _forward(lay, x)
     _compare_layer(lay, x, y, idx, np.arange(T))

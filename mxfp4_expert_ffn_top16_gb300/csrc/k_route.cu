@@ -36,7 +36,8 @@ __device__ __forceinline__ uint32_t sort_key(float v) {
 // experts by index and writes them with the softmax weights over their logits.
 constexpr int kTopkThreads = 256;
 constexpr int kTopkKeys = kMaxE / kTopkThreads;  // keys per thread
-__device__ void block_topk(const float* __restrict__ logits, int t, int E, int k, int32_t* idx, float* w) {
+// Returns, to thread lane < k of warp 0, the expert it wrote to slot lane (-1 elsewhere).
+__device__ int block_topk(const float* __restrict__ logits, int t, int E, int k, int32_t* idx, float* w) {
   __shared__ int hist[256];
   __shared__ int s_digit, s_above, s_nsel;
   __shared__ int wcnt[kTopkKeys][kTopkThreads / 32];
@@ -149,7 +150,9 @@ __device__ void block_topk(const float* __restrict__ logits, int t, int E, int k
       idx[(size_t)t * k + lane] = e;
       w[(size_t)t * k + lane] = ex / sum;
     }
+    return lane < k ? e : -1;
   }
+  return -1;
 }
 
 __global__ void __launch_bounds__(kTopkThreads) topk_block_kernel(const float* __restrict__ logits, int T, int E,
@@ -338,9 +341,10 @@ constexpr int kTinyRows = 64;
 // rows r = t * k + j (r < R <= kTinyRows), experts idx[r]: sorted rows grouped by expert, token
 // order inside an expert; the same outputs as the histogram / scan / scatter path. All threads
 // of the block take part.
+// own_e >= 0: thread tid's expert is own_e (one token: this block selected it), not re-read from idx.
 __device__ void block_route_tiny(const int32_t* idx, int T, int E, int k, int rows_max, int32_t* offsets,
                                  int32_t* row_token, int32_t* row_slot, int32_t* slot_row, int32_t* plan,
-                                 uint32_t* err) {
+                                 uint32_t* err, int own_e = -1) {
   __shared__ uint32_t s_key[kTinyRows];
   __shared__ int s_e[kTinyRows], s_start[kTinyRows], s_run[kTinyRows + 1], s_chunks[kTinyRows];
   const int tid = threadIdx.x;
@@ -348,7 +352,7 @@ __device__ void block_route_tiny(const int32_t* idx, int T, int E, int k, int ro
   // key = expert * kTinyRows + row: in key order, rows go by expert, then by row (token order)
   bool valid = false;
   if (tid < R) {
-    const int e = __ldcg(idx + tid);
+    const int e = own_e >= 0 ? own_e : __ldcg(idx + tid);
     valid = e >= 0 && e < E;
     if (!valid) {
       atomicOr(err, kErrIndex);
@@ -426,7 +430,11 @@ __global__ void __launch_bounds__(kTopkThreads) route_tiny_kernel(const float* _
   pdl_trigger();
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
-  block_topk(logits, blockIdx.x, E, k, idx, w);
+  const int own_e = block_topk(logits, blockIdx.x, E, k, idx, w);
+  if (T == 1) {  // the only block is the last: no count, and its own selection stays in registers
+    block_route_tiny(idx, T, E, k, k, offsets, row_token, row_slot, slot_row, plan, err, own_e);
+    return;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();  // this token's indices are visible before it is counted

@@ -39,7 +39,7 @@ constexpr int kTopkKeys = kMaxE / kTopkThreads;  // keys per thread
 // Returns, to thread lane < k of warp 0, the expert it wrote to slot lane (-1 elsewhere).
 __device__ int block_topk(const float* __restrict__ logits, int t, int E, int k, int32_t* idx, float* w) {
   __shared__ int hist[256];
-  __shared__ int s_digit, s_above, s_nsel;
+  __shared__ int s_digit, s_above, s_nsel, s_full;
   __shared__ int wcnt[kTopkKeys][kTopkThreads / 32];
   __shared__ int sel_e[32];
   __shared__ float sel_l[32];
@@ -84,6 +84,7 @@ __device__ int block_topk(const float* __restrict__ logits, int t, int E, int k,
           if (run < need && need <= run + c[j]) {
             s_digit = 255 - 8 * lane - j;
             s_above = run;
+            s_full = c[j] == need - run;  // the bucket holds exactly the keys still needed
           }
           run += c[j];
         }
@@ -93,12 +94,15 @@ __device__ int block_topk(const float* __restrict__ logits, int t, int E, int k,
     thr |= (uint32_t)s_digit << shift;
     pmask |= 255u << shift;
     need -= s_above;
+    if (s_full) break;  // every key with this prefix is selected: the lower digits decide nothing
   }
-  // thr is the k-th largest key; take `need` of the keys equal to it, lowest index first
+  // Keys compare on their top bytes kept so far (pmask): above thr are selected; equal to thr
+  // (the boundary; the k-th largest key itself when all four digits ran) take `need` of them,
+  // lowest index first
   int rank_in_warp[kTopkKeys];
 #pragma unroll
   for (int i = 0; i < kTopkKeys; ++i) {
-    const unsigned b = __ballot_sync(0xffffffffu, key[i] == thr);
+    const unsigned b = __ballot_sync(0xffffffffu, key[i] != 0u && (key[i] & pmask) == thr);
     rank_in_warp[i] = __popc(b & lt);
     if (lane == 0) wcnt[i][wid] = __popc(b);
   }
@@ -112,7 +116,8 @@ __device__ int block_topk(const float* __restrict__ logits, int t, int E, int k,
       bw += x < wid ? wcnt[i][x] : 0;
       tot += wcnt[i][x];
     }
-    const bool sel = key[i] > thr || (key[i] == thr && before + bw + rank_in_warp[i] < need);
+    const uint32_t km = key[i] & pmask;
+    const bool sel = key[i] != 0u && (km > thr || (km == thr && before + bw + rank_in_warp[i] < need));
     if (sel) {
       const int slot = atomicAdd(&s_nsel, 1);
       const int e = tid + kTopkThreads * i;

@@ -148,8 +148,10 @@ def test_expert_ffn_nan_scale_gives_nonfinite(dname, T):
 
 
 # ------------------------------------------------------------------ combine
-def test_combine():
-    d = synth.K3
+@pytest.mark.parametrize("k", [16, 1, 24, 32])  # k <= 16 and k > 16 take different kernel instances
+def test_combine(k):
+    import dataclasses
+    d = dataclasses.replace(synth.K3, top_k=k)
     T = 33
     rng = np.random.default_rng(1)
     o = rng.normal(0, 1e5, (T * d.top_k, d.latent)).astype(np.float32)

@@ -3,6 +3,7 @@
 // kernels; nothing here computes on the host.
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -13,15 +14,15 @@
 namespace k3moe {
 
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // zero-initialised (static storage); 0 = not yet queried
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 cudaError_t ensure_smem_attr(const void* fn, size_t bytes) {

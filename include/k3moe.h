@@ -35,7 +35,8 @@
  *
  * Conventions for every call:
  *   - Pointers are device pointers unless stated; the caller owns all memory. No call
- *     allocates device memory or synchronises the stream (except k3moe_check).
+ *     allocates device memory or synchronises the stream (except k3moe_check and
+ *     k3moe_layer_stats).
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *   - Work is enqueued asynchronously; a returned K3MOE_OK means the launches were accepted.
  *   - T = 0 is valid and does nothing.
@@ -183,6 +184,14 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
  * K3MOE_E_TIMEOUT (a bounded wait ran out) or K3MOE_E_DEVICE (another device-side check),
  * or K3MOE_E_CUDA if the stream reported an error. */
 k3moe_status k3moe_check(void* ws, void* stream);
+
+/* After k3moe_layer_forward or k3moe_permute + k3moe_expert_ffn_mxfp4 on T tokens with this
+ * workspace and dims: synchronises `stream` and reports how many distinct experts the step
+ * selected (*distinct) and the expert bytes that step had to read, distinct x the bytes of one
+ * expert (*expert_bytes; 17,547,264 per expert at K3 sizes). Either output may be NULL. Host
+ * pointers; K3MOE_E_CUDA if the stream reported an error. */
+k3moe_status k3moe_layer_stats(const k3moe_dims* dims, int32_t T, void* ws, size_t ws_bytes, void* stream,
+                               int32_t* distinct, int64_t* expert_bytes);
 
 /* Human-readable name of a status code (static string). */
 const char* k3moe_status_string(k3moe_status status);

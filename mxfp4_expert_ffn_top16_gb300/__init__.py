@@ -36,7 +36,8 @@ K3MOE_OK = 0
 # Exported symbols (kept in step with include/k3moe.h; a CPU test checks both).
 EXPORTS = ["k3moe_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_project",
            "k3moe_expert_ffn_mxfp4", "k3moe_combine", "k3moe_layer_forward", "k3moe_check",
-           "k3moe_status_string", "k3moe_profile", "k3moe_profile_name", "k3moe_route_noalloc"]
+           "k3moe_status_string", "k3moe_profile", "k3moe_profile_name", "k3moe_route_noalloc",
+           "k3moe_layer_stats"]
 
 
 def _newer(target: str, deps) -> bool:
@@ -102,6 +103,7 @@ def lib():
             "k3moe_layer_forward": [p, p, p, i32, p, p, p, p, sz, p],
             "k3moe_check": [p, p],
             "k3moe_route_noalloc": [p, p, i32, p, p, p, p, p, p],
+            "k3moe_layer_stats": [p, i32, p, sz, p, p, p],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -185,6 +187,15 @@ def k3moe_layer_forward(dims, weights, x, T, y, topk_idx_out, topk_w_out, ws, ws
     return _ck(lib().k3moe_layer_forward(_ref(dims), _ref(weights), x, T, y, topk_idx_out,
                                          topk_w_out, ws, ws_bytes, stream),
                "k3moe_layer_forward", check)
+
+
+def k3moe_layer_stats(dims, T, ws, ws_bytes, stream=0):
+    """(distinct experts selected in the last step, the expert bytes that step read)."""
+    dd = ctypes.c_int32(0)
+    eb = ctypes.c_int64(0)
+    _ck(lib().k3moe_layer_stats(_ref(dims), T, ws, ws_bytes, stream, ctypes.byref(dd), ctypes.byref(eb)),
+        "k3moe_layer_stats", True)
+    return dd.value, eb.value
 
 
 def k3moe_check(ws, stream=0):

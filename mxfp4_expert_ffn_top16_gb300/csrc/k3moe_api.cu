@@ -503,6 +503,29 @@ const char* k3moe_profile_name(int32_t id) {
   return (id >= 0 && id < P_COUNT) ? kProfNames[id] : nullptr;
 }
 
+k3moe_status k3moe_layer_stats(const k3moe_dims* dims, int32_t T, void* ws, size_t ws_bytes, void* stream,
+                               int32_t* distinct, int64_t* expert_bytes) {
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  if (T < 0) return K3MOE_E_SHAPE;
+  K3_TRY(check_ws(d, T, ws, ws_bytes));
+  int32_t D = 0;
+  if (T > 0) {
+    const WsLayout L = ws_layout(d, T);
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return K3MOE_E_CUDA;
+    // plan[0]: active experts of the step, written by the routing / plan kernels
+    if (cudaMemcpy(&D, at<int32_t>(ws, L.plan), sizeof(D), cudaMemcpyDeviceToHost) != cudaSuccess)
+      return K3MOE_E_CUDA;
+    if (D < 0 || D > d.n_experts) return K3MOE_E_DEVICE;
+  }
+  if (distinct) *distinct = D;
+  if (expert_bytes) {  // per expert: gate and up codes + scales, down codes + scales
+    const int64_t L_ = d.latent, I = d.inter;
+    *expert_bytes = (int64_t)D * (2 * (I * L_ / 2 + I * L_ / 32) + (L_ * I / 2 + L_ * I / 32));
+  }
+  return K3MOE_OK;
+}
+
 k3moe_status k3moe_check(void* ws, void* stream) {
   if (!ws) return K3MOE_E_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -109,3 +109,16 @@ def test_shared_expert_weights_checked(L):
     assert k3.k3moe_layer_forward(d, w, good, 1, good, None, None, good, 1 << 30, check=False) == 1
     w.w_shared_gate, w.w_shared_up, w.w_shared_down = good, good + 4, good
     assert k3.k3moe_layer_forward(d, w, good, 1, good, None, None, good, 1 << 30, check=False) == 3
+
+
+def test_layer_stats_arguments(L):
+    good = 0x10000
+    out = ctypes.c_int32(0)
+    assert L.k3moe_layer_stats(None, 1, good, 1 << 30, None, ctypes.byref(out), None) == 1
+    assert L.k3moe_layer_stats(ctypes.byref(dims()), -1, good, 1 << 30, None, ctypes.byref(out), None) == 2
+    assert L.k3moe_layer_stats(ctypes.byref(dims()), 1, good, 100, None, ctypes.byref(out), None) == 4
+    # T = 0: nothing was selected, no device access
+    eb = ctypes.c_int64(7)
+    assert L.k3moe_layer_stats(ctypes.byref(dims()), 0, good, 1 << 30, None, ctypes.byref(out),
+                               ctypes.byref(eb)) == 0
+    assert out.value == 0 and eb.value == 0

@@ -231,6 +231,25 @@ def test_layer_tiny_prefill_every_token(actq):
     _compare_layer(lay, x, y, idx, np.arange(T))
 
 
+@pytest.mark.parametrize("T", [1, 3, 40, 150])  # routing: one block, a few blocks, one permutation block, many
+def test_layer_stats_match_selection(T):
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=6)
+    x = synth.host_bf16_normal(8, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+    dm = lay.dims
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device=DEV)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=DEV)
+    ws, n = workspace(dm, T)
+    xd = up(x)
+    k3.k3moe_layer_forward(dm, lay.weights, xd.data_ptr(), T, y.data_ptr(), idx.data_ptr(), None, ws.data_ptr(),
+                           n, stream())
+    D, nbytes = k3.k3moe_layer_stats(dm, T, ws.data_ptr(), n, stream())
+    check_ok(ws)
+    want = len(np.unique(idx.cpu().numpy()))
+    assert D == want
+    assert nbytes == want * d.expert_bytes
+
+
 def test_layer_tiny_ragged_and_edge_T():
     d = synth.TINY
     lay = DeviceLayer(d, seed=1, bias=synth.host_f32_normal(1, synth.S_BIAS, 0, d.n_experts, 1.0))

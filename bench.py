@@ -363,19 +363,40 @@ def run_ours(args, w):
     setup_s = time.time() - t_setup
     nsteps_x = max(1, nx // T)
 
+    cur = {"stream": sh}  # the stream the layer calls go to (a capture stream while recording a graph)
+
     def step(i, xp=None, yp=None):
         xi = xp if xp is not None else x[(i % nsteps_x) * T:].data_ptr()
         yo = yp or y.data_ptr()
         if nl == 1:
             k3.k3moe_layer_forward(dims, wts[i % DENSE_COPIES], xi, T, yo, idx.data_ptr(), None,
-                                   ws.data_ptr(), nbytes, sh)
+                                   ws.data_ptr(), nbytes, cur["stream"])
             return
         # every layer takes the step's tokens (chaining the synthetic layers' outputs would
         # overflow within a few layers: the random experts amplify the activations)
         for layer in range(nl):
             dst = yo if layer == nl - 1 else hbuf[layer % 2].data_ptr()
             k3.k3moe_layer_forward(dims, wts[layer], xi, T, dst, idx.data_ptr(), None, ws.data_ptr(),
-                                   nbytes, sh)
+                                   nbytes, cur["stream"])
+
+    def capture(G):
+        """A CUDA graph of G consecutive steps (the layer calls neither allocate nor synchronise,
+        so they capture as they are, programmatic-launch edges included); None if capture fails."""
+        try:
+            g = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream()
+            cs.wait_stream(stream)
+            with torch.cuda.graph(g, stream=cs):
+                cur["stream"] = cs.cuda_stream
+                for j in range(G):
+                    step(args.warmup + j)
+            stream.wait_stream(cs)
+            return g
+        except Exception as e:  # fall back to stream launches
+            print(f"bench: graph capture failed ({e}); timing stream launches", file=sys.stderr)
+            return None
+        finally:
+            cur["stream"] = sh
 
     def barrier():
         torch.cuda.synchronize()
@@ -398,12 +419,25 @@ def run_ours(args, w):
     if st != 0:
         raise RuntimeError("warmup: " + k3.status_string(st))
 
-    # --- pass 1: device-timed value
+    # --- pass 1: device-timed value: exactly K steps, replayed from a CUDA graph of G captured
+    # steps (G the largest divisor of K up to --graph-steps; tokens cycle over G sets) or, with
+    # --graph-steps 0, launched step by step
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
+    G = min(args.graph_steps, args.steps)
+    while G > 1 and args.steps % G:
+        G -= 1
+    graph = capture(G) if G >= 1 and args.graph_steps > 0 else None
+    if graph is not None:
+        graph.replay()  # untimed: the first replay uploads the graph
+        barrier()
+        ev0.record(stream)
+        for r in range(args.steps // G):
+            graph.replay()
+    else:
+        barrier()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i)
     ev1.record(stream)
     barrier()
     ms = max_over_ranks(ev0.elapsed_time(ev1))
@@ -464,6 +498,9 @@ def run_ours(args, w):
                           if nl == 1 else f"{nl} layers with independent weights ({nl * 15.7:.0f} GB of experts) run back to "
                           "back on the same tokens; fresh tokens per step"),
                    "parallelism": f"replicas x{world}",
+                   "launch": (f"value: CUDA graph of {G} captured steps replayed {args.steps // G} times "
+                              f"(tokens cycle over {G} sets); per-kernel and e2e passes: stream launches"
+                              if graph is not None else "stream launches (programmatic dependent launch)"),
                    "shared_experts": (f"{ns} x {si} bf16 (width a parameter; not in the headline configuration)"
                                       if S else "none")},
         "roofline": roofline(name, per_launch_ms, kernel_cost(name, d, T, distinct, T * d.top_k, args.actq, S), pk),
@@ -523,6 +560,8 @@ def main():
     ap.add_argument("--workload", default="decode_b1")
     ap.add_argument("--actq", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph-steps", type=int, default=8,
+                    help="steps per captured CUDA graph for the device-timed value (0: launch step by step)")
     ap.add_argument("--shared-inter", type=int, default=0,
                     help="also run two always-on bf16 shared experts of this width (their width is not "
                          "on the pages; the headline metric is the routed layer without them)")

@@ -250,6 +250,41 @@ def test_layer_stats_match_selection(T):
     assert nbytes == want * d.expert_bytes
 
 
+@pytest.mark.parametrize("T", [1, 150])
+def test_layer_in_cuda_graph_matches_direct_call(T):
+    """The layer call neither allocates nor synchronises: captured in a CUDA graph and replayed,
+    it gives the same bits as a direct call (two different token sets, replayed twice)."""
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=7, shared=(2, 64))
+    dm = lay.dims
+    xs = [up(synth.host_bf16_normal(20 + i, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)) for i in range(2)]
+    ys = [torch.empty((T, d.hidden), dtype=torch.int16, device=DEV) for _ in range(2)]
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=DEV)
+    ws, n = workspace(dm, T)
+    direct = []
+    for i in range(2):
+        k3.k3moe_layer_forward(dm, lay.weights, xs[i].data_ptr(), T, ys[i].data_ptr(), idx.data_ptr(), None,
+                               ws.data_ptr(), n, stream())
+        direct.append(ys[i].clone())
+    check_ok(ws)
+    for yy in ys:
+        yy.zero_()
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=cs):
+        for i in range(2):
+            k3.k3moe_layer_forward(dm, lay.weights, xs[i].data_ptr(), T, ys[i].data_ptr(), idx.data_ptr(), None,
+                                   ws.data_ptr(), n, cs.cuda_stream)
+    torch.cuda.current_stream().wait_stream(cs)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    check_ok(ws)
+    for i in range(2):
+        assert torch.equal(ys[i], direct[i])
+
+
 def test_layer_tiny_ragged_and_edge_T():
     d = synth.TINY
     lay = DeviceLayer(d, seed=1, bias=synth.host_f32_normal(1, synth.S_BIAS, 0, d.n_experts, 1.0))

@@ -105,6 +105,21 @@ def algorithmic(d, T, distinct_experts, shared_width=0):
     return dense_w + expert + act, flops
 
 
+def max_over_ranks(v, dist=None, device="cpu"):
+    """The largest of every rank's v (a time: the job is as slow as its slowest rank)."""
+    if dist is None:
+        return v
+    import torch
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(steps, tokens_per_step, world, ms):
+    """Whole-job throughput: the tokens every rank processed over the max-over-ranks time."""
+    return steps * tokens_per_step * world / (ms / 1e3)
+
+
 def measured_traffic(workload, kernel):
     """DRAM bytes per launch of a kernel from the committed ncu capture (profiles/traffic.json),
     or None when there is none or the kernel's sources have changed since it was taken."""
@@ -404,13 +419,6 @@ def run_ours(args, w):
             dist.barrier()
             torch.cuda.synchronize()
 
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     clocks = ClockSampler(local)
     clocks.start()
     for i in range(args.warmup):
@@ -440,7 +448,7 @@ def run_ours(args, w):
             step(args.warmup + i)
     ev1.record(stream)
     barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1))
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     st = k3.k3moe_check(ws.data_ptr(), sh)
     if st != 0:
         raise RuntimeError("timed: " + k3.status_string(st))
@@ -469,12 +477,11 @@ def run_ours(args, w):
         yh[i].copy_(y, non_blocking=True)
     ev1.record(stream)
     barrier()
-    ms_e2e = max_over_ranks(ev0.elapsed_time(ev1))
+    ms_e2e = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
     clk = clocks.stop()
 
-    tokens_all = args.steps * T * world
-    value = tokens_all / (ms / 1e3)
-    e2e = tokens_all / (ms_e2e / 1e3)
+    value = job_tokens_per_s(args.steps, T, world, ms)
+    e2e = job_tokens_per_s(args.steps, T, world, ms_e2e)
     pk = peaks()
     # dominant kernel by time share
     top = max(prof.items(), key=lambda kv: kv[1][0])

@@ -196,6 +196,14 @@ k3moe_status k3moe_layer_stats(const k3moe_dims* dims, int32_t T, void* ws, size
 /* Human-readable name of a status code (static string). */
 const char* k3moe_status_string(k3moe_status status);
 
+/* Failure-detection self test (diagnostic; no counterpart on the pages): enqueues one kernel
+ * whose single thread waits on a shared-memory barrier that nothing completes, with the same
+ * bounded wait every kernel of the library uses (about 2 s of wall clock). The wait runs out,
+ * the kernel records a timeout in the workspace error word and returns; the context stays
+ * usable and the next k3moe_check reports K3MOE_E_TIMEOUT (and clears the word). `ws` is a
+ * device workspace of at least 256 bytes. Returns K3MOE_E_CUDA if the launch fails. */
+k3moe_status k3moe_selftest_timeout(void* ws, void* stream);
+
 /* Diagnostic per-kernel timing of k3moe_layer_forward (not needed for normal use; no
  * counterpart on the pages). mode = 1 starts recording: every kernel launch of later
  * layer_forward calls is bracketed by CUDA events on the caller's stream. mode = 0 stops,

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "k3moe.h"
+#include "k3moe_device.cuh"
 #include "k3moe_internal.cuh"
 
 namespace k3moe {
@@ -524,6 +525,35 @@ k3moe_status k3moe_layer_stats(const k3moe_dims* dims, int32_t T, void* ws, size
     *expert_bytes = (int64_t)D * (2 * (I * L_ / 2 + I * L_ / 32) + (L_ * I / 2 + L_ * I / 32));
   }
   return K3MOE_OK;
+}
+
+}  // extern "C"
+
+namespace k3moe {
+namespace {
+// One thread waits on a barrier nobody arrives on: mbar_wait_bounded gives up after its wall-clock
+// limit, sets the timeout bit of *err and returns (the self test of the failure path).
+__global__ void wait_selftest_kernel(uint32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait_bounded(&bar, 0, &abort_flag, err);
+}
+}  // namespace
+}  // namespace k3moe
+
+extern "C" {
+
+k3moe_status k3moe_selftest_timeout(void* ws, void* stream) {
+  if (!ws) return K3MOE_E_WORKSPACE;
+  if (misaligned(ws)) return K3MOE_E_ALIGN;
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(ws));
+  return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_E_CUDA;
 }
 
 k3moe_status k3moe_check(void* ws, void* stream) {

@@ -285,6 +285,20 @@ def test_layer_in_cuda_graph_matches_direct_call(T):
         assert torch.equal(ys[i], direct[i])
 
 
+def test_bounded_wait_runs_out_and_the_context_survives():
+    """Failure detection without a fault: a device wait that nothing completes runs out after its
+    wall-clock limit, the error word says so, and the next layer call runs and checks clean."""
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    k3.k3moe_selftest_timeout(ws.data_ptr(), stream())
+    assert k3.k3moe_check(ws.data_ptr(), stream()) == 7  # K3MOE_E_TIMEOUT
+    assert k3.k3moe_check(ws.data_ptr(), stream()) == k3.K3MOE_OK  # the word was cleared
+    d = synth.TINY
+    lay = DeviceLayer(d, seed=0)
+    x = synth.host_x(synth.WORKLOADS["tiny"])
+    y, idx, w = _forward(lay, x)  # checks the workspace error word itself
+    _compare_layer(lay, x, y, idx, np.arange(x.shape[0]))
+
+
 def test_layer_tiny_ragged_and_edge_T():
     d = synth.TINY
     lay = DeviceLayer(d, seed=1, bias=synth.host_f32_normal(1, synth.S_BIAS, 0, d.n_experts, 1.0))

@@ -65,6 +65,10 @@ def lib():
         L.k3o_e4m3_encode.restype = i
         L.k3o_mxfp8_block.argtypes = [p, p, p]
         L.k3o_mxfp8_roundtrip.argtypes = [p, i]
+        L.k3o_e2m1_encode.argtypes = [d]
+        L.k3o_e2m1_encode.restype = i
+        L.k3o_mxfp4_block.argtypes = [p, p, p]
+        L.k3o_mxfp4_roundtrip.argtypes = [p, i]
         L.k3o_mx_weight.argtypes = [p, p, i]
         L.k3o_mx_weight.restype = d
         L.k3o_dequant.argtypes = [p, p, i, i, p]
@@ -138,6 +142,25 @@ def mxfp8_block(v):
 def mxfp8_roundtrip(v):
     v = _c(v, np.float64).copy()
     lib().k3o_mxfp8_roundtrip(v.ctypes.data, v.size)
+    return v
+
+
+def e2m1_encode(v: float) -> int:
+    return lib().k3o_e2m1_encode(v)
+
+
+def mxfp4_block(v):
+    v = _c(v, np.float64)
+    assert v.shape == (32,)
+    codes = np.empty(32, np.uint8)
+    sc = np.empty(1, np.uint8)
+    lib().k3o_mxfp4_block(v.ctypes.data, codes.ctypes.data, sc.ctypes.data)
+    return codes, int(sc[0])
+
+
+def mxfp4_roundtrip(v):
+    v = _c(v, np.float64).copy()
+    lib().k3o_mxfp4_roundtrip(v.ctypes.data, v.size)
     return v
 
 

@@ -25,6 +25,10 @@
  *  - One shared latent-in W_in [L][H] and latent-out W_out [H][L] per layer; the combine
  *    runs in latent space before W_out.
  *  - bf16 round-to-nearest-even at z, at the GLU output a, at the combine c and at y.
+ *  - MXFP4 activations (actq = 2, the 4-bit activation mode that the fp4 tensor rate needs;
+ *    the library does not run it yet): z and a go through an OCP MX FP4 round trip (e2m1
+ *    elements, shared exponent floor(log2 amax) - 2, round-to-nearest-even, saturating at 6)
+ *    where the MXFP8 mode applies its E4M3 round trip.
  *  - Shared experts ("kimi-k3-mlx", Architecture table and LatentMoE: n_shared always-on
  *    experts per token that work on the H-wide residual, not in the latent space; the
  *    weights outside the routed experts are bf16, Quantisation tiers): each is a bf16 GLU
@@ -44,7 +48,7 @@
 typedef struct {
   int32_t hidden, latent, inter, n_experts, top_k;
   int32_t act;   /* 0 = SiLU-GLU */
-  int32_t actq;  /* 0 = bf16 activations, 1 = MXFP8 activations */
+  int32_t actq;  /* 0 = bf16 activations, 1 = MXFP8, 2 = MXFP4 (e2m1 + e8m0 per 32) */
   int32_t n_shared;      /* always-on shared experts (0 = none) */
   int32_t shared_inter;  /* intermediate width of each shared expert */
 } k3o_dims;
@@ -183,6 +187,57 @@ void k3o_mxfp8_roundtrip(double* v, int n) {
   for (int b = 0; b < n; b += 32) {
     k3o_mxfp8_block(v + b, codes, &sc);
     for (int i = 0; i < 32; ++i) v[b + i] = k3o_e4m3(codes[i]) * k3o_e8m0(sc);
+  }
+}
+
+/* Round a real value to e2m1 with round-to-nearest-even, saturating to +-6 (the element
+ * conversion of the OCP MX spec for FP4). Returns the 4-bit code. */
+int k3o_e2m1_encode(double v) {
+  const int s = signbit(v) ? 8 : 0;
+  const double a = fabs(v);
+  if (isnan(v)) return s | 7; /* no NaN in e2m1: saturate */
+  /* the 8 magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 at codes 0..7; pick the nearest, ties to the
+   * even code */
+  int best = 0;
+  double bd = INFINITY;
+  for (int c = 0; c < 8; ++c) {
+    const double d = fabs(a - k3o_e2m1(c));
+    if (d < bd || (d == bd && (c & 1) == 0)) {
+      bd = d;
+      best = c;
+    }
+  }
+  return s | best;
+}
+
+/* MXFP4 quantisation of one block of 32 values (OCP MX v1.0 conversion, FP4 E2M1 elements):
+ * shared exponent X = floor(log2(amax)) - emax_elem, emax_elem = 2 for E2M1, clamped to the
+ * e8m0 range [-127, 127]; elements are v / 2^X rounded to e2m1 (RNE, saturating at 6). An
+ * all-zero block gets X = -127 and zero elements. */
+void k3o_mxfp4_block(const double* v, uint8_t* codes, uint8_t* scale_e8m0) {
+  double amax = 0.0;
+  for (int i = 0; i < 32; ++i)
+    if (fabs(v[i]) > amax) amax = fabs(v[i]);
+  int X;
+  if (amax == 0.0 || !isfinite(amax)) {
+    X = (amax == 0.0) ? -127 : 127;
+  } else {
+    int e;
+    frexp(amax, &e);
+    X = (e - 1) - 2;
+    if (X < -127) X = -127;
+    if (X > 127) X = 127;
+  }
+  *scale_e8m0 = (uint8_t)(X + 127);
+  for (int i = 0; i < 32; ++i) codes[i] = (uint8_t)k3o_e2m1_encode(ldexp(v[i], -X));
+}
+
+/* Value after MXFP4 round trip, in place, for a vector whose length is a multiple of 32. */
+void k3o_mxfp4_roundtrip(double* v, int n) {
+  uint8_t codes[32], sc;
+  for (int b = 0; b < n; b += 32) {
+    k3o_mxfp4_block(v + b, codes, &sc);
+    for (int i = 0; i < 32; ++i) v[b + i] = k3o_e2m1(codes[i]) * k3o_e8m0(sc);
   }
 }
 
@@ -333,6 +388,7 @@ int k3o_expert_row(const k3o_dims* d, const k3o_weights* w, int e, const uint16_
   double* wu = (double*)malloc(sizeof(double) * (size_t)L);
   for (int k = 0; k < L; ++k) zin[k] = k3o_bf16_to_double(z[k]);
   if (d->actq == 1) k3o_mxfp8_roundtrip(zin, L);
+  if (d->actq == 2) k3o_mxfp4_roundtrip(zin, L);
   const uint8_t *gq = w->gate_q[e], *gs = w->gate_s[e], *uq = w->up_q[e], *us = w->up_s[e];
   for (int n = 0; n < I; ++n) {
     double g = 0.0, u = 0.0;
@@ -347,6 +403,7 @@ int k3o_expert_row(const k3o_dims* d, const k3o_weights* w, int e, const uint16_
     a[n] = k3o_bf16_to_double(ab);
   }
   if (d->actq == 1) k3o_mxfp8_roundtrip(a, I);
+  if (d->actq == 2) k3o_mxfp4_roundtrip(a, I);
   const uint8_t *dq = w->down_q[e], *ds = w->down_s[e];
   for (int n = 0; n < L; ++n) {
     double acc = 0.0;
@@ -417,7 +474,7 @@ int k3o_layer_forward(const k3o_dims* d, const k3o_weights* w, const uint16_t* x
                       uint16_t* y, int32_t* idx_out, double* w_out, double* logits_out,
                       uint16_t* z_out, uint16_t* c_out, int nthreads) {
   const int H = d->hidden, L = d->latent, E = d->n_experts, k = d->top_k;
-  if (d->act != 0 || d->actq < 0 || d->actq > 1) return -1;
+  if (d->act != 0 || d->actq < 0 || d->actq > 2) return -1;
   if (d->n_shared < 0 || (d->n_shared > 0 && (d->shared_inter <= 0 || !w->w_sgate || !w->w_sup || !w->w_sdown)))
     return -1;
   int bad = 0;

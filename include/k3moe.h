@@ -121,7 +121,7 @@ k3moe_status k3moe_route(const k3moe_dims* dims, const uint16_t* x, int32_t T,
 
 /* k3moe_route without a workspace: the same router logits and top-k (same kernels, same
  * results as k3moe_route), with the logits kept in a fixed scratch array inside the library.
- * The paper has no counterpart; this exists for callers that cannot allocate device memory
+ * The pages have no counterpart; this exists for callers that cannot allocate device memory
  * for a routing decision: a serving process whose device memory is all handed to its own
  * pool allocator, where cudaMalloc / cudaFree are off limits on the request path because
  * they can synchronise the whole device and stall every other stream.
@@ -173,8 +173,10 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights*
 k3moe_status k3moe_combine(const k3moe_dims* dims, const float* o_rows, const int32_t* slot_row,
                            const float* topk_w, int32_t T, uint16_t* c, void* stream);
 
-/* The whole routed-expert layer: x [T][H] bf16 -> y [T][H] bf16. topk_idx_out [T][k] and
- * topk_w_out [T][k] may be NULL; when given they receive the routing decisions. */
+/* The whole layer: x [T][H] bf16 -> y [T][H] bf16, the routed experts plus, when
+ * dims->n_shared > 0, the shared experts (y = bf16(W_out c + s), one rounding). topk_idx_out
+ * [T][k] and topk_w_out [T][k] may be NULL; when given they receive the routing decisions.
+ * Neither allocates nor synchronises: the call can be captured in a CUDA graph. */
 k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* weights,
                                  const uint16_t* x, int32_t T, uint16_t* y,
                                  int32_t* topk_idx_out, float* topk_w_out, void* ws,

@@ -363,3 +363,148 @@ def combine(o_rows, slot_row, w, T, k):
 
 def max_threads() -> int:
     return lib().k3o_max_threads()
+
+
+# ------------------------------------------------------------------ batched statement
+# The same layer, step for step and with the same rounding points, for checks over thousands of
+# tokens: the sums are numpy float64 matrix products (a library routine as the summation step)
+# instead of the scalar double loops above, and the experts are decoded once per expert instead
+# of once per row. It follows the same passages as k3moe_oracle.c ("kimi-k3-mlx", Architecture
+# table and Quantisation tiers; "kimi-k3-in-c", MXFP4 experts). Pinned against the scalar C
+# statement (tests/test_oracle_batched_pins.py): same selections, same bf16 values.
+
+_E2M1 = None
+
+
+def _e2m1_table() -> np.ndarray:
+    global _E2M1
+    if _E2M1 is None:
+        _E2M1 = np.array([e2m1(c) for c in range(16)], np.float64)
+    return _E2M1
+
+
+def bf16_from_f64_np(x) -> np.ndarray:
+    """double -> bf16 bits, round to nearest, ties to even, in one step: the rule of
+    k3o_bf16_from_double, on whole arrays (8 significant bits; below 2^-126 the fixed quantum
+    2^-133; overflow to infinity; NaN -> 0x7fc0)."""
+    x = np.asarray(x, np.float64)
+    a = np.abs(x)
+    with np.errstate(over="ignore", invalid="ignore"):
+        _, e = np.frexp(a)                     # a in [2^(e-1), 2^e)
+        q = np.ldexp(1.0, np.maximum(e - 1, -126) - 7)
+        r = np.rint(a / q) * q                 # a / q is exact; rint rounds ties to even
+        r = np.where(r >= 2.0**128, np.inf, r)
+    bits = (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    bits = bits | np.where(np.signbit(x), np.uint16(0x8000), np.uint16(0))
+    return np.where(np.isnan(x), np.uint16(0x7FC0), bits).astype(np.uint16)
+
+
+def dequant_np(q, s) -> np.ndarray:
+    """MXFP4 matrix [N][K] to doubles: weight j of a row is the nibble j (low nibble first)
+    looked up in the 16-entry e2m1 table, times 2^(s[j/32] - 127) (NaN for s = 255)."""
+    q = np.asarray(q, np.uint8)
+    s = np.asarray(s, np.uint8)
+    N, KB = q.shape
+    tab = _e2m1_table()
+    pairs = np.stack([tab[np.arange(256) & 0xF], tab[np.arange(256) >> 4]], axis=1)  # byte -> (even, odd)
+    sc = np.ldexp(1.0, s.astype(np.int64) - 127)
+    sc = np.where(s == 255, np.nan, sc)
+    w = pairs[q].reshape(N, KB // 16, 32)
+    w *= sc[:, :, None]
+    return w.reshape(N, 2 * KB)
+
+
+def _roundtrip_rows(v: np.ndarray, actq: int) -> np.ndarray:
+    """MXFP8 (actq 1) or MXFP4 (actq 2) round trip of every row (blocks of 32 along the row)."""
+    if actq == 0:
+        return v
+    out = np.ascontiguousarray(v, np.float64).copy()
+    f = lib().k3o_mxfp8_roundtrip if actq == 1 else lib().k3o_mxfp4_roundtrip
+    f(out.ctypes.data, out.size)
+    return out
+
+
+def expert_rows(d, ex, z_bits, actq=0) -> np.ndarray:
+    """One expert (tensors ex, as the C statement takes them) on z rows (bf16 bits [n][L]):
+    o rows [n][L] (double). Same steps as k3o_expert_row: (MXFP8 / MXFP4 round trip of z),
+    g, u = G z, U z; a = bf16(silu(g) * u) (round trip of a); o = D a."""
+    L, I = d.latent, d.inter
+    zq = _roundtrip_rows(bf16_to_f64(z_bits), actq)
+    G = dequant(ex["gate_q"], ex["gate_s"], I, L)
+    g = zq @ G.T
+    G = dequant(ex["up_q"], ex["up_s"], I, L)
+    u = zq @ G.T
+    del G
+    with np.errstate(over="ignore"):  # exp(-g) = inf for very negative g: silu = -0, as in C
+        a = bf16_to_f64(bf16_from_f64_np(g / (1.0 + np.exp(-g)) * u))
+    a = _roundtrip_rows(a, actq)
+    return a @ dequant(ex["down_q"], ex["down_s"], L, I).T
+
+
+def _layer_np_tail(layer, xf, z, idx, w, nthreads, rows_fn=None):
+    """Given the step's tokens xf (double), z (bf16 bits), a selection idx and its weights w:
+    expert rows, combine and latent out. Returns (y bits, c bits, o double [T][k][L]).
+    rows_fn(e, z_rows) -> o rows replaces expert_rows (e.g. to run the experts elsewhere)."""
+    from concurrent.futures import ThreadPoolExecutor
+    d = layer.d
+    T, k = idx.shape
+    actq = layer.dims.actq
+    if rows_fn is None:
+        rows_fn = lambda e, zr: expert_rows(d, layer.experts[e], zr, actq)
+    o = np.zeros((T, k, d.latent), np.float64)
+
+    def run(e):
+        t, j = np.nonzero(idx == e)
+        o[t, j] = rows_fn(int(e), z[t])
+
+    with ThreadPoolExecutor(max(1, nthreads)) as pool:
+        list(pool.map(run, np.unique(idx)))
+    acc = np.zeros((T, d.latent), np.float64)
+    for j in range(k):  # slot order, as the scalar combine
+        acc += w[:, j:j + 1] * o[:, j]
+    c = bf16_from_f64_np(acc)
+    yd = bf16_to_f64(c) @ bf16_to_f64(layer.wo).T
+    if layer.shared is not None:
+        ns, si = layer.dims.n_shared, layer.dims.shared_inter
+        sg, su, sd = (bf16_to_f64(a) for a in layer.shared)
+        g, u = xf @ sg.T, xf @ su.T
+        with np.errstate(over="ignore"):
+            a = bf16_to_f64(bf16_from_f64_np(g / (1.0 + np.exp(-g)) * u))
+        for j in range(ns):  # each shared expert summed on its own, in expert order
+            yd += a[:, j * si:(j + 1) * si] @ sd[:, j * si:(j + 1) * si].T
+    return bf16_from_f64_np(yd), c, o
+
+
+def _layer_forward_np(layer, x, nthreads=8, idx=None, rows_fn=None):
+    """Layer.forward for many tokens (see Layer.forward_np)."""
+    if layer.dims.act != 0:
+        raise ValueError("oracle: unsupported activation")
+    d = layer.d
+    x = _c(x, np.uint16)
+    xf = bf16_to_f64(x)
+    lg = xf @ bf16_to_f64(layer.wr).T
+    if layer.bias is not None:
+        lg = lg + layer.bias.astype(np.float64)
+    sel = select_topk(lg, d.top_k) if idx is None else _c(idx, np.int32)
+    w = route_weights(lg, sel)
+    z = bf16_from_f64_np(xf @ bf16_to_f64(layer.wi).T)
+    y, c, o = _layer_np_tail(layer, xf, z, sel, w, nthreads, rows_fn)
+    return {"y": y, "idx": sel, "w": w, "logits": lg, "z": z, "c": c, "o": o}
+
+
+def _forward_np(self, x, nthreads=8, rows_fn=None):
+    """The whole layer for many tokens (batched statement): same outputs as forward().
+    rows_fn(e, z_rows) -> o rows: optional replacement of expert_rows for expert e."""
+    return _layer_forward_np(self, x, nthreads, rows_fn=rows_fn)
+
+
+def _forward_with_selection(self, x, idx, nthreads=8, rows_fn=None):
+    """The layer completed with a given expert selection idx [T][k] (ascending per token)
+    instead of its own top-k: weights from the oracle's logits at those experts, then every
+    later step as in forward(). For tokens whose k-th and (k+1)-th logits are too close for an
+    fp32 computation to order, checked elsewhere to be a valid selection."""
+    return _layer_forward_np(self, x, nthreads, idx=idx, rows_fn=rows_fn)
+
+
+Layer.forward_np = _forward_np
+Layer.forward_with_selection = _forward_with_selection

@@ -264,11 +264,10 @@ void k3o_dequant_row(const uint8_t* q_row, const uint8_t* s_row, int K, double* 
   }
 }
 
-/* Whole MXFP4 matrix [N][K] to doubles (row-major). */
+/* Whole MXFP4 matrix [N][K] to doubles (row-major), row by row. */
 void k3o_dequant(const uint8_t* q, const uint8_t* s, int N, int K, double* out) {
   for (int n = 0; n < N; ++n)
-    for (int j = 0; j < K; ++j)
-      out[(size_t)n * K + j] = k3o_mx_weight(q + (size_t)n * (K / 2), s + (size_t)n * (K / 32), j);
+    k3o_dequant_row(q + (size_t)n * (K / 2), s + (size_t)n * (K / 32), K, out + (size_t)n * K);
 }
 
 /* ------------------------------------------------------------------ sizes (pins) */

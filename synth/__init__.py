@@ -262,6 +262,7 @@ def host_expert(d: Dims, seed: int, e: int) -> dict:
     gate/up codes [I][L/2], scales [I][L/32]; down codes [L][I/2], scales [L][I/32]."""
     gq, gs, dq, ds = d.gate_q_bytes, d.gate_s_bytes, d.down_q_bytes, d.down_s_bytes
     I, L = d.inter, d.latent
+    e = int(e)  # a numpy int32 index would overflow in the byte offsets below
     return {
         "gate_q": host_bytes(seed, S_GATE_Q, e * gq, gq).reshape(I, L // 2),
         "gate_s": host_uniform_u8(seed, S_GATE_S, e * gs, gs, E8M0_LO, E8M0_HI).reshape(I, L // 32),

@@ -8,6 +8,7 @@ library computes is fed to the oracle.
 from __future__ import annotations
 
 import ctypes
+import os
 
 import numpy as np
 import torch
@@ -19,13 +20,30 @@ import synth
 DEV = torch.device("cuda:0")
 NAMES = oracle.ExpertTables.NAMES
 
-# Tolerances (layer outputs within relative L2 error 2e-3 of the oracle; indices bit-exact).
-# REL_L2 bounds the relative L2 error of a whole compared output (all compared tokens).
-# Per token the layer's four bf16 rounding points (z, GLU output, combine, y) turn a
-# one-fp32-ulp difference upstream into ~1e-3 of rounding noise on that token, so a single
-# token is held to the looser PER_TOKEN guard.
+# Tolerances. Indices and permutations: bit-exact. Layer outputs against the oracle:
+# - bf16 activations: the relative L2 error of the compared output (all compared tokens
+#   together) within REL_L2 = 2e-3; every token within PER_TOKEN_CAP[0], and above REL_L2 on at
+#   most PER_TOKEN_OVER_FRAC[0] of the tokens when 32 or more are compared.
+# - MXFP8 activations: every token within PER_TOKEN_CAP[1], above REL_L2 on at most
+#   PER_TOKEN_OVER_FRAC[1] of the tokens (at most one token when fewer than 20 are compared), and
+#   the compared output within REL_L2 when WHOLE_MIN_TOKENS[1] or more tokens are compared.
+# Why a per-token envelope: the layer has four bf16 rounding points (z, the GLU output, the
+# combine, y); an fp32 sum that lands across a bf16 rounding midpoint flips that element, and
+# the flip perturbs every later rounding point. A plain fp32 evaluation of the layer on the CPU
+# (fp32_layer.py) against the oracle shows this envelope (1024 K3 prefill tokens): bf16 mode
+# whole 9.9e-4, per token max 2.9e-3 with 7% of the tokens above 2e-3; MXFP8 mode whole
+# 1.5e-3, median 1.6e-6, 1.7% of the tokens above 2e-3 and a few near 1e-2 (max 2.2e-2): where
+# a straddle of z falls on an E4M3 rounding midpoint the element moves by a whole E4M3 step.
+# test_tolerance_reading.py re-runs the bf16 case as a CPU test. Narrow layers (latent < 1024,
+# the small test shapes) have fewer elements per token, so one straddle weighs more: the same
+# fp32 evaluation on 3000 tokens of each small test shape reaches 4.8e-3 per token in bf16 mode
+# (1.7e-2 in MXFP8 mode), hence PER_TOKEN_CAP_NARROW.
 REL_L2 = 2e-3
-PER_TOKEN = 5e-3
+PER_TOKEN_CAP = {0: 4e-3, 1: 3e-2}
+PER_TOKEN_CAP_NARROW = {0: 6e-3, 1: 3e-2}
+PER_TOKEN_OVER_FRAC = {0: 0.2, 1: 0.05}
+WHOLE_MIN_TOKENS = {0: 1, 1: 1024}
+# Expert rows (one (token, expert) pair, fp32 out, no later rounding point): REL_L2 per row.
 # fp32 logits against double logits: |dl| <= LOGIT_ATOL + LOGIT_RTOL * |l|
 LOGIT_ATOL, LOGIT_RTOL = 1e-4, 1e-4
 
@@ -60,6 +78,7 @@ class DeviceLayer:
         if host_fill is None:
             host_fill = E * d.expert_bytes < 64 << 20
         self.host_fill = host_fill
+        self._custom_experts = experts is not None
         self.t = {}
         if host_fill:
             wr, wi, wo = synth.host_dense(d, seed)
@@ -106,6 +125,14 @@ class DeviceLayer:
                                   self.t["w_in"].data_ptr(), self.t["w_out"].data_ptr(),
                                   *[self.t[n].data_ptr() for n in NAMES], *sp)
 
+    def rows_fn(self, actq=None):
+        """For K3-sized layers whose experts come from the seeded generator: the oracle's expert
+        rows computed in a process pool (oracle_pool); else None (in process)."""
+        if self.d.latent < 1024 or self.host_fill and self._custom_experts:
+            return None
+        import oracle_pool
+        return oracle_pool.rows_fn(self.d, self.seed, self.actq if actq is None else actq)
+
     def dense(self):
         if self.dense_host is None:
             self.dense_host = synth.host_dense(self.d, self.seed)
@@ -118,8 +145,14 @@ class DeviceLayer:
         return self._experts_host[e]
 
     def oracle(self, experts=None, actq=None):
-        ids = range(self.d.n_experts) if experts is None else experts
-        ex = {int(e): self.expert_host(int(e)) for e in ids}
+        ids = [int(e) for e in (range(self.d.n_experts) if experts is None else experts)]
+        missing = [e for e in ids if e not in self._experts_host]
+        if len(missing) > 8:  # the host generator releases the GIL: fill them in parallel
+            from concurrent.futures import ThreadPoolExecutor
+            with ThreadPoolExecutor(os.cpu_count() or 8) as pool:
+                for e, t in zip(missing, pool.map(lambda e: synth.host_expert(self.d, self.seed, e), missing)):
+                    self._experts_host[e] = t
+        ex = {e: self.expert_host(e) for e in ids}
         wr, wi, wo = self.dense()
         sh = None
         if self.shared is not None:
@@ -146,9 +179,15 @@ def rel_l2_rows(got: np.ndarray, want: np.ndarray) -> np.ndarray:
     return np.where(den > 0, num / np.where(den > 0, den, 1), num)
 
 
+def boundary_tol(logits: np.ndarray) -> np.ndarray:
+    """Per token: twice the fp32 logit error bound at that token's own largest logit."""
+    return 2 * (LOGIT_ATOL + LOGIT_RTOL * np.abs(logits).max(axis=1))
+
+
 def topk_gap_ambiguous(logits: np.ndarray, k: int, tol: np.ndarray | float) -> np.ndarray:
-    """Tokens whose k-th and (k+1)-th largest oracle logits are closer than tol: there the
-    selection at the boundary is decided below the precision of fp32 logits."""
+    """Tokens whose k-th and (k+1)-th largest oracle logits are closer than tol (per token or
+    one value): there the selection at the boundary is decided below the precision of fp32
+    logits."""
     srt = -np.sort(-logits, axis=1)
     if k >= logits.shape[1]:
         return np.zeros(logits.shape[0], bool)
@@ -163,3 +202,139 @@ def selection_valid(logits_row: np.ndarray, sel: np.ndarray, k: int, tol: float)
     if len(set(sel.tolist())) != k:
         return False
     return logits_row[mask].min() >= logits_row[~mask].max() - tol
+
+
+def check_layer_output(got: np.ndarray, want: np.ndarray, what: str = "layer", actq: int = 0,
+                       latent: int = 3584) -> np.ndarray:
+    """Layer outputs (rows = tokens, values as doubles) against the oracle's, by the rules above
+    for the activation mode actq and the layer's latent width. Returns the per-token errors."""
+    err = rel_l2_rows(got, want)
+    whole = np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300)
+    over = int((err > REL_L2).sum())
+    n = len(err)
+    print(f"{what}: rel L2 whole {whole:.3e}, per token median {np.median(err):.3e} max {err.max():.3e}, "
+          f"{over} of {n} tokens above {REL_L2}")
+    m = 1 if actq else 0
+    if n >= WHOLE_MIN_TOKENS[m]:
+        assert whole <= REL_L2, (what, whole)
+    cap = (PER_TOKEN_CAP if latent >= 1024 else PER_TOKEN_CAP_NARROW)[m]
+    assert err.max() <= cap, (what, err.max(), cap)
+    if m == 0 and n >= 32:
+        assert over <= PER_TOKEN_OVER_FRAC[0] * n, (what, over, n)
+    if m == 1:
+        assert over <= max(1, PER_TOKEN_OVER_FRAC[1] * n), (what, over, n)
+    return err
+
+
+def compare_layer(lay, x: np.ndarray, y: np.ndarray, idx: np.ndarray, sample, nthreads: int = 8,
+                  what: str = "layer"):
+    """The GPU's y and selection for the sampled tokens against the oracle.
+    Selections: bit-exact, except on tokens whose k-th and (k+1)-th oracle logits are closer than
+    the fp32 logit error (boundary ties), where the GPU's selection must be valid (no unselected
+    logit above a selected one by more than the tolerance). Outputs: the oracle computes every
+    token with its own selection, and each boundary-tie token whose selection differs a second
+    time with the GPU's selection (the oracle completed with it); both go through
+    check_layer_output. Returns (per-token errors, number of boundary-tie tokens)."""
+    d = lay.d
+    sample = np.asarray(sample)
+    xs, gi = x[sample], idx[sample]
+    rf = lay.rows_fn()
+    ol = lay.oracle(experts=set() if rf else set(np.unique(gi).tolist()) | _own_selection(lay, xs))
+    nthreads = 2 * nthreads if rf else nthreads
+    ref = ol.forward_np(xs, nthreads=nthreads, rows_fn=rf)
+    lg = ref["logits"]
+    tol = boundary_tol(lg)
+    amb = topk_gap_ambiguous(lg, d.top_k, tol)
+    same = np.all(gi == ref["idx"], axis=1)
+    assert np.all(same | amb), f"{int((~same & ~amb).sum())} tokens select other experts"
+    want = ref["y"].copy()
+    flipped = np.nonzero(~same)[0]
+    for t in flipped:
+        assert selection_valid(lg[t], gi[t], d.top_k, 2 * tol[t]), t
+    if len(flipped):
+        want[flipped] = ol.forward_with_selection(xs[flipped], gi[flipped], nthreads=nthreads, rows_fn=rf)["y"]
+    err = check_layer_output(bf16_np_bits(y[sample]), oracle.bf16_to_f64(want), what, lay.actq, d.latent)
+    return err, len(flipped)
+
+
+def _own_selection(lay, xs) -> set:
+    wr = lay.dense()[0]
+    return set(oracle.select_topk(oracle.router_logits_np(xs, wr, lay.bias_host), lay.d.top_k).ravel().tolist())
+
+
+def bf16_np_bits(a) -> np.ndarray:
+    """bf16 values given as uint16 bits or as doubles already -> doubles."""
+    a = np.asarray(a)
+    return oracle.bf16_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def run_layer(lay, x_np: np.ndarray, weights=None, dm=None, ws=None):
+    """k3moe_layer_forward on x (host bf16 bits): (y as doubles, topk_idx, topk_w), with the
+    workspace error word checked. ws: (tensor, bytes) to reuse, else one is allocated."""
+    d = lay.d
+    dm = dm or lay.dims
+    T = x_np.shape[0]
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device=DEV)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, d.top_k), dtype=torch.float32, device=DEV)
+    wsb, n = ws if ws is not None else workspace(dm, T)
+    xd = up(x_np)
+    k3.k3moe_layer_forward(dm, weights or lay.weights, xd.data_ptr(), T, y.data_ptr(), idx.data_ptr(), w.data_ptr(),
+                           wsb.data_ptr(), n, stream())
+    check_ok(wsb)
+    return bf16_np(y), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def check_selection(lay, x: np.ndarray, idx: np.ndarray) -> int:
+    """The GPU's top-k of every token against the oracle's selection on double logits:
+    bit-exact except boundary ties, where the selection must be valid. Returns the number of
+    boundary-tie tokens that selected differently."""
+    wr = lay.dense()[0]
+    lg = oracle.router_logits_np(x, wr, lay.bias_host)
+    ref = oracle.select_topk(lg, lay.d.top_k)
+    tol = boundary_tol(lg)
+    same = np.all(idx == ref, axis=1)
+    amb = topk_gap_ambiguous(lg, lay.d.top_k, tol)
+    assert np.all(same | amb), f"{int((~same & ~amb).sum())} tokens select other experts"
+    for t in np.nonzero(~same)[0]:
+        assert selection_valid(lg[t], idx[t], lay.d.top_k, 2 * tol[t]), t
+    assert np.all(np.diff(idx, axis=1) > 0)
+    return int((~same).sum())
+
+
+def check_permutation(d, idx: np.ndarray, ws=None):
+    """k3moe_permute of a selection against the oracle's counting sort of the same selection
+    (integer work on the same input: bit-exact). Returns the expert offsets."""
+    T = idx.shape[0]
+    dm = dims(d)
+    off = torch.empty(d.n_experts + 1, dtype=torch.int32, device=DEV)
+    rt, rs, sr = (torch.empty(T * d.top_k, dtype=torch.int32, device=DEV) for _ in range(3))
+    wsb, n = ws if ws is not None else workspace(dm, T)
+    idd = up(np.ascontiguousarray(idx, np.int32))
+    k3.k3moe_permute(dm, idd.data_ptr(), T, off.data_ptr(), rt.data_ptr(), rs.data_ptr(), sr.data_ptr(),
+                     wsb.data_ptr(), n, stream())
+    check_ok(wsb)
+    want = oracle.permute(idx, d.n_experts)
+    for g, r in zip((off, rt, rs, sr), want):
+        np.testing.assert_array_equal(g.cpu().numpy(), r)
+    return want[0]
+
+
+def check_rounding_straddles(got_bits: np.ndarray, exact: np.ndarray, mag: np.ndarray, rel: float = 2.0**-20):
+    """bf16 results of fp32 sums against the exact sums: every element must be the bf16 rounding
+    of some value within rel * mag of the exact sum (mag = the sum of |terms|, which bounds an
+    fp32 sum's error), i.e. lie between the roundings of exact - rel * mag and exact + rel * mag.
+    Elsewhere than near a rounding midpoint (or near zero) that interval holds one bf16 value,
+    the correctly rounded one. Returns the number of elements per row that differ from the
+    correctly rounded exact sums."""
+    dlt = rel * mag
+    g = oracle.bf16_to_f64(got_bits)
+    lo = oracle.bf16_to_f64(bf16_from_exact(exact - dlt))
+    hi = oracle.bf16_to_f64(bf16_from_exact(exact + dlt))
+    bad = ~((lo <= g) & (g <= hi))
+    assert not bad.any(), (int(bad.sum()), exact[bad][:4], g[bad][:4])
+    return (got_bits != bf16_from_exact(exact)).sum(axis=-1)
+
+
+def bf16_from_exact(v: np.ndarray) -> np.ndarray:
+    return oracle.bf16_from_f64_np(v)

@@ -136,12 +136,20 @@ k3moe_status k3moe_route(const k3moe_dims* dims, const uint16_t* x, int32_t T,
  * The first call on a device looks up the scratch's device address (once, with that device
  * current); make that first call before any stream capture. All calls share the one scratch
  * array: calls whose work can overlap on the GPU (different streams, or several host threads)
- * race on it and must be ordered by the caller. */
+ * race on it and must be ordered by the caller. The looked-up address is kept per device
+ * ordinal for the life of the process: calls after a cudaDeviceReset, or from a context other
+ * than the device's primary context, are not supported (the kept address belongs to the old
+ * context). With err_word = NULL a device-side fault is recorded only inside the scratch, where
+ * no call can read it: pass an err_word to see it. */
 k3moe_status k3moe_route_noalloc(const k3moe_dims* dims, const uint16_t* x, int32_t T,
                                  const uint16_t* w_router, const float* bias, int32_t* topk_idx,
                                  float* topk_w, uint32_t* err_word, void* stream);
 
-/* Token-by-expert permutation: histogram over experts, exclusive scan, stable scatter.
+/* Token-by-expert permutation: histogram over experts, exclusive scan, stable scatter. The
+ * pages route each token to 16 of 896 experts ("kimi-k3-mlx", Architecture table) and run each
+ * expert once over the rows routed to it; this call groups the (token, slot) pairs by expert so
+ * that an expert's weights are read once per step. Rows of one expert keep token order, so the
+ * result is deterministic and equals a two-pass counting sort.
  *   topk_idx [T][k] int32 in [0, E): each token's experts, distinct.
  *   expert_offsets [E+1] out: rows of expert e are [offsets[e], offsets[e+1]).
  *   row_token, row_slot [T*k] out: the (token, slot) behind sorted row r; rows of one
@@ -168,8 +176,10 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights*
                                     size_t ws_bytes, void* stream);
 
 /* Routing-weighted combine in latent space: c[t] = bf16(sum_{j<k} w[t][j] o_rows[slot_row[t*k+j]]),
- * summed in fp32 with j ascending. o_rows [T*k][L] fp32, slot_row [T*k], topk_w [T][k],
- * c [T][L] bf16 out. */
+ * summed in fp32 with j ascending ("kimi-k3-mlx", Architecture table and LatentMoE: the routed
+ * experts' outputs are mixed by the router's renormalised weights in the 3584-wide latent space,
+ * before the projection back to the residual). o_rows [T*k][L] fp32, slot_row [T*k],
+ * topk_w [T][k], c [T][L] bf16 out. */
 k3moe_status k3moe_combine(const k3moe_dims* dims, const float* o_rows, const int32_t* slot_row,
                            const float* topk_w, int32_t T, uint16_t* c, void* stream);
 
@@ -205,6 +215,14 @@ const char* k3moe_status_string(k3moe_status status);
  * usable and the next k3moe_check reports K3MOE_E_TIMEOUT (and clears the word). `ws` is a
  * device workspace of at least 256 bytes. Returns K3MOE_E_CUDA if the launch fails. */
 k3moe_status k3moe_selftest_timeout(void* ws, void* stream);
+
+/* Scheduling self test (diagnostic; no counterpart on the pages): enqueues n_ctas CTAs, each
+ * holding about 200 KB of shared memory (so no other large-shared-memory CTA fits beside it on
+ * its SM) while one thread waits on the wall clock for `ms` milliseconds; then they exit. It
+ * stands for other work that keeps SMs from the layer's kernels, e.g. on another stream.
+ * 1 <= n_ctas <= 4096, 1 <= ms <= 10000 (K3MOE_E_SHAPE otherwise); K3MOE_E_CUDA if the launch
+ * fails. */
+k3moe_status k3moe_selftest_occupy(int32_t n_ctas, int32_t ms, void* stream);
 
 /* Diagnostic per-kernel timing of k3moe_layer_forward (not needed for normal use; no
  * counterpart on the pages). mode = 1 starts recording: every kernel launch of later

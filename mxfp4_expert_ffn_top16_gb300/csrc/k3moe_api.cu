@@ -91,7 +91,7 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
     L.bs = take(P * rows * (size_t)exp_pitch(d.latent));
     L.aq = take(P * rows * I);
     L.aqs = take(P * rows * (size_t)exp_pitch(d.inter));
-    L.chunk_done = take((size_t)plan_chunks_max(d, T) * 4);
+    L.chunk_done = take((size_t)decode_counters(d, T) * 4);
   }
   L.total = off;
   return L;
@@ -222,7 +222,7 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
       if (!z_rows_ready) {
         ProfScope p(P_QUANT, s);
         K3_CUDA(launch_quant_rows(z, nullptr, T, T, d.latent, P, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs),
-                                  cnt, plan_chunks_max(d, T), err, s));
+                                  cnt, decode_counters(d, T), err, s));
       }
       const bool both = d.latent % 256 == 0;
       {
@@ -271,7 +271,7 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
                                     at<int32_t>(ws, L.row_slot), at<int32_t>(ws, L.slot_row),
                                     at<int32_t>(ws, L.plan), at<int>(ws, L.route_done),
                                     umma_expert_ok(d) ? at<int>(ws, L.chunk_done) : nullptr,
-                                    umma_expert_ok(d) ? plan_chunks_max(d, T) : 0, err, s));
+                                    umma_expert_ok(d) ? decode_counters(d, T) : 0, err, s));
   } else {
     {
       ProfScope p(P_TOPK, s);
@@ -553,6 +553,33 @@ k3moe_status k3moe_selftest_timeout(void* ws, void* stream) {
   if (!ws) return K3MOE_E_WORKSPACE;
   if (misaligned(ws)) return K3MOE_E_ALIGN;
   wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint32_t*>(ws));
+  return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_E_CUDA;
+}
+
+}  // extern "C"
+
+namespace k3moe {
+namespace {
+// One thread per CTA waits on the wall clock until `ns` nanoseconds have passed and returns; the
+// CTA's dynamic shared memory (most of an SM's) keeps other large-shared-memory CTAs off its SM.
+__global__ void occupy_kernel(unsigned long long ns) {
+  extern __shared__ uint8_t occupy_smem[];
+  if (threadIdx.x != 0) return;
+  const unsigned long long t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) __nanosleep(100000);
+  occupy_smem[0] = 0;
+}
+constexpr size_t kOccupySmem = 200 * 1024;
+}  // namespace
+}  // namespace k3moe
+
+extern "C" {
+
+k3moe_status k3moe_selftest_occupy(int32_t n_ctas, int32_t ms, void* stream) {
+  if (n_ctas < 1 || n_ctas > 4096 || ms < 1 || ms > 10000) return K3MOE_E_SHAPE;
+  if (ensure_smem_attr(reinterpret_cast<const void*>(occupy_kernel), kOccupySmem) != cudaSuccess)
+    return K3MOE_E_CUDA;
+  occupy_kernel<<<n_ctas, 32, kOccupySmem, static_cast<cudaStream_t>(stream)>>>(1000000ull * (unsigned)ms);
   return cudaGetLastError() == cudaSuccess ? K3MOE_OK : K3MOE_E_CUDA;
 }
 

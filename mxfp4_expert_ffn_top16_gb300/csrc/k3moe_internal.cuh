@@ -166,7 +166,9 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s);
 // Decode (T < kUmmaExpertMinTokens): the same GEMMs with the weights on the MMA's N side (256
 // weight rows per MMA, 8-row chunks): the GLU pass, and with_down (needs latent % 256 == 0) the
-// down pass in the same launch. chunk_done: plan_chunks_max ints, zero at launch.
+// down pass in the same launch. chunk_done: decode_counters ints, zero at launch (GLU items
+// finished per chunk, then the kernel's item counter); the kernel leaves them non-zero, the next
+// routing or row-quantisation launch clears them.
 // zq / zqs: the latent activations as P E4M3 rows per token [T][P][L] with e8m0 scales
 // [T][P][exp_pitch(L)]; the kernel gathers a chunk's rows through row_token.
 cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* zq,
@@ -176,6 +178,8 @@ cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t*
 inline int plan_chunks_max(const k3moe_dims& d, long long T) {
   return (int)(T * d.top_k / kGemvTokens + d.n_experts + 1);
 }
+// Counters of the decode expert kernel in the workspace: one per chunk, then its item counter.
+inline int decode_counters(const k3moe_dims& d, long long T) { return plan_chunks_max(d, T) + 1; }
 // a[i] = bf16(silu(g[i]) * u[i]) for n elements (the shared experts' GLU, fp32 in).
 cudaError_t launch_glu(const float* g, const float* u, long long n, uint16_t* a, cudaStream_t s);
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,

@@ -24,13 +24,17 @@
 // lane of the converged warp). One 256-column accumulator per item; warps 4 and 8 (tensor-memory
 // lanes 0..31) each drain half its columns, add the hi and lo rows, and run the epilogue.
 //
-// One launch can run both passes: the GLU items, then the down items, dealt round-robin over
-// persistent CTAs in that order, so an SM that has no third GLU item starts on down items while
-// the others finish theirs. A down item needs the GLU output of its whole chunk: each epilogue
-// warp counts its finished GLU items per chunk in global memory (release), and the down item's
-// loaders wait (acquire, bounded) until the chunk is complete before reading its activations.
-// Every CTA runs its GLU items before any down item, and all CTAs are resident at once (one per
-// SM, grid <= SMs), so every awaited GLU item is running or done and the waits end.
+// One launch can run both passes: the GLU items, then the down items. Persistent CTAs claim
+// items from a global counter in that order (the loading thread claims, and passes each claimed
+// item to the CTA's other roles through a small shared-memory queue), so an SM that has no third
+// GLU item starts on down items while the others finish theirs. A down item needs the GLU output
+// of its whole chunk: each epilogue warp counts its finished GLU items per chunk in global memory
+// (release), and the down item's loaders wait (acquire, bounded) until the chunk is complete
+// before reading its activations. A down item is claimed only after every GLU item has been
+// claimed, and only running CTAs claim, each running its items in claim order (holding at most
+// one claimed item ahead): every awaited GLU item is therefore running, done or held behind a GLU
+// item, and the waits end, however many of the grid's CTAs the GPU can hold at once (other work
+// on the GPU may keep some of them from starting at all).
 #include <cuda_fp16.h>
 
 #include "k3moe_device.cuh"
@@ -78,8 +82,29 @@ struct UWnArgs {
   uint8_t* aqs;        //   its scales [P*rows][exp_pitch(inter)]
   float* o_out;        // down output [rows][latent] fp32
   int* chunk_done;     // GLU items finished per chunk, times 2 (one count per epilogue warp); zeroed
+  int* item_counter;   // items claimed so far; zeroed
   uint32_t* err;
 };
+
+constexpr int kQ = 4;  // claimed items in flight from the loading thread to the other roles
+// Roles that take each claimed item from the queue: gather warps 2 and 3, the MMA warp and the
+// two epilogue warps.
+constexpr int kQConsumers = 5;
+
+// Takes the next claimed item from the queue (whole warp): the item, -1 once the items are
+// exhausted, -2 if a wait gave up.
+__device__ __forceinline__ int queue_pop(uint64_t* qfull, uint64_t* qempty, const int* qitem, int& qs,
+                                         uint32_t& qph, volatile int* abort, uint32_t* err) {
+  if (!mbar_wait_warp(&qfull[qs], qph, abort, err)) return -2;
+  int u = 0;
+  if ((threadIdx.x & 31) == 0) {
+    u = qitem[qs];
+    mbar_arrive(&qempty[qs]);
+  }
+  u = __shfl_sync(0xffffffffu, u, 0);
+  if (++qs == kQ) { qs = 0; qph ^= 1; }
+  return u;
+}
 
 // Waits (bounded) until the chunk's GLU output is complete; acquire, then the async proxy may
 // read it.
@@ -171,7 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
   uint64_t* accf = empty + kStages;
   uint64_t* acce = accf + 1;
   uint64_t* drain = acce + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* qfull = drain + 1;
+  uint64_t* qempty = qfull + kQ;
+  int* qitem = reinterpret_cast<int*>(qempty + kQ);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qitem + kQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,6 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     mbar_init(accf, 1);
     mbar_init(acce, 2);
     mbar_init(drain, 1);
+    for (int q = 0; q < kQ; ++q) {
+      mbar_init(&qfull[q], 1);
+      mbar_init(&qempty[q], kQConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -225,12 +257,24 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     return ok;
   };
 
-  if (warp == 0) {  // ---------------- tile loads
+  if (warp == 0) {  // ---------------- item claims and tile loads
     if (lane == 0) {
-      int s = 0;
-      uint32_t ph = 0;
+      int s = 0, qs = 0;
+      uint32_t ph = 0, qph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+      // One claim ahead: the next item is claimed before this one's loads are issued, so the
+      // claim's round trip overlaps them. A CTA holds at most one unstarted item, claimed after
+      // its current one: a held GLU item sits behind a GLU item, which never waits, so every
+      // claimed GLU item still gets run.
+      int next = atomicAdd(A.item_counter, 1);
+      while (ok) {
+        const int u = next < items ? next : -1;
+        if (!mbar_wait_bounded(&qempty[qs], qph ^ 1, abort_flag, A.err)) break;
+        qitem[qs] = u;
+        mbar_arrive(&qfull[qs]);
+        if (++qs == kQ) { qs = 0; qph ^= 1; }
+        if (u < 0) break;
+        next = atomicAdd(A.item_counter, 1);
         Item it;
         if (!item_of(u, it)) atomicOr(A.err, kErrIndex);
         const WnPass& W = A.pass[it.glu ? 0 : 1];
@@ -260,10 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     // MMA reads (16-byte unit j of row m at unit j ^ (m & 7)); rows past the chunk are left out.
     const bool w2 = warp == 2;
     const int gl = lane + (w2 ? 0 : 32);  // 0..63 over the two warps
-    int s = 0;
-    uint32_t ph = 0;
+    int s = 0, qs = 0;
+    uint32_t ph = 0, qph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+    while (ok) {
+      const int u = queue_pop(qfull, qempty, qitem, qs, qph, abort_flag, A.err);
+      if (u < 0) break;
       Item it;
       item_of(u, it);
       const WnPass& W = A.pass[it.glu ? 0 : 1];
@@ -321,10 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // nothing lands after the block has gone
   } else if (warp == 1) {  // ---------------- MMA issue (converged warp, one elected lane)
-    int s = 0;
-    uint32_t ph = 0, aph = 0;
+    int s = 0, qs = 0;
+    uint32_t ph = 0, aph = 0, qph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
+    while (ok) {
+      const int u = queue_pop(qfull, qempty, qitem, qs, qph, abort_flag, A.err);
+      if (u < 0) break;
       const int nk = A.pass[u < items_g ? 0 : 1].K / BKE;
       if (!mbar_wait_warp(acce, aph ^ 1, abort_flag, A.err)) { ok = false; break; }
       for (int kc = 0; kc < nk; ++kc) {
@@ -363,8 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
     // row n of the item. This warp takes columns [h * 128, h * 128 + 128): for the GLU the gate
     // columns of its 64 features and the matching up columns.
     const int h = warp == kEpiWarp1 ? 1 : 0;
-    uint32_t aph = 0;
-    for (int u = blockIdx.x; u < items; u += gridDim.x) {
+    int qs = 0;
+    uint32_t aph = 0, qph = 0;
+    for (;;) {
+      const int u = queue_pop(qfull, qempty, qitem, qs, qph, abort_flag, A.err);
+      if (u < 0) break;
       Item it;
       item_of(u, it);
       if (!mbar_wait_warp(accf, aph, abort_flag, A.err)) break;
@@ -439,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
   }
 }
 
-constexpr size_t kSmem = 1024 + (size_t)kStages * (kBTile + kATile + kStgBytes) + (2 * kStages + 3) * 8 + 16;
+constexpr size_t kSmem = 1024 + (size_t)kStages * (kBTile + kATile + kStgBytes) + (2 * kStages + 3 + 2 * kQ) * 8 +
+                         kQ * 4 + 16;
 static_assert((size_t)kStages * kATile + kBTile >= (size_t)(kStages - 1) * kATile + kMA * BKE,
               "an MMA's 128-row read of the last activation tile stays inside shared memory");
 static_assert(kATile % 1024 == 0 && (kStages * kATile) % 1024 == 0, "128-byte swizzle alignment");
@@ -449,7 +501,7 @@ template <int P>
 cudaError_t launch_t(UWnArgs& a, int items_max, cudaStream_t s) {
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_wn_kernel<P>), kSmem);
   if (e != cudaSuccess) return e;
-  int grid = num_sms();  // one CTA per SM (the shared memory allows no second): all resident
+  int grid = num_sms();  // one CTA per SM (the shared memory allows no second)
   if (items_max < grid) grid = items_max > 0 ? items_max : 1;
   return launch_pdl(umma_wn_kernel<P>, dim3(grid), dim3(kThreads), kSmem, s, a);
 }
@@ -486,6 +538,7 @@ cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t*
   }
   A.plan = plan; A.row_token = row_token; A.ntok = T; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.o_out = o_rows; A.chunk_done = chunk_done; A.err = err;
+  A.item_counter = chunk_done + plan_chunks_max(d, T);
   return P == 1 ? launch_t<1>(A, items_max, s) : launch_t<2>(A, items_max, s);
 }
 

@@ -122,3 +122,9 @@ def test_layer_stats_arguments(L):
     assert L.k3moe_layer_stats(ctypes.byref(dims()), 0, good, 1 << 30, None, ctypes.byref(out),
                                ctypes.byref(eb)) == 0
     assert out.value == 0 and eb.value == 0
+
+
+def test_selftest_occupy_arguments(L):
+    """Out-of-range requests are refused before anything is launched (no GPU needed)."""
+    for n, ms in ((0, 10), (5000, 10), (4, 0), (4, 10001)):
+        assert L.k3moe_selftest_occupy(n, ms, None) == 2

@@ -233,10 +233,13 @@ def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads,
         lay.expert_row(e, z_all[t])
         oracle.dense_proj(wo[j * H_sl:(j + 1) * H_sl], z_all[t:t + 1])
 
+    def step_units(s):
+        """The units of step s: exactly units_per_step of them, cycling through the sample."""
+        n = len(units)
+        return [units[(s * units_per_step + i) % n] for i in range(units_per_step)]
+
     def run_step(s):
-        us = units[(s * units_per_step) % len(units):][:units_per_step]
-        if len(us) < units_per_step:
-            us = us + units[: units_per_step - len(us)]
+        us = step_units(s)
         ths = [threading.Thread(target=lambda grp=us[i::nthreads]: [run_unit(u) for u in grp])
                for i in range(min(nthreads, len(us)))]
         for th in ths:
@@ -244,6 +247,7 @@ def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads,
         for th in ths:
             th.join()
 
+    run_step.units = step_units
     return lay, run_step
 
 
@@ -255,7 +259,7 @@ def run_reference(args, w):
     import synth
     nth = os.cpu_count() or 1
     d = w.dims
-    T = min(w.tokens, 64)
+    T = min(w.x_count, 64)  # sample tokens (decode_b1 draws them from its 1000 fresh tokens)
     x = synth.host_x(w, 0, T)
     import oracle
     wr, _, _ = synth.host_dense(d, 0)
@@ -277,11 +281,11 @@ def run_reference(args, w):
         step(args.warmup + s)
     el = time.perf_counter() - t0
     nl = max(1, int(getattr(w, "layers", 1) or 1))
-    tokens = args.steps * units / d.top_k
+    tokens = args.steps * units / d.top_k  # every step runs exactly `units` units
     val = tokens / el / nl  # through the whole stack of layers
     sample = (f"{units} (token, expert-slot) units per step = {units / d.top_k:.3g} tokens through one "
-              f"layer of the {w.name} workload (expert row + 1/{d.top_k} of the token's dense rows each; "
-              f"tokens/s divided by its {nl} layer(s))")
+              f"layer of the {w.name} workload, cycling over the {T * d.top_k} units of {T} sample tokens "
+              f"(expert row + 1/{d.top_k} of the token's dense rows each; tokens/s divided by its {nl} layer(s))")
     out = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",

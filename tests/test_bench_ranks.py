@@ -57,3 +57,29 @@ def test_reference_arm_nonzero_rank_exits_without_work():
                         "--warmup", "3"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_cpu_sample_steps_run_exactly_their_units():
+    """The oracle sample that the reference arm and the cpu_baseline time: every step runs
+    exactly units_per_step (token, slot) units, cycling through the sample when it is smaller,
+    so the throughput counts the work that actually ran."""
+    import numpy as np
+    import oracle
+    import synth
+    w = synth.WORKLOADS["tiny"]
+    d = w.dims
+    x = synth.host_x(w, 0, 3)
+    wr, _, _ = synth.host_dense(d, 0)
+    idx = oracle.select_topk(oracle.router_logits_np(x, wr, None), d.top_k)  # 3 tokens x 4 slots = 12 units
+    for per_step in (5, 12, 50):
+        lay, step = bench.cpu_sample(w, 0, x, idx, per_step, 4, 2)
+        calls = []
+        real = lay.expert_row
+        lay.expert_row = lambda e, z: (calls.append(e), real(e, z))[1]
+        for s in range(3):
+            assert len(step.units(s)) == per_step
+            step(s)
+        assert len(calls) == 3 * per_step
+        flat = [u for s in range(3) for u in step.units(s)]
+        n = len(idx.ravel())
+        assert [u[2] for u in flat] == [int(idx.ravel()[i % n]) for i in range(3 * per_step)]

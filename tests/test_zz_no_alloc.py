@@ -12,8 +12,9 @@ import pytest
 import torch
 
 import mxfp4_expert_ffn_top16_gb300 as k3
+import oracle
 import synth
-from k3help import DEV, LOGIT_RTOL, stream, up
+from k3help import DEV, LOGIT_RTOL, boundary_tol, selection_valid, stream, topk_gap_ambiguous, up
 
 pytestmark = pytest.mark.gpu
 
@@ -62,6 +63,16 @@ def test_route_noalloc_matches_route_on_consecutive_calls():
         np.testing.assert_allclose(got_w, want_w, rtol=LOGIT_RTOL, atol=0)
         if call < 2:
             assert int(err.item()) == 0
+        # and against the oracle (double logits, brute-force top-k): bit-exact except tokens
+        # whose k-th and (k+1)-th logits tie within the fp32 error, which must select validly
+        ref_lg = oracle.router_logits_np(x, wr, None if b is None else bias)
+        ref_idx = oracle.select_topk(ref_lg, K)
+        tol = boundary_tol(ref_lg)
+        same = np.all(got_idx == ref_idx, axis=1)
+        assert np.all(same | topk_gap_ambiguous(ref_lg, K, tol))
+        for t in np.nonzero(~same)[0]:
+            assert selection_valid(ref_lg[t], got_idx[t], K, 2 * tol[t])
+        np.testing.assert_allclose(got_w[same], oracle.route_weights(ref_lg, ref_idx)[same], rtol=5e-4, atol=1e-6)
 
 
 def test_route_noalloc_rejects_requests_beyond_its_scratch():

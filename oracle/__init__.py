@@ -90,6 +90,7 @@ def lib():
         L.k3o_layer_forward.argtypes = [p, p, p, i, p, p, p, p, p, p, i]
         L.k3o_layer_forward.restype = i
         L.k3o_max_threads.restype = i
+        L.k3o_saliency_accumulate.argtypes = [p, i, p, p, p, p]
         _lib = L
     return _lib
 
@@ -508,3 +509,25 @@ def _forward_with_selection(self, x, idx, nthreads=8, rows_fn=None):
 
 Layer.forward_np = _forward_np
 Layer.forward_with_selection = _forward_with_selection
+
+
+# ------------------------------------------------------------------ REAP saliency
+def saliency_accumulate(d, idx, w, o, S=None) -> np.ndarray:
+    """k3o_saliency_accumulate: S[e] += w[t][j] * ||o[t][j]||_2 over every (t, j) with
+    idx[t][j] = e ("kimi-k3-mlx" digest, REAP pruning: S_j = (1/|C|) sum_x g_j(x) ||e_j(x)||_2;
+    the caller divides by |C|). idx [T][k], w [T][k] double, o [T][k][L] double."""
+    idx, w, o = _c(idx, np.int32), _c(w, np.float64), _c(o, np.float64)
+    T = idx.shape[0]
+    S = np.zeros(d.n_experts, np.float64) if S is None else S
+    assert S.dtype == np.float64 and S.flags.c_contiguous
+    lib().k3o_saliency_accumulate(ctypes.byref(make_dims(d)), T, idx.ctypes.data, w.ctypes.data, o.ctypes.data,
+                                  S.ctypes.data)
+    return S
+
+
+def saliency(layer, x, nthreads=8, rows_fn=None) -> np.ndarray:
+    """REAP saliency of every expert over the tokens x taken as the calibration set C:
+    S_j = (1/|C|) sum_x g_j(x) ||e_j(x)||_2, from the layer's own selection, weights and
+    expert outputs."""
+    ref = layer.forward_np(x, nthreads=nthreads, rows_fn=rows_fn)
+    return saliency_accumulate(layer.d, ref["idx"], ref["w"], ref["o"]) / x.shape[0]

@@ -526,6 +526,25 @@ int k3o_layer_forward(const k3o_dims* d, const k3o_weights* w, const uint16_t* x
   return bad ? -1 : 0;
 }
 
+/* REAP saliency ("kimi-k3-mlx" digest, REAP pruning section): S_j = (1/|C|) sum over the
+ * calibration tokens x of g_j(x) * ||e_j(x)||_2, the router's weight for expert j times the
+ * norm of that expert's output, averaged over the |C| tokens (g_j(x) = 0 where x does not
+ * select j). Reading taken: g_j is the renormalised routing weight the combine uses, e_j(x) the
+ * expert's output row in the latent space (o before the combine). This adds the sums of one
+ * step to S[E]: for each token t and slot j, S[idx[t][j]] += w[t][j] * sqrt(sum_n o[t][j][n]^2);
+ * the caller divides by the number of calibration tokens. o is [T][k][L] in slot order. */
+void k3o_saliency_accumulate(const k3o_dims* d, int T, const int32_t* idx, const double* w, const double* o,
+                             double* S) {
+  const int k = d->top_k, L = d->latent;
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      const double* row = o + ((size_t)t * k + j) * (size_t)L;
+      double ss = 0.0;
+      for (int n = 0; n < L; ++n) ss += row[n] * row[n];
+      S[idx[(size_t)t * k + j]] += w[(size_t)t * k + j] * sqrt(ss);
+    }
+}
+
 int k3o_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

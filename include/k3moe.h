@@ -106,8 +106,9 @@ typedef struct k3moe_weights {
 } k3moe_weights;
 
 /* Bytes of device workspace that every call below needs for up to `max_tokens` tokens.
- * The workspace is caller-owned scratch; its first 256 bytes hold the device error word.
- * Zero it once after allocation (cudaMemset) so the error word starts clear. */
+ * The workspace is caller-owned scratch; its first 256 bytes hold the device error word and a
+ * counter the routing kernels return to zero after each launch. Zero it once after allocation
+ * (cudaMemset); after that calls with any token count up to max_tokens may share it. */
 k3moe_status k3moe_workspace_size(const k3moe_dims* dims, int32_t max_tokens, size_t* bytes);
 
 /* Router scores and top-k ("kimi-k3-mlx", Architecture table: 896 experts, top-16).
@@ -204,6 +205,20 @@ k3moe_status k3moe_check(void* ws, void* stream);
  * pointers; K3MOE_E_CUDA if the stream reported an error. */
 k3moe_status k3moe_layer_stats(const k3moe_dims* dims, int32_t T, void* ws, size_t ws_bytes, void* stream,
                                int32_t* distinct, int64_t* expert_bytes);
+
+/* REAP saliency accumulation ("kimi-k3-mlx" digest, REAP pruning section: expert j's saliency
+ * S_j = (1/|C|) sum over calibration tokens x of g_j(x) * ||e_j(x)||_2). After
+ * k3moe_layer_forward on T tokens with this workspace, adds w[t][j] * ||o_tj||_2 to
+ * saliency[e] for every token t and slot j of that step, e = topk_idx[t][j], where o_tj is the
+ * expert's fp32 output row in the latent space (before the combine) and w the renormalised
+ * routing weight. Dividing the accumulated sums by the number of tokens gives S_j.
+ *   topk_idx [T][k], topk_w [T][k]: the routing the layer call returned through topk_idx_out /
+ *   topk_w_out, or NULL for the workspace's own copies (valid when that call passed NULL).
+ *   saliency [E] fp64, device, accumulated into; fp64 atomic adds, so the order of the
+ *   additions (and the last bits of the sums) varies between runs.
+ * Reads the step's expert rows from the workspace: call it before the workspace is reused. */
+k3moe_status k3moe_layer_saliency(const k3moe_dims* dims, int32_t T, const int32_t* topk_idx, const float* topk_w,
+                                  void* ws, size_t ws_bytes, double* saliency, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* k3moe_status_string(k3moe_status status);

@@ -37,7 +37,7 @@ K3MOE_OK = 0
 EXPORTS = ["k3moe_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_project",
            "k3moe_expert_ffn_mxfp4", "k3moe_combine", "k3moe_layer_forward", "k3moe_check",
            "k3moe_status_string", "k3moe_profile", "k3moe_profile_name", "k3moe_route_noalloc",
-           "k3moe_layer_stats", "k3moe_selftest_timeout", "k3moe_selftest_occupy"]
+           "k3moe_layer_stats", "k3moe_selftest_timeout", "k3moe_selftest_occupy", "k3moe_layer_saliency"]
 
 
 def _newer(target: str, deps) -> bool:
@@ -106,6 +106,7 @@ def lib():
             "k3moe_layer_stats": [p, i32, p, sz, p, p, p],
             "k3moe_selftest_timeout": [p, p],
             "k3moe_selftest_occupy": [i32, i32, p],
+            "k3moe_layer_saliency": [p, i32, p, p, p, sz, p, p],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -203,6 +204,12 @@ def k3moe_layer_stats(dims, T, ws, ws_bytes, stream=0):
 def k3moe_selftest_timeout(ws, stream=0):
     """Enqueues the failure-path self test (a bounded wait that runs out, about 2 s)."""
     return _ck(lib().k3moe_selftest_timeout(ws, stream), "k3moe_selftest_timeout", True)
+
+
+def k3moe_layer_saliency(dims, T, topk_idx, topk_w, ws, ws_bytes, saliency, stream=0, check=True):
+    """Adds the last layer step's REAP saliency sums (w * ||o||_2 per expert) to saliency [E] fp64."""
+    return _ck(lib().k3moe_layer_saliency(_ref(dims), T, topk_idx, topk_w, ws, ws_bytes, saliency, stream),
+               "k3moe_layer_saliency", check)
 
 
 def k3moe_selftest_occupy(n_ctas, ms, stream=0):

@@ -78,7 +78,9 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.o = take(rows * Lw * 4);
   L.c = take(Tt * Lw * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
-  L.route_done = take(4);
+  // the routing kernel's count of finished blocks must read zero at every launch, whatever T
+  // the previous call on this workspace had: it sits in the fixed header, after the error word
+  L.route_done = L.err + 4;
   {  // shared experts: gate and up (fp32), GLU output (bf16) [T][S]
     const size_t S = (size_t)d.n_shared * (size_t)d.shared_inter;
     L.sg = take(Tt * S * 4);
@@ -465,6 +467,23 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
                          nullptr, 0, at<uint16_t>(ws, L.c), T, d.latent, err, s, nullptr, nullptr, 0, nullptr,
                          S > 0 ? w.w_shared_down : nullptr, S > 0 ? at<uint16_t>(ws, L.sa) : nullptr, S));
   }
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_layer_saliency(const k3moe_dims* dims, int32_t T, const int32_t* topk_idx, const float* topk_w,
+                                  void* ws, size_t ws_bytes, double* saliency, void* stream) {
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  if (T < 0) return K3MOE_E_SHAPE;
+  if (!saliency) return K3MOE_E_NULL;
+  if (misaligned(topk_idx) || misaligned(topk_w) || misaligned(saliency)) return K3MOE_E_ALIGN;
+  K3_TRY(check_ws(d, T, ws, ws_bytes));
+  if (T == 0) return K3MOE_OK;
+  const WsLayout L = ws_layout(d, T);
+  K3_CUDA(launch_saliency(at<float>(ws, L.o), at<int32_t>(ws, L.row_token), at<int32_t>(ws, L.row_slot),
+                          topk_idx ? topk_idx : at<int32_t>(ws, L.idx), topk_w ? topk_w : at<float>(ws, L.wts), T,
+                          d.top_k, d.latent, d.n_experts, saliency, at<uint32_t>(ws, L.err),
+                          static_cast<cudaStream_t>(stream)));
   return K3MOE_OK;
 }
 

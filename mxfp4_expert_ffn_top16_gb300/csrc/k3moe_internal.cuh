@@ -49,7 +49,7 @@ struct WsLayout {
   size_t o;             // fp32 expert outputs per sorted row
   size_t c;             // bf16 combined latent
   size_t perm;          // int32 per-block histograms of the multi-block permutation
-  size_t route_done;    // int: top-k blocks finished (a few tokens); back to zero after each launch
+  size_t route_done;    // int in the header: top-k blocks finished (a few tokens); back to zero after each launch
   size_t sg, su, sa;    // shared experts: gate, up (fp32) and GLU output (bf16) [T][S]
   // block-scaled tensor-core expert path (only when umma_expert_ok): per sorted row, P e4m3
   // rows of z and of the GLU output with e8m0 scales per 32 (row pitch exp_pitch bytes)
@@ -184,6 +184,10 @@ inline int decode_counters(const k3moe_dims& d, long long T) { return plan_chunk
 cudaError_t launch_glu(const float* g, const float* u, long long n, uint16_t* a, cudaStream_t s);
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s);
+// S[idx[t][j]] += w[t][j] * ||o_rows[r]||_2 for every sorted row r of (t, j) (fp64 atomics).
+cudaError_t launch_saliency(const float* o_rows, const int32_t* row_token, const int32_t* row_slot,
+                            const int32_t* idx, const float* w, int T, int k, int L, int E, double* S,
+                            uint32_t* err, cudaStream_t s);
 
 int num_sms();
 

@@ -98,7 +98,56 @@ __global__ void act_prep_kernel(const uint16_t* __restrict__ z, int T, int L, in
   }
 }
 
+// REAP saliency ("kimi-k3-mlx" digest, REAP pruning section: S_j = (1/|C|) sum_x g_j(x)
+// ||e_j(x)||_2): one warp per sorted row r (token t, slot j, expert e = idx[t][j]) adds
+// w[t][j] * ||o[r]||_2 to S[e]. The squares are summed in fp32 (four per lane per 16-byte load,
+// then across the warp), the product and the sum over rows in fp64 (atomic adds, in no fixed
+// order).
+__global__ void __launch_bounds__(256) saliency_kernel(const float* __restrict__ o, const int32_t* __restrict__ row_token,
+                                                       const int32_t* __restrict__ row_slot,
+                                                       const int32_t* __restrict__ idx, const float* __restrict__ w,
+                                                       int rows, int T, int k, int L, int E, double* S, uint32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += nw) {
+    const float4* row = reinterpret_cast<const float4*>(o + (size_t)r * L);
+    float ss = 0.f;
+    for (int n = lane; n < L / 4; n += 32) {
+      const float4 v = __ldcs(row + n);
+      ss = fmaf(v.x, v.x, ss);
+      ss = fmaf(v.y, v.y, ss);
+      ss = fmaf(v.z, v.z, ss);
+      ss = fmaf(v.w, v.w, ss);
+    }
+#pragma unroll
+    for (int x = 16; x > 0; x >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, x);
+    if (lane == 0) {
+      const int t = row_token[r], j = row_slot[r];
+      const int e = (t >= 0 && t < T && j >= 0 && j < k) ? idx[(size_t)t * k + j] : -1;
+      if (e < 0 || e >= E) {
+        atomicOr(err, kErrIndex);
+      } else {
+        atomicAdd(S + e, (double)w[(size_t)t * k + j] * sqrt((double)ss));
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_saliency(const float* o_rows, const int32_t* row_token, const int32_t* row_slot,
+                            const int32_t* idx, const float* w, int T, int k, int L, int E, double* S,
+                            uint32_t* err, cudaStream_t s) {
+  const long long rows = (long long)T * k;
+  if (rows <= 0) return cudaSuccess;
+  if (L % 4) return cudaErrorInvalidValue;
+  long long blocks = (rows + 7) / 8;
+  if (blocks > 16LL * num_sms()) blocks = 16LL * num_sms();
+  return launch_pdl(saliency_kernel, dim3((unsigned)blocks), dim3(256), 0, s, o_rows, row_token, row_slot, idx, w,
+                    (int)rows, T, k, L, E, S, err);
+}
 
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s) {

@@ -128,3 +128,15 @@ def test_selftest_occupy_arguments(L):
     """Out-of-range requests are refused before anything is launched (no GPU needed)."""
     for n, ms in ((0, 10), (5000, 10), (4, 0), (4, 10001)):
         assert L.k3moe_selftest_occupy(n, ms, None) == 2
+
+
+def test_layer_saliency_arguments(L):
+    """Checks before any launch (no GPU needed): dims, the accumulator, alignment, workspace."""
+    dm = k3.Dims(7168, 3584, 3072, 896, 16, 0, 0, 0, 0)
+    good = 1 << 16
+    n = k3.k3moe_workspace_size(dm, 4)
+    assert L.k3moe_layer_saliency(ctypes.byref(dm), 4, None, None, good, n, None, None) == 1
+    assert L.k3moe_layer_saliency(ctypes.byref(dm), 4, None, None, good, n, good + 8, None) == 3
+    assert L.k3moe_layer_saliency(ctypes.byref(dm), 4, None, None, good, n - 1, good, None) == 4
+    assert L.k3moe_layer_saliency(ctypes.byref(dm), -1, None, None, good, n, good, None) == 2
+    assert L.k3moe_layer_saliency(ctypes.byref(dm), 0, None, None, good, n, good, None) == 0

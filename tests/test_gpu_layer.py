@@ -290,6 +290,18 @@ def test_decode_layer_completes_while_other_work_holds_most_sms(k3_layer, T):
         np.testing.assert_array_equal(g, w)
 
 
+def test_workspace_shared_across_token_counts(k3_layer):
+    """One workspace, zeroed once, serves calls with different token counts in any order (the
+    routing kernels' block counter sits in the fixed header): same bits as fresh workspaces."""
+    x = synth.host_x(synth.WORKLOADS["decode_b64"], 0, 64)
+    ws = workspace(k3_layer.dims, 64)
+    for T in (1, 16, 3, 64, 2, 40, 1):
+        got = run_layer(k3_layer, x[:T], ws=ws)
+        want = run_layer(k3_layer, x[:T])
+        for g, w in zip(got, want):
+            np.testing.assert_array_equal(g, w)
+
+
 def test_layer_tiny_ragged_and_edge_T():
     d = synth.TINY
     lay = DeviceLayer(d, seed=1, bias=synth.host_f32_normal(1, synth.S_BIAS, 0, d.n_experts, 1.0))

@@ -35,6 +35,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (decode b1/b64, prefill 4K/32K) + % of HBM / FP4 roofline"
+ACTQ_NAME = {0: "bf16", 1: "mxfp8", 2: "mxfp4"}
 DENSE_COPIES = 4
 
 
@@ -145,7 +146,10 @@ def kernel_cost(name, d, T, distinct, rows, actq, shared_width=0):
     L, I, H, E = d.latent, d.inter, d.hidden, d.n_experts
     glu_w = 2 * (d.gate_q_bytes + d.gate_s_bytes)
     down_w = d.down_q_bytes + d.down_s_bytes
-    P = 1 if actq else 2  # e4m3 rows per activation row on the tensor-core expert path
+    # activation bytes per value on the tensor-core expert path: bf16 as two e4m3 rows (2),
+    # MXFP8 one e4m3 row (1), MXFP4 one row of packed e2m1 codes (0.5)
+    P = {0: 2, 1: 1, 2: 0.5}[actq]
+    mma = "fp4" if actq == 2 else "fp8"  # the block-scaled MMA kind's rate
     gemv = T < 33  # token-at-a-time dense projections below 33 tokens
     table = {
         # router logits fp32 + z bf16 (+ its f16 block-scaled copy on the GEMV path)
@@ -154,14 +158,14 @@ def kernel_cost(name, d, T, distinct, rows, actq, shared_width=0):
         "latent_out": (2 * H * L + 2 * T * L + 2 * T * H, 2 * T * H * L, "bf16"),
         "expert_glu_gemv": (distinct * glu_w + rows * (2 * L + 4 * I), 4 * rows * L * I, None),
         "expert_down_gemv": (distinct * down_w + rows * (2 * I + 4 * L), 2 * rows * L * I, None),
-        "expert_act_quant": (rows * 2 * L + P * rows * (L + L // 32), 0, None),
-        "expert_glu_mma": (distinct * glu_w + P * rows * (L + L // 32) + P * rows * (I + I // 32),
-                           4 * rows * L * I, "fp8"),
-        "expert_down_mma": (distinct * down_w + P * rows * (I + I // 32) + 4 * rows * L,
-                            2 * rows * L * I, "fp8"),
+        "expert_act_quant": (rows * 2 * L + rows * (P * L + L // 32), 0, None),
+        "expert_glu_mma": (distinct * glu_w + rows * (P * L + L // 32) + rows * (P * I + I // 32),
+                           4 * rows * L * I, mma),
+        "expert_down_mma": (distinct * down_w + rows * (P * I + I // 32) + 4 * rows * L,
+                            2 * rows * L * I, mma),
         # both passes in one launch (decode): the GLU output is written and read back once
-        "expert_ffn_mma": (distinct * (glu_w + down_w) + P * rows * (L + L // 32) +
-                           2 * P * rows * (I + I // 32) + 4 * rows * L, 6 * rows * L * I, "fp8"),
+        "expert_ffn_mma": (distinct * (glu_w + down_w) + rows * (P * L + L // 32) +
+                           2 * rows * (P * I + I // 32) + 4 * rows * L, 6 * rows * L * I, mma),
         "combine": (rows * 4 * L + 2 * T * L, 0, None),
         # gate + up (fp32 out), GLU, down (fp32 out); S = n_shared x shared_inter
         "shared_experts": (2 * 3 * shared_width * H + 2 * T * H + 2 * 4 * T * shared_width +
@@ -174,20 +178,22 @@ def kernel_cost(name, d, T, distinct, rows, actq, shared_width=0):
 def roofline(name, per_launch_ms, cost, pk):
     """Roofline entry of a kernel: HBM-bound unless its algorithmic flops at the tensor peak of
     its dtype take longer than its bytes at the copy bandwidth. fp8 (the block-scaled
-    e2m1 x e4m3 MMA rate) = measured bf16 x 2, the nominal dense ratio (4.5 / 2.25 PFLOP/s)."""
+    e2m1 x e4m3 MMA rate) = measured bf16 x 2, the nominal dense ratio (4.5 / 2.25 PFLOP/s);
+    fp4 (kind::mxf4, e2m1 x e2m1) = measured bf16 x 6 (13.5 / 2.25 PFLOP/s)."""
+    ratio = {"fp8": 2.0, "fp4": 6.0}
     kb, fl, dt = cost
     if not kb:
         return {"bound": "hbm", "kernel": name, "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": None, "traffic": None}
     t = per_launch_ms / 1e3
-    tensor_peak = pk["bf16_tflops"] * (2.0 if dt == "fp8" else 1.0) if dt else None
+    tensor_peak = pk["bf16_tflops"] * ratio.get(dt, 1.0) if dt else None
     t_hbm = kb / (pk["hbm_gbs"] * 1e9)
     t_tc = fl / (tensor_peak * 1e12) if tensor_peak else 0.0
     if tensor_peak and t_tc > t_hbm:
         ach = fl / t / 1e12
         return {"bound": "tensor", "kernel": name, "achieved": ach, "peak": tensor_peak, "unit": "TFLOP/s",
                 "frac": ach / tensor_peak, "traffic": None,
-                "peak_src": pk["src"] + f" bf16 burst{' x 2 (fp8 nominal ratio)' if dt == 'fp8' else ''}",
+                "peak_src": pk["src"] + " bf16 burst" + (f" x {ratio[dt]:g} ({dt} nominal ratio)" if dt in ratio else ""),
                 "algorithmic_flops_per_launch": fl, "avg_launch_ms": per_launch_ms}
     ach = kb / t / 1e9
     return {"bound": "hbm", "kernel": name, "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
@@ -197,7 +203,7 @@ def roofline(name, per_launch_ms, cost, pk):
 
 
 # ---------------------------------------------------------------- CPU oracle sample
-def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads, pool=None):
+def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads, pool=None, actq=0):
     """Times the oracle on (token, slot) units: each unit is one routed expert row through the
     oracle (gate/up, GLU, down; ~33M MACs) plus 1/k of that token's dense work (router, latent
     in and latent out rows), i.e. 1/k of a token. Units run on `nthreads` host threads. With
@@ -221,7 +227,7 @@ def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads,
     need = {e for (_, _, e) in units[: units_per_step * steps]}
     for e in need:
         experts[e] = synth.host_expert(d, layer_seed, e)
-    lay = oracle.Layer(d, wr, wi, wo, experts)
+    lay = oracle.Layer(d, wr, wi, wo, experts, actq=actq)
     _, z_all = oracle.dense_proj(wi, x_np[: idx_sample.shape[0]])
     E_sl, L_sl, H_sl = d.n_experts // k, d.latent // k, d.hidden // k
 
@@ -500,11 +506,11 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "mxfp4 weights x " + ("mxfp8" if args.actq else "bf16") + " activations, fp32 accumulate",
+        "dtype": "mxfp4 weights x " + ACTQ_NAME[args.actq] + " activations, fp32 accumulate",
         "data": "synthetic (seeded SplitMix64; bf16 ~N(0,1) tokens, ~N(0,0.02) dense, U{0..15} codes, U{120..127} e8m0)",
         "config": {"workload": w.name, "tokens_per_step": T, "hidden": d.hidden, "latent": d.latent,
                    "inter": d.inter, "n_experts": d.n_experts, "top_k": d.top_k,
-                   "router_bias": w.bias, "actq": "mxfp8" if args.actq else "bf16", "layers": nl,
+                   "router_bias": w.bias, "actq": ACTQ_NAME[args.actq], "layers": nl,
                    "l2": ("expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 4 copies"
                           if nl == 1 else f"{nl} layers with independent weights ({nl * 15.7:.0f} GB of experts) run back to "
                           "back on the same tokens; fresh tokens per step"),
@@ -541,7 +547,7 @@ def run_ours(args, w):
         isamp = oracle.select_topk(oracle.router_logits_np(xs_np, wr, bias_np), d.top_k)
         # bounded sample: about 10 s of oracle work, calibrated on one step of nth units
         units = nth
-        _, cstep = cpu_sample(w, 0, xs_np, isamp, units, 64, nth, pool=2 * nth)
+        _, cstep = cpu_sample(w, 0, xs_np, isamp, units, 64, nth, pool=2 * nth, actq=args.actq)
         t0 = time.perf_counter()
         cstep(0)
         per_step = max(1e-3, time.perf_counter() - t0)
@@ -569,7 +575,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_b1")
-    ap.add_argument("--actq", type=int, default=0)
+    ap.add_argument("--actq", type=int, default=0, choices=[0, 1, 2],
+                    help="activations: 0 bf16 (the headline), 1 MXFP8, 2 MXFP4 (kind::mxf4 experts)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph-steps", type=int, default=8,
                     help="steps per captured CUDA graph for the device-timed value (0: launch step by step)")

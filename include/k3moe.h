@@ -25,7 +25,10 @@
  *   y_t    = bf16(W_out c_t + s_t)             latent out, [H][L], one rounding   (k3moe_project)
  * k3moe_layer_forward runs all of it. In MXFP8 mode (actq = 1) z and the GLU output go
  * through an MXFP8 round trip (E4M3 elements, one E8M0 scale per 32, OCP MX v1.0) before
- * they enter an expert matrix.
+ * they enter an expert matrix; in MXFP4 mode (actq = 2) through an MXFP4 round trip (E2M1
+ * elements, one E8M0 scale per 32, OCP MX v1.0), and the experts run on the FP4 tensor rate
+ * (the "Kimi K3 hardware deep dive", quantisation-aware training section, names MXFP4 weights
+ * with MXFP8 activations; 4-bit activations are the mode the FP4 rate needs).
  *
  * Storage (all row-major, K contiguous; bf16 as uint16_t bit patterns):
  *   w_router [E][H] bf16, router_bias [E] fp32 (may be NULL), w_in [L][H], w_out [H][L] bf16.
@@ -66,7 +69,8 @@ typedef enum k3moe_status {
   K3MOE_E_SHAPE = 2,     /* a size is out of range or not a supported multiple */
   K3MOE_E_ALIGN = 3,     /* a device pointer is not 16-byte aligned */
   K3MOE_E_WORKSPACE = 4, /* workspace missing or smaller than k3moe_workspace_size() */
-  K3MOE_E_MODE = 5,      /* act / actq not supported (act = 1, SiTU-GLU, has no formula) */
+  K3MOE_E_MODE = 5,      /* act / actq not supported (act = 1, SiTU-GLU, has no formula; actq = 2
+                            with latent or inter not a multiple of 256) */
   K3MOE_E_CUDA = 6,      /* a CUDA runtime call or launch failed */
   K3MOE_E_TIMEOUT = 7,   /* a device-side bounded wait ran out (see k3moe_check) */
   K3MOE_E_DEVICE = 8,    /* no usable sm_100-family device, or a device-side check failed */
@@ -80,7 +84,8 @@ typedef struct k3moe_dims {
   int32_t n_experts; /* E (K3: 896) */
   int32_t top_k;     /* k (K3: 16) */
   int32_t act;       /* 0 = SiLU-GLU silu(gate) * up, fp32; 1 = SiTU-GLU -> K3MOE_E_MODE */
-  int32_t actq;      /* 0 = bf16 activations; 1 = MXFP8 activations (E4M3 + E8M0 per 32) */
+  int32_t actq;      /* 0 = bf16 activations; 1 = MXFP8 activations (E4M3 + E8M0 per 32);
+                        2 = MXFP4 activations (E2M1 + E8M0 per 32; latent and inter multiples of 256) */
   int32_t n_shared;     /* always-on shared experts per token, 0..8 (K3: 2; 0 = none) */
   int32_t shared_inter; /* intermediate width of each shared expert (not on the pages; a
                            parameter); n_shared * shared_inter must be a multiple of 64 */

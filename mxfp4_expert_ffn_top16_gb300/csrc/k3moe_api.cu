@@ -88,10 +88,12 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
     L.sa = take(Tt * S * 2);
   }
   if (umma_expert_ok(d)) {
-    const size_t P = d.actq ? 1 : 2;
-    L.bq = take(P * rows * Lw);
+    // P activation rows per sorted row (bf16 as e4m3 hi + lo: 2; MXFP8: 1) of one byte per value,
+    // or for MXFP4 activations one row of packed e2m1 codes (half a byte per value)
+    const size_t P = d.actq ? 1 : 2, num = d.actq == 2 ? 1 : 2;
+    L.bq = take(P * rows * Lw * num / 2);
     L.bs = take(P * rows * (size_t)exp_pitch(d.latent));
-    L.aq = take(P * rows * I);
+    L.aq = take(P * rows * I * num / 2);
     L.aqs = take(P * rows * (size_t)exp_pitch(d.inter));
     L.chunk_done = take((size_t)decode_counters(d, T) * 4);
   }
@@ -119,7 +121,9 @@ k3moe_status check_dims(const k3moe_dims* d) {
   if (d->n_experts < 1 || d->n_experts > 1024) return K3MOE_E_SHAPE;
   if (d->top_k < 1 || d->top_k > 32 || d->top_k > d->n_experts) return K3MOE_E_SHAPE;
   if (d->act != 0) return K3MOE_E_MODE;
-  if (d->actq != 0 && d->actq != 1) return K3MOE_E_MODE;
+  if (d->actq < 0 || d->actq > 2) return K3MOE_E_MODE;
+  // MXFP4 activations run on the kind::mxf4 tensor-core path only: K = 256 per stage
+  if (d->actq == 2 && (d->latent % 256 || d->inter % 256)) return K3MOE_E_MODE;
   if (d->n_shared < 0 || d->n_shared > 8) return K3MOE_E_SHAPE;
   if (d->n_shared > 0 && (d->shared_inter <= 0 || ((int64_t)d->n_shared * d->shared_inter) % 64 ||
                           (int64_t)d->n_shared * d->shared_inter > (1 << 20)))
@@ -214,11 +218,12 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* plan = at<int32_t>(ws, L.plan);
   if (umma_expert_ok(d)) {
-    const int P = d.actq ? 1 : 2;
+    // activation rows per sorted row: 2 (bf16 as e4m3 hi + lo), 1 (MXFP8), 0 = one MXFP4 row
+    const int P = d.actq == 2 ? 0 : (d.actq ? 1 : 2);
     int* cnt = at<int>(ws, L.chunk_done);
     uint8_t* aq = at<uint8_t>(ws, L.aq);
     uint8_t* aqs = at<uint8_t>(ws, L.aqs);
-    if (T < kUmmaExpertMinTokens) {
+    if (T < kUmmaExpertMinTokens && P != 0) {
       // decode: z as P E4M3 rows per token (the expert kernel gathers a chunk's rows by token),
       // weights on the MMA's N side; both passes in one launch when latent % 256 == 0
       if (!z_rows_ready) {
@@ -238,7 +243,7 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
       }
       return K3MOE_OK;
     }
-    {  // many tokens: z gathered into P E4M3 rows per sorted row
+    {  // many tokens (and MXFP4 activations at any count): z gathered into rows per sorted row
       ProfScope p(P_QUANT, s);
       K3_CUDA(launch_quant_rows(z, row_token, T * d.top_k, T, d.latent, P, at<uint8_t>(ws, L.bq),
                                 at<uint8_t>(ws, L.bs), cnt, 0, err, s));
@@ -290,7 +295,7 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
   K3_TRY(run_expert_gemms(d, w, at<uint16_t>(ws, L.z), T, at<int32_t>(ws, L.offsets),
                           at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s,
                           T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens &&
-                              umma_expert_ok(d)));
+                              umma_expert_ok(d) && d.actq != 2));
   {
     ProfScope p(P_COMBINE, s);
     K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,
@@ -445,7 +450,8 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
     ProfScope p(P_ROUTER_LATENT, s);
     const bool f16_copy = !umma_expert_ok(d);
     // decode on the tensor-core experts: z also as P E4M3 rows per token for the expert kernel
-    const bool rows = !f16_copy && T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens;
+    const bool rows = !f16_copy && d.actq != 2 && T <= kSmallRouteTokens && T < kUmmaExpertMinTokens &&
+                      T < kUmmaDenseMinTokens;
     K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr, w.router_bias, w.w_in,
                          d.latent, at<uint16_t>(ws, L.z), f16_copy ? at<__half>(ws, L.zh) : nullptr,
                          f16_copy ? at<int8_t>(ws, L.zs) : nullptr, d.actq, x, T, d.hidden, err, s,

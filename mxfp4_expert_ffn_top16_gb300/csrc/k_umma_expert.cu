@@ -44,15 +44,28 @@
 namespace k3moe {
 namespace {
 
-constexpr int BM = 128, BKE = 128;        // weight rows, K elements per stage
-constexpr int kATile = BM * BKE;          // bytes in shared memory (e2m1 padded to bytes)
-constexpr int kAPacked = BM * BKE / 2;    // bytes the copy transfers
+constexpr int BM = 128, BKE = 128;        // weight rows, K elements per stage (e4m3 activations)
+constexpr int kATile = BM * 128;          // bytes in shared memory: 128-byte rows
+// Bytes a stage's weight copy transfers: e4m3 activations (kind::mxf8f6f4) take the weights as
+// e2m1 padded to one code per byte in shared memory (K = 128 per stage, 64 packed bytes per row);
+// MXFP4 activations (kind::mxf4) take both operands packed, two codes per byte (K = 256 per
+// stage in the same 128-byte rows).
+template <bool FP4>
+constexpr int kAPacked = FP4 ? BM * 128 : BM * 128 / 2;
+template <bool FP4>
+constexpr int kKStage = FP4 ? 256 : 128;  // K per stage
 constexpr int kThreads = 384;             // 0 TMA, 1 MMA, 2-9 epilogue, 10-11 scale gather
 constexpr int kEpiWarps = 8;
 constexpr int kGather0 = 2 + kEpiWarps;   // first scale-gather warp
 constexpr int kAccSlots = 2;
-constexpr int kSfPerStage = 16;           // tensor-memory columns: A 4, B rows 0..127 4, B rows 128.. 4
-constexpr int kStgBytes = 1536;           // per stage: A block, B block rows 0..127, rows 128..255
+// Tensor-memory scale columns per stage. e4m3: A 4, B rows 0..127 4, B rows 128..255 4 (one
+// 32-bit word of four K-block scales per row and stage). MXFP4: two words per row and stage
+// (K = 256): A 4 + 4, B 4 + 4 (B rows <= 128).
+constexpr int kSfPerStage = 16;
+// Scale staging blocks of 32 x 16 bytes per stage: e4m3 A, B rows 0..127, B rows 128..255;
+// MXFP4 A word 0, A word 1, B word 0, B word 1.
+template <bool FP4>
+constexpr int kStgBytes = FP4 ? 2048 : 1536;
 
 // Shapes by chunk size R (sorted rows per item): R = kUmmaChunkRows (many tokens: N up to 224,
 // four deep stages) or R = kGemvTokens (few tokens: N up to 16, small activation tiles, so
@@ -100,6 +113,40 @@ __device__ __forceinline__ uint32_t idesc_mx(int N, int kk) {
   return ((uint32_t)kk << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
          ((uint32_t)(BM >> 4) << 24) | ((uint32_t)kk << 29);
 }
+// kind::mxf4: A and B e2m1 (packed), e8m0 scales, fp32 accumulation, K-major, K = 64 per MMA
+// (scale_vec::2X: two scale bytes per row, starting at byte sf of the scale word).
+__device__ __forceinline__ uint32_t idesc_mxf4(int N, int sf) {
+  return ((uint32_t)sf << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(BM >> 4) << 24) | ((uint32_t)sf << 29);
+}
+__device__ __forceinline__ void umma_mxf4(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t sfa,
+                                          uint32_t sfb, uint32_t acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %6, 0; tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X "
+      "[%0], %1, %2, %3, [%4], [%5], p; }" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(sfa), "r"(sfb), "r"(acc)
+      : "memory");
+}
+// Eight values -> eight e2m1 codes (nearest even, saturating at +-6), packed low nibble first.
+__device__ __forceinline__ uint32_t e2m1x8(const float* v) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    uint32_t b;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(b) : "f"(v[i + 1]), "f"(v[i]));
+    r |= b << (4 * i);
+  }
+  return r;
+}
+// Shared exponent of an MXFP4 block from its amax (OCP MX v1.0: floor(log2 amax) - 2, clamped to
+// the e8m0 range); an all-zero block gets -127.
+__device__ __forceinline__ int mxfp4_block_exp(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  if (!(amax <= 3.4028235e38f)) return 127;
+  const int X = ilog2_floor(amax) - 2;
+  return X < -127 ? -127 : (X > 127 ? 127 : X);
+}
+
 // Descriptor of a 32 x 16-byte scale staging block: no swizzle, 8-row groups 128 bytes apart.
 __device__ __forceinline__ uint64_t sdesc_sf(uint32_t addr) {
   return (uint64_t)((addr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
@@ -147,8 +194,10 @@ __device__ __forceinline__ void quant_block32(float (&v)[32], uint32_t (&codes)[
   }
 }
 
-template <bool GLU, int P, int R>
+template <bool GLU, int P, int R, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_constant__ UExpertArgs A) {
+  static_assert(!FP4 || P == 1, "MXFP4 activations: one row per sorted row");
+  constexpr int kStg = kStgBytes<FP4>;
   using CF = Cfg<R>;
   constexpr int kOut = CF::kOut, kNMax = CF::kNMax, kBTile = CF::kBTile, kStages = CF::kStages;
   constexpr int kXPitch = CF::kXPitch;
@@ -162,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATile;
   uint8_t* stg = sB + kStages * kBTile;                            // kStages x kStgBytes
-  float* xg = reinterpret_cast<float*>(stg + kStages * kStgBytes);  // GLU: [64][kXPitch]
+  float* xg = reinterpret_cast<float*>(stg + kStages * kStg);  // GLU: [64][kXPitch]
   uint64_t* full = reinterpret_cast<uint64_t*>(xg + (GLU ? 64 * kXPitch : 0));
   uint64_t* empty = full + kStages;
   uint64_t* accf = empty + kStages;
@@ -210,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   }
   const int fbs = A.N / kFB;
   const int items = (C > 0 && C <= A.rows_max / R + A.E) ? C * fbs : 0;
-  const int nk = A.K / BKE;
+  const int nk = A.K / kKStage<FP4>;
 
   // item u -> (expert, first sorted row, rows, first feature); false for a corrupt entry
   auto item_of = [&](int u, int& e, int& r0, int& nr, int& f0) -> bool {
@@ -235,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         const int wrow = e * A.N + f0;
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], kAPacked + kBTx);
+          mbar_arrive_expect_tx(&full[s], kAPacked<FP4> + kBTx);
           tma_load_2d(sA + s * kATile, &A.ta0, kc * BKE, wrow, &full[s]);
           if (GLU) tma_load_2d(sA + s * kATile + 64 * 128, &A.ta1, kc * BKE, wrow, &full[s]);
           tma_load_2d(sB + s * kBTile, &A.tb, kc * BKE, P * r0, &full[s]);
@@ -266,6 +315,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
           dst[w] = st_lane + 4 * w;
         }
         n = 4;
+      } else if (FP4) {  // B rows <= 128: word 0 in block 2, word 1 in block 3
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int rb = 32 * w + lane;
+          src[w] = A.sb + ((size_t)r0 + rb) * spb;
+          dst[w] = st_lane + 1024 + 4 * w;
+          if (rb < nr) n = w + 1;
+        }
       } else {
 #pragma unroll
         for (int w = 0; w < 7; ++w) {
@@ -277,10 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
       }
       for (int kc = 0; kc < nk; ++kc) {
         if (!mbar_wait_warp(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
-        const uint32_t so = (uint32_t)(s * kStgBytes);
+        const uint32_t so = (uint32_t)(s * kStg);
+        if (FP4) {  // eight K-block scales per row and stage: two words, the second 512 bytes on
 #pragma unroll
-        for (int w = 0; w < 7; ++w)
-          if (w < n) cp_async4(dst[w] + so, src[w] + 4 * kc);
+          for (int w = 0; w < 4; ++w)
+            if (w < n) {
+              cp_async4(dst[w] + so, src[w] + 8 * kc);
+              cp_async4(dst[w] + so + 512, src[w] + 8 * kc + 4);
+            }
+        } else {
+#pragma unroll
+          for (int w = 0; w < 7; ++w)
+            if (w < n) cp_async4(dst[w] + so, src[w] + 4 * kc);
+        }
         cp_async_arrive(&full[s]);
         if (++s == kStages) { s = 0; ph ^= 1; }
       }
@@ -301,9 +367,25 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         if (!mbar_wait_warp(&full[s], ph, abort_flag, A.err)) { ok = false; break; }
         // scale columns: A (4), then B rows 0..127 (4) and B rows 128..255 (4)
         const uint32_t tsa = tmem + kSfCol + kSfPerStage * s, tsb = tsa + 4;
-        const uint32_t st0 = smem_u32(stg + s * kStgBytes);
+        const uint32_t st0 = smem_u32(stg + s * kStg);
         const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
-        if (elect_one()) {
+        if (FP4) {
+          // scale columns: A word 0 (4), A word 1 (4), B word 0 (4), B word 1 (4); the MMA of
+          // K block pair kk uses word kk / 2, bytes 2 (kk % 2) and 2 (kk % 2) + 1
+          if (elect_one()) {
+            fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
+            tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa + 4 * q),
+                           "l"(sdesc_sf(st0 + 512 * q)));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              umma_mxf4(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_mxf4(Nc, 2 * (kk & 1)),
+                        tsa + 4 * (kk >> 1), tsa + 8 + 4 * (kk >> 1), (kc | kk) != 0 ? 1u : 0u);
+            umma_commit(&empty[s]);
+          }
+        } else if (elect_one()) {
           fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
           tc_fence_after();
           asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa), "l"(sdesc_sf(st0)));
@@ -407,7 +489,21 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         // (sorted row, 32-feature block) units: kOut rows x 2 blocks over the 256 threads
         for (int unit = et; unit < 2 * kOut; unit += 32 * kEpiWarps) {
           const int jr = unit % kOut, b = unit / kOut;
-          if (jr < nr) {
+          if (jr < nr && FP4) {  // MXFP4: 32 e2m1 codes (16 bytes) and the block exponent
+            float v[32], am = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              v[i] = xg[(32 * b + i) * kXPitch + jr];
+              am = fmaxf(am, fabsf(v[i]));
+            }
+            const int X = mxfp4_block_exp(am);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = mul_pow2(v[i], -X);
+            const size_t brow = (size_t)(r0 + jr);
+            *reinterpret_cast<uint4*>(A.aq + brow * (A.N / 2) + (f0 + 32 * b) / 2) =
+                make_uint4(e2m1x8(v), e2m1x8(v + 8), e2m1x8(v + 16), e2m1x8(v + 24));
+            A.aqs[brow * exp_pitch(A.N) + (f0 + 32 * b) / 32] = (uint8_t)(X + 127);
+          } else if (jr < nr) {
             float v[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = xg[(32 * b + i) * kXPitch + jr];
@@ -441,35 +537,45 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   }
 }
 
-template <bool GLU, int R>
+template <bool GLU, int R, bool FP4>
 constexpr size_t smem_bytes() {
   using CF = Cfg<R>;
-  return 1024 + (size_t)CF::kStages * (kATile + CF::kBTile) + CF::kStages * kStgBytes +
+  return 1024 + (size_t)CF::kStages * (kATile + CF::kBTile) + CF::kStages * kStgBytes<FP4> +
          (GLU ? 64 * CF::kXPitch * 4 : 0) + (2 * CF::kStages + 2 * kAccSlots + 2) * 8 + 16;
 }
-static_assert(smem_bytes<true, kGemvTokens>() <= 227 * 1024 && smem_bytes<true, kUmmaChunkRows>() <= 227 * 1024,
+static_assert(smem_bytes<true, kGemvTokens, true>() <= 227 * 1024 &&
+                  smem_bytes<true, kUmmaChunkRows, true>() <= 227 * 1024,
               "shared memory");
 
-template <bool GLU, int P, int R>
+template <bool GLU, int P, int R, bool FP4>
 cudaError_t launch_t(UExpertArgs& a, int items_max, cudaStream_t s) {
-  const size_t smem = smem_bytes<GLU, R>();
-  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_expert_kernel<GLU, P, R>), smem);
+  const size_t smem = smem_bytes<GLU, R, FP4>();
+  cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_expert_kernel<GLU, P, R, FP4>), smem);
   if (e != cudaSuccess) return e;
   int grid = num_sms();
   if (items_max < grid) grid = items_max > 0 ? items_max : 1;
-  return launch_pdl(umma_expert_kernel<GLU, P, R>, dim3(grid), dim3(kThreads), smem, s, a);
+  return launch_pdl(umma_expert_kernel<GLU, P, R, FP4>, dim3(grid), dim3(kThreads), smem, s, a);
 }
 
+// P: activation rows per sorted row for e4m3 activations (1 MXFP8, 2 bf16 as hi + lo); P = 0
+// selects MXFP4 activations (kind::mxf4, one packed row per sorted row).
 template <bool GLU>
 cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t s) {
-  if (R == kGemvTokens)
-    return P == 1 ? launch_t<GLU, 1, kGemvTokens>(a, items_max, s) : launch_t<GLU, 2, kGemvTokens>(a, items_max, s);
-  return P == 1 ? launch_t<GLU, 1, kUmmaChunkRows>(a, items_max, s) : launch_t<GLU, 2, kUmmaChunkRows>(a, items_max, s);
+  if (R == kGemvTokens) {
+    if (P == 0) return launch_t<GLU, 1, kGemvTokens, true>(a, items_max, s);
+    return P == 1 ? launch_t<GLU, 1, kGemvTokens, false>(a, items_max, s)
+                  : launch_t<GLU, 2, kGemvTokens, false>(a, items_max, s);
+  }
+  if (P == 0) return launch_t<GLU, 1, kUmmaChunkRows, true>(a, items_max, s);
+  return P == 1 ? launch_t<GLU, 1, kUmmaChunkRows, false>(a, items_max, s)
+                : launch_t<GLU, 2, kUmmaChunkRows, false>(a, items_max, s);
 }
 
-// z[row_token[r]] (bf16) -> P e4m3 rows with e8m0 block scales per sorted row r. One warp per
-// (sorted row, 256-value segment), so every load of a launch is in flight at once; each lane
-// takes 8 consecutive values, four lanes one 32-value block.
+// z[row_token[r]] (bf16) -> P e4m3 rows with e8m0 block scales per sorted row r (P = 0: one
+// MXFP4 row of packed e2m1 codes, OCP MX v1.0 conversion: shared exponent floor(log2 amax) - 2,
+// elements rounded to nearest even, saturating at +-6). One warp per (sorted row, 256-value
+// segment), so every load of a launch is in flight at once; each lane takes 8 consecutive
+// values, four lanes one 32-value block.
 template <int P>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ z,
                                                          const int32_t* __restrict__ row_token, int rows,
@@ -505,6 +611,19 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = 0.f;
   }
+  if constexpr (P == 0) {
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+    const int X = mxfp4_block_exp(max_in_group4(am));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = mul_pow2(v[i], -X);
+    const uint32_t packed = e2m1x8(v);
+    if (act) {
+      *reinterpret_cast<uint32_t*>(bq + (size_t)r * (L / 2) + col / 2) = packed;
+      if ((lane & 3) == 0) bs[(size_t)r * sp + col / 32] = (uint8_t)(X + 127);
+    }
+  } else {
 #pragma unroll
   for (int p = 0; p < P; ++p) {
     float am = 0.f;
@@ -528,6 +647,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
       if ((lane & 3) == 0) bs[row * sp + col / 32] = (uint8_t)(X + 127);
     }
   }
+  }
 }
 
 }  // namespace
@@ -538,6 +658,8 @@ cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int r
   const int warps = 8;
   const long long units = (long long)rows * ((L + 255) / 256);
   const dim3 grid((unsigned)((units + warps - 1) / warps)), block(32 * warps);
+  if (P == 0)
+    return launch_pdl(quant_rows_kernel<0>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
   if (P == 1)
     return launch_pdl(quant_rows_kernel<1>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
   return launch_pdl(quant_rows_kernel<2>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
@@ -549,12 +671,18 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
   const int R = umma_chunk_rows(T);
   UExpertArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
-  if (!make_tmap_fp4(&A.ta0, w.gate_q, d.latent, wrows, pitch, 64) ||
-      !make_tmap_fp4(&A.ta1, w.up_q, d.latent, wrows, pitch, 64))
-    return cudaErrorInvalidValue;
   const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, R * P, true))
+  if (P == 0) {  // MXFP4 activations: both operands packed, 128-byte boxes of 256 codes per row
+    if (!make_tmap_2d(&A.ta0, w.gate_q, 1, pitch, wrows, pitch, 128, 64, true) ||
+        !make_tmap_2d(&A.ta1, w.up_q, 1, pitch, wrows, pitch, 128, 64, true) ||
+        !make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent / 2, (uint64_t)rows, (uint64_t)d.latent / 2, 128, R, true))
+      return cudaErrorInvalidValue;
+  } else if (!make_tmap_fp4(&A.ta0, w.gate_q, d.latent, wrows, pitch, 64) ||
+             !make_tmap_fp4(&A.ta1, w.up_q, d.latent, wrows, pitch, 64) ||
+             !make_tmap_2d(&A.tb, bq, 1, (uint64_t)d.latent, (uint64_t)P * rows, (uint64_t)d.latent, BKE, R * P,
+                           true)) {
     return cudaErrorInvalidValue;
+  }
   A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
   A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.err = err;
@@ -566,11 +694,17 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s) {
   const int R = umma_chunk_rows(T);
   UExpertArgs A{};
-  if (!make_tmap_fp4(&A.ta0, w.down_q, d.inter, (uint64_t)d.n_experts * d.latent, (uint64_t)d.inter / 2, 128))
-    return cudaErrorInvalidValue;
   const int rows = T * d.top_k;
-  if (!make_tmap_2d(&A.tb, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, R * P, true))
+  const uint64_t pitch = (uint64_t)d.inter / 2, wrows = (uint64_t)d.n_experts * d.latent;
+  if (P == 0) {  // MXFP4 activations (see launch_umma_glu)
+    if (!make_tmap_2d(&A.ta0, w.down_q, 1, pitch, wrows, pitch, 128, 128, true) ||
+        !make_tmap_2d(&A.tb, aq, 1, pitch, (uint64_t)rows, pitch, 128, R, true))
+      return cudaErrorInvalidValue;
+  } else if (!make_tmap_fp4(&A.ta0, w.down_q, d.inter, wrows, pitch, 128) ||
+             !make_tmap_2d(&A.tb, aq, 1, (uint64_t)d.inter, (uint64_t)P * rows, (uint64_t)d.inter, BKE, R * P,
+                           true)) {
     return cudaErrorInvalidValue;
+  }
   A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
   A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
   A.o_out = o_rows; A.err = err;

@@ -45,12 +45,33 @@ def mxfp8(v: torch.Tensor) -> torch.Tensor:
     return (q * torch.pow(2.0, X)).reshape(sh)
 
 
+_E2M1_POS = torch.tensor([0, 0.5, 1, 1.5, 2, 3, 4, 6], dtype=torch.float32)
+
+
+def mxfp4(v: torch.Tensor) -> torch.Tensor:
+    """MXFP4 round trip along the last axis in blocks of 32 (OCP MX v1.0: shared exponent
+    floor(log2 amax) - 2, elements rounded to the nearest e2m1 value, ties to the even code,
+    saturating at +-6)."""
+    sh = v.shape
+    b = v.reshape(-1, 32)
+    amax = b.abs().amax(dim=1, keepdim=True)
+    X = torch.where(amax > 0, torch.floor(torch.log2(torch.where(amax > 0, amax, 1.0))) - 2, -127.0).clamp(-127, 127)
+    a = (b.abs() * torch.pow(2.0, -X)).clamp(max=6.0)
+    dist = (a[..., None] - _E2M1_POS).abs()
+    best = dist.min(dim=-1, keepdim=True).values
+    codes = torch.arange(8)
+    # among equally near values, the even code
+    cand = torch.where(dist == best, codes + 16 * (codes % 2), 99)
+    q = _E2M1_POS[(cand.argmin(dim=-1)) % 16]
+    return (torch.sign(b) * q * torch.pow(2.0, X)).reshape(sh)
+
+
 def forward(d, w_router, w_in, w_out, experts: dict, x: np.ndarray, idx: np.ndarray, wts: np.ndarray,
             actq: int = 0) -> np.ndarray:
     """y (bf16 bits) for tokens x with the selection idx [T][k] and routing weights wts [T][k]
     (taken from the oracle so that only the fp32 arithmetic of the rest differs). actq = 1:
-    MXFP8 activations (z and the GLU output go through an MXFP8 round trip)."""
-    q = mxfp8 if actq == 1 else (lambda t: t)
+    MXFP8 activations, 2: MXFP4 activations (z and the GLU output go through that round trip)."""
+    q = mxfp8 if actq == 1 else (mxfp4 if actq == 2 else (lambda t: t))
     X = _f32(x)
     z = q(_bf16(X @ _f32(w_in).T))
     T, k = idx.shape

@@ -38,11 +38,17 @@ NAMES = oracle.ExpertTables.NAMES
 # the small test shapes) have fewer elements per token, so one straddle weighs more: the same
 # fp32 evaluation on 3000 tokens of each small test shape reaches 4.8e-3 per token in bf16 mode
 # (1.7e-2 in MXFP8 mode), hence PER_TOKEN_CAP_NARROW.
+# MXFP4 activations (actq 2; the target states no tolerance for this mode, so it is derived the
+# same way): the e2m1 rounding points are coarser still. The fp32 evaluation on 512 tokens: median
+# 5.9e-7, p99 5.5e-4, one token at 3.9e-2 (a straddle of z on an e2m1 boundary) that alone makes
+# the whole-output error 1.4e-3; hence a per-token cap of 8e-2, at most 2% of the tokens above
+# 2e-3, and the compared output within WHOLE_BOUND[2] over 1024 tokens or more.
 REL_L2 = 2e-3
-PER_TOKEN_CAP = {0: 4e-3, 1: 3e-2}
-PER_TOKEN_CAP_NARROW = {0: 6e-3, 1: 3e-2}
-PER_TOKEN_OVER_FRAC = {0: 0.2, 1: 0.05}
-WHOLE_MIN_TOKENS = {0: 1, 1: 1024}
+PER_TOKEN_CAP = {0: 4e-3, 1: 3e-2, 2: 8e-2}
+PER_TOKEN_CAP_NARROW = {0: 6e-3, 1: 3e-2, 2: 8e-2}
+PER_TOKEN_OVER_FRAC = {0: 0.2, 1: 0.05, 2: 0.02}
+WHOLE_MIN_TOKENS = {0: 1, 1: 1024, 2: 1024}
+WHOLE_BOUND = {0: REL_L2, 1: REL_L2, 2: 2 * REL_L2}
 # Expert rows (one (token, expert) pair, fp32 out, no later rounding point): REL_L2 per row.
 # fp32 logits against double logits: |dl| <= LOGIT_ATOL + LOGIT_RTOL * |l|
 LOGIT_ATOL, LOGIT_RTOL = 1e-4, 1e-4
@@ -214,15 +220,15 @@ def check_layer_output(got: np.ndarray, want: np.ndarray, what: str = "layer", a
     n = len(err)
     print(f"{what}: rel L2 whole {whole:.3e}, per token median {np.median(err):.3e} max {err.max():.3e}, "
           f"{over} of {n} tokens above {REL_L2}")
-    m = 1 if actq else 0
+    m = actq
     if n >= WHOLE_MIN_TOKENS[m]:
-        assert whole <= REL_L2, (what, whole)
+        assert whole <= WHOLE_BOUND[m], (what, whole)
     cap = (PER_TOKEN_CAP if latent >= 1024 else PER_TOKEN_CAP_NARROW)[m]
     assert err.max() <= cap, (what, err.max(), cap)
     if m == 0 and n >= 32:
         assert over <= PER_TOKEN_OVER_FRAC[0] * n, (what, over, n)
-    if m == 1:
-        assert over <= max(1, PER_TOKEN_OVER_FRAC[1] * n), (what, over, n)
+    if m != 0:
+        assert over <= max(1, PER_TOKEN_OVER_FRAC[m] * n), (what, over, n)
     return err
 
 

@@ -55,7 +55,8 @@ def test_workspace_size_monotone(L):
 @pytest.mark.parametrize("kw,status", [
     (dict(hidden=7000), 2), (dict(latent=0), 2), (dict(inter=100), 2), (dict(n_experts=2000), 2),
     (dict(top_k=0), 2), (dict(top_k=33), 2), (dict(n_experts=8, top_k=9), 2),
-    (dict(act=1), 5), (dict(actq=2), 5)])
+    (dict(act=1), 5), (dict(actq=3), 5), (dict(actq=2, latent=3648), 5), (dict(actq=2, inter=3136), 5),
+    (dict(actq=2), 0)])
 def test_bad_dims_rejected(L, kw, status):
     out = ctypes.c_size_t(0)
     assert L.k3moe_workspace_size(ctypes.byref(dims(**kw)), 4, ctypes.byref(out)) == status

@@ -2,7 +2,7 @@
 
 prefill 4K: 4096 tokens with the Zipf(1.1) log-bias; every token's selection and the
 permutation bit-exact (boundary ties checked for validity), and every token's output against
-the oracle, with bf16 and with MXFP8 activations.
+the oracle, with bf16, MXFP8 and MXFP4 activations.
 prefill 32K: four layers with independent weights (seeds 0..3), 32768 tokens each; every
 token's selection and the permutation of every layer, and per layer the output of a stratified
 1024-token subset: every token of the hottest expert's last chunk of rows, every token of the
@@ -42,7 +42,7 @@ def _subset(idx: np.ndarray, offsets: np.ndarray, n: int, E: int) -> np.ndarray:
     return np.array(sorted(pick))[: max(n, len(pick))]
 
 
-def test_prefill_4k_every_token_bf16_and_mxfp8():
+def test_prefill_4k_every_token_all_activation_modes():
     w = synth.WORKLOADS["prefill_4k"]
     d = w.dims
     lay = DeviceLayer(d, seed=0, bias=synth.router_bias(w))
@@ -50,7 +50,7 @@ def test_prefill_4k_every_token_bf16_and_mxfp8():
         x = synth.host_x(w)
         T = x.shape[0]
         ws = workspace(dims(d, 0), T)
-        for actq in (0, 1):
+        for actq in (0, 1, 2):
             lay.actq = actq
             y, idx, _ = run_layer(lay, x, dm=dims(d, actq), ws=ws)
             flips = check_selection(lay, x, idx)

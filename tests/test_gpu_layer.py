@@ -78,9 +78,17 @@ DIMS = {"tiny": synth.TINY, "wide": WIDE, "deep": DEEP}
 
 @pytest.mark.parametrize("dname,T", [("tiny", 24), ("tiny", 100), ("wide", 7), ("wide", 200), ("deep", 3),
                                      ("deep", 20)])
-@pytest.mark.parametrize("actq", [0, 1])
+@pytest.mark.parametrize("actq", [0, 1, 2])
 def test_expert_ffn_tiny_all_rows(actq, dname, T):
+    """actq 2 (MXFP4 activations, kind::mxf4) needs latent and inter multiples of 256: the tiny
+    shape is refused with K3MOE_E_MODE; the wide and deep shapes run it at 8- and 112-row chunks."""
     d = DIMS[dname]
+    if actq == 2 and d.latent % 256:
+        ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+        st = k3.k3moe_expert_ffn_mxfp4(dims(d, 2), k3.Weights(), 16, 1, 16, 16, 16, ws.data_ptr(), 256, stream(),
+                                       check=False)
+        assert st == 5  # K3MOE_E_MODE
+        return
     lay = DeviceLayer(d, seed=0, actq=actq)
     z = synth.host_bf16_normal(3, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
     idx = synth.host_topk_sets(4, T, d.n_experts, d.top_k, "zipf")
@@ -104,7 +112,7 @@ def test_expert_ffn_gemv_path_all_rows(T):
     assert rel_l2_rows(o, want).max() <= REL_L2
 
 
-@pytest.mark.parametrize("T,actq", [(40, 0), (40, 1), (96, 0), (96, 1)])
+@pytest.mark.parametrize("T,actq", [(40, 0), (40, 1), (40, 2), (96, 0), (96, 1), (96, 2)])
 def test_expert_ffn_k3_sampled_rows(k3_layer, T, actq):
     d = synth.K3
     z = synth.host_bf16_normal(7, synth.S_X, 0, T * d.latent, 1.7).reshape(T, d.latent)
@@ -118,19 +126,21 @@ def test_expert_ffn_k3_sampled_rows(k3_layer, T, actq):
         assert rel_l2_rows(o[r], want) <= REL_L2, (r, rel_l2_rows(o[r], want))
 
 
-@pytest.mark.parametrize("dname,T", [("tiny", 8), ("tiny", 80), ("wide", 80), ("deep", 5)])
-def test_expert_ffn_invariants_bit_exact(dname, T):
-    """All-zero codes give exactly 0; +1 on every up exponent doubles every output exactly."""
+@pytest.mark.parametrize("dname,T,actq", [("tiny", 8, 0), ("tiny", 80, 0), ("wide", 80, 0), ("deep", 5, 0),
+                                          ("wide", 6, 2), ("wide", 80, 2), ("deep", 5, 2)])
+def test_expert_ffn_invariants_bit_exact(dname, T, actq):
+    """All-zero codes give exactly 0; +1 on every up exponent doubles every output exactly (in
+    MXFP4 mode too: the GLU output doubles, its block exponents rise by one, its codes stay)."""
     d = DIMS[dname]
     z = synth.host_bf16_normal(2, synth.S_X, 0, T * d.latent, 1.0).reshape(T, d.latent)
     idx = synth.host_topk_sets(5, T, d.n_experts, d.top_k, "uniform")
     base = {e: synth.host_expert(d, 0, e) for e in range(d.n_experts)}
     zero = {e: {n: (np.zeros_like(a) if n.endswith("_q") else a) for n, a in t.items()} for e, t in base.items()}
     dbl = {e: dict(t, up_s=(t["up_s"] + 1).astype(np.uint8)) for e, t in base.items()}
-    o0, _ = _expert_ffn(DeviceLayer(d, experts=zero), z, idx)
+    o0, _ = _expert_ffn(DeviceLayer(d, experts=zero, actq=actq), z, idx, actq)
     assert np.all(o0 == 0.0)
-    o1, _ = _expert_ffn(DeviceLayer(d, experts=base), z, idx)
-    o2, _ = _expert_ffn(DeviceLayer(d, experts=dbl), z, idx)
+    o1, _ = _expert_ffn(DeviceLayer(d, experts=base, actq=actq), z, idx, actq)
+    o2, _ = _expert_ffn(DeviceLayer(d, experts=dbl, actq=actq), z, idx, actq)
     np.testing.assert_array_equal(o2, 2 * o1)
 
 
@@ -324,11 +334,13 @@ HIDE = synth.Dims(hidden=1536, latent=512, inter=256, n_experts=64, top_k=4)
 ODD = synth.Dims(hidden=256, latent=192, inter=192, n_experts=16, top_k=4)
 
 
-@pytest.mark.parametrize("dname,T", [("deep", 1), ("deep", 5), ("deep", 40), ("hide", 1), ("hide", 9),
-                                     ("hide", 64), ("odd", 3), ("odd", 70), ("odd", 300)])
-def test_layer_other_dims_every_token(dname, T):
-    d = {"deep": DEEP, "hide": HIDE, "odd": ODD}[dname]
-    lay = DeviceLayer(d, seed=4)
+@pytest.mark.parametrize("dname,T,actq", [("deep", 1, 0), ("deep", 5, 0), ("deep", 40, 0), ("hide", 1, 0),
+                                          ("hide", 9, 0), ("hide", 64, 0), ("odd", 3, 0), ("odd", 70, 0),
+                                          ("odd", 300, 0), ("wide", 7, 2), ("wide", 80, 2), ("deep", 5, 2),
+                                          ("deep", 40, 2), ("hide", 64, 2), ("hide", 150, 2)])
+def test_layer_other_dims_every_token(dname, T, actq):
+    d = {"deep": DEEP, "hide": HIDE, "odd": ODD, "wide": WIDE}[dname]
+    lay = DeviceLayer(d, seed=4, actq=actq)
     x = synth.host_bf16_normal(5, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
     y, idx, w = _forward(lay, x)
     _compare_layer(lay, x, y, idx, np.arange(T))
@@ -371,7 +383,7 @@ def test_layer_k3_shared_experts_alone(T, sample):
         torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("actq", [0, 1])
+@pytest.mark.parametrize("actq", [0, 1, 2])
 def test_layer_k3_decode_b1(k3_layer, actq):
     w = synth.WORKLOADS["decode_b1"]
     n = 8
@@ -389,7 +401,7 @@ def test_layer_k3_decode_b1(k3_layer, actq):
         k3_layer.actq = 0
 
 
-@pytest.mark.parametrize("actq", [0, 1])
+@pytest.mark.parametrize("actq", [0, 1, 2])
 def test_layer_k3_decode_b64_biased(k3_layer, actq):
     w = synth.WORKLOADS["decode_b64"]
     bias = synth.router_bias(w)

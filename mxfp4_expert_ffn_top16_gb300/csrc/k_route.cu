@@ -425,6 +425,39 @@ __device__ void block_route_tiny(const int32_t* idx, int T, int E, int k, int ro
   }
 }
 
+// One token, k distinct valid experts held in ascending order by threads 0..k-1 (own_e): slot j
+// is sorted row j, each expert one run of one row and one chunk. The same outputs as
+// block_route_tiny gives for this case, in a few short loops.
+__device__ void route_one_token(int E, int k, int own_e, int32_t* offsets, int32_t* row_token, int32_t* row_slot,
+                                int32_t* slot_row, int32_t* plan) {
+  __shared__ int s_sel[32];
+  const int tid = threadIdx.x;
+  if (tid < k) s_sel[tid] = own_e;
+  __syncthreads();
+  for (int e = tid; e <= E; e += blockDim.x) {  // rows of the experts below e
+    int c = 0;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) c += s_sel[j] < e ? 1 : 0;
+    offsets[e] = c;
+  }
+  if (tid < k) {
+    const int4 run = make_int4(own_e, tid, 1, 0);
+    row_token[tid] = 0;
+    row_slot[tid] = tid;
+    slot_row[tid] = tid;
+    plan[2 + tid] = own_e;
+    plan[2 + E + tid] = tid;
+    plan_ctab(plan, E)[tid] = run;
+    plan_ctab64(plan, E, k)[1 + tid] = run;
+  }
+  if (tid == 0) {
+    plan[0] = k;
+    plan[1] = k;
+    plan[2 + E + k] = k;
+    plan_ctab64(plan, E, k)[0] = make_int4(k, 0, 0, 0);
+  }
+}
+
 __global__ void __launch_bounds__(kTopkThreads) route_tiny_kernel(const float* __restrict__ logits, int T, int E,
                                                                   int k, int32_t* idx, float* w, int32_t* offsets,
                                                                   int32_t* row_token, int32_t* row_slot,
@@ -437,7 +470,10 @@ __global__ void __launch_bounds__(kTopkThreads) route_tiny_kernel(const float* _
     for (int i = threadIdx.x; i < ncnt; i += blockDim.x) cnt[i] = 0;
   const int own_e = block_topk(logits, blockIdx.x, E, k, idx, w);
   if (T == 1) {  // the only block is the last: no count, and its own selection stays in registers
-    block_route_tiny(idx, T, E, k, k, offsets, row_token, row_slot, slot_row, plan, err, own_e);
+    if (__syncthreads_or(threadIdx.x < k && (own_e < 0 || own_e >= E)))
+      block_route_tiny(idx, T, E, k, k, offsets, row_token, row_slot, slot_row, plan, err, own_e);
+    else
+      route_one_token(E, k, own_e, offsets, row_token, row_slot, slot_row, plan);
     return;
   }
   __syncthreads();

@@ -102,6 +102,43 @@ def test_route_integer_exact_with_ties():
                                rtol=2e-6, atol=1e-7)
 
 
+def test_route_ties_across_expert_groups_and_nan():
+    """The selection's order on exact logits (the routing rule: the k largest logits, equal
+    logits to the lower expert index, NaN below every number) on 896 experts, with tie groups
+    that straddle the device's 128-expert sort groups. Integer router weights and one-hot
+    tokens make every logit exact on both sides."""
+    d = synth.Dims(hidden=128, latent=64, inter=64, n_experts=896, top_k=16)
+    E, H = d.n_experts, d.hidden
+    wr = np.zeros((E, H), np.float32)
+    wr[:, 0] = 1.0
+    wr[100:140, 0] = 2.0                 # token 1: a 40-way tie across the group at 128
+    wr[125:132, 1] = 3.0                 # token 2: 7 above the rest, across 128 ...
+    wr[0:E:50, 1] = 2.0                  # ... then the lowest 9 of an 18-way tie
+    wr[5, :] = -1.0                      # token 0 (x = 0): every finite logit 0
+    wr[3, :] = np.nan                    # every token: expert 3's logit is NaN
+    xs = np.zeros((4, H), np.float32)
+    xs[1, 0] = 1.0
+    xs[2, 1] = 1.0
+    xs[3, 2] = np.nan                    # token 3: every logit NaN -> the lowest k indices
+    to_bf16 = lambda a: (a.view(np.uint32) >> 16).astype(np.uint16)
+    lg, idx, w = _route(d, to_bf16(xs), to_bf16(wr))
+    want = [
+        [0, 1, 2] + list(range(4, 17)),
+        list(range(100, 116)),
+        sorted(list(range(125, 132)) + list(range(0, 450, 50))),
+        list(range(16)),
+    ]
+    for t in range(4):
+        assert list(idx[t]) == want[t], (t, list(idx[t]))
+    ref_lg = oracle.router_logits(d, to_bf16(xs), to_bf16(wr))
+    np.testing.assert_array_equal(idx, oracle.select_topk(ref_lg, d.top_k))
+    # weights: softmax over the kept logits (equal to softmax over all renormalised, for finite logits)
+    for t in range(3):
+        kept = ref_lg[t, idx[t]]
+        e = np.exp(kept - kept.max())
+        np.testing.assert_allclose(w[t], e / e.sum(), rtol=2e-6)
+
+
 @pytest.mark.parametrize("k", [1, 32])
 def test_route_k_edge(k):
     d = synth.Dims(hidden=128, latent=64, inter=64, n_experts=32, top_k=k)

@@ -37,9 +37,9 @@
  *   down_q [E][L][I/2], down_s [E][L][I/32] likewise.
  *
  * Conventions for every call:
- *   - Pointers are device pointers unless stated; the caller owns all memory. No call
- *     allocates device memory or synchronises the stream (except k3moe_check and
- *     k3moe_layer_stats).
+ *   - Pointers are device pointers unless stated; the caller owns all memory (except the
+ *     prepared-layer handle). No call allocates device memory or synchronises the stream
+ *     (except k3moe_layer_init, k3moe_layer_free, k3moe_check and k3moe_layer_stats).
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *   - Work is enqueued asynchronously; a returned K3MOE_OK means the launches were accepted.
  *   - T = 0 is valid and does nothing.
@@ -197,6 +197,27 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
                                  const uint16_t* x, int32_t T, uint16_t* y,
                                  int32_t* topk_idx_out, float* topk_w_out, void* ws,
                                  size_t ws_bytes, void* stream);
+
+/* Prepared layer (optional, once per layer, outside the hot path). k3moe_layer_init checks dims
+ * and weights as k3moe_layer_forward does and keeps a copy of both (the weight buffers must
+ * outlive the handle). When latent and inter are multiples of 128 it also repacks the expert
+ * scales gate_s, up_s and down_s into the image the decode expert kernel copies to tensor memory:
+ * for every 128 weight rows and 128 codes of K, one 512-byte block whose byte 16 l + 4 w + q is
+ * the scale of row 32 w + l, K-block 4 c + q. That copy (as many bytes as the three scale
+ * arrays) is device memory the handle owns; init allocates it, launches the repacking on
+ * `stream` and synchronises the stream. On failure *layer is NULL and nothing is kept.
+ * k3moe_layer_run is k3moe_layer_forward on the prepared layer, with the same arguments after
+ * the handle and the same results bit for bit; the decode expert kernel (T <= 64) then loads each
+ * stage's weight scales with one bulk copy next to the weight tile instead of gathering them row
+ * by row. It neither allocates nor synchronises. k3moe_layer_free releases the handle and its
+ * device memory (NULL is accepted; it synchronises the device while freeing). */
+typedef struct k3moe_layer k3moe_layer;
+k3moe_status k3moe_layer_init(const k3moe_dims* dims, const k3moe_weights* weights, k3moe_layer** layer,
+                              void* stream);
+k3moe_status k3moe_layer_run(const k3moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
+                             int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                             void* stream);
+k3moe_status k3moe_layer_free(k3moe_layer* layer);
 
 /* Synchronises `stream`, reads and clears the workspace error word. Returns K3MOE_OK,
  * K3MOE_E_TIMEOUT (a bounded wait ran out) or K3MOE_E_DEVICE (another device-side check),

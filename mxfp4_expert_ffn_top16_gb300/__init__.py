@@ -23,7 +23,7 @@ _LIBDIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(_LIBDIR, "libk3moe.so")
 
 SOURCES = ["k3moe_api.cu", "k_dense_gemv.cu", "k_expert_gemv.cu", "k_route.cu", "k_misc.cu",
-           "k_tma.cu", "k_umma_dense.cu", "k_umma_expert.cu", "k_umma_wn.cu",
+           "k_tma.cu", "k_umma_dense.cu", "k_umma_expert.cu", "k_umma_wm.cu",
            "k3moe_noalloc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-I" + _INCLUDE]
@@ -37,7 +37,8 @@ K3MOE_OK = 0
 EXPORTS = ["k3moe_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_project",
            "k3moe_expert_ffn_mxfp4", "k3moe_combine", "k3moe_layer_forward", "k3moe_check",
            "k3moe_status_string", "k3moe_profile", "k3moe_profile_name", "k3moe_route_noalloc",
-           "k3moe_layer_stats", "k3moe_selftest_timeout", "k3moe_selftest_occupy", "k3moe_layer_saliency"]
+           "k3moe_layer_stats", "k3moe_selftest_timeout", "k3moe_selftest_occupy", "k3moe_layer_saliency",
+           "k3moe_layer_init", "k3moe_layer_run", "k3moe_layer_free"]
 
 
 def _newer(target: str, deps) -> bool:
@@ -107,6 +108,9 @@ def lib():
             "k3moe_selftest_timeout": [p, p],
             "k3moe_selftest_occupy": [i32, i32, p],
             "k3moe_layer_saliency": [p, i32, p, p, p, sz, p, p],
+            "k3moe_layer_init": [p, p, p, p],
+            "k3moe_layer_run": [p, p, i32, p, p, p, p, sz, p],
+            "k3moe_layer_free": [p],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -190,6 +194,23 @@ def k3moe_layer_forward(dims, weights, x, T, y, topk_idx_out, topk_w_out, ws, ws
     return _ck(lib().k3moe_layer_forward(_ref(dims), _ref(weights), x, T, y, topk_idx_out,
                                          topk_w_out, ws, ws_bytes, stream),
                "k3moe_layer_forward", check)
+
+
+def k3moe_layer_init(dims, weights, stream=0):
+    """A prepared-layer handle (an integer) for k3moe_layer_run; release it with k3moe_layer_free.
+    dims and weights are copied into the handle; the weight buffers must outlive it."""
+    h = ctypes.c_void_p()
+    _ck(lib().k3moe_layer_init(_ref(dims), _ref(weights), ctypes.byref(h), stream), "k3moe_layer_init", True)
+    return h.value
+
+
+def k3moe_layer_run(layer, x, T, y, topk_idx_out, topk_w_out, ws, ws_bytes, stream=0, check=True):
+    return _ck(lib().k3moe_layer_run(layer, x, T, y, topk_idx_out, topk_w_out, ws, ws_bytes, stream),
+               "k3moe_layer_run", check)
+
+
+def k3moe_layer_free(layer):
+    return _ck(lib().k3moe_layer_free(layer), "k3moe_layer_free", True)
 
 
 def k3moe_layer_stats(dims, T, ws, ws_bytes, stream=0):

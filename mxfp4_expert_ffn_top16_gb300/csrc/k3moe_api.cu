@@ -5,6 +5,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <new>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -214,7 +215,8 @@ struct ProfScope {
 // token into bq / bs, and the routing kernel cleared the chunk counters.
 k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const uint16_t* z, int32_t T,
                               const int32_t* offsets, const int32_t* row_token, float* o_rows, void* ws,
-                              const WsLayout& L, cudaStream_t s, bool z_rows_ready = false) {
+                              const WsLayout& L, cudaStream_t s, bool z_rows_ready = false,
+                              const PackedScales* ps = nullptr) {
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* plan = at<int32_t>(ws, L.plan);
   if (umma_expert_ok(d)) {
@@ -225,22 +227,15 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
     uint8_t* aqs = at<uint8_t>(ws, L.aqs);
     if (T < kUmmaExpertMinTokens && P != 0) {
       // decode: z as P E4M3 rows per token (the expert kernel gathers a chunk's rows by token),
-      // weights on the MMA's N side; both passes in one launch when latent % 256 == 0
+      // weights on the MMA's M side, both passes in one launch
       if (!z_rows_ready) {
         ProfScope p(P_QUANT, s);
         K3_CUDA(launch_quant_rows(z, nullptr, T, T, d.latent, P, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs),
                                   cnt, decode_counters(d, T), err, s));
       }
-      const bool both = d.latent % 256 == 0;
-      {
-        ProfScope p(both ? P_FFN_MMA : P_GLU_MMA, s);
-        K3_CUDA(launch_umma_wn(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), row_token, P, T, aq,
-                               aqs, both, o_rows, cnt, err, s));
-      }
-      if (!both) {
-        ProfScope p(P_DOWN_MMA, s);
-        K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s));
-      }
+      ProfScope p(P_FFN_MMA, s);
+      K3_CUDA(launch_umma_decode(d, w, ps, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), row_token, P, T,
+                                 aq, aqs, o_rows, cnt, err, s));
       return K3MOE_OK;
     }
     {  // many tokens (and MXFP4 activations at any count): z gathered into rows per sorted row
@@ -269,7 +264,8 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
 
 // Route + permute + experts + combine for T tokens whose logits / z are already in ws.
 k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int32_t T, void* ws,
-                                const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s) {
+                                const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s,
+                                const PackedScales* ps) {
   uint32_t* err = at<uint32_t>(ws, L.err);
   if (T <= kSmallRouteTokens) {
     ProfScope p(P_PERMUTE, s);  // top-k, then permutation and plan (one kernel for a few tokens)
@@ -295,7 +291,8 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
   K3_TRY(run_expert_gemms(d, w, at<uint16_t>(ws, L.z), T, at<int32_t>(ws, L.offsets),
                           at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s,
                           T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens &&
-                              umma_expert_ok(d) && d.actq != 2));
+                              umma_expert_ok(d) && d.actq != 2,
+                          ps));
   {
     ProfScope p(P_COMBINE, s);
     K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,
@@ -424,10 +421,12 @@ k3moe_status k3moe_combine(const k3moe_dims* dims, const float* o_rows, const in
   return K3MOE_OK;
 }
 
-k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* weights,
-                                 const uint16_t* x, int32_t T, uint16_t* y,
-                                 int32_t* topk_idx_out, float* topk_w_out, void* ws,
-                                 size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+k3moe_status layer_forward(const k3moe_dims* dims, const k3moe_weights* weights, const PackedScales* ps,
+                           const uint16_t* x, int32_t T, uint16_t* y, int32_t* topk_idx_out, float* topk_w_out,
+                           void* ws, size_t ws_bytes, void* stream) {
   K3_TRY(check_dims(dims));
   const k3moe_dims& d = *dims;
   K3_TRY(check_weights(weights, true, true));
@@ -458,7 +457,7 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
                          rows ? at<uint8_t>(ws, L.bq) : nullptr, rows ? at<uint8_t>(ws, L.bs) : nullptr,
                          d.actq ? 1 : 2));
   }
-  K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s));
+  K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s, ps));
   // shared experts on the residual: g, u = G x, U x (fp32); a = bf16(silu(g) u)
   const int S = d.n_shared * d.shared_inter;
   if (S > 0) {
@@ -474,6 +473,76 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
                          S > 0 ? w.w_shared_down : nullptr, S > 0 ? at<uint16_t>(ws, L.sa) : nullptr, S));
   }
   return K3MOE_OK;
+}
+}  // namespace
+
+// A prepared layer: the caller's dims and weight pointers, and the expert scales repacked for
+// the decode expert kernel (device memory the handle owns).
+struct k3moe_layer {
+  k3moe_dims dims;
+  k3moe_weights weights;
+  void* packed;  // gate, up, down staging images back to back; null when the shapes have none
+  PackedScales ps;
+};
+
+extern "C" {
+
+k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* weights,
+                                 const uint16_t* x, int32_t T, uint16_t* y,
+                                 int32_t* topk_idx_out, float* topk_w_out, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  return layer_forward(dims, weights, nullptr, x, T, y, topk_idx_out, topk_w_out, ws, ws_bytes, stream);
+}
+
+k3moe_status k3moe_layer_init(const k3moe_dims* dims, const k3moe_weights* weights, k3moe_layer** layer,
+                              void* stream) {
+  if (!layer) return K3MOE_E_NULL;
+  *layer = nullptr;
+  K3_TRY(check_dims(dims));
+  const k3moe_dims& d = *dims;
+  K3_TRY(check_weights(weights, true, true));
+  K3_TRY(check_shared(d, weights));
+  k3moe_layer* h = new (std::nothrow) k3moe_layer();
+  if (!h) return K3MOE_E_CUDA;
+  h->dims = d;
+  h->weights = *weights;
+  if (umma_expert_ok(d)) {
+    const size_t gbytes = (size_t)d.n_experts * d.inter * (d.latent / 32);
+    const size_t dbytes = (size_t)d.n_experts * d.latent * (d.inter / 32);
+    uint8_t* p = nullptr;
+    if (cudaMalloc(&p, 2 * gbytes + dbytes) != cudaSuccess) {
+      delete h;
+      return K3MOE_E_CUDA;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long grows = (long long)d.n_experts * d.inter, drows = (long long)d.n_experts * d.latent;
+    if (launch_pack_scales(weights->gate_s, grows, d.latent, p, s) != cudaSuccess ||
+        launch_pack_scales(weights->up_s, grows, d.latent, p + gbytes, s) != cudaSuccess ||
+        launch_pack_scales(weights->down_s, drows, d.inter, p + 2 * gbytes, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+      cudaFree(p);
+      delete h;
+      return K3MOE_E_CUDA;
+    }
+    h->packed = p;
+    h->ps = PackedScales{p, p + gbytes, p + 2 * gbytes};
+  }
+  *layer = h;
+  return K3MOE_OK;
+}
+
+k3moe_status k3moe_layer_free(k3moe_layer* layer) {
+  if (!layer) return K3MOE_OK;
+  const bool ok = !layer->packed || cudaFree(layer->packed) == cudaSuccess;
+  delete layer;
+  return ok ? K3MOE_OK : K3MOE_E_CUDA;
+}
+
+k3moe_status k3moe_layer_run(const k3moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
+                             int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!layer) return K3MOE_E_NULL;
+  return layer_forward(&layer->dims, &layer->weights, layer->packed ? &layer->ps : nullptr, x, T, y, topk_idx_out,
+                       topk_w_out, ws, ws_bytes, stream);
 }
 
 k3moe_status k3moe_layer_saliency(const k3moe_dims* dims, int32_t T, const int32_t* topk_idx, const float* topk_w,

@@ -31,6 +31,11 @@ bool make_tmap_3d_chunks(CUtensorMap* out, const void* base, int elem_bytes, uin
 // multiples of 128 codes and 16 bytes.
 bool make_tmap_fp4(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
                    uint32_t box_rows);
+// e2m1 codes [rows][inner] as 3-D {128 codes, rows, inner / 128 chunks} (inner a multiple of
+// 128): a box of box_rows rows x box_chunks consecutive 128-code chunks, each chunk a 128-byte
+// swizzled tile of box_rows rows in shared memory.
+bool make_tmap_fp4_chunks(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                          uint32_t box_rows, uint32_t box_chunks);
 
 // ------------------------------------------------------------------ error word
 // Bits of the uint32 error word at offset 0 of the workspace.
@@ -164,17 +169,26 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
                             cudaStream_t s);
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s);
-// Decode (T < kUmmaExpertMinTokens): the same GEMMs with the weights on the MMA's N side (256
-// weight rows per MMA, 8-row chunks): the GLU pass, and with_down (needs latent % 256 == 0) the
-// down pass in the same launch. chunk_done: decode_counters ints, zero at launch (GLU items
-// finished per chunk, then the kernel's item counter); the kernel leaves them non-zero, the next
-// routing or row-quantisation launch clears them.
+// Decode (T < kUmmaExpertMinTokens): both GEMMs in one launch, the weights on the MMA's M side
+// (128 weight rows per MMA) and a chunk's up to 8 sorted rows on N. chunk_done: decode_counters
+// ints, zero at launch (GLU items finished per chunk, then the kernel's item counter); the kernel
+// leaves them non-zero, the next routing or row-quantisation launch clears them.
 // zq / zqs: the latent activations as P E4M3 rows per token [T][P][L] with e8m0 scales
 // [T][P][exp_pitch(L)]; the kernel gathers a chunk's rows through row_token.
-cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* zq,
-                           const uint8_t* zqs, const int32_t* row_token, int P, int T, uint8_t* aq,
-                           uint8_t* aqs, bool with_down, float* o_rows, int* chunk_done, uint32_t* err,
-                           cudaStream_t s);
+// ps (may be null): the weight scales repacked by launch_pack_scales.
+struct PackedScales {
+  const uint8_t* gate;  // gate_s, rows E * I, K = L
+  const uint8_t* up;    // up_s
+  const uint8_t* down;  // down_s, rows E * L, K = I
+};
+cudaError_t launch_umma_decode(const k3moe_dims& d, const k3moe_weights& w, const PackedScales* ps, int32_t* plan,
+                               const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,
+                               uint8_t* aq, uint8_t* aqs, float* o_rows, int* chunk_done, uint32_t* err,
+                               cudaStream_t s);
+// e8m0 scales [rows][K/32] (rows a multiple of 128, K of 128) -> the decode kernel's staging
+// image (same size): per 128 rows and 128-code chunk a 512-byte block whose byte 16 l + 4 w + q
+// is the scale of row 32 w + l, K-block 4 chunk + q.
+cudaError_t launch_pack_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t s);
 inline int plan_chunks_max(const k3moe_dims& d, long long T) {
   return (int)(T * d.top_k / kGemvTokens + d.n_experts + 1);
 }

@@ -61,7 +61,8 @@ bool encode_cached(CUtensorMap* out, const Key& k) {
   // dim 0: `inner` contiguous elements; dim 1: rows `pitch` bytes apart; dim 2 (3-D only):
   // consecutive chunks of `inner` elements along a row (inner * elem bytes apart)
   cuuint64_t dims[3] = {k.inner, k.rows, k.chunks};
-  cuuint64_t strides[2] = {k.pitch, (cuuint64_t)k.inner * k.elem};
+  // (an e2m1 chunk of `inner` codes takes inner / 2 bytes)
+  cuuint64_t strides[2] = {k.pitch, k.elem == kElemFp4 ? (cuuint64_t)k.inner / 2 : (cuuint64_t)k.inner * k.elem};
   cuuint32_t box[3] = {k.box_inner, k.box_rows, k.box_chunks};
   cuuint32_t estr[3] = {1, 1, 1};
   CUtensorMap m;
@@ -131,6 +132,23 @@ bool make_tmap_3d_chunks(CUtensorMap* out, const void* base, int elem_bytes, uin
   k.box_chunks = box_chunks;
   k.elem = (uint32_t)elem_bytes;
   k.swz = swizzle128 ? 1u : 0u;
+  return encode_cached(out, k);
+}
+
+bool make_tmap_fp4_chunks(CUtensorMap* out, const void* base, uint64_t inner, uint64_t rows, uint64_t pitch_bytes,
+                          uint32_t box_rows, uint32_t box_chunks) {
+  Key k;
+  std::memset(&k, 0, sizeof(k));
+  k.base = base;
+  k.inner = 128;
+  k.rows = rows;
+  k.pitch = pitch_bytes;
+  k.chunks = inner / 128;
+  k.box_inner = 128;
+  k.box_rows = box_rows;
+  k.box_chunks = box_chunks;
+  k.elem = kElemFp4;
+  k.swz = 1u;
   return encode_cached(out, k);
 }
 

@@ -141,3 +141,21 @@ def test_layer_saliency_arguments(L):
     assert L.k3moe_layer_saliency(ctypes.byref(dm), 4, None, None, good, n - 1, good, None) == 4
     assert L.k3moe_layer_saliency(ctypes.byref(dm), -1, None, None, good, n, good, None) == 2
     assert L.k3moe_layer_saliency(ctypes.byref(dm), 0, None, None, good, n, good, None) == 0
+
+
+def test_prepared_layer_arguments(L):
+    """k3moe_layer_init / k3moe_layer_run / k3moe_layer_free reject bad arguments before any
+    allocation or launch (no GPU needed); freeing NULL is allowed."""
+    good = 1 << 16
+    h = ctypes.c_void_p(123)
+    w = k3.Weights(good, None, good, good, good, good, good, good, good, good)
+    assert L.k3moe_layer_init(ctypes.byref(dims()), ctypes.byref(w), None, None) == 1
+    assert L.k3moe_layer_init(ctypes.byref(dims(latent=100)), ctypes.byref(w), ctypes.byref(h), None) == 2
+    assert h.value is None  # a failed init leaves no handle
+    w.up_s = good + 4
+    assert L.k3moe_layer_init(ctypes.byref(dims()), ctypes.byref(w), ctypes.byref(h), None) == 3
+    w.up_s = None
+    assert L.k3moe_layer_init(ctypes.byref(dims()), ctypes.byref(w), ctypes.byref(h), None) == 1
+    assert L.k3moe_layer_init(ctypes.byref(dims(act=1)), ctypes.byref(w), ctypes.byref(h), None) == 5
+    assert L.k3moe_layer_run(None, good, 1, good, None, None, good, 1 << 30, None) == 1
+    assert L.k3moe_layer_free(None) == 0

@@ -435,3 +435,41 @@ def test_layer_k3_prefill_sampled(k3_layer):
         _compare_layer(k3_layer, x, y, idx, np.arange(0, T, 16))
     finally:
         k3_layer.bias_host = None
+
+
+def _run_prepared(lay, h, x_np, ws):
+    d = lay.d
+    T = x_np.shape[0]
+    y = torch.empty((T, d.hidden), dtype=torch.int16, device=DEV)
+    idx = torch.empty((T, d.top_k), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, d.top_k), dtype=torch.float32, device=DEV)
+    xd = up(x_np)
+    k3.k3moe_layer_run(h, xd.data_ptr(), T, y.data_ptr(), idx.data_ptr(), w.data_ptr(), ws[0].data_ptr(), ws[1],
+                       stream())
+    check_ok(ws[0])
+    return bf16_np(y), idx.cpu().numpy(), w.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,actq,Ts", [("tiny", 0, (1, 5, 8)), ("tiny", 1, (1, 8)), ("wide", 0, (1, 4)),
+                                          ("deep", 1, (2,)), ("k3", 0, (1, 3, 64)), ("k3", 1, (1, 16)),
+                                          ("k3", 2, (1,))])
+def test_prepared_layer_same_bits_as_forward(name, actq, Ts, k3_layer):
+    """k3moe_layer_run on a prepared layer (scales repacked once into the tensor-memory staging
+    image) gives the bits k3moe_layer_forward gives: a misplaced scale would change them, since
+    every expert's scales vary. tiny and wide cover stages of one 128-code chunk and a single
+    two-chunk stage; K3 the full decode kernel."""
+    d = {"tiny": synth.TINY, "wide": WIDE, "deep": DEEP, "k3": synth.K3}[name]
+    lay = k3_layer if name == "k3" else DeviceLayer(d, seed=3, actq=actq)
+    dm = dims(d, actq=actq)  # (the weights do not depend on the activation mode)
+    h = k3.k3moe_layer_init(dm, lay.weights, stream())
+    try:
+        for T in Ts:
+            x = synth.host_x(synth.WORKLOADS["decode_b1"], 11, T) if name == "k3" else \
+                synth.host_bf16_normal(9, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+            ws = workspace(dm, T)
+            want = run_layer(lay, x, dm=dm, ws=ws)
+            got = _run_prepared(lay, h, x, ws)
+            for a, b in zip(got, want):
+                np.testing.assert_array_equal(a, b)
+    finally:
+        k3.k3moe_layer_free(h)

@@ -21,6 +21,17 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return (uint16_t)(u >> 16);
 }
 
+// One term of the routing-weighted combine: s += w * v as a Kahan-compensated fp32 sum (c the
+// compensation), the product rounded on its own. Explicit round-to-nearest operations, so the
+// product is never contracted into the sum and the result does not depend on the compiler.
+__device__ __forceinline__ void combine_term(float& s, float& c, float w, float v) {
+  const float y = __fsub_rn(__fmul_rn(w, v), c);
+  const float t = __fadd_rn(s, y);
+  c = __fsub_rn(__fsub_rn(t, s), y);
+  s = t;
+}
+__device__ __forceinline__ uint16_t combine_result(float s, float c) { return f32_to_bf16(__fsub_rn(s, c)); }
+
 // floor(log2|v|) for a finite nonzero normal fp32 v; -127 for zero and subnormals.
 __device__ __forceinline__ int ilog2_floor(float v) {
   int e = (int)((__float_as_uint(v) >> 23) & 0xff);
@@ -190,6 +201,31 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
           smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Streaming loads of weights that are read once per step: an L2 policy that evicts them first,
+// so that what the next kernels read again (their code, the small activation and routing
+// tensors) is not pushed out of L2 by hundreds of MB of weights.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void tma_load_3d_stream(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                                   uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 

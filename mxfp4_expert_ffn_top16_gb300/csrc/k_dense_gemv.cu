@@ -84,18 +84,32 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
     fence_mbar_init();
   }
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
 
   const int KC = 64 * NB;
   const int nkc0 = K / KC, nkc = nkc0 + args.nkc1;
   const int nchunks = (T + ntok - 1) / ntok;
+  // No earlier kernel writes the weights: the loading thread sends the first stages' weight
+  // tiles out before the grid dependency wait, while the kernel before this one finishes (its
+  // token tiles, which that kernel may write, follow after the wait).
+  const int npre = blockIdx.x < args.units ? (NS < nkc0 ? NS : nkc0) : 0;
+  if (threadIdx.x == 0) {
+    const int u = blockIdx.x, pi = u < args.units0 ? 0 : 1;
+    const int row0 = (pi == 0 ? u : u - args.units0) * kUnitRows;
+    const uint64_t pol = l2_evict_first();
+    for (int kc = 0; kc < npre; ++kc) {
+      mbar_arrive_expect_tx(&full[kc], (uint32_t)stage_bytes);
+      tma_load_3d_stream(stages + kc * stage_bytes, &args.tw[pi], 0, row0, kc * NB, &full[kc], pol);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     // ---------------- producer (lane 0 issues)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    const uint64_t pol = l2_evict_first();
     for (int u = blockIdx.x; u < args.units && ok; u += gridDim.x) {
       const int pi = u < args.units0 ? 0 : 1;
       const int row0 = (pi == 0 ? u : u - args.units0) * kUnitRows;
@@ -103,10 +117,13 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
         for (int kc = 0; kc < nkc; ++kc) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, args.err)) { ok = false; break; }
           if (lane == 0) {  // one copy for the NB weight tiles, one for the NB token tiles
-            mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
             uint8_t* dst = stages + s * stage_bytes;
             const bool seg2 = kc >= nkc0;  // second K segment (problem 0 only)
-            tma_load_3d(dst, seg2 ? &args.tw2 : &args.tw[pi], 0, row0, (seg2 ? kc - nkc0 : kc) * NB, &full[s]);
+            if (u != (int)blockIdx.x || ch != 0 || kc >= npre) {  // (else sent before the wait)
+              mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+              tma_load_3d_stream(dst, seg2 ? &args.tw2 : &args.tw[pi], 0, row0, (seg2 ? kc - nkc0 : kc) * NB,
+                                 &full[s], pol);
+            }
             tma_load_3d(dst + NB * wbox, seg2 ? &args.tx2 : &args.tx, 0, ch * ntok, (seg2 ? kc - nkc0 : kc) * NB,
                         &full[s]);
           }

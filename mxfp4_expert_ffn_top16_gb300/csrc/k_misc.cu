@@ -47,18 +47,14 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
 #pragma unroll
   for (int j = 0; j < KB; ++j) {
     if (rr[j] < 0) continue;
-    const float p[4] = {wj[j] * v[j].x, wj[j] * v[j].y, wj[j] * v[j].z, wj[j] * v[j].w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float yk = p[q] - cc[q];
-      const float tk = s[q] + yk;
-      cc[q] = (tk - s[q]) - yk;
-      s[q] = tk;
-    }
+    combine_term(s[0], cc[0], wj[j], v[j].x);
+    combine_term(s[1], cc[1], wj[j], v[j].y);
+    combine_term(s[2], cc[2], wj[j], v[j].z);
+    combine_term(s[3], cc[3], wj[j], v[j].w);
   }
   uint2 packed;
-  packed.x = (uint32_t)f32_to_bf16(s[0] - cc[0]) | ((uint32_t)f32_to_bf16(s[1] - cc[1]) << 16);
-  packed.y = (uint32_t)f32_to_bf16(s[2] - cc[2]) | ((uint32_t)f32_to_bf16(s[3] - cc[3]) << 16);
+  packed.x = (uint32_t)combine_result(s[0], cc[0]) | ((uint32_t)combine_result(s[1], cc[1]) << 16);
+  packed.y = (uint32_t)combine_result(s[2], cc[2]) | ((uint32_t)combine_result(s[3], cc[3]) << 16);
   *reinterpret_cast<uint2*>(c + (size_t)t * L + n) = packed;
 }
 

@@ -267,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wm_kernel(const __grid_const
       // its current one: a held GLU item sits behind a GLU item, which never waits, so every
       // claimed GLU item still gets run.
       int next = atomicAdd(A.item_counter, 1);
+      const uint64_t stream_policy = l2_evict_first();
       while (ok) {
         const int u = next < items ? next : -1;
         if (!mbar_wait_bounded(&qempty[qs], qph ^ 1, abort_flag, A.err)) break;
@@ -298,10 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wm_kernel(const __grid_const
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[s], wbytes + abytes);
           const int kr = it.glu ? kc >> 1 : kc;  // K range of the stage
-          tma_load_3d(sA + s * kATile, (it.glu && (kc & 1)) ? &W.tw1 : &W.tw0, 0, wrow, kr * cps, &full[s]);
+          tma_load_3d_stream(sA + s * kATile, (it.glu && (kc & 1)) ? &W.tw1 : &W.tw0, 0, wrow, kr * cps, &full[s],
+                             stream_policy);
           if (W.p0)
-            bulk_g2s(stg + s * kSfBytes, ((it.glu && (kc & 1)) ? W.p1 : W.p0) + (pblk + (size_t)kr * cps) * 512,
-                     512u * cps, &full[s]);
+            bulk_g2s_stream(stg + s * kSfBytes,
+                            ((it.glu && (kc & 1)) ? W.p1 : W.p0) + (pblk + (size_t)kr * cps) * 512, 512u * cps,
+                            &full[s], stream_policy);
           if (!it.glu && kc >= npre) tma_load_3d(sB + s * kBTile, &W.ta, 0, P * it.r0, kr * cps, &full[s]);
           if (++s == kStages) { s = 0; ph ^= 1; }
         }

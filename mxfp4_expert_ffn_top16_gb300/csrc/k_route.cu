@@ -436,8 +436,8 @@ __device__ void route_one_token(int E, int k, int own_e, int32_t* offsets, int32
   __syncthreads();
   for (int e = tid; e <= E; e += blockDim.x) {  // rows of the experts below e
     int c = 0;
-#pragma unroll 1
-    for (int j = 0; j < k; ++j) c += s_sel[j] < e ? 1 : 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c += (j < k && s_sel[j] < e) ? 1 : 0;  // independent loads
     offsets[e] = c;
   }
   if (tid < k) {

@@ -23,7 +23,7 @@ _LIBDIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(_LIBDIR, "libk3moe.so")
 
 SOURCES = ["k3moe_api.cu", "k_dense_gemv.cu", "k_expert_gemv.cu", "k_route.cu", "k_misc.cu",
-           "k_tma.cu", "k_umma_dense.cu", "k_umma_expert.cu", "k_umma_wm.cu",
+           "k_tma.cu", "k_umma_dense.cu", "k_umma_expert.cu", "k_umma_wm.cu", "k_umma_wn.cu",
            "k3moe_noalloc.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-I" + _INCLUDE]

@@ -226,16 +226,29 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
     uint8_t* aq = at<uint8_t>(ws, L.aq);
     uint8_t* aqs = at<uint8_t>(ws, L.aqs);
     if (T < kUmmaExpertMinTokens && P != 0) {
-      // decode: z as P E4M3 rows per token (the expert kernel gathers a chunk's rows by token),
-      // weights on the MMA's M side, both passes in one launch
+      // decode: z as P E4M3 rows per token (the expert kernel gathers a chunk's rows by token);
+      // both passes in one launch (on the N side when latent % 256 == 0)
       if (!z_rows_ready) {
         ProfScope p(P_QUANT, s);
         K3_CUDA(launch_quant_rows(z, nullptr, T, T, d.latent, P, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs),
                                   cnt, decode_counters(d, T), err, s));
       }
-      ProfScope p(P_FFN_MMA, s);
-      K3_CUDA(launch_umma_decode(d, w, ps, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), row_token, P, T,
-                                 aq, aqs, o_rows, cnt, err, s));
+      if (decode_weights_on_m(P, T)) {
+        ProfScope p(P_FFN_MMA, s);
+        K3_CUDA(launch_umma_decode(d, w, ps, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), row_token, P, T,
+                                   aq, aqs, o_rows, cnt, err, s));
+      } else {
+        const bool both = d.latent % 256 == 0;
+        {
+          ProfScope p(both ? P_FFN_MMA : P_GLU_MMA, s);
+          K3_CUDA(launch_umma_wn(d, w, ps, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), row_token, P, T, aq,
+                                 aqs, both, o_rows, cnt, err, s));
+        }
+        if (!both) {
+          ProfScope p(P_DOWN_MMA, s);
+          K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s));
+        }
+      }
       return K3MOE_OK;
     }
     {  // many tokens (and MXFP4 activations at any count): z gathered into rows per sorted row

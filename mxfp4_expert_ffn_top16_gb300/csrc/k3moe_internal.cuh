@@ -185,6 +185,19 @@ cudaError_t launch_umma_decode(const k3moe_dims& d, const k3moe_weights& w, cons
                                const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,
                                uint8_t* aq, uint8_t* aqs, float* o_rows, int* chunk_done, uint32_t* err,
                                cudaStream_t s);
+// The same GEMMs with the weights on the MMA's N side (256 weight rows per MMA, the chunk's
+// activation rows on M = 128): half the MMA instructions per weight byte, which pays once chunks
+// carry more than 8 activation rows. GLU pass, and with_down (latent % 256 == 0) the down pass in
+// the same launch; chunk_done and zq / zqs as for launch_umma_decode.
+cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, const PackedScales* ps, int32_t* plan,
+                           const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,
+                           uint8_t* aq, uint8_t* aqs, bool with_down, float* o_rows, int* chunk_done,
+                           uint32_t* err, cudaStream_t s);
+// Which decode kernel: the weights on M for bf16 activations (P = 2) with at most 4 tokens (a
+// chunk then carries at most 8 activation rows), on N otherwise. Measured at decode_b1: 92.5
+// against 94.1 us per step for bf16, 92.6 against 91.8 for MXFP8; at decode_b64 the N side is
+// ahead in both modes.
+inline bool decode_weights_on_m(int P, long long T) { return P == 2 && T <= 4; }
 // e8m0 scales [rows][K/32] (rows a multiple of 128, K of 128) -> the decode kernel's staging
 // image (same size): per 128 rows and 128-code chunk a 512-byte block whose byte 16 l + 4 w + q
 // is the scale of row 32 w + l, K-block 4 chunk + q.

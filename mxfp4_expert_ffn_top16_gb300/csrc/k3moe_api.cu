@@ -216,7 +216,7 @@ struct ProfScope {
 k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const uint16_t* z, int32_t T,
                               const int32_t* offsets, const int32_t* row_token, float* o_rows, void* ws,
                               const WsLayout& L, cudaStream_t s, bool z_rows_ready = false,
-                              const PackedScales* ps = nullptr) {
+                              const PackedScales* ps = nullptr, const DecodeSelect* sel = nullptr) {
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* plan = at<int32_t>(ws, L.plan);
   if (umma_expert_ok(d)) {
@@ -236,7 +236,7 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
       if (decode_weights_on_m(P, T)) {
         ProfScope p(P_FFN_MMA, s);
         K3_CUDA(launch_umma_decode(d, w, ps, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), row_token, P, T,
-                                   aq, aqs, o_rows, cnt, err, s));
+                                   aq, aqs, o_rows, cnt, err, s, sel));
       } else {
         const bool both = d.latent % 256 == 0;
         {
@@ -276,11 +276,21 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
 }
 
 // Route + permute + experts + combine for T tokens whose logits / z are already in ws.
+// One token on the tensor-core expert kernel with the weights on M: that kernel selects the
+// experts itself (the dense kernel before it clears its counters), no routing kernel runs.
+inline bool decode_select_in_experts(const k3moe_dims& d, int32_t T) {
+  return T == 1 && umma_expert_ok(d) && d.actq == 0 && decode_weights_on_m(2, T) && T < kUmmaDenseMinTokens &&
+         d.top_k <= 32;
+}
+
 k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int32_t T, void* ws,
                                 const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s,
                                 const PackedScales* ps) {
   uint32_t* err = at<uint32_t>(ws, L.err);
-  if (T <= kSmallRouteTokens) {
+  const bool fused_select = decode_select_in_experts(d, T);
+  if (fused_select) {
+    // (no routing kernel: the expert kernel selects the experts and writes the routing outputs)
+  } else if (T <= kSmallRouteTokens) {
     ProfScope p(P_PERMUTE, s);  // top-k, then permutation and plan (one kernel for a few tokens)
     K3_CUDA(launch_route_tail_small(at<float>(ws, L.logits), T, d.n_experts, d.top_k, idx, wts,
                                     at<int32_t>(ws, L.offsets), at<int32_t>(ws, L.row_token),
@@ -301,11 +311,13 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
   }
   // (decode, tensor-core experts: the dense kernel wrote z's E4M3 rows, the routing cleared the
   // chunk counters)
+  const DecodeSelect sel{at<float>(ws, L.logits), idx, wts, at<int32_t>(ws, L.offsets),
+                         at<int32_t>(ws, L.row_token), at<int32_t>(ws, L.row_slot), at<int32_t>(ws, L.slot_row)};
   K3_TRY(run_expert_gemms(d, w, at<uint16_t>(ws, L.z), T, at<int32_t>(ws, L.offsets),
                           at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s,
                           T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens &&
                               umma_expert_ok(d) && d.actq != 2,
-                          ps));
+                          ps, fused_select ? &sel : nullptr));
   {
     ProfScope p(P_COMBINE, s);
     K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,
@@ -464,11 +476,15 @@ k3moe_status layer_forward(const k3moe_dims* dims, const k3moe_weights* weights,
     // decode on the tensor-core experts: z also as P E4M3 rows per token for the expert kernel
     const bool rows = !f16_copy && d.actq != 2 && T <= kSmallRouteTokens && T < kUmmaExpertMinTokens &&
                       T < kUmmaDenseMinTokens;
+    // (when the expert kernel selects the experts itself, this kernel clears its counters)
+    const bool fused_select = decode_select_in_experts(d, T);
     K3_CUDA(launch_dense(w.w_router, d.n_experts, at<float>(ws, L.logits), nullptr, w.router_bias, w.w_in,
                          d.latent, at<uint16_t>(ws, L.z), f16_copy ? at<__half>(ws, L.zh) : nullptr,
                          f16_copy ? at<int8_t>(ws, L.zs) : nullptr, d.actq, x, T, d.hidden, err, s,
                          rows ? at<uint8_t>(ws, L.bq) : nullptr, rows ? at<uint8_t>(ws, L.bs) : nullptr,
-                         d.actq ? 1 : 2));
+                         d.actq ? 1 : 2, nullptr, nullptr, nullptr, 0,
+                         fused_select ? at<int>(ws, L.chunk_done) : nullptr,
+                         fused_select ? decode_counters(d, T) : 0));
   }
   K3_TRY(run_experts_decode(d, w, T, ws, L, idx, wts, s, ps));
   // shared experts on the residual: g, u = G x, U x (fp32); a = bf16(silu(g) u)

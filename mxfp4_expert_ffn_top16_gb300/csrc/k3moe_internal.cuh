@@ -98,12 +98,15 @@ inline __host__ __device__ size_t plan_bytes(int E, long long rows) {
 
 // ------------------------------------------------------------------ launchers
 // Each returns cudaSuccess or the launch error.
+// zero / nzero (optional): ints the kernel clears after its grid dependency wait (the decode
+// expert kernel's counters, when no routing kernel runs in between).
 cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
                               int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q = nullptr,
                               uint8_t* out1_qs = nullptr, int q1P = 0, float* out1_f32 = nullptr,
-                              const uint16_t* W0b = nullptr, const uint16_t* xb = nullptr, int Kb = 0);
+                              const uint16_t* W0b = nullptr, const uint16_t* xb = nullptr, int Kb = 0,
+                              int* zero = nullptr, int nzero = 0);
 // Same contract as launch_dense_gemv (less the E4M3 rows), on tcgen05 tiles (for many tokens).
 cudaError_t launch_umma_dense(const uint16_t* W0, int N0, float* out0_f32, uint16_t* out0_bf16,
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
@@ -121,12 +124,13 @@ inline cudaError_t launch_dense(const uint16_t* W0, int N0, float* out0_f32, uin
                                 __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T, int K,
                                 uint32_t* err, cudaStream_t s, uint8_t* out1_q = nullptr,
                                 uint8_t* out1_qs = nullptr, int q1P = 0, float* out1_f32 = nullptr,
-                                const uint16_t* W0b = nullptr, const uint16_t* xb = nullptr, int Kb = 0) {
+                                const uint16_t* W0b = nullptr, const uint16_t* xb = nullptr, int Kb = 0,
+                                int* zero = nullptr, int nzero = 0) {
   if (T >= kUmmaDenseMinTokens)
     return launch_umma_dense(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
                              T, K, err, s, out1_f32, W0b, xb, Kb);
   return launch_dense_gemv(W0, N0, out0_f32, out0_bf16, bias0, W1, N1, out1_bf16, out1_h, out1_s, actq1, x,
-                           T, K, err, s, out1_q, out1_qs, q1P, out1_f32, W0b, xb, Kb);
+                           T, K, err, s, out1_q, out1_qs, q1P, out1_f32, W0b, xb, Kb, zero, nzero);
 }
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, float* w,
                         cudaStream_t s);
@@ -181,10 +185,22 @@ struct PackedScales {
   const uint8_t* up;    // up_s
   const uint8_t* down;  // down_s, rows E * L, K = I
 };
+// sel (optional, one token): the kernel selects the experts itself from the router logits (no
+// routing kernel before it); every CTA builds the plan in shared memory, CTA 0 also writes the
+// routing outputs (topk_idx, topk_w, offsets, row_token, row_slot, slot_row, plan).
+struct DecodeSelect {
+  const float* logits;
+  int32_t* idx;
+  float* wts;
+  int32_t* offsets;
+  int32_t* row_token;
+  int32_t* row_slot;
+  int32_t* slot_row;
+};
 cudaError_t launch_umma_decode(const k3moe_dims& d, const k3moe_weights& w, const PackedScales* ps, int32_t* plan,
                                const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,
                                uint8_t* aq, uint8_t* aqs, float* o_rows, int* chunk_done, uint32_t* err,
-                               cudaStream_t s);
+                               cudaStream_t s, const DecodeSelect* sel = nullptr);
 // The same GEMMs with the weights on the MMA's N side (256 weight rows per MMA, the chunk's
 // activation rows on M = 128): half the MMA instructions per weight byte, which pays once chunks
 // carry more than 8 activation rows. GLU pass, and with_down (latent % 256 == 0) the down pass in

@@ -54,6 +54,8 @@ struct DenseArgs {
   // K steps follow the first K / (64 NB)
   CUtensorMap tw2, tx2;
   int nkc1;
+  int* zero;           // optional: cleared after the grid dependency wait
+  int nzero;
   uint32_t* err;
 };
 
@@ -103,6 +105,8 @@ __global__ void __launch_bounds__(kThreads, 1) dense_gemv_kernel(const __grid_co
   }
   pdl_wait();
   pdl_trigger();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < args.nzero; i += blockDim.x) args.zero[i] = 0;
 
   if (warp == 0) {
     // ---------------- producer (lane 0 issues)
@@ -302,7 +306,8 @@ cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint1
                               const float* bias0, const uint16_t* W1, int N1, uint16_t* out1_bf16,
                               __half* out1_h, int8_t* out1_s, int actq1, const uint16_t* x, int T,
                               int K, uint32_t* err, cudaStream_t s, uint8_t* out1_q, uint8_t* out1_qs, int q1P,
-                              float* out1_f32, const uint16_t* W0b, const uint16_t* xb, int Kb) {
+                              float* out1_f32, const uint16_t* W0b, const uint16_t* xb, int Kb, int* zero,
+                              int nzero) {
   if (T <= 0) return cudaSuccess;
   if (W0b && (W1 || !xb || Kb <= 0 || Kb % 64)) return cudaErrorInvalidValue;
   DenseArgs a{};
@@ -314,6 +319,8 @@ cudaError_t launch_dense_gemv(const uint16_t* W0, int N0, float* out0_f32, uint1
   a.T = T;
   a.K = K;
   a.err = err;
+  a.zero = zero;
+  a.nzero = zero ? nzero : 0;
   if (a.units == 0) return cudaSuccess;
   const uint16_t* W[2] = {W0, W1};
   const int N[2] = {N0, N1};

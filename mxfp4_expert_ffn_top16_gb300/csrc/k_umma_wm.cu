@@ -29,6 +29,12 @@
 // item's accumulator and run the epilogue. Two accumulator buffers: the next item's MMAs start
 // while the epilogue still reads the last one.
 //
+// For one token the kernel can also do the routing: after the grid dependency wait every CTA
+// selects the token's experts from the router logits (the same block-wide selection as the
+// routing kernel) and keeps the plan in shared memory (chunk c = selected expert c, sorted row
+// c); CTA 0 also writes the routing outputs. That saves a launch, its hand-off and the plan's
+// round trip through global memory.
+//
 // One launch runs both passes: the GLU items, then the down items. Persistent CTAs claim items
 // from a global counter in that order (the loading thread claims, one item ahead, and passes each
 // claimed item to the CTA's other roles through a small shared-memory queue), so an SM that has
@@ -44,6 +50,7 @@
 
 #include "k3moe_device.cuh"
 #include "k3moe_internal.cuh"
+#include "k3moe_select.cuh"
 #include "k3moe_umma.cuh"
 
 namespace k3moe {
@@ -103,6 +110,8 @@ struct UWmArgs {
   float* o_out;        // down output [rows][latent] fp32
   int* chunk_done;     // GLU items finished per chunk, times 4 (one count per epilogue warp); zeroed
   int* item_counter;   // items claimed so far; zeroed
+  DecodeSelect sel;    // logits non-null: one token, the kernel selects its experts (see launch_umma_decode)
+  int k;
   uint32_t* err;
 };
 
@@ -225,9 +234,22 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wm_kernel(const __grid_const
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
 
-  const int4* ctab = plan_ctab(A.plan, A.E);
-  const int C0 = A.plan[1];
-  const int C = (C0 > 0 && C0 <= A.rows_max / kRows + A.E) ? C0 : 0;
+  __shared__ int4 s_ctab[32];
+  const int4* ctab;
+  int C;
+  if (A.sel.logits) {  // one token: select its experts here (all 256 threads)
+    const int own_e = block_topk(A.sel.logits, 0, A.E, A.k, A.sel.idx, A.sel.wts, blockIdx.x == 0);
+    if (threadIdx.x < A.k) s_ctab[threadIdx.x] = make_int4(own_e, threadIdx.x, 1, 0);
+    if (blockIdx.x == 0)  // (CTA-uniform)
+      route_one_token(A.E, A.k, own_e, A.sel.offsets, A.sel.row_token, A.sel.row_slot, A.sel.slot_row, A.plan);
+    __syncthreads();
+    ctab = s_ctab;
+    C = A.k;
+  } else {
+    ctab = plan_ctab(A.plan, A.E);
+    const int C0 = A.plan[1];
+    C = (C0 > 0 && C0 <= A.rows_max / kRows + A.E) ? C0 : 0;
+  }
   const int fbs_g = A.pass[0].N / kMW, fbs_d = A.pass[1].N / kMW;
   const int items_g = C * fbs_g;
   const int items = items_g + C * fbs_d;
@@ -339,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wm_kernel(const __grid_const
       const size_t wrow = (size_t)it.e * W.N + it.f0;
       // token of a sorted row (checked: a bad one reads token 0 and sets the error word)
       auto token = [&](int r) -> size_t {
+        if (A.ntok == 1) return 0;  // (one token: every row is its; the table may still be written)
         const int t = __ldg(A.row_token + r);
         if (t >= 0 && t < A.ntok) return (size_t)t;
         atomicOr(A.err, kErrIndex);
@@ -597,8 +620,9 @@ cudaError_t launch_pack_scales(const uint8_t* src, long long rows, int K, uint8_
 cudaError_t launch_umma_decode(const k3moe_dims& d, const k3moe_weights& w, const PackedScales* ps, int32_t* plan,
                                const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,
                                uint8_t* aq, uint8_t* aqs, float* o_rows, int* chunk_done, uint32_t* err,
-                               cudaStream_t s) {
+                               cudaStream_t s, const DecodeSelect* sel) {
   if (d.latent % 128 || d.inter % 128 || (P != 1 && P != 2)) return cudaErrorInvalidValue;
+  if (sel && (T != 1 || d.top_k > 32)) return cudaErrorInvalidValue;
   // activation rows per chunk: P x (sorted rows of one expert, at most T and kRows)
   const int RB = P * (T < kRows ? T : kRows) <= 8 ? 8 : 16;
   UWmArgs A{};
@@ -627,6 +651,8 @@ cudaError_t launch_umma_decode(const k3moe_dims& d, const k3moe_weights& w, cons
   A.plan = plan; A.row_token = row_token; A.ntok = T; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.o_out = o_rows; A.chunk_done = chunk_done; A.err = err;
   A.item_counter = chunk_done + plan_chunks_max(d, T);
+  if (sel) A.sel = *sel;
+  A.k = d.top_k;
   if (P == 1) return launch_t<1, 8>(A, items_max, s);
   return RB == 8 ? launch_t<2, 8>(A, items_max, s) : launch_t<2, 16>(A, items_max, s);
 }

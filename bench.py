@@ -10,7 +10,7 @@ line. ``value`` is device-timed throughput (CUDA events around exactly K steps, 
 resident in HBM); ``e2e`` is the same through the C ABI with the step's tokens copied from
 pinned host memory and its output copied back inside the timed region. Caches: the expert
 store (15.7 GB) is far larger than L2, tokens are fresh every step, and the dense weights
-rotate over 4 copies (462 MB) so no step finds them in L2.
+rotate over 8 copies (923 MB) so no step finds them in L2.
 
 --impl reference times the CPU oracle (plain C, double accumulation) on the host cores on a
 bounded sample of the same workload; see cpu_sample().
@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (decode b1/b64, prefill 4K/32K) + % of HBM / FP4 roofline"
 ACTQ_NAME = {0: "bf16", 1: "mxfp8", 2: "mxfp4"}
-DENSE_COPIES = 4
+DENSE_COPIES = 8
 
 
 def peaks():
@@ -525,7 +525,7 @@ def run_ours(args, w):
         "config": {"workload": w.name, "tokens_per_step": T, "hidden": d.hidden, "latent": d.latent,
                    "inter": d.inter, "n_experts": d.n_experts, "top_k": d.top_k,
                    "router_bias": w.bias, "actq": ACTQ_NAME[args.actq], "layers": nl,
-                   "l2": ("expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 4 copies"
+                   "l2": ("expert store 15.7 GB >> L2; fresh tokens per step; dense weights rotate over 8 copies"
                           if nl == 1 else f"{nl} layers with independent weights ({nl * 15.7:.0f} GB of experts) run back to "
                           "back on the same tokens; fresh tokens per step"),
                    "parallelism": f"replicas x{world}",

@@ -283,6 +283,12 @@ inline bool decode_select_in_experts(const k3moe_dims& d, int32_t T) {
          d.top_k <= 32;
 }
 
+// Bytes of the latent-out weight the one-token expert kernel fetches into L2 ahead of its use.
+inline long long l2_next_bytes(const k3moe_dims& d) {
+  const long long b = (long long)d.hidden * d.latent * 2;
+  return (long long)(kL2NextFraction * (double)b) / 256 * 256;
+}
+
 k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int32_t T, void* ws,
                                 const WsLayout& L, int32_t* idx, float* wts, cudaStream_t s,
                                 const PackedScales* ps) {
@@ -312,7 +318,8 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
   // (decode, tensor-core experts: the dense kernel wrote z's E4M3 rows, the routing cleared the
   // chunk counters)
   const DecodeSelect sel{at<float>(ws, L.logits), idx, wts, at<int32_t>(ws, L.offsets),
-                         at<int32_t>(ws, L.row_token), at<int32_t>(ws, L.row_slot), at<int32_t>(ws, L.slot_row)};
+                         at<int32_t>(ws, L.row_token), at<int32_t>(ws, L.row_slot), at<int32_t>(ws, L.slot_row),
+                         w.w_out, l2_next_bytes(d)};
   K3_TRY(run_expert_gemms(d, w, at<uint16_t>(ws, L.z), T, at<int32_t>(ws, L.offsets),
                           at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s,
                           T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens &&

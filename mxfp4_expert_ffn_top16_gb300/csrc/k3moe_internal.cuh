@@ -185,6 +185,11 @@ struct PackedScales {
   const uint8_t* up;    // up_s
   const uint8_t* down;  // down_s, rows E * L, K = I
 };
+// Share of the latent-out weight the one-token expert kernel fetches into L2 while it selects
+// the experts (the memory is otherwise idle then). Measured at one token: 0.25 -1.3 us per
+// step, 0.35 -1.4 us, 0.5 -0.7 us, all of it -0.2 us (more of it competes with the expert
+// weights' stream; the latent-out GEMV is not bound by HBM alone).
+constexpr double kL2NextFraction = 0.35;
 // sel (optional, one token): the kernel selects the experts itself from the router logits (no
 // routing kernel before it); every CTA builds the plan in shared memory, CTA 0 also writes the
 // routing outputs (topk_idx, topk_w, offsets, row_token, row_slot, slot_row, plan).
@@ -196,6 +201,10 @@ struct DecodeSelect {
   int32_t* row_token;
   int32_t* row_slot;
   int32_t* slot_row;
+  // Optional: bytes [0, l2_next_bytes) of a weight the next kernel of the step reads (the
+  // latent-out projection), fetched into L2 while the selection runs and the memory is idle.
+  const void* l2_next;
+  long long l2_next_bytes;
 };
 cudaError_t launch_umma_decode(const k3moe_dims& d, const k3moe_weights& w, const PackedScales* ps, int32_t* plan,
                                const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,

@@ -115,6 +115,19 @@ struct UWmArgs {
   uint32_t* err;
 };
 
+// This CTA's share of [p, p + bytes) into L2 with bulk prefetches (bytes a multiple of 256, p
+// 16-byte aligned); the lines keep the normal eviction priority, above the streamed weights'.
+__device__ __forceinline__ void l2_fetch_slice(const void* p, long long bytes) {
+  const long long per = (bytes / gridDim.x + 255) / 256 * 256;
+  const long long b0 = per * blockIdx.x;
+  const long long b1 = b0 + per < bytes ? b0 + per : bytes;
+  for (long long b = b0; b < b1; b += 32768) {
+    const uint32_t n = (uint32_t)(b1 - b < 32768 ? b1 - b : 32768);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(static_cast<const uint8_t*>(p) + b), "r"(n)
+                 : "memory");
+  }
+}
+
 // Roles that take each claimed item from the queue: gather warps 2 and 3, the MMA warp and the
 // four epilogue warps.
 constexpr int kQConsumers = 7;
@@ -233,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wm_kernel(const __grid_const
   pdl_wait();
   pdl_trigger();
   const uint32_t tmem = *tmem_slot;
+  if (A.sel.l2_next_bytes > 0 && threadIdx.x == 64) l2_fetch_slice(A.sel.l2_next, A.sel.l2_next_bytes);
 
   __shared__ int4 s_ctab[32];
   const int4* ctab;

@@ -12,6 +12,11 @@ pinned host memory and its output copied back inside the timed region. Caches: t
 store (15.7 GB) is far larger than L2, tokens are fresh every step, and the dense weights
 rotate over 8 copies (923 MB) so no step finds them in L2.
 
+The default run (decode_b1, one GPU) then measures the metric's other configurations in child
+processes of their own (decode_b64, prefill_4k with bf16 and with MXFP4 activations,
+prefill_32k; a few steps each) and summarises their lines under "workloads";
+--no-secondary skips them.
+
 --impl reference times the CPU oracle (plain C, double accumulation) on the host cores on a
 bounded sample of the same workload; see cpu_sample().
 
@@ -256,6 +261,44 @@ def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads,
 
     run_step.units = step_units
     return lay, run_step
+
+
+# The other configurations the metric is quoted on, measured after the headline (decode_b1) in
+# the default run, each in a child process of its own (its memory freed at exit) with a fixed
+# number of steps; their lines are summarised under "workloads" of the one JSON line.
+SECONDARY = (("decode_b64", 0, 100), ("prefill_4k", 0, 10), ("prefill_4k", 2, 10), ("prefill_32k", 0, 3))
+
+
+def summarize_line(line):
+    """The figures of one bench JSON line that the headline line carries for it."""
+    j = json.loads(line)
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "distinct_experts_last_step", "init_s")
+    out = {k: j.get(k) for k in keep}
+    out["e2e"] = j.get("e2e", {}).get("value")
+    r = j.get("roofline") or {}
+    out["roofline"] = {k: r.get(k) for k in ("kernel", "bound", "achieved", "peak", "unit", "frac", "traffic")}
+    out["step_frac_hbm"] = (j.get("step_roofline") or {}).get("frac_hbm")
+    out["clocks"] = j.get("clocks")
+    out["config"] = {k: (j.get("config") or {}).get(k) for k in ("workload", "tokens_per_step", "actq", "layers")}
+    return out
+
+
+def run_secondary(timeout_s=900):
+    res = {}
+    for wl, actq, steps in SECONDARY:
+        key = wl + ("" if actq == 0 else "_" + ACTQ_NAME[actq])
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", wl, "--actq", str(actq), "--steps",
+               str(steps), "--warmup", "3", "--no-cpu-baseline", "--no-secondary"]
+        try:
+            p = subprocess.run(cmd, capture_output=True, text=True, timeout=timeout_s)
+            lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+            if p.returncode != 0 or not lines:
+                res[key] = {"error": f"exit {p.returncode}: " + (p.stderr.strip().splitlines() or ["no output"])[-1][:300]}
+            else:
+                res[key] = summarize_line(lines[-1])
+        except (subprocess.TimeoutExpired, OSError, ValueError) as e:
+            res[key] = {"error": f"{type(e).__name__}: {e}"[:300]}
+    return res
 
 
 def run_reference(args, w):
@@ -553,6 +596,7 @@ def run_ours(args, w):
     }
     for h in handles or []:
         k3.k3moe_layer_free(h)
+    handles = None
     out["gpu_launches"] = int(launches_total)
     if not args.actq and not args.experts:
         out["roofline"]["traffic"] = measured_traffic(w.name, name)
@@ -579,10 +623,9 @@ def run_ours(args, w):
             "sample": f"{steps_cpu * units} (token, expert-slot) units = {steps_cpu * units / d.top_k:.2f} "
                       f"tokens through one layer of {w.name} (tokens/s divided by its {nl} layer(s)); each "
                       f"unit = one expert row + 1/{d.top_k} of the token's dense rows, {el:.1f} s on {nth} threads"}
-    if rank == 0:
-        print(json.dumps(out), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+    return out if rank == 0 else None
 
 
 def main():
@@ -603,6 +646,9 @@ def main():
     ap.add_argument("--shared-inter", type=int, default=0,
                     help="also run two always-on bf16 shared experts of this width (their width is not "
                          "on the pages; the headline metric is the routed layer without them)")
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false",
+                    help="decode_b1 only: skip the runs of decode_b64, prefill_4k (bf16 and MXFP4 "
+                         "activations) and prefill_32k that the default run adds under \"workloads\"")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling aid: the same workload with fewer experts (fits an ncu capture); "
                          "not a bench configuration")
@@ -620,8 +666,18 @@ def main():
     args.warmup = max(3, args.warmup)
     if args.impl == "reference":
         run_reference(args, w)
-    else:
-        run_ours(args, w)
+        return
+    out = run_ours(args, w)
+    if out is None:
+        return
+    if out["n_gpus"] == 1 and args.secondary and w.name == "decode_b1" and not args.experts:
+        # the headline's device memory is released (run_ours has returned) before the children
+        # run; nothing of this process runs on the GPU meanwhile
+        import torch
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        out["workloads"] = run_secondary()
+    print(json.dumps(out), flush=True)
 
 
 if __name__ == "__main__":

@@ -146,10 +146,31 @@ def measured_traffic(workload, kernel):
         return None
 
 
-def kernel_cost(name, d, T, distinct, rows, actq, shared_width=0):
+# Many tokens with e4m3 activations: the library runs the experts with at most this many rows on
+# the weights-on-N kernel ("expert_ffn_mma") and the others on the many-token kernels.
+SMALL_EXPERT_ROWS = 8
+
+
+def expert_split(idx, n_experts, T, actq):
+    """(distinct experts, sorted rows) of the many-token kernels ("big") and of the small-expert
+    kernel, from one step's selections; None where the library does not split."""
+    if T < 65 or actq == 2:
+        return None
+    c = np.bincount(np.asarray(idx).ravel(), minlength=n_experts)
+    big = c > SMALL_EXPERT_ROWS
+    small = (c > 0) & ~big
+    return {"big": (int(big.sum()), int(c[big].sum())), "small": (int(small.sum()), int(c[small].sum()))}
+
+
+def kernel_cost(name, d, T, distinct, rows, actq, shared_width=0, split=None):
     """Algorithmic (bytes, flops, tensor dtype) of one launch of a profiled kernel: weights read
-    once per launch, activations read and results written once."""
+    once per launch, activations read and results written once. split (expert_split): the
+    many-token expert kernels and the small-expert kernel each count their own experts and rows."""
     L, I, H, E = d.latent, d.inter, d.hidden, d.n_experts
+    if split and name in ("expert_glu_mma", "expert_down_mma"):
+        distinct, rows = split["big"]
+    elif split and name == "expert_ffn_mma":
+        distinct, rows = split["small"]
     glu_w = 2 * (d.gate_q_bytes + d.gate_s_bytes)
     down_w = d.down_q_bytes + d.down_s_bytes
     # activation bytes per value on the tensor-core expert path: bf16 as two e4m3 rows (2),
@@ -521,6 +542,7 @@ def run_ours(args, w):
         raise RuntimeError("timed: " + k3.status_string(st))
     idx_last = idx.cpu().numpy()
     distinct = int(len(np.unique(idx_last)))
+    split = expert_split(idx_last, E, T, args.actq)
 
     # --- pass 2: the same steps with per-kernel CUDA events (roofline of the top kernel)
     barrier()
@@ -577,14 +599,14 @@ def run_ours(args, w):
                               if graph is not None else "stream launches (programmatic dependent launch)"),
                    "shared_experts": (f"{ns} x {si} bf16 (width a parameter; not in the headline configuration)"
                                       if S else "none")},
-        "roofline": roofline(name, per_launch_ms, kernel_cost(name, d, T, distinct, T * d.top_k, args.actq, S), pk),
+        "roofline": roofline(name, per_launch_ms, kernel_cost(name, d, T, distinct, T * d.top_k, args.actq, S, split), pk),
         # (traffic filled in below from the committed capture of this workload, bf16 mode only)
         "step_roofline": {"algorithmic_bytes": step_bytes, "flops": step_flops,
                           "achieved_gbs": step_bytes / (ms / args.steps / 1e3) / 1e9,
                           "frac_hbm": step_bytes / (ms / args.steps / 1e3) / 1e9 / pk["hbm_gbs"]},
         "kernels": {n: dict(ms_per_launch=(t / c if c else None), launches=c,
                             share=t / sum(v[0] for v in prof.values()),
-                            frac=roofline(n, t / max(1, c), kernel_cost(n, d, T, distinct, T * d.top_k, args.actq, S),
+                            frac=roofline(n, t / max(1, c), kernel_cost(n, d, T, distinct, T * d.top_k, args.actq, S, split),
                                           pk)["frac"]) for n, (t, c) in prof.items() if c},
         "distinct_experts_last_step": distinct,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * d.hidden * 2,

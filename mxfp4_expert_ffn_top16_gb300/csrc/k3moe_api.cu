@@ -251,17 +251,29 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
       }
       return K3MOE_OK;
     }
+    // Many tokens with e4m3 activations: the experts with at most kSmallExpertRows rows (one
+    // chunk each) run on the weights-on-N decode kernel, which streams a weight tile for a few
+    // rows at a far higher rate than the 112-row tiles; the others on the many-token kernel.
+    const bool small_split = T >= kUmmaExpertMinTokens && P != 0 && d.latent % 256 == 0;
     {  // many tokens (and MXFP4 activations at any count): z gathered into rows per sorted row
       ProfScope p(P_QUANT, s);
       K3_CUDA(launch_quant_rows(z, row_token, T * d.top_k, T, d.latent, P, at<uint8_t>(ws, L.bq),
-                                at<uint8_t>(ws, L.bs), cnt, 0, err, s));
+                                at<uint8_t>(ws, L.bs), cnt, small_split ? decode_counters(d, T) : 0, err, s));
     }
     {
       ProfScope p(P_GLU_MMA, s);
-      K3_CUDA(launch_umma_glu(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T, aq, aqs, err, s));
+      K3_CUDA(launch_umma_glu(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T, aq, aqs, err, s,
+                              small_split));
     }
-    ProfScope p(P_DOWN_MMA, s);
-    K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s));
+    {
+      ProfScope p(P_DOWN_MMA, s);
+      K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s, small_split));
+    }
+    if (small_split) {
+      ProfScope p(P_FFN_MMA, s);
+      K3_CUDA(launch_umma_wn(d, w, ps, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), nullptr, P, T, aq, aqs,
+                             true, o_rows, cnt, err, s, true));
+    }
     return K3MOE_OK;
   }
   {

@@ -86,6 +86,9 @@ inline __host__ __device__ int4* plan_ctab(int32_t* plan, int E) {
 // A second table for the tensor-core expert GEMM follows: entry 0 = {chunks C64, 0, 0, 0},
 // entries 1..C64 = {expert, first sorted row, rows (<= kUmmaChunkRows), 0}.
 constexpr int kUmmaChunkRows = 112;
+// Experts with at most this many sorted rows (one chunk of the decode kernels) are listed after
+// the others in that table; with many tokens they run on the weights-on-N decode kernel.
+constexpr int kSmallExpertRows = kGemvTokens;
 inline __host__ __device__ size_t plan_ctab64_offset(int E, long long rows) {
   return plan_ctab_offset(E) + (size_t)(rows / kGemvTokens + E + 1) * 16;
 }
@@ -168,11 +171,14 @@ inline int umma_chunk_rows(long long T) { return T >= kUmmaExpertMinTokens ? kUm
 // per-chunk GLU completion counts).
 cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
                               uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s);
+// big_only (many tokens): only the chunks of the experts with more than kSmallExpertRows rows
+// (the others then go to launch_umma_wn with small_experts).
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
-                            cudaStream_t s);
+                            cudaStream_t s, bool big_only = false);
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
-                             const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s);
+                             const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s,
+                             bool big_only = false);
 // Decode (T < kUmmaExpertMinTokens): both GEMMs in one launch, the weights on the MMA's M side
 // (128 weight rows per MMA) and a chunk's up to 8 sorted rows on N. chunk_done: decode_counters
 // ints, zero at launch (GLU items finished per chunk, then the kernel's item counter); the kernel
@@ -214,10 +220,13 @@ cudaError_t launch_umma_decode(const k3moe_dims& d, const k3moe_weights& w, cons
 // activation rows on M = 128): half the MMA instructions per weight byte, which pays once chunks
 // carry more than 8 activation rows. GLU pass, and with_down (latent % 256 == 0) the down pass in
 // the same launch; chunk_done and zq / zqs as for launch_umma_decode.
+// small_experts (many tokens): the chunks are those of the experts with at most
+// kSmallExpertRows rows (the tail of the many-token chunk table), row_token is null and zq / zqs
+// hold P rows per sorted row (the many-token quantised rows).
 cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, const PackedScales* ps, int32_t* plan,
                            const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,
                            uint8_t* aq, uint8_t* aqs, bool with_down, float* o_rows, int* chunk_done,
-                           uint32_t* err, cudaStream_t s);
+                           uint32_t* err, cudaStream_t s, bool small_experts = false);
 // Which decode kernel: the weights on M for bf16 activations (P = 2) with at most 4 tokens (a
 // chunk then carries at most 8 activation rows), on N otherwise. Measured at decode_b1: 92.5
 // against 94.1 us per step for bf16, 92.6 against 91.8 for MXFP8; at decode_b64 the N side is

@@ -61,7 +61,9 @@ __device__ int block_excl_scan(int* cnt, int n, int* tmp) {
 // Plan from offsets[E+1] held in shared memory: active experts, chunk prefix, the chunk
 // table ctab[c] = {expert, first sorted row, rows (<= 8), 0} in expert order, and the table of
 // chunks of up to kUmmaChunkRows rows for the tensor-core expert GEMM. rows_max = T * k fixes
-// where the second table sits.
+// where the second table sits. The second table lists the chunks of the experts with more than
+// kSmallExpertRows rows first, then one chunk per expert with fewer; its header is
+// {chunks, chunks of the first kind, 0, 0}.
 __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, int* tmp, int* flag,
                            int* chunks) {
   const int tid = threadIdx.x;
@@ -87,14 +89,20 @@ __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, i
     plan[2 + E + D] = C;
   }
   __syncthreads();
-  if (tid < E) flag[tid] = (m + kUmmaChunkRows - 1) / kUmmaChunkRows;
+  const bool big = m > kSmallExpertRows;
+  if (tid < E) {
+    flag[tid] = big ? (m + kUmmaChunkRows - 1) / kUmmaChunkRows : 0;
+    chunks[tid] = (m > 0 && !big) ? 1 : 0;
+  }
   __syncthreads();
-  const int C64 = block_excl_scan(flag, E, tmp);
-  if (tid < E)
+  const int Cbig = block_excl_scan(flag, E, tmp);
+  const int Csmall = block_excl_scan(chunks, E, tmp);
+  if (tid < E && big)
     for (int q = 0; q * kUmmaChunkRows < m; ++q)
       ctab64[1 + flag[tid] + q] =
           make_int4(tid, off[tid] + q * kUmmaChunkRows, min(kUmmaChunkRows, m - q * kUmmaChunkRows), 0);
-  if (tid == 0) ctab64[0] = make_int4(C64, 0, 0, 0);
+  if (tid < E && m > 0 && !big) ctab64[1 + Cbig + chunks[tid]] = make_int4(tid, off[tid], m, 0);
+  if (tid == 0) ctab64[0] = make_int4(Cbig + Csmall, Cbig, 0, 0);
 }
 
 // Scatter of tokens [t0, t1) by one warp, given base[e] = first free row of each expert.

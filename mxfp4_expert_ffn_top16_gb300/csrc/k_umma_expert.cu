@@ -97,6 +97,7 @@ struct UExpertArgs {
   uint8_t* aq;         // GLU: quantised output for the down pass [P*rows][N] e4m3
   uint8_t* aqs;        //      its scales [P*rows][exp_pitch(N)]
   float* o_out;        // down: [rows][N] fp32
+  int big_only;        // many tokens: only the chunks of the experts with more than kSmallExpertRows rows
   uint32_t* err;
 };
 
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   int C;
   if (R == kUmmaChunkRows) {
     ctab = plan_ctab64(A.plan, A.E, A.rows_max) + 1;
-    C = ctab[-1].x;
+    C = A.big_only ? ctab[-1].y : ctab[-1].x;
   } else {
     ctab = plan_ctab(A.plan, A.E);
     C = A.plan[1];
@@ -667,7 +668,7 @@ cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int r
 
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
-                            cudaStream_t s) {
+                            cudaStream_t s, bool big_only) {
   const int R = umma_chunk_rows(T);
   UExpertArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
@@ -686,12 +687,14 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
   A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
   A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.err = err;
+  A.big_only = big_only && R == kUmmaChunkRows;
   const int items_max = (rows / R + d.n_experts) * (d.inter / 64);
   return launch_pr<true>(A, P, R, items_max, s);
 }
 
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
-                             const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s) {
+                             const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s,
+                             bool big_only) {
   const int R = umma_chunk_rows(T);
   UExpertArgs A{};
   const int rows = T * d.top_k;
@@ -708,6 +711,7 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
   A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
   A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
   A.o_out = o_rows; A.err = err;
+  A.big_only = big_only && R == kUmmaChunkRows;
   const int items_max = (rows / R + d.n_experts) * (d.latent / 128);
   return launch_pr<false>(A, P, R, items_max, s);
 }

@@ -78,7 +78,8 @@ struct UWnArgs {
   WnPass pass[2];      // [0] GLU, [1] down
   int npass;           // 1: the GLU pass only; 2: GLU then down
   int32_t* plan;
-  const int32_t* row_token;  // sorted row -> token
+  int small_experts;   // chunks: the many-token table's tail (experts with <= kSmallExpertRows rows)
+  const int32_t* row_token;  // sorted row -> token (null: activation row r is sorted row r)
   int ntok;            // tokens (T)
   int E;               // experts
   int rows_max;        // T * k
@@ -234,7 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   const int4* ctab = plan_ctab(A.plan, A.E);
-  const int C0 = A.plan[1];
+  int C0 = A.plan[1];
+  if (A.small_experts) {
+    const int4* t64 = plan_ctab64(A.plan, A.E, A.rows_max);
+    const int4 h = t64[0];  // {chunks, chunks of the experts with more rows (listed first), ...}
+    const bool hok = h.y >= 0 && h.x >= h.y && h.x <= A.rows_max / kUmmaChunkRows + A.E;
+    ctab = t64 + 1 + (hok ? h.y : 0);
+    C0 = hok ? h.x - h.y : 0;
+  }
   const int C = (C0 > 0 && C0 <= A.rows_max / kRows + A.E) ? C0 : 0;
   const int fbs_g = A.pass[0].N / (kNW / 2), fbs_d = A.pass[1].N / kNW;
   const int items_g = C * fbs_g;
@@ -337,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
       const bool act = w2 && lane < P * it.nr;
       // token of a sorted row (checked: a bad one reads token 0 and sets the error word)
       auto token = [&](int r) -> size_t {
-        const int t = __ldg(A.row_token + r);
+        const int t = A.row_token ? __ldg(A.row_token + r) : r;
         if (t >= 0 && t < A.ntok) return (size_t)t;
         atomicOr(A.err, kErrIndex);
         return 0;
@@ -525,7 +533,7 @@ cudaError_t launch_t(UWnArgs& a, int items_max, cudaStream_t s) {
 cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, const PackedScales* ps, int32_t* plan,
                            const uint8_t* zq, const uint8_t* zqs, const int32_t* row_token, int P, int T,
                            uint8_t* aq, uint8_t* aqs, bool with_down, float* o_rows, int* chunk_done,
-                           uint32_t* err, cudaStream_t s) {
+                           uint32_t* err, cudaStream_t s, bool small_experts) {
   UWnArgs A{};
   const int rows = T * d.top_k;
   WnPass& G = A.pass[0];
@@ -552,7 +560,8 @@ cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, const Pa
     A.pass[1].N = kNW;  // unused; keeps the item arithmetic defined
     A.pass[1].K = BKE;
   }
-  A.plan = plan; A.row_token = row_token; A.ntok = T; A.E = d.n_experts; A.rows_max = rows;
+  A.plan = plan; A.row_token = row_token; A.ntok = row_token ? T : rows; A.E = d.n_experts; A.rows_max = rows;
+  A.small_experts = small_experts ? 1 : 0;
   A.aq = aq; A.aqs = aqs; A.o_out = o_rows; A.chunk_done = chunk_done; A.err = err;
   A.item_counter = chunk_done + plan_chunks_max(d, T);
   return P == 1 ? launch_t<1>(A, items_max, s) : launch_t<2>(A, items_max, s);

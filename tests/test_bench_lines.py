@@ -55,3 +55,24 @@ def test_children_commands_and_a_failing_child(monkeypatch):
         assert int(cmd[cmd.index("--warmup") + 1]) >= 3
     actq = {c[c.index("--workload") + 1] + c[c.index("--actq") + 1] for c in seen}
     assert actq == {"decode_b640", "prefill_4k0", "prefill_4k2", "prefill_32k0"}
+
+
+def test_expert_split_counts_big_and_small_experts():
+    import numpy as np
+    # 80 tokens, top-2: expert 0 gets every token (80 rows), expert 1 the first 6 tokens, expert 2
+    # the next 9, expert 3 the rest (65)
+    idx = np.zeros((80, 2), np.int32)
+    idx[:6, 1] = 1
+    idx[6:15, 1] = 2
+    idx[15:, 1] = 3
+    s = bench.expert_split(idx, 5, 80, 0)
+    assert s == {"big": (3, 80 + 9 + 65), "small": (1, 6)}
+    assert bench.expert_split(idx, 5, 64, 0) is None   # the decode kernels take every expert
+    assert bench.expert_split(idx, 5, 80, 2) is None   # MXFP4 activations: no split
+    # the split changes which experts each kernel is charged for
+    import synth
+    d = synth.K3
+    full = bench.kernel_cost("expert_glu_mma", d, 80, 4, 160, 0)
+    big = bench.kernel_cost("expert_glu_mma", d, 80, 4, 160, 0, split=s)
+    small = bench.kernel_cost("expert_ffn_mma", d, 80, 4, 160, 0, split=s)
+    assert big[0] < full[0] and small[0] > 0 and big[1] == 4 * 154 * d.latent * d.inter

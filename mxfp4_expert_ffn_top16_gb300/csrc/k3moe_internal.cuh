@@ -83,12 +83,19 @@ inline __host__ __device__ size_t plan_ctab_offset(int E) { return (plan_ints(E)
 inline __host__ __device__ int4* plan_ctab(int32_t* plan, int E) {
   return reinterpret_cast<int4*>(reinterpret_cast<char*>(plan) + plan_ctab_offset(E));
 }
-// A second table for the tensor-core expert GEMM follows: entry 0 = {chunks C64, 0, 0, 0},
-// entries 1..C64 = {expert, first sorted row, rows (<= kUmmaChunkRows), 0}.
+// A second table for the tensor-core expert GEMM follows: entry 0 = {chunks C64, chunks of the
+// experts with more than kSmallExpertRows rows, 0, 0}, entries 1..C64 = {expert, first sorted
+// row, rows, 0}: first those experts' chunks of up to kUmmaChunkRows rows, then the other
+// experts' chunks of up to kGemvTokens rows.
 constexpr int kUmmaChunkRows = 112;
-// Experts with at most this many sorted rows (one chunk of the decode kernels) are listed after
-// the others in that table; with many tokens they run on the weights-on-N decode kernel.
+// With many tokens the experts with at most this many sorted rows run on the weights-on-N
+// decode kernel, in chunks of kGemvTokens rows (kSmallChunksMax at most per expert).
 constexpr int kSmallExpertRows = kGemvTokens;
+constexpr int kSmallChunksMax = (kSmallExpertRows + kGemvTokens - 1) / kGemvTokens;
+// Bound on the entries of the second table.
+inline __host__ __device__ long long plan_ctab64_max(int E, long long rows) {
+  return rows / kUmmaChunkRows + (long long)E * kSmallChunksMax;
+}
 inline __host__ __device__ size_t plan_ctab64_offset(int E, long long rows) {
   return plan_ctab_offset(E) + (size_t)(rows / kGemvTokens + E + 1) * 16;
 }
@@ -96,7 +103,7 @@ inline __host__ __device__ int4* plan_ctab64(int32_t* plan, int E, long long row
   return reinterpret_cast<int4*>(reinterpret_cast<char*>(plan) + plan_ctab64_offset(E, rows));
 }
 inline __host__ __device__ size_t plan_bytes(int E, long long rows) {
-  return plan_ctab64_offset(E, rows) + (size_t)(rows / kUmmaChunkRows + E + 2) * 16;
+  return plan_ctab64_offset(E, rows) + (size_t)(plan_ctab64_max(E, rows) + 2) * 16;
 }
 
 // ------------------------------------------------------------------ launchers

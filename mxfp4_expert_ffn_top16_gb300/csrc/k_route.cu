@@ -62,8 +62,8 @@ __device__ int block_excl_scan(int* cnt, int n, int* tmp) {
 // table ctab[c] = {expert, first sorted row, rows (<= 8), 0} in expert order, and the table of
 // chunks of up to kUmmaChunkRows rows for the tensor-core expert GEMM. rows_max = T * k fixes
 // where the second table sits. The second table lists the chunks of the experts with more than
-// kSmallExpertRows rows first, then one chunk per expert with fewer; its header is
-// {chunks, chunks of the first kind, 0, 0}.
+// kSmallExpertRows rows first, then the other experts' chunks of up to kGemvTokens rows; its
+// header is {chunks, chunks of the first kind, 0, 0}.
 __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, int* tmp, int* flag,
                            int* chunks) {
   const int tid = threadIdx.x;
@@ -92,7 +92,7 @@ __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, i
   const bool big = m > kSmallExpertRows;
   if (tid < E) {
     flag[tid] = big ? (m + kUmmaChunkRows - 1) / kUmmaChunkRows : 0;
-    chunks[tid] = (m > 0 && !big) ? 1 : 0;
+    chunks[tid] = (m > 0 && !big) ? (m + kGemvTokens - 1) / kGemvTokens : 0;
   }
   __syncthreads();
   const int Cbig = block_excl_scan(flag, E, tmp);
@@ -101,7 +101,10 @@ __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, i
     for (int q = 0; q * kUmmaChunkRows < m; ++q)
       ctab64[1 + flag[tid] + q] =
           make_int4(tid, off[tid] + q * kUmmaChunkRows, min(kUmmaChunkRows, m - q * kUmmaChunkRows), 0);
-  if (tid < E && m > 0 && !big) ctab64[1 + Cbig + chunks[tid]] = make_int4(tid, off[tid], m, 0);
+  if (tid < E && !big)
+    for (int q = 0; q * kGemvTokens < m; ++q)
+      ctab64[1 + Cbig + chunks[tid] + q] =
+          make_int4(tid, off[tid] + q * kGemvTokens, min(kGemvTokens, m - q * kGemvTokens), 0);
   if (tid == 0) ctab64[0] = make_int4(Cbig + Csmall, Cbig, 0, 0);
 }
 

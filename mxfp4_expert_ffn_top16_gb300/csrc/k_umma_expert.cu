@@ -259,7 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
     C = A.plan[1];
   }
   const int fbs = A.N / kFB;
-  const int items = (C > 0 && C <= A.rows_max / R + A.E) ? C * fbs : 0;
+  const long long cmax = R == kUmmaChunkRows ? plan_ctab64_max(A.E, A.rows_max) : A.rows_max / R + A.E;
+  const int items = (C > 0 && C <= cmax) ? C * fbs : 0;
   const int nk = A.K / kKStage<FP4>;
 
   // item u -> (expert, first sorted row, rows, first feature); false for a corrupt entry

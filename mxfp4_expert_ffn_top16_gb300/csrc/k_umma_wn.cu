@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_wn_kernel(const __grid_const
   if (A.small_experts) {
     const int4* t64 = plan_ctab64(A.plan, A.E, A.rows_max);
     const int4 h = t64[0];  // {chunks, chunks of the experts with more rows (listed first), ...}
-    const bool hok = h.y >= 0 && h.x >= h.y && h.x <= A.rows_max / kUmmaChunkRows + A.E;
+    const bool hok = h.y >= 0 && h.x >= h.y && h.x <= plan_ctab64_max(A.E, A.rows_max);
     ctab = t64 + 1 + (hok ? h.y : 0);
     C0 = hok ? h.x - h.y : 0;
   }

@@ -263,11 +263,11 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
     {
       ProfScope p(P_GLU_MMA, s);
       K3_CUDA(launch_umma_glu(d, w, plan, at<uint8_t>(ws, L.bq), at<uint8_t>(ws, L.bs), P, T, aq, aqs, err, s,
-                              small_split));
+                              small_split, ps));
     }
     {
       ProfScope p(P_DOWN_MMA, s);
-      K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s, small_split));
+      K3_CUDA(launch_umma_down(d, w, plan, aq, aqs, P, T, o_rows, err, s, small_split, ps));
     }
     if (small_split) {
       ProfScope p(P_FFN_MMA, s);
@@ -558,7 +558,7 @@ k3moe_status k3moe_layer_init(const k3moe_dims* dims, const k3moe_weights* weigh
     const size_t gbytes = (size_t)d.n_experts * d.inter * (d.latent / 32);
     const size_t dbytes = (size_t)d.n_experts * d.latent * (d.inter / 32);
     uint8_t* p = nullptr;
-    if (cudaMalloc(&p, 2 * gbytes + dbytes) != cudaSuccess) {
+    if (cudaMalloc(&p, 4 * gbytes + dbytes) != cudaSuccess) {
       delete h;
       return K3MOE_E_CUDA;
     }
@@ -567,13 +567,15 @@ k3moe_status k3moe_layer_init(const k3moe_dims* dims, const k3moe_weights* weigh
     if (launch_pack_scales(weights->gate_s, grows, d.latent, p, s) != cudaSuccess ||
         launch_pack_scales(weights->up_s, grows, d.latent, p + gbytes, s) != cudaSuccess ||
         launch_pack_scales(weights->down_s, drows, d.inter, p + 2 * gbytes, s) != cudaSuccess ||
+        launch_pack_scales_glu(weights->gate_s, weights->up_s, grows, d.latent, p + 2 * gbytes + dbytes, s) !=
+            cudaSuccess ||
         cudaStreamSynchronize(s) != cudaSuccess) {
       cudaFree(p);
       delete h;
       return K3MOE_E_CUDA;
     }
     h->packed = p;
-    h->ps = PackedScales{p, p + gbytes, p + 2 * gbytes};
+    h->ps = PackedScales{p, p + gbytes, p + 2 * gbytes, p + 2 * gbytes + dbytes};
   }
   *layer = h;
   return K3MOE_OK;

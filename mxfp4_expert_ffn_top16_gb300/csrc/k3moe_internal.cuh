@@ -180,12 +180,15 @@ cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int r
                               uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s);
 // big_only (many tokens): only the chunks of the experts with more than kSmallExpertRows rows
 // (the others then go to launch_umma_wn with small_experts).
+// ps (may be null): the weight scales from the prepared layer's staging images, one bulk copy
+// per stage instead of a gather per weight row.
+struct PackedScales;
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
-                            cudaStream_t s, bool big_only = false);
+                            cudaStream_t s, bool big_only = false, const PackedScales* ps = nullptr);
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s,
-                             bool big_only = false);
+                             bool big_only = false, const PackedScales* ps = nullptr);
 // Decode (T < kUmmaExpertMinTokens): both GEMMs in one launch, the weights on the MMA's M side
 // (128 weight rows per MMA) and a chunk's up to 8 sorted rows on N. chunk_done: decode_counters
 // ints, zero at launch (GLU items finished per chunk, then the kernel's item counter); the kernel
@@ -197,6 +200,7 @@ struct PackedScales {
   const uint8_t* gate;  // gate_s, rows E * I, K = L
   const uint8_t* up;    // up_s
   const uint8_t* down;  // down_s, rows E * L, K = I
+  const uint8_t* glu;   // gate_s and up_s interleaved per 64 features (launch_pack_scales_glu)
 };
 // Share of the latent-out weight the one-token expert kernel fetches into L2 while it selects
 // the experts (the memory is otherwise idle then). Measured at one token: 0.25 -1.3 us per
@@ -243,6 +247,11 @@ inline bool decode_weights_on_m(int P, long long T) { return P == 2 && T <= 4; }
 // image (same size): per 128 rows and 128-code chunk a 512-byte block whose byte 16 l + 4 w + q
 // is the scale of row 32 w + l, K-block 4 chunk + q.
 cudaError_t launch_pack_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t s);
+// The gate and up scales (rows each, a multiple of 64) -> the many-token GLU tile's image (twice
+// the size of one): per 64 features and 128-code chunk a 512-byte block whose byte 16 l + 4 w + q
+// is the scale of tile row 32 w + l (rows 0..63 gate, 64..127 up of the same features).
+cudaError_t launch_pack_scales_glu(const uint8_t* gate, const uint8_t* up, long long rows, int K, uint8_t* dst,
+                                   cudaStream_t s);
 inline int plan_chunks_max(const k3moe_dims& d, long long T) {
   return (int)(T * d.top_k / kGemvTokens + d.n_experts + 1);
 }

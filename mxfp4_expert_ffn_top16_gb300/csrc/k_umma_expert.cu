@@ -98,6 +98,8 @@ struct UExpertArgs {
   uint8_t* aqs;        //      its scales [P*rows][exp_pitch(N)]
   float* o_out;        // down: [rows][N] fp32
   int big_only;        // many tokens: only the chunks of the experts with more than kSmallExpertRows rows
+  const uint8_t* pw;   // weight scales in the staging image (null: gathered row by row): per tile
+                       // row-block (GLU: 64 features, down: 128 rows) and 128-code chunk, 512 bytes
   uint32_t* err;
 };
 
@@ -225,7 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1 + 64);  // the expect_tx arrival + one cp.async arrival per gathering lane
+      // the expect_tx arrival + one cp.async arrival per gathering lane (weight rows: none when
+      // their scales come with the tiles)
+      mbar_init(&full[s], 1 + (A.pw ? 32 : 64));
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < kAccSlots; ++b) {
@@ -284,9 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         int e, r0, nr, f0;
         if (!item_of(u, e, r0, nr, f0)) atomicOr(A.err, kErrIndex);
         const int wrow = e * A.N + f0;
+        constexpr uint32_t kSfTx = FP4 ? 1024u : 512u;  // the tile's weight-scale blocks per stage
+        const size_t pblk = (size_t)(wrow / (GLU ? 64 : 128)) * (A.K / 128);
         for (int kc = 0; kc < nk; ++kc) {
           if (!mbar_wait_bounded(&empty[s], ph ^ 1, abort_flag, A.err)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[s], kAPacked<FP4> + kBTx);
+          mbar_arrive_expect_tx(&full[s], kAPacked<FP4> + kBTx + (A.pw ? kSfTx : 0u));
+          if (A.pw)
+            bulk_g2s_stream(stg + s * kStg, A.pw + (pblk + (size_t)kc * (FP4 ? 2 : 1)) * 512, kSfTx, &full[s],
+                            l2_evict_first());
           tma_load_2d(sA + s * kATile, &A.ta0, kc * BKE, wrow, &full[s]);
           if (GLU) tma_load_2d(sA + s * kATile + 64 * 128, &A.ta1, kc * BKE, wrow, &full[s]);
           tma_load_2d(sB + s * kBTile, &A.tb, kc * BKE, P * r0, &full[s]);
@@ -300,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
     const bool wa = warp == kGather0;
     int s = 0;
     uint32_t ph = 0;
-    bool ok = true;
+    bool ok = !(wa && A.pw);  // (the weight scales come with the tiles)
     for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
       int e, r0, nr, f0;
       item_of(u, e, r0, nr, f0);
@@ -669,7 +678,7 @@ cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int r
 
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
-                            cudaStream_t s, bool big_only) {
+                            cudaStream_t s, bool big_only, const PackedScales* ps) {
   const int R = umma_chunk_rows(T);
   UExpertArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
@@ -689,13 +698,14 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
   A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.err = err;
   A.big_only = big_only && R == kUmmaChunkRows;
+  A.pw = ps && d.latent % 128 == 0 ? ps->glu : nullptr;
   const int items_max = (rows / R + d.n_experts) * (d.inter / 64);
   return launch_pr<true>(A, P, R, items_max, s);
 }
 
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s,
-                             bool big_only) {
+                             bool big_only, const PackedScales* ps) {
   const int R = umma_chunk_rows(T);
   UExpertArgs A{};
   const int rows = T * d.top_k;
@@ -713,6 +723,7 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
   A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
   A.o_out = o_rows; A.err = err;
   A.big_only = big_only && R == kUmmaChunkRows;
+  A.pw = ps && d.inter % 128 == 0 ? ps->down : nullptr;
   const int items_max = (rows / R + d.n_experts) * (d.latent / 128);
   return launch_pr<false>(A, P, R, items_max, s);
 }

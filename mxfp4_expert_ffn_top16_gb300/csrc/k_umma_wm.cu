@@ -620,7 +620,32 @@ __global__ void pack_scales_kernel(const uint32_t* __restrict__ src, long long w
   }
 }
 
+// The same image for the many-token GLU tile of 64 gate rows and their 64 up rows: block (fb, c)
+// holds, at lane l, word w, the four scales of tile row 32 w + l (gate row 64 fb + 32 w + l for
+// w < 2, up row 64 fb + 32 (w - 2) + l otherwise) for K-blocks 4c .. 4c + 3.
+__global__ void pack_scales_glu_kernel(const uint32_t* __restrict__ gate, const uint32_t* __restrict__ up,
+                                       long long words, int kc, uint32_t* dst) {
+  for (long long o = blockIdx.x * (long long)blockDim.x + threadIdx.x; o < words; o += (long long)gridDim.x * blockDim.x) {
+    const long long blk = o >> 7;
+    const int l = (int)(o >> 2) & 31, w = (int)o & 3;
+    const long long fb = blk / kc;
+    const int c = (int)(blk - fb * kc);
+    dst[o] = (w < 2 ? gate : up)[(fb * 64 + 32 * (w & 1) + l) * kc + c];
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_pack_scales_glu(const uint8_t* gate, const uint8_t* up, long long rows, int K, uint8_t* dst,
+                                   cudaStream_t s) {
+  if (rows % 64 || K % 128) return cudaErrorInvalidValue;
+  const long long words = 2 * rows * (K / 128);
+  const int grid = (int)((words + 255) / 256 < 4096 ? (words + 255) / 256 : 4096);
+  pack_scales_glu_kernel<<<grid > 0 ? grid : 1, 256, 0, s>>>(reinterpret_cast<const uint32_t*>(gate),
+                                                           reinterpret_cast<const uint32_t*>(up), words, K / 128,
+                                                           reinterpret_cast<uint32_t*>(dst));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack_scales(const uint8_t* src, long long rows, int K, uint8_t* dst, cudaStream_t s) {
   if (rows % kMW || K % 128) return cudaErrorInvalidValue;

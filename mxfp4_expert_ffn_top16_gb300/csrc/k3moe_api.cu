@@ -216,7 +216,8 @@ struct ProfScope {
 k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const uint16_t* z, int32_t T,
                               const int32_t* offsets, const int32_t* row_token, float* o_rows, void* ws,
                               const WsLayout& L, cudaStream_t s, bool z_rows_ready = false,
-                              const PackedScales* ps = nullptr, const DecodeSelect* sel = nullptr) {
+                              const PackedScales* ps = nullptr, const DecodeSelect* sel = nullptr,
+                              const int32_t* slot_row = nullptr) {
   uint32_t* err = at<uint32_t>(ws, L.err);
   int32_t* plan = at<int32_t>(ws, L.plan);
   if (umma_expert_ok(d)) {
@@ -257,8 +258,10 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
     const bool small_split = T >= kUmmaExpertMinTokens && P != 0 && d.latent % 256 == 0;
     {  // many tokens (and MXFP4 activations at any count): z gathered into rows per sorted row
       ProfScope p(P_QUANT, s);
+      // (with the permutation's slot -> row table: each token converted once, stored to its k rows)
       K3_CUDA(launch_quant_rows(z, row_token, T * d.top_k, T, d.latent, P, at<uint8_t>(ws, L.bq),
-                                at<uint8_t>(ws, L.bs), cnt, small_split ? decode_counters(d, T) : 0, err, s));
+                                at<uint8_t>(ws, L.bs), cnt, small_split ? decode_counters(d, T) : 0, err, s,
+                                slot_row, d.top_k));
     }
     {
       ProfScope p(P_GLU_MMA, s);
@@ -336,7 +339,7 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
                           at<int32_t>(ws, L.row_token), at<float>(ws, L.o), ws, L, s,
                           T <= kSmallRouteTokens && T < kUmmaExpertMinTokens && T < kUmmaDenseMinTokens &&
                               umma_expert_ok(d) && d.actq != 2,
-                          ps, fused_select ? &sel : nullptr));
+                          ps, fused_select ? &sel : nullptr, at<int32_t>(ws, L.slot_row)));
   {
     ProfScope p(P_COMBINE, s);
     K3_CUDA(launch_combine(at<float>(ws, L.o), at<int32_t>(ws, L.slot_row), wts, T, d.top_k,

@@ -176,8 +176,11 @@ inline int umma_chunk_rows(long long T) { return T >= kUmmaExpertMinTokens ? kUm
 // z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)]
 // (row_token null: row r is token r). Also clears the ncnt counters at cnt (the decode kernel's
 // per-chunk GLU completion counts).
+// slot_row (optional, with k): convert each token once and store it to the sorted rows of its k
+// slots (rows = T * k) instead of converting every sorted row from its token.
 cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
-                              uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s);
+                              uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s,
+                              const int32_t* slot_row = nullptr, int k = 0);
 // big_only (many tokens): only the chunks of the experts with more than kSmallExpertRows rows
 // (the others then go to launch_umma_wn with small_experts).
 // ps (may be null): the weight scales from the prepared layer's staging images, one bulk copy

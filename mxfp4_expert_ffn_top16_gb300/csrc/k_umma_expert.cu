@@ -587,11 +587,14 @@ cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t 
 // elements rounded to nearest even, saturating at +-6). One warp per (sorted row, 256-value
 // segment), so every load of a launch is in flight at once; each lane takes 8 consecutive
 // values, four lanes one 32-value block.
+// slot_row non-null: one warp per (token, 256-value segment) instead; the token's values are
+// converted once and stored to the sorted row of each of its k slots (slot_row[t * k + j]).
 template <int P>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restrict__ z,
                                                          const int32_t* __restrict__ row_token, int rows,
                                                          int T, int L, uint8_t* bq, uint8_t* bs, int* cnt,
-                                                         int ncnt, uint32_t* err) {
+                                                         int ncnt, uint32_t* err,
+                                                         const int32_t* __restrict__ slot_row, int k) {
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == 0)
@@ -599,13 +602,24 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
   const int lane = threadIdx.x & 31;
   const int segs = (L + 255) / 256;
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (wid >= (long long)rows * segs) return;  // warp-uniform
+  if (wid >= (long long)(slot_row ? T : rows) * segs) return;  // warp-uniform
   const int r = (int)(wid / segs), base = (int)(wid % segs) * 256;
-  int t = row_token ? row_token[r] : r;
+  int t = slot_row ? r : (row_token ? row_token[r] : r);
   if (t < 0 || t >= T) {
     if (lane == 0 && base == 0) atomicOr(err, kErrIndex);
     t = 0;
   }
+  // the sorted rows the result goes to: r itself, or each slot's row of token t
+  const int nout = slot_row ? k : 1;
+  auto out_row = [&](int j) -> int {
+    if (!slot_row) return r;
+    const int o = __ldg(slot_row + (size_t)t * k + j);
+    if (o < 0 || o >= rows) {
+      if (lane == 0 && base == 0) atomicOr(err, kErrIndex);
+      return -1;
+    }
+    return o;
+  };
   const int sp = exp_pitch(L);
   const int col = base + 8 * lane;
   const bool act = col < L;  // L is a multiple of 32: a block is all in or all out
@@ -630,10 +644,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = mul_pow2(v[i], -X);
     const uint32_t packed = e2m1x8(v);
-    if (act) {
-      *reinterpret_cast<uint32_t*>(bq + (size_t)r * (L / 2) + col / 2) = packed;
-      if ((lane & 3) == 0) bs[(size_t)r * sp + col / 32] = (uint8_t)(X + 127);
-    }
+    if (act)
+      for (int j = 0; j < nout; ++j) {
+        const int o = out_row(j);
+        if (o < 0) continue;
+        *reinterpret_cast<uint32_t*>(bq + (size_t)o * (L / 2) + col / 2) = packed;
+        if ((lane & 3) == 0) bs[(size_t)o * sp + col / 32] = (uint8_t)(X + 127);
+      }
   } else {
 #pragma unroll
   for (int p = 0; p < P; ++p) {
@@ -651,12 +668,15 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
         v[2 * i + 1] -= mul_pow2(h.y, X);
       }
     }
-    if (act) {
-      const size_t row = (size_t)P * r + p;
-      *reinterpret_cast<uint2*>(bq + row * L + col) =
-          make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16));
-      if ((lane & 3) == 0) bs[row * sp + col / 32] = (uint8_t)(X + 127);
-    }
+    if (act)
+      for (int j = 0; j < nout; ++j) {
+        const int o = out_row(j);
+        if (o < 0) continue;
+        const size_t row = (size_t)P * o + p;
+        *reinterpret_cast<uint2*>(bq + row * L + col) =
+            make_uint2(codes[0] | (codes[1] << 16), codes[2] | (codes[3] << 16));
+        if ((lane & 3) == 0) bs[row * sp + col / 32] = (uint8_t)(X + 127);
+      }
   }
   }
 }
@@ -664,16 +684,20 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(const uint16_t* __restr
 }  // namespace
 
 cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int rows, int T, int L, int P,
-                              uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s) {
+                              uint8_t* bq, uint8_t* bs, int* cnt, int ncnt, uint32_t* err, cudaStream_t s,
+                              const int32_t* slot_row, int k) {
   if (rows <= 0) return cudaSuccess;
   const int warps = 8;
-  const long long units = (long long)rows * ((L + 255) / 256);
+  const long long units = (long long)(slot_row ? T : rows) * ((L + 255) / 256);
   const dim3 grid((unsigned)((units + warps - 1) / warps)), block(32 * warps);
   if (P == 0)
-    return launch_pdl(quant_rows_kernel<0>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
+    return launch_pdl(quant_rows_kernel<0>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err,
+                      slot_row, k);
   if (P == 1)
-    return launch_pdl(quant_rows_kernel<1>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
-  return launch_pdl(quant_rows_kernel<2>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err);
+    return launch_pdl(quant_rows_kernel<1>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err,
+                      slot_row, k);
+  return launch_pdl(quant_rows_kernel<2>, grid, block, 0, s, z, row_token, rows, T, L, bq, bs, cnt, ncnt, err,
+                    slot_row, k);
 }
 
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,

@@ -451,13 +451,14 @@ def _run_prepared(lay, h, x_np, ws):
 
 
 @pytest.mark.parametrize("name,actq,Ts", [("tiny", 0, (1, 5, 8)), ("tiny", 1, (1, 8)), ("wide", 0, (1, 4)),
-                                          ("deep", 1, (2,)), ("k3", 0, (1, 3, 64)), ("k3", 1, (1, 16)),
-                                          ("k3", 2, (1,))])
+                                          ("deep", 1, (2, 80)), ("k3", 0, (1, 3, 64, 200)), ("k3", 1, (1, 16, 100)),
+                                          ("k3", 2, (1, 70))])
 def test_prepared_layer_same_bits_as_forward(name, actq, Ts, k3_layer):
     """k3moe_layer_run on a prepared layer (scales repacked once into the tensor-memory staging
     image) gives the bits k3moe_layer_forward gives: a misplaced scale would change them, since
     every expert's scales vary. tiny and wide cover stages of one 128-code chunk and a single
-    two-chunk stage; K3 the full decode kernel."""
+    two-chunk stage; K3 the full decode kernel; 70 tokens and more the many-token kernels, which
+    take the GLU tile's interleaved image and the down image."""
     d = {"tiny": synth.TINY, "wide": WIDE, "deep": DEEP, "k3": synth.K3}[name]
     lay = k3_layer if name == "k3" else DeviceLayer(d, seed=3, actq=actq)
     dm = dims(d, actq=actq)  # (the weights do not depend on the activation mode)
@@ -471,5 +472,32 @@ def test_prepared_layer_same_bits_as_forward(name, actq, Ts, k3_layer):
             got = _run_prepared(lay, h, x, ws)
             for a, b in zip(got, want):
                 np.testing.assert_array_equal(a, b)
+    finally:
+        k3.k3moe_layer_free(h)
+
+
+# Many tokens with e4m3 activations: the experts with at most 8 rows run on the weights-on-N
+# kernel and the others on the many-token kernel (in chunks of 112 rows). A Zipf bias over
+# WIDE's 16 experts gives both kinds, with counts on either side of the threshold (7, 8 / 9, 11
+# at T = 96; 8 / 9, 13 and experts of more than one 112-row chunk at T = 200). Every token is
+# compared with the oracle, and the prepared layer (scales from the packed images) gives the
+# same bits as the unprepared one.
+@pytest.mark.parametrize("wseed,bseed,T,actq", [(3, 3, 96, 0), (7, 4, 200, 0), (7, 4, 200, 1)])
+def test_layer_small_and_large_experts(wseed, bseed, T, actq):
+    d = WIDE
+    lay = DeviceLayer(d, seed=wseed, bias=synth.zipf_bias(d.n_experts, bseed, s=0.7), actq=actq)
+    x = synth.host_bf16_normal(5, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+    y, idx, w = _forward(lay, x)
+    cnt = np.bincount(idx.ravel(), minlength=d.n_experts)
+    assert ((cnt > 0) & (cnt <= 8)).sum() >= 2 and (cnt > 8).sum() >= 3, sorted(cnt.tolist())
+    _compare_layer(lay, x, y, idx, np.arange(T))
+    dm = dims(d, actq=actq)
+    h = k3.k3moe_layer_init(dm, lay.weights, stream())
+    try:
+        ws = workspace(dm, T)
+        want = run_layer(lay, x, dm=dm, ws=ws)
+        got = _run_prepared(lay, h, x, ws)
+        for a, b in zip(got, want):
+            np.testing.assert_array_equal(a, b)
     finally:
         k3.k3moe_layer_free(h)

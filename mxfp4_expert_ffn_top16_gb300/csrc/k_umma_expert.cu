@@ -26,11 +26,14 @@
 // tens of cycles to issue from the single MMA thread, so N is made as large as tensor memory
 // allows (two 224-column accumulators) to keep the tensor pipe, not the issue, the limit.
 // Warp 0 (lane 0) loads the packed e2m1 weight tiles (16U4_ALIGN16B tensor map) and the e4m3
-// activation tiles, both with the 128-byte swizzle. Warps 10 and 11 gather each stage's weight
-// and activation scales with 4-byte cp.async straight into the 32 x 16-byte blocks that
-// tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l, word w = the four K-block scales
-// of row 32w + l); the stage's full barrier counts the tile bytes and one cp.async arrival per
-// gathering lane. Warp 1: tensor-memory owner and MMA issuer, one commit per stage.
+// activation tiles, both with the 128-byte swizzle. The stage's scales go into the 32 x 16-byte
+// blocks that tcgen05.cp.32x128b.warpx4 copies to tensor memory (lane l, word w = the four
+// K-block scales of row 32w + l): the weight rows' block comes with the tiles as one bulk copy
+// from a prepared layer's staging image (else warp 10 gathers it with 4-byte cp.async), and warp
+// 11 gathers the activation rows' scales the same way; the stage's full barrier counts the bytes
+// and one cp.async arrival per gathering lane. Warp 1: tensor-memory owner and MMA issuer, one
+// commit per stage. With many tokens the plan lists the experts that received at most 8 rows
+// last, and this kernel leaves them to the weights-on-N kernel (big_only).
 // Each item accumulates its whole K in one of two tensor-memory slots, so the epilogue of one
 // item overlaps the MMAs of the next; eight epilogue warps (two per lane quadrant, one lane = one
 // weight row, each half of the sorted rows) drain it and run the epilogue; the GLU epilogue

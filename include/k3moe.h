@@ -201,15 +201,17 @@ k3moe_status k3moe_layer_forward(const k3moe_dims* dims, const k3moe_weights* we
 /* Prepared layer (optional, once per layer, outside the hot path). k3moe_layer_init checks dims
  * and weights as k3moe_layer_forward does and keeps a copy of both (the weight buffers must
  * outlive the handle). When latent and inter are multiples of 128 it also repacks the expert
- * scales gate_s, up_s and down_s into the image the decode expert kernel copies to tensor memory:
- * for every 128 weight rows and 128 codes of K, one 512-byte block whose byte 16 l + 4 w + q is
- * the scale of row 32 w + l, K-block 4 c + q. That copy (as many bytes as the three scale
- * arrays) is device memory the handle owns; init allocates it, launches the repacking on
+ * scales gate_s, up_s and down_s into the image the expert kernels copy to tensor memory: for
+ * every 128 weight rows and 128 codes of K, one 512-byte block whose byte 16 l + 4 w + q is the
+ * scale of row 32 w + l, K-block 4 c + q; and gate_s with up_s once more, interleaved per 64
+ * features (rows 0..63 of a block the gate rows, 64..127 the up rows of the same features) for
+ * the many-token GLU tile. Those copies (twice the gate and up scale bytes plus the down scale
+ * bytes) are device memory the handle owns; init allocates them, launches the repacking on
  * `stream` and synchronises the stream. On failure *layer is NULL and nothing is kept.
  * k3moe_layer_run is k3moe_layer_forward on the prepared layer, with the same arguments after
- * the handle and the same results bit for bit; the decode expert kernel (T <= 64) then loads each
- * stage's weight scales with one bulk copy next to the weight tile instead of gathering them row
- * by row. It neither allocates nor synchronises. k3moe_layer_free releases the handle and its
+ * the handle and the same results bit for bit; the expert kernels then load each stage's weight
+ * scales with one bulk copy next to the weight tile instead of gathering them row by row. It
+ * neither allocates nor synchronises. k3moe_layer_free releases the handle and its
  * device memory (NULL is accepted; it synchronises the device while freeing). */
 typedef struct k3moe_layer k3moe_layer;
 k3moe_status k3moe_layer_init(const k3moe_dims* dims, const k3moe_weights* weights, k3moe_layer** layer,

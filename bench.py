@@ -557,13 +557,21 @@ def run_ours(args, w):
     xh.copy_(x.cpu())
     yh = torch.empty((args.steps, T, d.hidden), dtype=torch.int16, pin_memory=True)
     xs = torch.empty((T, d.hidden), dtype=torch.int16, device=dev)
+    # one layer on a prepared handle: k3moe_layer_run_host takes the pinned buffers themselves (its
+    # own kernels read the tokens from and write the output to host memory); otherwise copies
+    # from and to pinned memory around each layer call
+    host_call = bool(handles) and nl == 1
     barrier()
     ev0.record(stream)
     for i in range(args.steps):
         j = (args.warmup + i) % nsteps_x
-        xs.copy_(xh[j * T:(j + 1) * T], non_blocking=True)
-        step(args.warmup + i, xp=xs.data_ptr())
-        yh[i].copy_(y, non_blocking=True)
+        if host_call:
+            k3.k3moe_layer_run_host(handles[(args.warmup + i) % DENSE_COPIES], xh[j * T:(j + 1) * T].data_ptr(), T,
+                                    yh[i].data_ptr(), idx.data_ptr(), None, ws.data_ptr(), nbytes, cur["stream"])
+        else:
+            xs.copy_(xh[j * T:(j + 1) * T], non_blocking=True)
+            step(args.warmup + i, xp=xs.data_ptr())
+            yh[i].copy_(y, non_blocking=True)
     ev1.record(stream)
     barrier()
     ms_e2e = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
@@ -610,7 +618,10 @@ def run_ours(args, w):
                                           pk)["frac"]) for n, (t, c) in prof.items() if c},
         "distinct_experts_last_step": distinct,
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": T * d.hidden * 2,
-                "d2h_bytes_per_step": T * d.hidden * 2},
+                "d2h_bytes_per_step": T * d.hidden * 2,
+                "call": ("k3moe_layer_run_host on pinned host buffers (the library's kernels read the tokens "
+                         "and write the output over the CPU-GPU link)" if host_call else
+                         "pinned-memory copies around each layer call")},
         "gpu_launches": int(launches_total / max(1, 1)),
         "clocks": clk,
         "setup_s": setup_s,

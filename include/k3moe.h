@@ -74,7 +74,8 @@ typedef enum k3moe_status {
   K3MOE_E_CUDA = 6,      /* a CUDA runtime call or launch failed */
   K3MOE_E_TIMEOUT = 7,   /* a device-side bounded wait ran out (see k3moe_check) */
   K3MOE_E_DEVICE = 8,    /* no usable sm_100-family device, or a device-side check failed */
-  K3MOE_E_SCRATCH = 9    /* request larger than k3moe_route_noalloc's fixed scratch */
+  K3MOE_E_SCRATCH = 9,   /* request larger than k3moe_route_noalloc's fixed scratch */
+  K3MOE_E_HOSTMEM = 10   /* a host buffer is not page-locked memory the device can address */
 } k3moe_status;
 
 typedef struct k3moe_dims {
@@ -219,6 +220,18 @@ k3moe_status k3moe_layer_init(const k3moe_dims* dims, const k3moe_weights* weigh
 k3moe_status k3moe_layer_run(const k3moe_layer* layer, const uint16_t* x, int32_t T, uint16_t* y,
                              int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
                              void* stream);
+/* k3moe_layer_run on host buffers: x_host [T][hidden] and y_host [T][hidden] (bf16 bits) are
+ * page-locked host memory mapped into the device's address space (cudaMallocHost, cudaHostAlloc
+ * or cudaHostRegister on a system with unified addressing); topk_idx_out / topk_w_out (optional)
+ * and ws stay device memory. A kernel reads the tokens from host memory into the workspace
+ * over the CPU-GPU link, the layer runs as k3moe_layer_run (same bits), and a kernel writes
+ * y into y_host: no DMA copy call, and the three launches chain like the layer's own. y_host
+ * holds the result once `stream` has completed. K3MOE_E_HOSTMEM if either buffer is not such
+ * memory (checked on the host: nothing is launched), K3MOE_E_ALIGN if its device address is not
+ * 16-byte aligned, K3MOE_E_SHAPE if T * hidden * 2 is not a multiple of 16. */
+k3moe_status k3moe_layer_run_host(const k3moe_layer* layer, const uint16_t* x_host, int32_t T, uint16_t* y_host,
+                                  int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                                  void* stream);
 k3moe_status k3moe_layer_free(k3moe_layer* layer);
 
 /* Synchronises `stream`, reads and clears the workspace error word. Returns K3MOE_OK,

@@ -30,7 +30,7 @@ NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", 
 
 STATUS = {0: "K3MOE_OK", 1: "K3MOE_E_NULL", 2: "K3MOE_E_SHAPE", 3: "K3MOE_E_ALIGN",
           4: "K3MOE_E_WORKSPACE", 5: "K3MOE_E_MODE", 6: "K3MOE_E_CUDA", 7: "K3MOE_E_TIMEOUT",
-          8: "K3MOE_E_DEVICE", 9: "K3MOE_E_SCRATCH"}
+          8: "K3MOE_E_DEVICE", 9: "K3MOE_E_SCRATCH", 10: "K3MOE_E_HOSTMEM"}
 K3MOE_OK = 0
 
 # Exported symbols (kept in step with include/k3moe.h; a CPU test checks both).
@@ -38,7 +38,7 @@ EXPORTS = ["k3moe_workspace_size", "k3moe_route", "k3moe_permute", "k3moe_projec
            "k3moe_expert_ffn_mxfp4", "k3moe_combine", "k3moe_layer_forward", "k3moe_check",
            "k3moe_status_string", "k3moe_profile", "k3moe_profile_name", "k3moe_route_noalloc",
            "k3moe_layer_stats", "k3moe_selftest_timeout", "k3moe_selftest_occupy", "k3moe_layer_saliency",
-           "k3moe_layer_init", "k3moe_layer_run", "k3moe_layer_free"]
+           "k3moe_layer_init", "k3moe_layer_run", "k3moe_layer_run_host", "k3moe_layer_free"]
 
 
 def _newer(target: str, deps) -> bool:
@@ -110,6 +110,7 @@ def lib():
             "k3moe_layer_saliency": [p, i32, p, p, p, sz, p, p],
             "k3moe_layer_init": [p, p, p, p],
             "k3moe_layer_run": [p, p, i32, p, p, p, p, sz, p],
+            "k3moe_layer_run_host": [p, p, i32, p, p, p, p, sz, p],
             "k3moe_layer_free": [p],
         }
         for name, args in sig.items():
@@ -207,6 +208,12 @@ def k3moe_layer_init(dims, weights, stream=0):
 def k3moe_layer_run(layer, x, T, y, topk_idx_out, topk_w_out, ws, ws_bytes, stream=0, check=True):
     return _ck(lib().k3moe_layer_run(layer, x, T, y, topk_idx_out, topk_w_out, ws, ws_bytes, stream),
                "k3moe_layer_run", check)
+
+
+def k3moe_layer_run_host(layer, x_host, T, y_host, topk_idx_out, topk_w_out, ws, ws_bytes, stream=0, check=True):
+    """k3moe_layer_run with x and y in page-locked host memory (e.g. torch pinned tensors)."""
+    return _ck(lib().k3moe_layer_run_host(layer, x_host, T, y_host, topk_idx_out, topk_w_out, ws, ws_bytes, stream),
+               "k3moe_layer_run_host", check)
 
 
 def k3moe_layer_free(layer):

@@ -78,6 +78,8 @@ WsLayout ws_layout(const k3moe_dims& d, int64_t T) {
   L.as = take(rows * (size_t)exp_pitch(d.inter));
   L.o = take(rows * Lw * 4);
   L.c = take(Tt * Lw * 2);
+  L.xin = take(Tt * (size_t)d.hidden * 2);
+  L.yout = take(Tt * (size_t)d.hidden * 2);
   L.perm = take(((Tt + 255) / 256) * E * 4);
   // the routing kernel's count of finished blocks must read zero at every launch, whatever T
   // the previous call on this workspace had: it sits in the fixed header, after the error word
@@ -365,6 +367,8 @@ const char* k3moe_status_string(k3moe_status s) {
     case K3MOE_E_DEVICE: return "K3MOE_E_DEVICE: device-side check failed";
     case K3MOE_E_SCRATCH:
       return "K3MOE_E_SCRATCH: T * n_experts exceeds the 65536 logits of k3moe_route_noalloc's fixed scratch";
+    case K3MOE_E_HOSTMEM:
+      return "K3MOE_E_HOSTMEM: a host buffer is not page-locked memory the device can address";
   }
   return "K3MOE: unknown status";
 }
@@ -596,6 +600,43 @@ k3moe_status k3moe_layer_run(const k3moe_layer* layer, const uint16_t* x, int32_
   if (!layer) return K3MOE_E_NULL;
   return layer_forward(&layer->dims, &layer->weights, layer->packed ? &layer->ps : nullptr, x, T, y, topk_idx_out,
                        topk_w_out, ws, ws_bytes, stream);
+}
+
+// The device address of page-locked host memory mapped into the device's address space; null
+// for any other pointer (pageable, device or managed memory).
+static void* host_device_ptr(const void* p) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+k3moe_status k3moe_layer_run_host(const k3moe_layer* layer, const uint16_t* x_host, int32_t T, uint16_t* y_host,
+                                  int32_t* topk_idx_out, float* topk_w_out, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  if (!layer) return K3MOE_E_NULL;
+  const k3moe_dims& d = layer->dims;
+  if (T < 0) return K3MOE_E_SHAPE;
+  if (!x_host || !y_host) return K3MOE_E_NULL;
+  K3_TRY(check_ws(d, T, ws, ws_bytes));
+  if (T == 0) return K3MOE_OK;
+  const size_t bytes = (size_t)T * d.hidden * 2;
+  if (bytes % 16) return K3MOE_E_SHAPE;
+  void* xd = host_device_ptr(x_host);
+  void* yd = host_device_ptr(y_host);
+  if (!xd || !yd) return K3MOE_E_HOSTMEM;
+  if (misaligned(xd) || misaligned(yd)) return K3MOE_E_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const WsLayout L = ws_layout(d, T);
+  uint16_t* xin = at<uint16_t>(ws, L.xin);
+  uint16_t* yout = at<uint16_t>(ws, L.yout);
+  K3_CUDA(launch_copy16(xd, xin, bytes, s));
+  K3_TRY(layer_forward(&layer->dims, &layer->weights, layer->packed ? &layer->ps : nullptr, xin, T, yout,
+                       topk_idx_out, topk_w_out, ws, ws_bytes, stream));
+  K3_CUDA(launch_copy16(yout, yd, bytes, s));
+  return K3MOE_OK;
 }
 
 k3moe_status k3moe_layer_saliency(const k3moe_dims* dims, int32_t T, const int32_t* topk_idx, const float* topk_w,

@@ -60,6 +60,7 @@ struct WsLayout {
   // rows of z and of the GLU output with e8m0 scales per 32 (row pitch exp_pitch bytes)
   size_t bq, bs, aq, aqs;
   size_t chunk_done;    // int per chunk: GLU items finished (decode kernel running both passes)
+  size_t xin, yout;     // k3moe_layer_run_host: the tokens and the output on the device [T][H] bf16
   size_t total;
 };
 WsLayout ws_layout(const k3moe_dims& d, int64_t T);
@@ -264,6 +265,9 @@ inline int decode_counters(const k3moe_dims& d, long long T) { return plan_chunk
 cudaError_t launch_glu(const float* g, const float* u, long long n, uint16_t* a, cudaStream_t s);
 cudaError_t launch_combine(const float* o_rows, const int32_t* slot_row, const float* w, int T,
                            int k, int L, uint16_t* c, cudaStream_t s);
+// dst[0, bytes) = src[0, bytes) with 16-byte loads and stores (either side may be page-locked host
+// memory mapped into the device's address space); bytes a multiple of 16, both 16-byte aligned.
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
 // S[idx[t][j]] += w[t][j] * ||o_rows[r]||_2 for every sorted row r of (t, j) (fp64 atomics).
 cudaError_t launch_saliency(const float* o_rows, const int32_t* row_token, const int32_t* row_slot,
                             const int32_t* idx, const float* w, int T, int k, int L, int E, double* S,

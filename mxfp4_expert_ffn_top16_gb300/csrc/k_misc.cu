@@ -131,6 +131,15 @@ __global__ void __launch_bounds__(256) saliency_kernel(const float* __restrict__
   }
 }
 
+// 16-byte copy, one launch in the programmatic-launch chain (the host-buffer layer call's token
+// read and output write).
+__global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n) {
+  pdl_wait();
+  pdl_trigger();
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    dst[i] = src[i];
+}
+
 }  // namespace
 
 cudaError_t launch_saliency(const float* o_rows, const int32_t* row_token, const int32_t* row_slot,
@@ -172,6 +181,14 @@ cudaError_t launch_act_prep(const uint16_t* z, int T, int L, int actq, __half* z
   const int warps = 8;
   act_prep_kernel<<<(unsigned)((nblk + warps - 1) / warps), 32 * warps, 0, s>>>(z, T, L, actq, zh, zs);
   return cudaGetLastError();
+}
+
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  const long long n = (long long)(bytes / 16);
+  if (n == 0) return cudaSuccess;
+  const long long blocks = (n + 255) / 256;
+  return launch_pdl(copy16_kernel, dim3((unsigned)(blocks < 1024 ? blocks : 1024)), dim3(256), 0, s,
+                    static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
 }
 
 }  // namespace k3moe

@@ -158,4 +158,5 @@ def test_prepared_layer_arguments(L):
     assert L.k3moe_layer_init(ctypes.byref(dims()), ctypes.byref(w), ctypes.byref(h), None) == 1
     assert L.k3moe_layer_init(ctypes.byref(dims(act=1)), ctypes.byref(w), ctypes.byref(h), None) == 5
     assert L.k3moe_layer_run(None, good, 1, good, None, None, good, 1 << 30, None) == 1
+    assert L.k3moe_layer_run_host(None, good, 1, good, None, None, good, 1 << 30, None) == 1
     assert L.k3moe_layer_free(None) == 0

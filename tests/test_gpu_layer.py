@@ -501,3 +501,35 @@ def test_layer_small_and_large_experts(wseed, bseed, T, actq):
             np.testing.assert_array_equal(a, b)
     finally:
         k3.k3moe_layer_free(h)
+
+
+@pytest.mark.parametrize("name,Ts", [("tiny", (1, 8, 100)), ("k3", (1, 64))])
+def test_layer_run_host_same_bits(name, Ts, k3_layer):
+    """k3moe_layer_run_host (tokens read from and output written to page-locked host memory by
+    the library's own copy kernels) gives the bits k3moe_layer_run gives; a pageable buffer is
+    refused with K3MOE_E_HOSTMEM before anything is launched."""
+    d = {"tiny": synth.TINY, "k3": synth.K3}[name]
+    lay = k3_layer if name == "k3" else DeviceLayer(d, seed=3)
+    dm = dims(d)
+    h = k3.k3moe_layer_init(dm, lay.weights, stream())
+    try:
+        for T in Ts:
+            x = synth.host_bf16_normal(13, synth.S_X, 0, T * d.hidden, 1.0).reshape(T, d.hidden)
+            ws = workspace(dm, T)
+            want = _run_prepared(lay, h, x, ws)
+            xh = torch.from_numpy(x.view(np.int16).copy()).pin_memory()
+            yh = torch.full((T, d.hidden), -1, dtype=torch.int16).pin_memory()
+            idx = torch.empty((T, d.top_k), dtype=torch.int32, device=DEV)
+            w = torch.empty((T, d.top_k), dtype=torch.float32, device=DEV)
+            k3.k3moe_layer_run_host(h, xh.data_ptr(), T, yh.data_ptr(), idx.data_ptr(), w.data_ptr(),
+                                    ws[0].data_ptr(), ws[1], stream())
+            check_ok(ws[0])
+            np.testing.assert_array_equal(bf16_np(yh), want[0])
+            np.testing.assert_array_equal(idx.cpu().numpy(), want[1])
+            np.testing.assert_array_equal(w.cpu().numpy(), want[2])
+            pageable = np.zeros((T, d.hidden), np.int16)
+            st = k3.k3moe_layer_run_host(h, pageable.ctypes.data, T, yh.data_ptr(), None, None, ws[0].data_ptr(),
+                                         ws[1], stream(), check=False)
+            assert st == 10, k3.status_string(st)
+    finally:
+        k3.k3moe_layer_free(h)

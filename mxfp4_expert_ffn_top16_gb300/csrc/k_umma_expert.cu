@@ -70,15 +70,17 @@ constexpr int kSfPerStage = 16;
 template <bool FP4>
 constexpr int kStgBytes = FP4 ? 2048 : 1536;
 
-// Shapes by chunk size R (sorted rows per item): R = kUmmaChunkRows (many tokens: N up to 224,
-// four deep stages) or R = kGemvTokens (few tokens: N up to 16, small activation tiles, so
-// eleven stages keep enough weight bytes in flight to stream at HBM speed).
-template <int R>
+// Shapes by chunk size R (sorted rows per item) and activation rows per sorted row P:
+// R = kUmmaChunkRows (many tokens: N up to 224 with P = 2, four deep stages; up to 112 with one
+// row per sorted row, whose smaller activation tiles leave room for six stages) or
+// R = kGemvTokens (few tokens: N up to 16, small activation tiles, so eleven stages keep enough
+// weight bytes in flight to stream at HBM speed).
+template <int R, int P>
 struct Cfg {
   static constexpr int kOut = R;                  // sorted rows per item (max)
-  static constexpr int kNMax = 2 * R;             // B rows per tile (P = 2)
-  static constexpr int kBTile = kNMax * BKE;      // e4m3
-  static constexpr int kStages = R == kGemvTokens ? 11 : 4;
+  static constexpr int kNMax = R == kGemvTokens ? 2 * R : P * R;  // B rows per tile (MMA N <= kNMax)
+  static constexpr int kBTile = kNMax * BKE;      // e4m3 (MXFP4: half of it used)
+  static constexpr int kStages = R == kGemvTokens ? 11 : (P == 1 ? 6 : 4);
   static constexpr int kXPitch = R + 1;           // GLU exchange row pitch (floats)
   static constexpr uint32_t kSfCol = kAccSlots * kNMax;  // scale columns, kSfPerStage per stage
   static constexpr uint32_t kTmemCols = R == kGemvTokens ? 256 : 512;
@@ -204,7 +206,7 @@ template <bool GLU, int P, int R, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_constant__ UExpertArgs A) {
   static_assert(!FP4 || P == 1, "MXFP4 activations: one row per sorted row");
   constexpr int kStg = kStgBytes<FP4>;
-  using CF = Cfg<R>;
+  using CF = Cfg<R, P>;
   constexpr int kOut = CF::kOut, kNMax = CF::kNMax, kBTile = CF::kBTile, kStages = CF::kStages;
   constexpr int kXPitch = CF::kXPitch;
   constexpr uint32_t kSfCol = CF::kSfCol, kTmemCols = CF::kTmemCols;
@@ -551,19 +553,22 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   }
 }
 
-template <bool GLU, int R, bool FP4>
+template <bool GLU, int P, int R, bool FP4>
 constexpr size_t smem_bytes() {
-  using CF = Cfg<R>;
+  using CF = Cfg<R, P>;
   return 1024 + (size_t)CF::kStages * (kATile + CF::kBTile) + CF::kStages * kStgBytes<FP4> +
          (GLU ? 64 * CF::kXPitch * 4 : 0) + (2 * CF::kStages + 2 * kAccSlots + 2) * 8 + 16;
 }
-static_assert(smem_bytes<true, kGemvTokens, true>() <= 227 * 1024 &&
-                  smem_bytes<true, kUmmaChunkRows, true>() <= 227 * 1024,
+static_assert(smem_bytes<true, 2, kGemvTokens, false>() <= 227 * 1024 &&
+                  smem_bytes<true, 2, kUmmaChunkRows, false>() <= 227 * 1024 &&
+                  smem_bytes<true, 1, kUmmaChunkRows, false>() <= 227 * 1024 &&
+                  smem_bytes<true, 1, kUmmaChunkRows, true>() <= 227 * 1024 &&
+                  smem_bytes<true, 1, kGemvTokens, true>() <= 227 * 1024,
               "shared memory");
 
 template <bool GLU, int P, int R, bool FP4>
 cudaError_t launch_t(UExpertArgs& a, int items_max, cudaStream_t s) {
-  const size_t smem = smem_bytes<GLU, R, FP4>();
+  const size_t smem = smem_bytes<GLU, P, R, FP4>();
   cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(umma_expert_kernel<GLU, P, R, FP4>), smem);
   if (e != cudaSuccess) return e;
   int grid = num_sms();

@@ -478,23 +478,29 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         // 3. every epilogue thread quantises one (sorted row, 32-feature block) of a into P
         // e4m3 rows for the down pass. All rows are handled without a per-row test so the
         // compiler can interleave them; rows past nr hold unused values and are never stored.
+        // (a quarter with no row of the chunk is skipped: its values are never read)
         float* xr = xg + (lrow & 63) * kXPitch + j0;
+        const bool lo_live = j0 < nr, hi_live = j0 + kQ < nr;  // warp-uniform
         if (q < 2) {
+          if (hi_live) {
 #pragma unroll
-          for (int i = kQ; i < kHalf; ++i) xr[i] = sum[i];
-        } else {
+            for (int i = kQ; i < kHalf; ++i) xr[i] = sum[i];
+          }
+        } else if (lo_live) {
 #pragma unroll
           for (int i = 0; i < kQ; ++i) xr[i] = sum[i];
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
         // silu(g) = g / (1 + e^-g) in the fast forms, ~1e-6 relative, far below bf16 rounding
         if (q < 2) {
+          if (lo_live) {
 #pragma unroll
-          for (int i = 0; i < kQ; ++i) {
-            const float g = sum[i];
-            xr[i] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * xr[i]));
+            for (int i = 0; i < kQ; ++i) {
+              const float g = sum[i];
+              xr[i] = bf16_to_f32(f32_to_bf16(__fdividef(g, 1.0f + __expf(-g)) * xr[i]));
+            }
           }
-        } else {
+        } else if (hi_live) {
 #pragma unroll
           for (int i = kQ; i < kHalf; ++i) {
             const float g = xr[i];

@@ -330,7 +330,7 @@ k3moe_status run_experts_decode(const k3moe_dims& d, const k3moe_weights& w, int
     K3_CUDA(launch_permute(idx, T, d.n_experts, d.top_k, at<int32_t>(ws, L.offsets),
                            at<int32_t>(ws, L.row_token), at<int32_t>(ws, L.row_slot),
                            at<int32_t>(ws, L.slot_row), at<int32_t>(ws, L.plan),
-                           at<int32_t>(ws, L.perm), err, s));
+                           at<int32_t>(ws, L.perm), err, s, many_chunk_rows(d.actq)));
   }
   // (decode, tensor-core experts: the dense kernel wrote z's E4M3 rows, the routing cleared the
   // chunk counters)
@@ -418,7 +418,7 @@ k3moe_status k3moe_permute(const k3moe_dims* dims, const int32_t* topk_idx, int3
   const WsLayout L = ws_layout(d, T);
   K3_CUDA(launch_permute(topk_idx, T, d.n_experts, d.top_k, expert_offsets, row_token, row_slot,
                          slot_row, at<int32_t>(ws, L.plan), at<int32_t>(ws, L.perm),
-                         at<uint32_t>(ws, L.err), s));
+                         at<uint32_t>(ws, L.err), s, many_chunk_rows(d.actq)));
   return K3MOE_OK;
 }
 
@@ -453,7 +453,8 @@ k3moe_status k3moe_expert_ffn_mxfp4(const k3moe_dims* dims, const k3moe_weights*
   uint32_t* err = at<uint32_t>(ws, L.err);
   if (!umma_expert_ok(d))
     K3_CUDA(launch_act_prep(z, T, d.latent, d.actq, at<__half>(ws, L.zh), at<int8_t>(ws, L.zs), s));
-  K3_CUDA(launch_plan(expert_offsets, d.n_experts, T * d.top_k, at<int32_t>(ws, L.plan), err, s));
+  K3_CUDA(launch_plan(expert_offsets, d.n_experts, T * d.top_k, at<int32_t>(ws, L.plan), err, s,
+                      many_chunk_rows(d.actq)));
   K3_TRY(run_expert_gemms(d, *weights, z, T, expert_offsets, row_token, o_rows, ws, L, s));
   return K3MOE_OK;
 }

@@ -89,6 +89,11 @@ inline __host__ __device__ int4* plan_ctab(int32_t* plan, int E) {
 // row, rows, 0}: first those experts' chunks of up to kUmmaChunkRows rows, then the other
 // experts' chunks of up to kGemvTokens rows.
 constexpr int kUmmaChunkRows = 112;
+// With MXFP8 activations (one e4m3 row per sorted row) the chunks of the experts with more than
+// kSmallExpertRows rows hold up to this many rows (the same MMA N and tile bytes as 112 rows of
+// bf16 hi + lo pairs), so the big experts' weight tiles are streamed half as often.
+constexpr int kUmmaChunkRowsWide = 224;
+inline __host__ __device__ int many_chunk_rows(int actq) { return actq == 1 ? kUmmaChunkRowsWide : kUmmaChunkRows; }
 // With many tokens the experts with at most this many sorted rows run on the weights-on-N
 // decode kernel, in chunks of kGemvTokens rows (kSmallChunksMax at most per expert).
 constexpr int kSmallExpertRows = kGemvTokens;
@@ -147,9 +152,12 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, 
                         cudaStream_t s);
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* offsets,
                            int32_t* row_token, int32_t* row_slot, int32_t* slot_row,
-                           int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s);
+                           int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s,
+                           int big_rows = kUmmaChunkRows);
+// big_rows: rows per chunk of the experts with more than kSmallExpertRows rows in the plan's
+// many-token chunk table (many_chunk_rows of the activation mode).
 cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,
-                        cudaStream_t s);
+                        cudaStream_t s, int big_rows = kUmmaChunkRows);
 // Top-k (one block per token), then permutation + plan in one block, for T <= kSmallRouteTokens.
 constexpr int kSmallRouteTokens = 64;
 // done: a workspace counter that is zero between launches (the workspace starts zeroed). Also
@@ -173,7 +181,10 @@ cudaError_t launch_expert_down(const k3moe_dims& d, const k3moe_weights& w, cons
 // kUmmaExpertMinTokens tokens on, of up to kGemvTokens rows below.
 constexpr int kUmmaExpertMinTokens = 65;
 inline bool umma_expert_ok(const k3moe_dims& d) { return d.latent % 128 == 0 && d.inter % 128 == 0; }
-inline int umma_chunk_rows(long long T) { return T >= kUmmaExpertMinTokens ? kUmmaChunkRows : kGemvTokens; }
+// Rows per chunk of the tensor-core expert kernels: P activation rows per sorted row (0: MXFP4).
+inline int umma_chunk_rows(long long T, int P) {
+  return T < kUmmaExpertMinTokens ? kGemvTokens : (P == 1 ? kUmmaChunkRowsWide : kUmmaChunkRows);
+}
 // z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)]
 // (row_token null: row r is token r). Also clears the ncnt counters at cnt (the decode kernel's
 // per-chunk GLU completion counts).

@@ -60,12 +60,12 @@ __device__ int block_excl_scan(int* cnt, int n, int* tmp) {
 
 // Plan from offsets[E+1] held in shared memory: active experts, chunk prefix, the chunk
 // table ctab[c] = {expert, first sorted row, rows (<= 8), 0} in expert order, and the table of
-// chunks of up to kUmmaChunkRows rows for the tensor-core expert GEMM. rows_max = T * k fixes
+// chunks of up to big_rows rows for the tensor-core expert GEMM. rows_max = T * k fixes
 // where the second table sits. The second table lists the chunks of the experts with more than
 // kSmallExpertRows rows first, then the other experts' chunks of up to kGemvTokens rows; its
 // header is {chunks, chunks of the first kind, 0, 0}.
 __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, int* tmp, int* flag,
-                           int* chunks) {
+                           int* chunks, int big_rows) {
   const int tid = threadIdx.x;
   int4* ctab = plan_ctab(plan, E);
   int4* ctab64 = plan_ctab64(plan, E, rows_max);
@@ -91,16 +91,15 @@ __device__ void build_plan(const int* off, int E, int rows_max, int32_t* plan, i
   __syncthreads();
   const bool big = m > kSmallExpertRows;
   if (tid < E) {
-    flag[tid] = big ? (m + kUmmaChunkRows - 1) / kUmmaChunkRows : 0;
+    flag[tid] = big ? (m + big_rows - 1) / big_rows : 0;
     chunks[tid] = (m > 0 && !big) ? (m + kGemvTokens - 1) / kGemvTokens : 0;
   }
   __syncthreads();
   const int Cbig = block_excl_scan(flag, E, tmp);
   const int Csmall = block_excl_scan(chunks, E, tmp);
   if (tid < E && big)
-    for (int q = 0; q * kUmmaChunkRows < m; ++q)
-      ctab64[1 + flag[tid] + q] =
-          make_int4(tid, off[tid] + q * kUmmaChunkRows, min(kUmmaChunkRows, m - q * kUmmaChunkRows), 0);
+    for (int q = 0; q * big_rows < m; ++q)
+      ctab64[1 + flag[tid] + q] = make_int4(tid, off[tid] + q * big_rows, min(big_rows, m - q * big_rows), 0);
   if (tid < E && !big)
     for (int q = 0; q * kGemvTokens < m; ++q)
       ctab64[1 + Cbig + chunks[tid] + q] =
@@ -173,7 +172,8 @@ constexpr int kSmallIdx = 2048;
 __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* idx, int T, int E, int k,
                                                              int32_t* offsets, int32_t* row_token,
                                                              int32_t* row_slot, int32_t* slot_row,
-                                                             int32_t* plan, int* zcnt, int nzcnt, uint32_t* err) {
+                                                             int32_t* plan, int* zcnt, int nzcnt, uint32_t* err,
+                                                             int big_rows) {
   __shared__ int cnt[kMaxE + 1];
   __shared__ int tmp[1024];
   __shared__ int flag[kMaxE];
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(1024) permute_small_kernel(const int32_t* idx,
   if (tid <= E) offsets[tid] = cnt[tid];
   __syncthreads();
   // plan reads the offsets before the scatter turns cnt into running bases
-  build_plan(cnt, E, T * k, plan, tmp, flag, chunks);
+  build_plan(cnt, E, T * k, plan, tmp, flag, chunks, big_rows);
   __syncthreads();
   if (tid < 32) warp_scatter(ix, 0, T, E, k, cnt, mask, row_token, row_slot, slot_row, err);
 }
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
 // One block of 1024 threads: per-expert running sums over token blocks -> offsets, then
 // hist[b][e] becomes the first row of expert e for token block b; plan from offsets.
 __global__ void __launch_bounds__(1024) scan_kernel(int32_t* hist, int nblk, int E, int rows_max,
-                                                    int32_t* offsets, int32_t* plan) {
+                                                    int32_t* offsets, int32_t* plan, int big_rows) {
   __shared__ int cnt[kMaxE + 1];
   __shared__ int tmp[1024];
   __shared__ int flag[kMaxE];
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int32_t* hist, int nblk, int
     }
   }
   __syncthreads();
-  build_plan(cnt, E, rows_max, plan, tmp, flag, chunks);
+  build_plan(cnt, E, rows_max, plan, tmp, flag, chunks, big_rows);
 }
 
 __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__ idx, int T, int E,
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(32) scatter_kernel(const int32_t* __restrict__
 // Plan from caller-supplied offsets. Offsets that are not a non-decreasing sequence from 0
 // to at most rows_max set the index bit of the error word and give an empty plan.
 __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ offsets, int E,
-                                                    int rows_max, int32_t* plan, uint32_t* err) {
+                                                    int rows_max, int32_t* plan, uint32_t* err, int big_rows) {
   __shared__ int off[kMaxE + 1];
   __shared__ int tmp[1024];
   __shared__ int flag[kMaxE];
@@ -417,7 +417,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const int32_t* __restrict__ 
     }
     return;
   }
-  build_plan(off, E, rows_max, plan, tmp, flag, chunks);
+  build_plan(off, E, rows_max, plan, tmp, flag, chunks, big_rows);
 }
 
 }  // namespace
@@ -430,15 +430,15 @@ cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* idx, 
 
 cudaError_t launch_permute(const int32_t* idx, int T, int E, int k, int32_t* offsets,
                            int32_t* row_token, int32_t* row_slot, int32_t* slot_row,
-                           int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s) {
+                           int32_t* plan, int32_t* scratch, uint32_t* err, cudaStream_t s, int big_rows) {
   if (T <= kBlockTokens) {
     permute_small_kernel<<<1, 1024, 0, s>>>(idx, T, E, k, offsets, row_token, row_slot, slot_row, plan, nullptr,
-                                            0, err);
+                                            0, err, big_rows);
     return cudaGetLastError();
   }
   const int nblk = (T + kBlockTokens - 1) / kBlockTokens;
   hist_kernel<<<nblk, 256, 0, s>>>(idx, T, E, k, scratch);
-  scan_kernel<<<1, 1024, 0, s>>>(scratch, nblk, E, T * k, offsets, plan);
+  scan_kernel<<<1, 1024, 0, s>>>(scratch, nblk, E, T * k, offsets, plan, big_rows);
   scatter_kernel<<<nblk, 32, 0, s>>>(idx, T, E, k, scratch, row_token, row_slot, slot_row, err);
   return cudaGetLastError();
 }
@@ -453,12 +453,12 @@ cudaError_t launch_route_tail_small(const float* logits, int T, int E, int k, in
   cudaError_t e = launch_pdl(topk_block_kernel, dim3(T), dim3(kTopkThreads), 0, s, logits, T, E, k, idx, w);
   if (e != cudaSuccess) return e;
   return launch_pdl(permute_small_kernel, dim3(1), dim3(1024), 0, s, (const int32_t*)idx, T, E, k, offsets,
-                    row_token, row_slot, slot_row, plan, cnt, ncnt, err);
+                    row_token, row_slot, slot_row, plan, cnt, ncnt, err, (int)kUmmaChunkRows);
 }
 
 cudaError_t launch_plan(const int32_t* offsets, int E, int rows_max, int32_t* plan, uint32_t* err,
-                        cudaStream_t s) {
-  plan_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, plan, err);
+                        cudaStream_t s, int big_rows) {
+  plan_kernel<<<1, 1024, 0, s>>>(offsets, E, rows_max, plan, err, big_rows);
   return cudaGetLastError();
 }
 

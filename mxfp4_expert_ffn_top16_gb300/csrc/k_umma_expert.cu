@@ -80,11 +80,16 @@ struct Cfg {
   static constexpr int kOut = R;                  // sorted rows per item (max)
   static constexpr int kNMax = R == kGemvTokens ? 2 * R : P * R;  // B rows per tile (MMA N <= kNMax)
   static constexpr int kBTile = kNMax * BKE;      // e4m3 (MXFP4: half of it used)
-  static constexpr int kStages = R == kGemvTokens ? 11 : (P == 1 ? 6 : 4);
-  static constexpr int kXPitch = R + 1;           // GLU exchange row pitch (floats)
+  static constexpr int kStages = R == kGemvTokens ? 11 : (P == 1 && R == kUmmaChunkRows ? 6 : 4);
+  // the epilogue takes the rows in passes of at most kUmmaChunkRows (its registers and exchange
+  // buffer are sized for one pass)
+  static constexpr int kRowsPass = R > kUmmaChunkRows ? kUmmaChunkRows : R;
+  static constexpr int kPasses = R / kRowsPass;
+  static constexpr int kXPitch = kRowsPass + 1;   // GLU exchange row pitch (floats)
   static constexpr uint32_t kSfCol = kAccSlots * kNMax;  // scale columns, kSfPerStage per stage
   static constexpr uint32_t kTmemCols = R == kGemvTokens ? 256 : 512;
-  static_assert(R == kGemvTokens || R == kUmmaChunkRows, "chunk size");
+  static_assert(R == kGemvTokens || R == kUmmaChunkRows || R == kUmmaChunkRowsWide, "chunk size");
+  static_assert(R % kRowsPass == 0, "epilogue passes");
   static_assert(kSfCol + kSfPerStage * kStages <= kTmemCols, "tensor memory");
   static_assert(kNMax <= 256 && kNMax % 16 == 0, "MMA N");
 };
@@ -260,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   // chunk table of the plan for this chunk size (entries {expert, first row, rows, 0})
   const int4* ctab;
   int C;
-  if (R == kUmmaChunkRows) {
+  if (R != kGemvTokens) {
     ctab = plan_ctab64(A.plan, A.E, A.rows_max) + 1;
     C = A.big_only ? ctab[-1].y : ctab[-1].x;
   } else {
@@ -268,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
     C = A.plan[1];
   }
   const int fbs = A.N / kFB;
-  const long long cmax = R == kUmmaChunkRows ? plan_ctab64_max(A.E, A.rows_max) : A.rows_max / R + A.E;
+  const long long cmax = R != kGemvTokens ? plan_ctab64_max(A.E, A.rows_max) : A.rows_max / R + A.E;
   const int items = (C > 0 && C <= cmax) ? C * fbs : 0;
   const int nk = A.K / kKStage<FP4>;
 
@@ -431,24 +436,27 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
     }
     __syncwarp();
   } else {  // ---------------- epilogue warps 2..9: lane quadrant q = warp % 4, row half h
-    constexpr int kHalf = kOut / 2;       // sorted rows per epilogue warp
+    constexpr int kRowsPass = CF::kRowsPass, kPasses = CF::kPasses;
+    constexpr int kHalf = kRowsPass / 2;  // sorted rows per epilogue warp and pass
     constexpr int kQ = kHalf / 2;         // GLU exchange split within a half
     const int eq = warp - 2, q = warp & 3, h = eq >> 2;
     const int lrow = q * 32 + lane;       // tile row = tensor-memory lane
     const int et = eq * 32 + lane;        // 0..255 over the epilogue threads
-    const int j0 = h * kHalf;             // first sorted row of this warp's half
     int slot = 0;
     uint32_t aph = 0, eph = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < items && ok; u += gridDim.x) {
       int e, r0, nr, f0;
       item_of(u, e, r0, nr, f0);
+      if (!mbar_wait_warp(&accf[slot], aph, abort_flag, A.err)) { ok = false; break; }
+      tc_fence_after();
+      for (int pass = 0; pass < kPasses && ok; ++pass) {
+      const int pbase = pass * kRowsPass;  // first sorted row of this pass
+      const int j0 = pbase + h * kHalf;    // first sorted row of this warp's half
       const int ncols = P * (nr - j0);    // live accumulator columns of this half (may be <= 0)
       float sum[kHalf];
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) sum[i] = 0.f;
-      if (!mbar_wait_warp(&accf[slot], aph, abort_flag, A.err)) { ok = false; break; }
-      tc_fence_after();
       const uint32_t base =
           tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(slot * kNMax + P * j0);
 #pragma unroll
@@ -467,10 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce[slot]);
-      if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
+      if (pass == kPasses - 1) {  // the accumulator is free once its last columns are read
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce[slot]);
+      }
       if (GLU) {
         // 1. within each half of the sorted rows, the gate row (lanes 0..63) of feature f parks
         // its sums for the half's upper kQ rows and the up row (lanes 64..127) its sums for the
@@ -479,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         // e4m3 rows for the down pass. All rows are handled without a per-row test so the
         // compiler can interleave them; rows past nr hold unused values and are never stored.
         // (a quarter with no row of the chunk is skipped: its values are never read)
-        float* xr = xg + (lrow & 63) * kXPitch + j0;
+        float* xr = xg + (lrow & 63) * kXPitch + (j0 - pbase);
         const bool lo_live = j0 < nr, hi_live = j0 + kQ < nr;  // warp-uniform
         if (q < 2) {
           if (hi_live) {
@@ -508,14 +517,14 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
           }
         }
         if (!group_barrier_warp(ebar, eph, abort_flag, A.err)) { ok = false; break; }
-        // (sorted row, 32-feature block) units: kOut rows x 2 blocks over the 256 threads
-        for (int unit = et; unit < 2 * kOut; unit += 32 * kEpiWarps) {
-          const int jr = unit % kOut, b = unit / kOut;
+        // (sorted row, 32-feature block) units: the pass's rows x 2 blocks over the 256 threads
+        for (int unit = et; unit < 2 * kRowsPass; unit += 32 * kEpiWarps) {
+          const int jl = unit % kRowsPass, b = unit / kRowsPass, jr = pbase + jl;
           if (jr < nr && FP4) {  // MXFP4: 32 e2m1 codes (16 bytes) and the block exponent
             float v[32], am = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              v[i] = xg[(32 * b + i) * kXPitch + jr];
+              v[i] = xg[(32 * b + i) * kXPitch + jl];
               am = fmaxf(am, fabsf(v[i]));
             }
             const int X = mxfp4_block_exp(am);
@@ -528,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
           } else if (jr < nr) {
             float v[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = xg[(32 * b + i) * kXPitch + jr];
+            for (int i = 0; i < 32; ++i) v[i] = xg[(32 * b + i) * kXPitch + jl];
             uint32_t codes[P][8];
             int X[P];
             quant_block32<P>(v, codes, X);
@@ -549,6 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         for (int i = 0; i < kHalf; ++i)
           if (j0 + i < nr) A.o_out[(size_t)(r0 + j0 + i) * A.N + f0 + lrow] = sum[i];
       }
+      }  // pass
+      if (++slot == kAccSlots) { slot = 0; aph ^= 1; }
     }
   }
   tc_fence_before();
@@ -569,6 +580,7 @@ static_assert(smem_bytes<true, 2, kGemvTokens, false>() <= 227 * 1024 &&
                   smem_bytes<true, 2, kUmmaChunkRows, false>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kUmmaChunkRows, false>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kUmmaChunkRows, true>() <= 227 * 1024 &&
+                  smem_bytes<true, 1, kUmmaChunkRowsWide, false>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kGemvTokens, true>() <= 227 * 1024,
               "shared memory");
 
@@ -592,8 +604,9 @@ cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t 
                   : launch_t<GLU, 2, kGemvTokens, false>(a, items_max, s);
   }
   if (P == 0) return launch_t<GLU, 1, kUmmaChunkRows, true>(a, items_max, s);
-  return P == 1 ? launch_t<GLU, 1, kUmmaChunkRows, false>(a, items_max, s)
-                : launch_t<GLU, 2, kUmmaChunkRows, false>(a, items_max, s);
+  if (R == kUmmaChunkRowsWide && P == 1) return launch_t<GLU, 1, kUmmaChunkRowsWide, false>(a, items_max, s);
+  if (R != kUmmaChunkRows || P != 2) return cudaErrorInvalidValue;
+  return launch_t<GLU, 2, kUmmaChunkRows, false>(a, items_max, s);
 }
 
 // z[row_token[r]] (bf16) -> P e4m3 rows with e8m0 block scales per sorted row r (P = 0: one
@@ -717,7 +730,7 @@ cudaError_t launch_quant_rows(const uint16_t* z, const int32_t* row_token, int r
 cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* bq,
                             const uint8_t* bs, int P, int T, uint8_t* aq, uint8_t* aqs, uint32_t* err,
                             cudaStream_t s, bool big_only, const PackedScales* ps) {
-  const int R = umma_chunk_rows(T);
+  const int R = umma_chunk_rows(T, P);
   UExpertArgs A{};
   const uint64_t pitch = (uint64_t)d.latent / 2, wrows = (uint64_t)d.n_experts * d.inter;
   const int rows = T * d.top_k;
@@ -735,7 +748,7 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
   A.s0 = w.gate_s; A.s1 = w.up_s; A.sb = bs; A.plan = plan;
   A.N = d.inter; A.K = d.latent; A.E = d.n_experts; A.rows_max = rows;
   A.aq = aq; A.aqs = aqs; A.err = err;
-  A.big_only = big_only && R == kUmmaChunkRows;
+  A.big_only = big_only && R != kGemvTokens;
   A.pw = ps && d.latent % 128 == 0 ? ps->glu : nullptr;
   const int items_max = (rows / R + d.n_experts) * (d.inter / 64);
   return launch_pr<true>(A, P, R, items_max, s);
@@ -744,7 +757,7 @@ cudaError_t launch_umma_glu(const k3moe_dims& d, const k3moe_weights& w, int32_t
 cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_t* plan, const uint8_t* aq,
                              const uint8_t* aqs, int P, int T, float* o_rows, uint32_t* err, cudaStream_t s,
                              bool big_only, const PackedScales* ps) {
-  const int R = umma_chunk_rows(T);
+  const int R = umma_chunk_rows(T, P);
   UExpertArgs A{};
   const int rows = T * d.top_k;
   const uint64_t pitch = (uint64_t)d.inter / 2, wrows = (uint64_t)d.n_experts * d.latent;
@@ -760,7 +773,7 @@ cudaError_t launch_umma_down(const k3moe_dims& d, const k3moe_weights& w, int32_
   A.s0 = w.down_s; A.sb = aqs; A.plan = plan;
   A.N = d.latent; A.K = d.inter; A.E = d.n_experts; A.rows_max = rows;
   A.o_out = o_rows; A.err = err;
-  A.big_only = big_only && R == kUmmaChunkRows;
+  A.big_only = big_only && R != kGemvTokens;
   A.pw = ps && d.inter % 128 == 0 ? ps->down : nullptr;
   const int items_max = (rows / R + d.n_experts) * (d.latent / 128);
   return launch_pr<false>(A, P, R, items_max, s);

@@ -93,7 +93,12 @@ constexpr int kUmmaChunkRows = 112;
 // kSmallExpertRows rows hold up to this many rows (the same MMA N and tile bytes as 112 rows of
 // bf16 hi + lo pairs), so the big experts' weight tiles are streamed half as often.
 constexpr int kUmmaChunkRowsWide = 224;
-inline __host__ __device__ int many_chunk_rows(int actq) { return actq == 1 ? kUmmaChunkRowsWide : kUmmaChunkRows; }
+// With MXFP4 activations: 192 rows (a second 128-row block of activation scales then fits in
+// tensor memory beside two accumulators).
+constexpr int kUmmaChunkRowsFp4 = 192;
+inline __host__ __device__ int many_chunk_rows(int actq) {
+  return actq == 1 ? kUmmaChunkRowsWide : (actq == 2 ? kUmmaChunkRowsFp4 : kUmmaChunkRows);
+}
 // With many tokens the experts with at most this many sorted rows run on the weights-on-N
 // decode kernel, in chunks of kGemvTokens rows (kSmallChunksMax at most per expert).
 constexpr int kSmallExpertRows = kGemvTokens;
@@ -183,7 +188,8 @@ constexpr int kUmmaExpertMinTokens = 65;
 inline bool umma_expert_ok(const k3moe_dims& d) { return d.latent % 128 == 0 && d.inter % 128 == 0; }
 // Rows per chunk of the tensor-core expert kernels: P activation rows per sorted row (0: MXFP4).
 inline int umma_chunk_rows(long long T, int P) {
-  return T < kUmmaExpertMinTokens ? kGemvTokens : (P == 1 ? kUmmaChunkRowsWide : kUmmaChunkRows);
+  return T < kUmmaExpertMinTokens ? kGemvTokens
+                                  : (P == 1 ? kUmmaChunkRowsWide : (P == 0 ? kUmmaChunkRowsFp4 : kUmmaChunkRows));
 }
 // z rows gathered by row_token into P e4m3 rows per sorted row: bq [P*rows][L], bs [P*rows][exp_pitch(L)]
 // (row_token null: row r is token r). Also clears the ncnt counters at cnt (the decode kernel's

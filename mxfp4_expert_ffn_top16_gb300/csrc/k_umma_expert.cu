@@ -61,36 +61,40 @@ constexpr int kThreads = 384;             // 0 TMA, 1 MMA, 2-9 epilogue, 10-11 s
 constexpr int kEpiWarps = 8;
 constexpr int kGather0 = 2 + kEpiWarps;   // first scale-gather warp
 constexpr int kAccSlots = 2;
-// Tensor-memory scale columns per stage. e4m3: A 4, B rows 0..127 4, B rows 128..255 4 (one
-// 32-bit word of four K-block scales per row and stage). MXFP4: two words per row and stage
-// (K = 256): A 4 + 4, B 4 + 4 (B rows <= 128).
-constexpr int kSfPerStage = 16;
-// Scale staging blocks of 32 x 16 bytes per stage: e4m3 A, B rows 0..127, B rows 128..255;
-// MXFP4 A word 0, A word 1, B word 0, B word 1.
-template <bool FP4>
-constexpr int kStgBytes = FP4 ? 2048 : 1536;
+// Tensor-memory scale columns per stage (Cfg::kSfPer). e4m3: A 4, B rows 0..127 4, B rows
+// 128..255 4 (one 32-bit word of four K-block scales per row and stage), 16 reserved. MXFP4: two
+// words per row and stage (K = 256): A 4 + 4, B 4 + 4 (B rows <= 128); with more than 128 B rows,
+// each B word takes 8 columns (rows 0..127, then rows 128..255): 24.
+// Scale staging blocks of 32 x 16 bytes per stage (Cfg::kStg): e4m3 A, B rows 0..127, B rows
+// 128..255; MXFP4 A word 0, A word 1, B word 0, B word 1 (rows 0..127), then B word 0 and word 1
+// of rows 128..255.
 
 // Shapes by chunk size R (sorted rows per item) and activation rows per sorted row P:
 // R = kUmmaChunkRows (many tokens: N up to 224 with P = 2, four deep stages; up to 112 with one
 // row per sorted row, whose smaller activation tiles leave room for six stages) or
 // R = kGemvTokens (few tokens: N up to 16, small activation tiles, so eleven stages keep enough
 // weight bytes in flight to stream at HBM speed).
-template <int R, int P>
+template <int R, int P, bool FP4>
 struct Cfg {
   static constexpr int kOut = R;                  // sorted rows per item (max)
   static constexpr int kNMax = R == kGemvTokens ? 2 * R : P * R;  // B rows per tile (MMA N <= kNMax)
   static constexpr int kBTile = kNMax * BKE;      // e4m3 (MXFP4: half of it used)
   static constexpr int kStages = R == kGemvTokens ? 11 : (P == 1 && R == kUmmaChunkRows ? 6 : 4);
+  static constexpr bool kWideSf = FP4 && kNMax > 128;  // MXFP4 B scales in two 128-row blocks
+  static constexpr int kSfPer = kWideSf ? 24 : 16;
+  static constexpr int kStg = FP4 ? (kWideSf ? 3072 : 2048) : 1536;
   // the epilogue takes the rows in passes of at most kUmmaChunkRows (its registers and exchange
   // buffer are sized for one pass)
-  static constexpr int kRowsPass = R > kUmmaChunkRows ? kUmmaChunkRows : R;
-  static constexpr int kPasses = R / kRowsPass;
+  static constexpr int kPasses = (R + kUmmaChunkRows - 1) / kUmmaChunkRows;
+  static constexpr int kRowsPass = R / kPasses;
   static constexpr int kXPitch = kRowsPass + 1;   // GLU exchange row pitch (floats)
-  static constexpr uint32_t kSfCol = kAccSlots * kNMax;  // scale columns, kSfPerStage per stage
+  static constexpr uint32_t kSfCol = kAccSlots * kNMax;  // scale columns, kSfPer per stage
   static constexpr uint32_t kTmemCols = R == kGemvTokens ? 256 : 512;
-  static_assert(R == kGemvTokens || R == kUmmaChunkRows || R == kUmmaChunkRowsWide, "chunk size");
-  static_assert(R % kRowsPass == 0, "epilogue passes");
-  static_assert(kSfCol + kSfPerStage * kStages <= kTmemCols, "tensor memory");
+  static_assert(R == kGemvTokens || R == kUmmaChunkRows || R == kUmmaChunkRowsWide || R == kUmmaChunkRowsFp4,
+                "chunk size");
+  static_assert(R % kPasses == 0 && kRowsPass % 4 == 0, "epilogue passes");
+  static_assert(kSfCol + kSfPer * kStages <= kTmemCols, "tensor memory");
+  static_assert(kNMax <= 7 * 32, "scale gather groups");
   static_assert(kNMax <= 256 && kNMax % 16 == 0, "MMA N");
 };
 
@@ -210,8 +214,9 @@ __device__ __forceinline__ void quant_block32(float (&v)[32], uint32_t (&codes)[
 template <bool GLU, int P, int R, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_constant__ UExpertArgs A) {
   static_assert(!FP4 || P == 1, "MXFP4 activations: one row per sorted row");
-  constexpr int kStg = kStgBytes<FP4>;
-  using CF = Cfg<R, P>;
+  using CF = Cfg<R, P, FP4>;
+  constexpr int kStg = CF::kStg, kSfPerStage = CF::kSfPer;
+  constexpr bool kWideSf = CF::kWideSf;
   constexpr int kOut = CF::kOut, kNMax = CF::kNMax, kBTile = CF::kBTile, kStages = CF::kStages;
   constexpr int kXPitch = CF::kXPitch;
   constexpr uint32_t kSfCol = CF::kSfCol, kTmemCols = CF::kTmemCols;
@@ -223,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
   const int srow = A.K / 32, spb = exp_pitch(A.K);
   uint8_t* sA = smem;
   uint8_t* sB = sA + kStages * kATile;
-  uint8_t* stg = sB + kStages * kBTile;                            // kStages x kStgBytes
+  uint8_t* stg = sB + kStages * kBTile;                            // kStages x kStg
   float* xg = reinterpret_cast<float*>(stg + kStages * kStg);  // GLU: [64][kXPitch]
   uint64_t* full = reinterpret_cast<uint64_t*>(xg + (GLU ? 64 * kXPitch : 0));
   uint64_t* empty = full + kStages;
@@ -336,12 +341,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
           dst[w] = st_lane + 4 * w;
         }
         n = 4;
-      } else if (FP4) {  // B rows <= 128: word 0 in block 2, word 1 in block 3
+      } else if (FP4) {  // word 0 of rows 0..127 in block 2, word 1 in block 3 (rows 128..: 4, 5)
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
+        for (int w = 0; w < (kNMax + 31) / 32 && w < 7; ++w) {
           const int rb = 32 * w + lane;
           src[w] = A.sb + ((size_t)r0 + rb) * spb;
-          dst[w] = st_lane + 1024 + 4 * w;
+          dst[w] = st_lane + (w < 4 ? 1024 + 4 * w : 2048 + 4 * (w - 4));
           if (rb < nr) n = w + 1;
         }
       } else {
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         const uint32_t so = (uint32_t)(s * kStg);
         if (FP4) {  // eight K-block scales per row and stage: two words, the second 512 bytes on
 #pragma unroll
-          for (int w = 0; w < 4; ++w)
+          for (int w = 0; w < 7; ++w)
             if (w < n) {
               cp_async4(dst[w] + so, src[w] + 8 * kc);
               cp_async4(dst[w] + so + 512, src[w] + 8 * kc + 4);
@@ -392,18 +397,28 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
         const uint32_t a0 = smem_u32(sA + s * kATile), b0 = smem_u32(sB + s * kBTile);
         if (FP4) {
           // scale columns: A word 0 (4), A word 1 (4), B word 0 (4), B word 1 (4); the MMA of
-          // K block pair kk uses word kk / 2, bytes 2 (kk % 2) and 2 (kk % 2) + 1
+          // K block pair kk uses word kk / 2, bytes 2 (kk % 2) and 2 (kk % 2) + 1. With more than
+          // 128 B rows each B word takes 8 columns, rows 128.. in its upper 4.
+          constexpr uint32_t kBw = kWideSf ? 8 : 4;  // columns per B word
           if (elect_one()) {
             fence_async_smem();  // the scales arrived through cp.async; tcgen05.cp reads them
             tc_fence_after();
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa + 4 * q),
-                           "l"(sdesc_sf(st0 + 512 * q)));
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa), "l"(sdesc_sf(st0)));
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa + 4), "l"(sdesc_sf(st0 + 512)));
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa + 8),
+                         "l"(sdesc_sf(st0 + 1024)));
+            asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa + 8 + kBw),
+                         "l"(sdesc_sf(st0 + 1536)));
+            if (kWideSf && Nc > 128) {
+              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa + 12),
+                           "l"(sdesc_sf(st0 + 2048)));
+              asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(tsa + 12 + kBw),
+                           "l"(sdesc_sf(st0 + 2560)));
+            }
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               umma_mxf4(d, sdesc_sw128(a0 + kk * 32), sdesc_sw128(b0 + kk * 32), idesc_mxf4(Nc, 2 * (kk & 1)),
-                        tsa + 4 * (kk >> 1), tsa + 8 + 4 * (kk >> 1), (kc | kk) != 0 ? 1u : 0u);
+                        tsa + 4 * (kk >> 1), tsa + 8 + kBw * (kk >> 1), (kc | kk) != 0 ? 1u : 0u);
             umma_commit(&empty[s]);
           }
         } else if (elect_one()) {
@@ -572,15 +587,15 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
 
 template <bool GLU, int P, int R, bool FP4>
 constexpr size_t smem_bytes() {
-  using CF = Cfg<R, P>;
-  return 1024 + (size_t)CF::kStages * (kATile + CF::kBTile) + CF::kStages * kStgBytes<FP4> +
+  using CF = Cfg<R, P, FP4>;
+  return 1024 + (size_t)CF::kStages * (kATile + CF::kBTile) + CF::kStages * CF::kStg +
          (GLU ? 64 * CF::kXPitch * 4 : 0) + (2 * CF::kStages + 2 * kAccSlots + 2) * 8 + 16;
 }
 static_assert(smem_bytes<true, 2, kGemvTokens, false>() <= 227 * 1024 &&
                   smem_bytes<true, 2, kUmmaChunkRows, false>() <= 227 * 1024 &&
-                  smem_bytes<true, 1, kUmmaChunkRows, false>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kUmmaChunkRows, true>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kUmmaChunkRowsWide, false>() <= 227 * 1024 &&
+                  smem_bytes<true, 1, kUmmaChunkRowsFp4, true>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kGemvTokens, true>() <= 227 * 1024,
               "shared memory");
 
@@ -603,7 +618,10 @@ cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t 
     return P == 1 ? launch_t<GLU, 1, kGemvTokens, false>(a, items_max, s)
                   : launch_t<GLU, 2, kGemvTokens, false>(a, items_max, s);
   }
-  if (P == 0) return launch_t<GLU, 1, kUmmaChunkRows, true>(a, items_max, s);
+  if (P == 0) {
+    if (R == kUmmaChunkRowsFp4) return launch_t<GLU, 1, kUmmaChunkRowsFp4, true>(a, items_max, s);
+    return R == kUmmaChunkRows ? launch_t<GLU, 1, kUmmaChunkRows, true>(a, items_max, s) : cudaErrorInvalidValue;
+  }
   if (R == kUmmaChunkRowsWide && P == 1) return launch_t<GLU, 1, kUmmaChunkRowsWide, false>(a, items_max, s);
   if (R != kUmmaChunkRows || P != 2) return cudaErrorInvalidValue;
   return launch_t<GLU, 2, kUmmaChunkRows, false>(a, items_max, s);

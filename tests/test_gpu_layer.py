@@ -76,12 +76,15 @@ DEEP = synth.Dims(hidden=256, latent=1024, inter=1024, n_experts=8, top_k=2)
 DIMS = {"tiny": synth.TINY, "wide": WIDE, "deep": DEEP}
 
 
-@pytest.mark.parametrize("dname,T", [("tiny", 24), ("tiny", 100), ("wide", 7), ("wide", 200), ("deep", 3),
-                                     ("deep", 20)])
+@pytest.mark.parametrize("dname,T", [("tiny", 24), ("tiny", 100), ("wide", 7), ("wide", 200), ("wide", 700),
+                                     ("deep", 3), ("deep", 20)])
 @pytest.mark.parametrize("actq", [0, 1, 2])
 def test_expert_ffn_tiny_all_rows(actq, dname, T):
     """actq 2 (MXFP4 activations, kind::mxf4) needs latent and inter multiples of 256: the tiny
-    shape is refused with K3MOE_E_MODE; the wide and deep shapes run it at 8- and 112-row chunks."""
+    shape is refused with K3MOE_E_MODE; the wide and deep shapes run it at 8-row and many-token
+    chunks. wide at 700 tokens gives experts of several hundred rows: full chunks of 112 (bf16),
+    224 (MXFP8) and 192 rows (MXFP4, whose second 128-row block of activation scales only such
+    chunks use)."""
     d = DIMS[dname]
     if actq == 2 and d.latent % 256:
         ws = torch.zeros(256, dtype=torch.uint8, device=DEV)

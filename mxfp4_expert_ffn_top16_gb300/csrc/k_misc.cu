@@ -133,11 +133,21 @@ __global__ void __launch_bounds__(256) saliency_kernel(const float* __restrict__
 
 // 16-byte copy, one launch in the programmatic-launch chain (the host-buffer layer call's token
 // read and output write).
+// Four 16-byte loads in flight per thread before their stores: the reads cross the CPU-GPU link
+// (or the writes do), whose latency a single load per thread would expose.
 __global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, long long n) {
   pdl_wait();
   pdl_trigger();
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-    dst[i] = src[i];
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i + j * stride < n) v[j] = src[i + j * stride];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i + j * stride < n) dst[i + j * stride] = v[j];
+  }
 }
 
 }  // namespace
@@ -187,7 +197,7 @@ cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t
   const long long n = (long long)(bytes / 16);
   if (n == 0) return cudaSuccess;
   const long long blocks = (n + 255) / 256;
-  return launch_pdl(copy16_kernel, dim3((unsigned)(blocks < 1024 ? blocks : 1024)), dim3(256), 0, s,
+  return launch_pdl(copy16_kernel, dim3((unsigned)(blocks < 2048 ? blocks : 2048)), dim3(256), 0, s,
                     static_cast<const uint4*>(src), static_cast<uint4*>(dst), n);
 }
 

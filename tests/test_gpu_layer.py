@@ -480,12 +480,13 @@ def test_prepared_layer_same_bits_as_forward(name, actq, Ts, k3_layer):
 
 
 # Many tokens with e4m3 activations: the experts with at most 8 rows run on the weights-on-N
-# kernel and the others on the many-token kernel (in chunks of 112 rows). A Zipf bias over
+# kernel and the others on the many-token kernel (chunks of 112 rows; 224 with MXFP8). A Zipf bias over
 # WIDE's 16 experts gives both kinds, with counts on either side of the threshold (7, 8 / 9, 11
 # at T = 96; 8 / 9, 13 and experts of more than one 112-row chunk at T = 200). Every token is
 # compared with the oracle, and the prepared layer (scales from the packed images) gives the
-# same bits as the unprepared one.
-@pytest.mark.parametrize("wseed,bseed,T,actq", [(3, 3, 96, 0), (7, 4, 200, 0), (7, 4, 200, 1)])
+# same bits as the unprepared one. With MXFP4 activations (no small-expert kernel) the 200-row
+# experts fill a 192-row chunk, whose activation rows 128.. take the second block of scales.
+@pytest.mark.parametrize("wseed,bseed,T,actq", [(3, 3, 96, 0), (7, 4, 200, 0), (7, 4, 200, 1), (7, 4, 200, 2)])
 def test_layer_small_and_large_experts(wseed, bseed, T, actq):
     d = WIDE
     lay = DeviceLayer(d, seed=wseed, bias=synth.zipf_bias(d.n_experts, bseed, s=0.7), actq=actq)

@@ -13,8 +13,8 @@ store (15.7 GB) is far larger than L2, tokens are fresh every step, and the dens
 rotate over 8 copies (923 MB) so no step finds them in L2.
 
 The default run (decode_b1, one GPU) then measures the metric's other configurations in child
-processes of their own (decode_b64, prefill_4k with bf16 and with MXFP4 activations,
-prefill_32k; a few steps each) and summarises their lines under "workloads";
+processes of their own (decode_b64, prefill_4k with bf16, MXFP8 and MXFP4 activations,
+prefill_32k with bf16 and MXFP4; a few steps each) and summarises their lines under "workloads";
 --no-secondary skips them.
 
 --impl reference times the CPU oracle (plain C, double accumulation) on the host cores on a
@@ -287,7 +287,8 @@ def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads,
 # The other configurations the metric is quoted on, measured after the headline (decode_b1) in
 # the default run, each in a child process of its own (its memory freed at exit) with a fixed
 # number of steps; their lines are summarised under "workloads" of the one JSON line.
-SECONDARY = (("decode_b64", 0, 100), ("prefill_4k", 0, 10), ("prefill_4k", 2, 10), ("prefill_32k", 0, 3))
+SECONDARY = (("decode_b64", 0, 100), ("prefill_4k", 0, 10), ("prefill_4k", 1, 10), ("prefill_4k", 2, 10),
+             ("prefill_32k", 0, 3), ("prefill_32k", 2, 3))
 
 
 def summarize_line(line):
@@ -680,8 +681,9 @@ def main():
                     help="also run two always-on bf16 shared experts of this width (their width is not "
                          "on the pages; the headline metric is the routed layer without them)")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false",
-                    help="decode_b1 only: skip the runs of decode_b64, prefill_4k (bf16 and MXFP4 "
-                         "activations) and prefill_32k that the default run adds under \"workloads\"")
+                    help="decode_b1 only: skip the runs of decode_b64, prefill_4k (bf16, MXFP8 and MXFP4 "
+                         "activations) and prefill_32k (bf16, MXFP4) that the default run adds under "
+                         "\"workloads\"")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling aid: the same workload with fewer experts (fits an ncu capture); "
                          "not a bench configuration")

@@ -19,9 +19,10 @@
 //          adds the two results.
 //
 // Tile: M = 128 weight rows (GLU: 64 gate rows and the 64 up rows of the same features, so
-// lane i and lane i + 64 pair up), N = P x (up to 112) activation rows, K = 128 per pipeline
-// stage (four MMAs of K = 32, each with its scale byte). Work item = (chunk of up to 112 sorted
-// rows of one expert, feature block), feature block fastest: the CTAs working at one time
+// lane i and lane i + 64 pair up), N = the chunk's activation rows (up to 224: 112 sorted rows
+// of bf16 hi + lo pairs, 224 of MXFP8, 192 of MXFP4), K = 128 per pipeline stage (four MMAs of
+// K = 32, each with its scale byte; MXFP4: K = 256). Work item = (chunk of one expert's sorted
+// rows, feature block), feature block fastest: the CTAs working at one time
 // share a chunk's activations and an expert's weights in L2. Each tcgen05 instruction costs
 // tens of cycles to issue from the single MMA thread, so N is made as large as tensor memory
 // allows (two 224-column accumulators) to keep the tensor pipe, not the issue, the limit.
@@ -70,10 +71,10 @@ constexpr int kAccSlots = 2;
 // of rows 128..255.
 
 // Shapes by chunk size R (sorted rows per item) and activation rows per sorted row P:
-// R = kUmmaChunkRows (many tokens: N up to 224 with P = 2, four deep stages; up to 112 with one
-// row per sorted row, whose smaller activation tiles leave room for six stages) or
-// R = kGemvTokens (few tokens: N up to 16, small activation tiles, so eleven stages keep enough
-// weight bytes in flight to stream at HBM speed).
+// many tokens: R = kUmmaChunkRows with P = 2 (N up to 224, four stages), kUmmaChunkRowsWide with
+// MXFP8 (N up to 224, four stages) or kUmmaChunkRowsFp4 with MXFP4 (N up to 192, four stages; a
+// 112-row one-row chunk would leave room for six); few tokens: R = kGemvTokens (N up to 16, small
+// activation tiles, so eleven stages keep enough weight bytes in flight to stream at HBM speed).
 template <int R, int P, bool FP4>
 struct Cfg {
   static constexpr int kOut = R;                  // sorted rows per item (max)

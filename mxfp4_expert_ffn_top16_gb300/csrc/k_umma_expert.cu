@@ -71,16 +71,16 @@ constexpr int kAccSlots = 2;
 // of rows 128..255.
 
 // Shapes by chunk size R (sorted rows per item) and activation rows per sorted row P:
-// many tokens: R = kUmmaChunkRows with P = 2 (N up to 224, four stages), kUmmaChunkRowsWide with
-// MXFP8 (N up to 224, four stages) or kUmmaChunkRowsFp4 with MXFP4 (N up to 192, four stages; a
-// 112-row one-row chunk would leave room for six); few tokens: R = kGemvTokens (N up to 16, small
-// activation tiles, so eleven stages keep enough weight bytes in flight to stream at HBM speed).
+// many tokens: R = kUmmaChunkRows with P = 2 (N up to 224), kUmmaChunkRowsWide with MXFP8 (N up
+// to 224) or kUmmaChunkRowsFp4 with MXFP4 (N up to 192), four stages each; few tokens:
+// R = kGemvTokens (N up to 16, small activation tiles, so eleven stages keep enough weight bytes
+// in flight to stream at HBM speed).
 template <int R, int P, bool FP4>
 struct Cfg {
   static constexpr int kOut = R;                  // sorted rows per item (max)
   static constexpr int kNMax = R == kGemvTokens ? 2 * R : P * R;  // B rows per tile (MMA N <= kNMax)
   static constexpr int kBTile = kNMax * BKE;      // e4m3 (MXFP4: half of it used)
-  static constexpr int kStages = R == kGemvTokens ? 11 : (P == 1 && R == kUmmaChunkRows ? 6 : 4);
+  static constexpr int kStages = R == kGemvTokens ? 11 : 4;
   static constexpr bool kWideSf = FP4 && kNMax > 128;  // MXFP4 B scales in two 128-row blocks
   static constexpr int kSfPer = kWideSf ? 24 : 16;
   static constexpr int kStg = FP4 ? (kWideSf ? 3072 : 2048) : 1536;
@@ -594,7 +594,6 @@ constexpr size_t smem_bytes() {
 }
 static_assert(smem_bytes<true, 2, kGemvTokens, false>() <= 227 * 1024 &&
                   smem_bytes<true, 2, kUmmaChunkRows, false>() <= 227 * 1024 &&
-                  smem_bytes<true, 1, kUmmaChunkRows, true>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kUmmaChunkRowsWide, false>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kUmmaChunkRowsFp4, true>() <= 227 * 1024 &&
                   smem_bytes<true, 1, kGemvTokens, true>() <= 227 * 1024,
@@ -619,10 +618,8 @@ cudaError_t launch_pr(UExpertArgs& a, int P, int R, int items_max, cudaStream_t 
     return P == 1 ? launch_t<GLU, 1, kGemvTokens, false>(a, items_max, s)
                   : launch_t<GLU, 2, kGemvTokens, false>(a, items_max, s);
   }
-  if (P == 0) {
-    if (R == kUmmaChunkRowsFp4) return launch_t<GLU, 1, kUmmaChunkRowsFp4, true>(a, items_max, s);
-    return R == kUmmaChunkRows ? launch_t<GLU, 1, kUmmaChunkRows, true>(a, items_max, s) : cudaErrorInvalidValue;
-  }
+  if (P == 0)
+    return R == kUmmaChunkRowsFp4 ? launch_t<GLU, 1, kUmmaChunkRowsFp4, true>(a, items_max, s) : cudaErrorInvalidValue;
   if (R == kUmmaChunkRowsWide && P == 1) return launch_t<GLU, 1, kUmmaChunkRowsWide, false>(a, items_max, s);
   if (R != kUmmaChunkRows || P != 2) return cudaErrorInvalidValue;
   return launch_t<GLU, 2, kUmmaChunkRows, false>(a, items_max, s);

@@ -75,15 +75,17 @@ constexpr int kAccSlots = 2;
 // to 224) or kUmmaChunkRowsFp4 with MXFP4 (N up to 192), four stages each; few tokens:
 // R = kGemvTokens (N up to 16, small activation tiles, so eleven stages keep enough weight bytes
 // in flight to stream at HBM speed).
-template <int R, int P, bool FP4>
+template <int R, int P, bool FP4, bool GLU>
 struct Cfg {
   static constexpr int kOut = R;                  // sorted rows per item (max)
   static constexpr int kNMax = R == kGemvTokens ? 2 * R : P * R;  // B rows per tile (MMA N <= kNMax)
   static constexpr int kBTile = kNMax * BKE;      // e4m3 (MXFP4: half of it used)
-  static constexpr int kStages = R == kGemvTokens ? 11 : 4;
+  static constexpr int kStg = FP4 ? (FP4 && P * R > 128 ? 3072 : 2048) : 1536;
+  // the down pass has no exchange buffer: a fifth stage fits where its stages are small enough
+  static constexpr int kStages =
+      R == kGemvTokens ? 11 : (!GLU && 5 * (128 * BKE + kNMax * BKE + kStg) + 1024 + 256 <= 227 * 1024 ? 5 : 4);
   static constexpr bool kWideSf = FP4 && kNMax > 128;  // MXFP4 B scales in two 128-row blocks
   static constexpr int kSfPer = kWideSf ? 24 : 16;
-  static constexpr int kStg = FP4 ? (kWideSf ? 3072 : 2048) : 1536;
   // the epilogue takes the rows in passes of at most kUmmaChunkRows (its registers and exchange
   // buffer are sized for one pass)
   static constexpr int kPasses = (R + kUmmaChunkRows - 1) / kUmmaChunkRows;
@@ -215,7 +217,7 @@ __device__ __forceinline__ void quant_block32(float (&v)[32], uint32_t (&codes)[
 template <bool GLU, int P, int R, bool FP4>
 __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_constant__ UExpertArgs A) {
   static_assert(!FP4 || P == 1, "MXFP4 activations: one row per sorted row");
-  using CF = Cfg<R, P, FP4>;
+  using CF = Cfg<R, P, FP4, GLU>;
   constexpr int kStg = CF::kStg, kSfPerStage = CF::kSfPer;
   constexpr bool kWideSf = CF::kWideSf;
   constexpr int kOut = CF::kOut, kNMax = CF::kNMax, kBTile = CF::kBTile, kStages = CF::kStages;
@@ -588,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_expert_kernel(const __grid_c
 
 template <bool GLU, int P, int R, bool FP4>
 constexpr size_t smem_bytes() {
-  using CF = Cfg<R, P, FP4>;
+  using CF = Cfg<R, P, FP4, GLU>;
   return 1024 + (size_t)CF::kStages * (kATile + CF::kBTile) + CF::kStages * CF::kStg +
          (GLU ? 64 * CF::kXPitch * 4 : 0) + (2 * CF::kStages + 2 * kAccSlots + 2) * 8 + 16;
 }

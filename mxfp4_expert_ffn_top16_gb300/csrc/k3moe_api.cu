@@ -296,8 +296,8 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
 // One token on the tensor-core expert kernel with the weights on M: that kernel selects the
 // experts itself (the dense kernel before it clears its counters), no routing kernel runs.
 inline bool decode_select_in_experts(const k3moe_dims& d, int32_t T) {
-  return T == 1 && umma_expert_ok(d) && d.actq == 0 && decode_weights_on_m(2, T) && T < kUmmaDenseMinTokens &&
-         d.top_k <= 32;
+  return T == 1 && umma_expert_ok(d) && d.actq != 2 && decode_weights_on_m(d.actq ? 1 : 2, T) &&
+         T < kUmmaDenseMinTokens && d.top_k <= 32;
 }
 
 // Bytes of the latent-out weight the one-token expert kernel fetches into L2 ahead of its use.

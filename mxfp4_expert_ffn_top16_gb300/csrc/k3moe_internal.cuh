@@ -260,10 +260,12 @@ cudaError_t launch_umma_wn(const k3moe_dims& d, const k3moe_weights& w, const Pa
                            uint8_t* aq, uint8_t* aqs, bool with_down, float* o_rows, int* chunk_done,
                            uint32_t* err, cudaStream_t s, bool small_experts = false);
 // Which decode kernel: the weights on M for bf16 activations (P = 2) with at most 4 tokens (a
-// chunk then carries at most 8 activation rows), on N otherwise. Measured at decode_b1: 92.5
-// against 94.1 us per step for bf16, 92.6 against 91.8 for MXFP8; at decode_b64 the N side is
-// ahead in both modes.
-inline bool decode_weights_on_m(int P, long long T) { return P == 2 && T <= 4; }
+// chunk then carries at most 8 activation rows) and for MXFP8 at one token, on N otherwise.
+// Measured at decode_b1: 92.5 against 94.1 us per step for bf16, 92.6 against 91.8 for MXFP8
+// before the one-token kernel selected its experts itself; with that (and the latent-out
+// prefetch) MXFP8 takes 86.7 against 91.5 on the M side. At decode_b64 the N side is ahead in
+// both modes.
+inline bool decode_weights_on_m(int P, long long T) { return (P == 2 && T <= 4) || (P == 1 && T == 1); }
 // e8m0 scales [rows][K/32] (rows a multiple of 128, K of 128) -> the decode kernel's staging
 // image (same size): per 128 rows and 128-code chunk a 512-byte block whose byte 16 l + 4 w + q
 // is the scale of row 32 w + l, K-block 4 chunk + q.

@@ -256,7 +256,7 @@ k3moe_status run_expert_gemms(const k3moe_dims& d, const k3moe_weights& w, const
     }
     // Many tokens with e4m3 activations: the experts with at most kSmallExpertRows rows (one
     // chunk each) run on the weights-on-N decode kernel, which streams a weight tile for a few
-    // rows at a far higher rate than the 112-row tiles; the others on the many-token kernel.
+    // rows at a far higher rate than the many-token tiles; the others on the many-token kernel.
     const bool small_split = T >= kUmmaExpertMinTokens && P != 0 && d.latent % 256 == 0;
     {  // many tokens (and MXFP4 activations at any count): z gathered into rows per sorted row
       ProfScope p(P_QUANT, s);

@@ -3,7 +3,7 @@
 // for chunks of more than 8 activation rows (P = 2 from 5 tokens on), where a 256-wide weight
 // side needs half the MMA instructions per weight byte of the 128-wide one. With many tokens it
 // also takes the experts that received at most 8 rows (the tail of the many-token chunk table):
-// for them it streams the weights far faster than the many-token kernel's 112-row tiles.
+// for them it streams the weights far faster than the many-token kernel's wide tiles.
 //
 // "kimi-k3-in-c", MXFP4 experts: 4-bit codes into a 16-entry table, one 8-bit exponent per 32
 // consecutive weights. For sorted row r of expert e (token t):

@@ -14,7 +14,8 @@ rotate over 8 copies (923 MB) so no step finds them in L2.
 
 The default run (decode_b1, one GPU) then measures the metric's other configurations in child
 processes of their own (decode_b64, prefill_4k with bf16, MXFP8 and MXFP4 activations,
-prefill_32k with bf16 and MXFP4; a few steps each) and summarises their lines under "workloads";
+prefill_32k with bf16 and MXFP4, and prefill_32k with unbiased routing; a few steps each) and
+summarises their lines under "workloads";
 --no-secondary skips them.
 
 --impl reference times the CPU oracle (plain C, double accumulation) on the host cores on a
@@ -288,7 +289,7 @@ def cpu_sample(w, layer_seed, x_np, idx_sample, units_per_step, steps, nthreads,
 # the default run, each in a child process of its own (its memory freed at exit) with a fixed
 # number of steps; their lines are summarised under "workloads" of the one JSON line.
 SECONDARY = (("decode_b64", 0, 100), ("prefill_4k", 0, 10), ("prefill_4k", 1, 10), ("prefill_4k", 2, 10),
-             ("prefill_32k", 0, 3), ("prefill_32k", 2, 3))
+             ("prefill_32k", 0, 3), ("prefill_32k_uniform", 0, 3), ("prefill_32k", 2, 3))
 
 
 def summarize_line(line):
@@ -682,8 +683,8 @@ def main():
                          "on the pages; the headline metric is the routed layer without them)")
     ap.add_argument("--no-secondary", dest="secondary", action="store_false",
                     help="decode_b1 only: skip the runs of decode_b64, prefill_4k (bf16, MXFP8 and MXFP4 "
-                         "activations) and prefill_32k (bf16, MXFP4) that the default run adds under "
-                         "\"workloads\"")
+                         "activations) and prefill_32k (bf16 with Zipf and with unbiased routing, MXFP4) "
+                         "that the default run adds under \"workloads\"")
     ap.add_argument("--experts", type=int, default=None,
                     help="profiling aid: the same workload with fewer experts (fits an ncu capture); "
                          "not a bench configuration")
@@ -693,7 +694,7 @@ def main():
     w = synth.WORKLOADS[args.workload]
     if args.experts:
         w = dataclasses.replace(w, dims=dataclasses.replace(w.dims, n_experts=args.experts))
-    default_steps = {"decode_b1": 1000, "decode_b64": 200, "prefill_4k": 20, "prefill_32k": 4}
+    default_steps = {"decode_b1": 1000, "decode_b64": 200, "prefill_4k": 20, "prefill_32k": 4, "prefill_32k_uniform": 4}
     if args.steps is None:
         args.steps = default_steps.get(w.name, 20)
     if args.warmup is None:

@@ -41,22 +41,24 @@ def test_children_commands_and_a_failing_child(monkeypatch):
     def fake_run(cmd, capture_output, text, timeout):
         seen.append(cmd)
         wl = cmd[cmd.index("--workload") + 1]
-        if wl == "prefill_32k":
+        if wl.startswith("prefill_32k"):
             return subprocess.CompletedProcess(cmd, 1, "", "Traceback ...\nRuntimeError: out of memory\n")
         return subprocess.CompletedProcess(cmd, 0, "log line\n" + _line() + "\n", "")
 
     monkeypatch.setattr(bench.subprocess, "run", fake_run)
     res = bench.run_secondary()
     assert set(res) == {"decode_b64", "prefill_4k", "prefill_4k_mxfp8", "prefill_4k_mxfp4", "prefill_32k",
-                        "prefill_32k_mxfp4"}
+                        "prefill_32k_uniform", "prefill_32k_mxfp4"}
     assert res["prefill_32k"] == {"error": "exit 1: RuntimeError: out of memory"}
     assert res["prefill_32k_mxfp4"] == {"error": "exit 1: RuntimeError: out of memory"}
+    assert res["prefill_32k_uniform"] == {"error": "exit 1: RuntimeError: out of memory"}
     assert res["prefill_4k"]["value"] == 537900.0
     for cmd in seen:  # every child: its own workload, at least 3 warm-up steps, no recursion
         assert "--no-secondary" in cmd and "--no-cpu-baseline" in cmd
         assert int(cmd[cmd.index("--warmup") + 1]) >= 3
     actq = {c[c.index("--workload") + 1] + c[c.index("--actq") + 1] for c in seen}
-    assert actq == {"decode_b640", "prefill_4k0", "prefill_4k1", "prefill_4k2", "prefill_32k0", "prefill_32k2"}
+    assert actq == {"decode_b640", "prefill_4k0", "prefill_4k1", "prefill_4k2", "prefill_32k0", "prefill_32k2",
+                    "prefill_32k_uniform0"}
 
 
 def test_expert_split_counts_big_and_small_experts():
